@@ -1,0 +1,109 @@
+"""CPU oracle for TopK selection -- test infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package.  The product path (``topk_selection_gb300``)
+never does, and the two share no code.
+
+``oracle.cc`` holds the definitions (plain single-threaded C++17: std::sort
+descending for int32; std::stable_sort of column indices for rows, so the
+lower index wins among equal values) and an exact one-pass checker for int32
+results at sizes where a full sort is too slow.  Each function cites the page
+section it follows; the tests pin each against brute force, hand-worked
+fixtures, closed forms and invariants.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_DIR = os.path.join(_HERE, "_lib")
+_SRC = os.path.join(_HERE, "oracle.cc")
+_lock = threading.Lock()
+_libs: dict = {}
+
+# Deliberately wrong variants, built only by the tests that show the pins
+# reject them.  The plain build defines none of these.
+PLANTED = ("ORACLE_PLANT_ASCENDING", "ORACLE_PLANT_DEDUP", "ORACLE_PLANT_UNSTABLE",
+           "ORACLE_PLANT_NAN_LOW", "ORACLE_PLANT_SIGNED_ZERO")
+
+
+def _lib_path(plant):
+    return os.path.join(_LIB_DIR, "liboracle.so" if plant is None else f"liboracle_{plant.lower()}.so")
+
+
+def build(plant: str | None = None, force: bool = False) -> str:
+    """Compile oracle.cc with g++ -O2 (one translation unit, a second or two)."""
+    if plant is not None and plant not in PLANTED:
+        raise ValueError(plant)
+    path = _lib_path(plant)
+    if not force and os.path.exists(path) and os.path.getmtime(path) >= os.path.getmtime(_SRC):
+        return path
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    tmp = path + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-o", tmp, _SRC]
+    if plant is not None:
+        cmd.insert(1, f"-D{plant}=1")
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, path)
+    return path
+
+
+def load(plant: str | None = None):
+    with _lock:
+        lib = _libs.get(plant)
+        if lib is None:
+            lib = ctypes.CDLL(build(plant))
+            vp, sz, ci = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+            lib.oracle_topk_i32.argtypes = [vp, sz, ci, vp]
+            lib.oracle_topk_i32.restype = ci
+            lib.oracle_topk_rows_f32.argtypes = [vp, ci, ci, ci, vp, vp]
+            lib.oracle_topk_rows_f32.restype = ci
+            lib.oracle_check_topk_i32.argtypes = [vp, sz, ci, vp]
+            lib.oracle_check_topk_i32.restype = ci
+            _libs[plant] = lib
+    return lib
+
+
+class OracleError(ValueError):
+    pass
+
+
+def topk_i32(x, k: int, plant: str | None = None) -> np.ndarray:
+    """The k largest values of int32 array ``x``, sorted descending."""
+    a = np.ascontiguousarray(x, dtype=np.int32).reshape(-1)
+    out = np.empty(max(k, 0), dtype=np.int32)
+    rc = load(plant).oracle_topk_i32(a.ctypes.data, a.size, int(k), out.ctypes.data)
+    if rc != 0:
+        raise OracleError(f"oracle_topk_i32 rejected n={a.size} k={k}")
+    return out
+
+
+def topk_rows_f32(x, k: int, plant: str | None = None):
+    """Per-row TopK of a 2-D float32 array: (values, column indices), rows x k."""
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    if a.ndim != 2:
+        raise OracleError("rows input must be 2-D")
+    rows, cols = a.shape
+    vals = np.empty((rows, max(k, 0)), dtype=np.float32)
+    idx = np.empty((rows, max(k, 0)), dtype=np.int32)
+    rc = load(plant).oracle_topk_rows_f32(a.ctypes.data, rows, cols, int(k), vals.ctypes.data, idx.ctypes.data)
+    if rc != 0:
+        raise OracleError(f"oracle_topk_rows_f32 rejected rows={rows} cols={cols} k={k}")
+    return vals, idx
+
+
+def check_topk_i32(x, k: int, out) -> bool:
+    """True when ``out`` is exactly the TopK of ``x`` (one pass; any size)."""
+    a = np.ascontiguousarray(x, dtype=np.int32).reshape(-1)
+    o = np.ascontiguousarray(out, dtype=np.int32).reshape(-1)
+    if o.size != k:
+        return False
+    rc = load().oracle_check_topk_i32(a.ctypes.data, a.size, int(k), o.ctypes.data)
+    if rc < 0:
+        raise OracleError(f"oracle_check_topk_i32 rejected n={a.size} k={k}")
+    return rc == 1

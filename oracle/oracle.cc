@@ -1,0 +1,149 @@
+// CPU oracle for TopK selection -- TEST INFRASTRUCTURE ONLY.
+//
+// Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+// load this library.  The CUDA path never calls it and shares no code with it.
+//
+// What the pages define ("CUDA parallel optimisation: TopK, shared memory and
+// two-stage reduction"):
+//   * section 2.1-2.2: gpu_topk(input, output, length, k) keeps the k largest
+//     int values; after the second pass the result is stated to be exactly
+//     the CPU's result.  The per-thread lists are kept in descending order
+//     (section 4.2 shifts smaller entries down), so the output order is
+//     descending.
+//   * section 6: update_candidates(candidates, k, item, score) -- the same
+//     selection keyed by a score that carries an item id; here a row of
+//     float32 scores whose item id is the column index.
+//
+// The method is exact, so the oracle is the plain definition:
+//   topk_i32:      copy, std::sort descending, take the first k.  The output
+//                  is the multiset of the k largest values; equal values
+//                  appear as often as they occur in the input.
+//   topk_rows_f32: per row, std::stable_sort of the column indices by value
+//                  descending, take the first k.  Stability makes the lower
+//                  column index come first among equal values.
+//
+// Readings where the pages are silent (each is listed in the design notes):
+//   * n == 0, k < 1, k > n, cols < k, rows < 1, null pointers: invalid (-1).
+//   * Float order: NaN ranks above +inf and all NaNs are equal to each
+//     other; -0.0 and +0.0 are equal (IEEE comparison); +-inf are ordinary.
+//     Output values are the input's bits, copied, never recomputed.
+//
+// Parity pins: every function here is checked by tests that do not reuse it
+// (exhaustive brute force on tiny inputs, hand-worked fixtures, closed forms,
+// invariants).  The ORACLE_PLANT_* switches exist only so that a test can
+// build a deliberately wrong oracle and show that those pins reject it; the
+// normal build defines none of them.
+#include <algorithm>
+#include <cmath>
+#include <cstddef>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+#include <numeric>
+#include <vector>
+
+namespace {
+
+#if defined(ORACLE_PLANT_NAN_LOW)
+bool ranks_above(float a, float b) {  // planted mistake: NaN ranked lowest
+    bool na = std::isnan(a), nb = std::isnan(b);
+    if (na || nb) return !na && nb;
+    return a > b;
+}
+#elif defined(ORACLE_PLANT_SIGNED_ZERO)
+bool ranks_above(float a, float b) {  // planted mistake: +0.0 above -0.0
+    bool na = std::isnan(a), nb = std::isnan(b);
+    if (na || nb) return na && !nb;
+    if (a == 0.0f && b == 0.0f) return !std::signbit(a) && std::signbit(b);
+    return a > b;
+}
+#else
+// True when a comes strictly before b in the descending score order.
+bool ranks_above(float a, float b) {
+    bool na = std::isnan(a), nb = std::isnan(b);
+    if (na || nb) return na && !nb;
+    return a > b;
+}
+#endif
+
+}  // namespace
+
+extern "C" {
+
+// The k largest values of in[0..n), sorted descending, written to out[0..k).
+// Returns 0, or -1 for invalid arguments (nothing written).
+int oracle_topk_i32(const int32_t* in, size_t n, int k, int32_t* out) {
+    if (!in || !out || n == 0 || k < 1 || (size_t)k > n) return -1;
+    std::vector<int32_t> v(in, in + n);
+#if defined(ORACLE_PLANT_ASCENDING)
+    std::sort(v.begin(), v.end());
+#else
+    std::sort(v.begin(), v.end(), std::greater<int32_t>());
+#endif
+#if defined(ORACLE_PLANT_DEDUP)
+    v.erase(std::unique(v.begin(), v.end()), v.end());  // planted: drops repeats
+    if (v.size() < (size_t)k) v.resize((size_t)k, v.back());
+#endif
+    std::copy(v.begin(), v.begin() + k, out);
+    return 0;
+}
+
+// Row-wise TopK with indices over a row-major rows x cols float matrix.
+// vals and idx are rows x k, row-major: entry j of row r is the j-th best
+// (value descending, lower column index first among equal values).
+// Returns 0, or -1 for invalid arguments.
+int oracle_topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32_t* idx) {
+    if (!in || !vals || !idx || rows < 1 || cols < 1 || k < 1 || k > cols) return -1;
+    std::vector<int32_t> order((size_t)cols);
+    for (int r = 0; r < rows; ++r) {
+        const float* row = in + (size_t)r * (size_t)cols;
+        std::iota(order.begin(), order.end(), 0);
+        auto cmp = [row](int32_t a, int32_t b) { return ranks_above(row[a], row[b]); };
+#if defined(ORACLE_PLANT_UNSTABLE)
+        std::sort(order.begin(), order.end(), cmp);  // planted: tie order lost
+#else
+        std::stable_sort(order.begin(), order.end(), cmp);
+#endif
+        for (int j = 0; j < k; ++j) {
+            int32_t c = order[(size_t)j];
+            idx[(size_t)r * k + j] = c;
+            std::memcpy(&vals[(size_t)r * k + j], &row[c], sizeof(float));
+        }
+    }
+    return 0;
+}
+
+// Exact check of a claimed int32 TopK result at any size, in one pass.
+//
+// out[0..k) is the TopK of in[0..n) exactly when, with t = out[k-1]:
+//   out is sorted descending; fewer than k inputs exceed t and at least k
+//   inputs are >= t (so t is the k-th largest value); and the inputs greater
+//   than t, sorted descending, are exactly out[0..c) with c their count, the
+//   rest of out being copies of t.
+// Returns 1 if out is the TopK, 0 if not, -1 for invalid arguments.
+int oracle_check_topk_i32(const int32_t* in, size_t n, int k, const int32_t* out) {
+    if (!in || !out || n == 0 || k < 1 || (size_t)k > n) return -1;
+    for (int j = 1; j < k; ++j)
+        if (out[j] > out[j - 1]) return 0;
+    const int32_t t = out[k - 1];
+    std::vector<int32_t> above;
+    size_t n_ge = 0;
+    for (size_t i = 0; i < n; ++i) {
+        if (in[i] >= t) {
+            ++n_ge;
+            if (in[i] > t) {
+                if (above.size() + 1 >= (size_t)k) return 0;  // k or more exceed t
+                above.push_back(in[i]);
+            }
+        }
+    }
+    if (n_ge < (size_t)k) return 0;
+    std::sort(above.begin(), above.end(), std::greater<int32_t>());
+    for (size_t j = 0; j < above.size(); ++j)
+        if (out[j] != above[j]) return 0;
+    for (size_t j = above.size(); j < (size_t)k; ++j)
+        if (out[j] != t) return 0;
+    return 1;
+}
+
+}  // extern "C"

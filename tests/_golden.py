@@ -1,0 +1,36 @@
+"""Readers for the hand-worked fixtures under tests/golden/."""
+import os
+import struct
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield [part.strip() for part in line.split("|")]
+
+
+def i32_cases():
+    for inp, k, exp in _lines("topk_i32_hand.txt"):
+        yield (np.array([int(v) for v in inp.split()], dtype=np.int32), int(k),
+               np.array([int(v) for v in exp.split()], dtype=np.int32))
+
+
+def rows_cases():
+    for inp, k, idx, vals in _lines("topk_rows_hand.txt"):
+        yield (np.array([float(v) for v in inp.split()], dtype=np.float32), int(k),
+               np.array([int(v) for v in idx.split()], dtype=np.int32),
+               np.array([float(v) for v in vals.split()], dtype=np.float32))
+
+
+def bits(a):
+    return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+
+
+def f32_from_bits(u):
+    return struct.unpack("<f", struct.pack("<I", u & 0xFFFFFFFF))[0]

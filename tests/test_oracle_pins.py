@@ -1,0 +1,267 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+* exhaustive brute force on tiny inputs (a different algorithm: repeatedly
+  take and remove the best element, written here in plain Python);
+* hand-worked fixtures under tests/golden/ (each cites the page section that
+  defines the operation);
+* closed forms (ascending input, k = 1 is the maximum, k = n is a full
+  descending sort done by numpy, all-equal input);
+* invariants on random inputs (sorted, sub-multiset, k-th value rank);
+* for rows, numpy's stable argsort on inputs without NaN.
+
+The planted-mistake test at the end rebuilds the oracle with one plausible
+bug at a time (on the CPU) and shows that at least one pin rejects it.
+"""
+import collections
+import itertools
+import math
+import struct
+
+import numpy as np
+import pytest
+
+import oracle
+from _golden import bits, i32_cases, rows_cases
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+INT_MIN, INT_MAX = -(2**31), 2**31 - 1
+I32_ALPHABET = [INT_MIN, -1, 0, 1, INT_MAX]
+F32_ALPHABET = [math.nan, -math.inf, -1.0, -0.0, 0.0, 1.0, math.inf]
+
+
+# ---------------------------------------------------------------- helpers --
+
+def brute_topk_i32(values, k):
+    """Take the largest remaining value k times."""
+    pool = list(values)
+    out = []
+    for _ in range(k):
+        best = max(pool)
+        pool.remove(best)
+        out.append(best)
+    return out
+
+
+def _rank_key(v):
+    # Order used by the brute force below: NaN above everything, then value.
+    # -0.0 and +0.0 compare equal under Python float comparison.
+    return (1, 0.0) if math.isnan(v) else (0, v)
+
+
+def brute_topk_row(row, k):
+    """Pick the best remaining column k times; the lowest column wins ties."""
+    remaining = list(range(len(row)))
+    picked = []
+    for _ in range(k):
+        best = remaining[0]
+        for c in remaining[1:]:
+            if _rank_key(row[c]) > _rank_key(row[best]):
+                best = c
+        remaining.remove(best)
+        picked.append(best)
+    return picked
+
+
+# Each pin below takes `plant` so the planted-mistake test can rerun it
+# against a deliberately wrong oracle build.
+
+def pin_golden_i32(plant=None):
+    for x, k, exp in i32_cases():
+        got = oracle.topk_i32(x, k, plant=plant)
+        assert got.tolist() == exp.tolist(), (x.tolist(), k)
+
+
+def pin_golden_rows(plant=None):
+    for row, k, exp_idx, exp_vals in rows_cases():
+        vals, idx = oracle.topk_rows_f32(row[None, :], k, plant=plant)
+        assert idx[0].tolist() == exp_idx.tolist(), (row.tolist(), k)
+        assert bits(vals[0]).tolist() == bits(exp_vals).tolist(), (row.tolist(), k)
+
+
+def pin_exhaustive_i32(plant=None, max_n=5):
+    for n in range(1, max_n + 1):
+        for combo in itertools.product(I32_ALPHABET, repeat=n):
+            x = np.array(combo, dtype=np.int32)
+            for k in range(1, n + 1):
+                got = oracle.topk_i32(x, k, plant=plant).tolist()
+                assert got == brute_topk_i32(combo, k), (combo, k)
+
+
+def pin_exhaustive_rows(plant=None, max_cols=4):
+    for cols in range(1, max_cols + 1):
+        rows = np.array(list(itertools.product(F32_ALPHABET, repeat=cols)), dtype=np.float32)
+        for k in range(1, cols + 1):
+            vals, idx = oracle.topk_rows_f32(rows, k, plant=plant)
+            for r in range(rows.shape[0]):
+                exp = brute_topk_row(rows[r].tolist(), k)
+                assert idx[r].tolist() == exp, (rows[r].tolist(), k)
+                assert bits(vals[r]).tolist() == bits(rows[r][exp]).tolist()
+
+
+def pin_closed_forms_i32(plant=None):
+    n = 100_003
+    asc = np.arange(n, dtype=np.int32)
+    for k in (1, 20, 100):
+        assert oracle.topk_i32(asc, k, plant=plant).tolist() == list(range(n - 1, n - 1 - k, -1))
+    rng = np.random.default_rng(7)
+    x = rng.integers(INT_MIN, INT_MAX, size=50_000, endpoint=True, dtype=np.int64).astype(np.int32)
+    assert oracle.topk_i32(x, 1, plant=plant)[0] == x.max()
+    full = oracle.topk_i32(x, x.size, plant=plant)
+    assert np.array_equal(full, np.sort(x)[::-1])
+    dup = rng.integers(0, 1000, size=200_000).astype(np.int32)
+    assert oracle.topk_i32(dup, 20, plant=plant).tolist() == [999] * 20
+    same = np.full(1000, -5, dtype=np.int32)
+    assert oracle.topk_i32(same, 999, plant=plant).tolist() == [-5] * 999
+
+
+def pin_rows_numpy(plant=None):
+    # Without NaN the order is numpy's stable argsort of the negated values
+    # (-0.0 and +0.0 compare equal in numpy's sort as well).
+    rng = np.random.default_rng(11)
+    x = np.round(rng.standard_normal((64, 300)) * 4) / 4  # many exact ties
+    x = x.astype(np.float32)
+    x[0, :5] = [-0.0, 0.0, -0.0, 0.0, 0.0]
+    x[1, :] = np.float32(2.0)
+    for k in (1, 7, 64, 300):
+        vals, idx = oracle.topk_rows_f32(x, k, plant=plant)
+        exp_idx = np.argsort(-x, axis=1, kind="stable")[:, :k]
+        assert np.array_equal(idx, exp_idx)
+        assert np.array_equal(bits(vals), bits(np.take_along_axis(x, exp_idx, axis=1)))
+
+
+ALL_PINS = [pin_golden_i32, pin_golden_rows, pin_exhaustive_i32, pin_exhaustive_rows,
+            pin_closed_forms_i32, pin_rows_numpy]
+
+
+# ------------------------------------------------------------------ tests --
+
+def test_golden_i32():
+    pin_golden_i32()
+
+
+def test_golden_rows():
+    pin_golden_rows()
+
+
+def test_exhaustive_i32_bruteforce():
+    pin_exhaustive_i32(max_n=6)
+
+
+def test_exhaustive_rows_bruteforce():
+    pin_exhaustive_rows(max_cols=4)
+
+
+def test_closed_forms_i32():
+    pin_closed_forms_i32()
+
+
+def test_rows_match_numpy_stable_argsort():
+    pin_rows_numpy()
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_invariants_i32_random(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 20_000))
+    k = int(rng.integers(1, n + 1))
+    lo, hi = [(INT_MIN, INT_MAX), (-50, 50), (0, 3)][seed % 3]
+    x = rng.integers(lo, hi, size=n, endpoint=True, dtype=np.int64).astype(np.int32)
+    out = oracle.topk_i32(x, k)
+    assert out.size == k
+    assert np.all(out[:-1] >= out[1:])
+    have = collections.Counter(x.tolist())
+    for v, c in collections.Counter(out.tolist()).items():
+        assert have[v] >= c
+    t = out[-1]
+    assert np.count_nonzero(x > t) < k
+    assert np.count_nonzero(x >= t) >= k
+
+
+def test_invariants_rows_random():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((40, 513)).astype(np.float32)
+    x[:, ::7] = x[:, :1]  # ties with each row's first value
+    k = 33
+    vals, idx = oracle.topk_rows_f32(x, k)
+    for r in range(x.shape[0]):
+        assert len(set(idx[r].tolist())) == k
+        assert np.array_equal(bits(vals[r]), bits(x[r, idx[r]]))
+        for j in range(1, k):
+            a, b = vals[r, j - 1], vals[r, j]
+            assert a > b or (a == b and idx[r, j - 1] < idx[r, j])
+        kth, kidx = vals[r, -1], idx[r, -1]
+        better = np.count_nonzero((x[r] > kth) | ((x[r] == kth) & (np.arange(x.shape[1]) < kidx)))
+        assert better == k - 1
+
+
+def test_nan_payload_bits_are_copied():
+    payload = struct.unpack("<f", struct.pack("<I", 0xFFC12345))[0]  # a negative NaN with payload
+    row = np.array([1.0, payload, 2.0], dtype=np.float32)
+    vals, idx = oracle.topk_rows_f32(row[None, :], 2)
+    assert idx[0].tolist() == [1, 2]
+    assert bits(vals[0]).tolist() == [0xFFC12345, bits(np.float32(2.0)).item()]
+
+
+def test_invalid_arguments_rejected():
+    x = np.arange(10, dtype=np.int32)
+    for k in (0, -1, 11):
+        with pytest.raises(oracle.OracleError):
+            oracle.topk_i32(x, k)
+    with pytest.raises(oracle.OracleError):
+        oracle.topk_i32(np.zeros(0, dtype=np.int32), 1)
+    m = np.zeros((3, 4), dtype=np.float32)
+    for k in (0, 5):
+        with pytest.raises(oracle.OracleError):
+            oracle.topk_rows_f32(m, k)
+
+
+# -------------------------------------------------- the exact checker --
+
+def test_checker_accepts_oracle_results():
+    rng = np.random.default_rng(5)
+    for trial in range(20):
+        n = int(rng.integers(1, 5000))
+        k = int(rng.integers(1, min(n, 300) + 1))
+        x = rng.integers(-40, 40, size=n).astype(np.int32) if trial % 2 else \
+            rng.integers(INT_MIN, INT_MAX, size=n, endpoint=True, dtype=np.int64).astype(np.int32)
+        assert oracle.check_topk_i32(x, k, oracle.topk_i32(x, k))
+
+
+def test_checker_rejects_wrong_results():
+    x = np.array([5, 3, 3, 9, -1, 3, 7, 7], dtype=np.int32)
+    good = oracle.topk_i32(x, 4)  # 9 7 7 5
+    assert good.tolist() == [9, 7, 7, 5]
+    assert oracle.check_topk_i32(x, 4, good)
+    wrong = [
+        [9, 7, 7, 3],   # k-th value too small
+        [9, 7, 5, 3],   # a repeat dropped
+        [9, 9, 7, 7],   # a value repeated more often than in the input
+        [7, 9, 7, 5],   # not sorted
+        [9, 7, 7, 6],   # 6 is not in the input
+        [9, 7, 5, 5],   # 5 occurs once
+    ]
+    for w in wrong:
+        assert not oracle.check_topk_i32(x, 4, np.array(w, dtype=np.int32)), w
+    assert not oracle.check_topk_i32(x, 4, good[:3])
+    y = np.array([5, 3, 3], dtype=np.int32)
+    assert oracle.check_topk_i32(y, 2, np.array([5, 3], dtype=np.int32))
+    assert not oracle.check_topk_i32(y, 2, np.array([3, 3], dtype=np.int32))
+
+
+# -------------------------------------------- planted mistakes (CPU only) --
+
+@pytest.mark.parametrize("plant", oracle.PLANTED)
+def test_pins_reject_planted_mistake(plant):
+    failures = 0
+    for pin in ALL_PINS:
+        try:
+            if pin is pin_exhaustive_i32:
+                pin(plant=plant, max_n=4)
+            elif pin is pin_exhaustive_rows:
+                pin(plant=plant, max_cols=3)
+            else:
+                pin(plant=plant)
+        except AssertionError:
+            failures += 1
+    assert failures >= 1, f"no pin caught {plant}"

@@ -1,0 +1,120 @@
+/*
+ * topk.h -- C ABI of libtopk.so, TopK selection on one NVIDIA GB300 (sm_103a).
+ *
+ * Two operations, both from "CUDA parallel optimisation: TopK, shared memory
+ * and two-stage reduction":
+ *
+ *   topk_i32       the k largest values of an int32 array, sorted descending
+ *                  (sections 2.1-2.2: a block-level pass that leaves k
+ *                  candidates per block, then a second pass over the
+ *                  candidates; the result equals the CPU's exactly).
+ *   topk_rows_f32  per row of a float32 matrix, the k best scores with their
+ *                  column indices (section 6, update_candidates: TopK keyed
+ *                  by a score that carries an item id).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers may be device memory (cudaMalloc, managed) or host memory
+ *     (pageable or pinned).  The library asks the CUDA runtime which one it
+ *     is.  Device pointers: the call only enqueues work on `stream` and
+ *     returns; read the outputs after synchronising the stream.  If any
+ *     pointer is host memory: inputs are copied to device staging, outputs
+ *     are copied back, and the call returns only after `stream` has
+ *     finished, so host outputs are ready on return.
+ *   - `stream` is a cudaStream_t; NULL means the legacy default stream.
+ *   - Inputs are read-only.  Outputs must not overlap inputs.  Any 4-byte
+ *     aligned address is accepted.
+ *   - The caller owns every buffer it passes.  The library owns a cached
+ *     device workspace per (device, stream), grown on demand with
+ *     cudaMalloc and freed by topk_release_workspace().  Calls on one stream
+ *     share that stream's workspace in stream order; calls on different
+ *     streams never share one.
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and leave the outputs untouched.
+ *   - The current CUDA device is the one used.
+ */
+#ifndef TOPK_GB300_TOPK_H
+#define TOPK_GB300_TOPK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+
+/* Status codes returned by every entry point. */
+enum topk_status {
+    TOPK_OK = 0,
+    TOPK_ERR_INVALID_ARG = 1, /* null pointer, n == 0, k < 1, k > n, rows < 1, cols < k, overlap */
+    TOPK_ERR_UNSUPPORTED = 2, /* k > TOPK_MAX_K, or a size the kernels do not take */
+    TOPK_ERR_NO_MEMORY = 3,   /* workspace or staging allocation failed */
+    TOPK_ERR_CUDA = 4         /* a CUDA runtime call or launch failed; see topk_last_cuda_error() */
+};
+
+/* Largest k accepted by either operation. */
+#define TOPK_MAX_K 1024
+
+/*
+ * topk_i32 -- the k largest values of in[0..n), written to out[0..k) in
+ * descending order.  Equal values appear as often as they occur in the input
+ * (the result is a multiset; there are no indices, so no tie order).
+ *
+ *   in     int32[n], read-only.
+ *   n      number of elements, 1 <= n <= 2^40.
+ *   k      1 <= k <= min(n, TOPK_MAX_K).
+ *   out    int32[k], written.
+ *
+ * Work is two passes over the data on the GPU: every block filters its share
+ * of the input against a running k-th-value threshold and leaves k
+ * candidates; the last block to finish merges the candidates (section 2.2's
+ * second pass, fused into the same launch).
+ *
+ * Returns TOPK_OK or an error code; on error nothing is written to out.
+ */
+int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_st* stream);
+
+/*
+ * topk_rows_f32 -- for each row r of the row-major rows x cols matrix `in`,
+ * the k best entries: vals[r*k + j] is the j-th best value of row r and
+ * idx[r*k + j] its column.
+ *
+ * Order: value descending; among equal values the lower column index comes
+ * first.  -0.0 and +0.0 are equal.  NaN ranks above +inf and all NaNs are
+ * equal (so among NaNs the lower column wins).  Values are copied bit for bit
+ * from the input (a -0.0 stays -0.0, a NaN keeps its payload).
+ *
+ *   in     float32[rows * cols], row-major, read-only.
+ *   rows   1 <= rows <= 2^31 - 1.
+ *   cols   k <= cols <= 2^31 - 1.
+ *   k      1 <= k <= min(cols, TOPK_MAX_K).
+ *   vals   float32[rows * k], written.
+ *   idx    int32[rows * k], written.
+ *
+ * Returns TOPK_OK or an error code; on error nothing is written.
+ */
+int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
+                  struct CUstream_st* stream);
+
+/* A static, human-readable name for a status code. */
+const char* topk_status_string(int status);
+
+/* The cudaError_t value behind the last TOPK_ERR_CUDA returned on the
+ * calling thread (0 if none). */
+int topk_last_cuda_error(void);
+
+/* Free every cached workspace of the calling process (all devices, all
+ * streams).  The caller must make sure no TopK work is still running.
+ * Returns TOPK_OK or TOPK_ERR_CUDA. */
+int topk_release_workspace(void);
+
+/* Number of CUDA kernels this library has launched in this process; a
+ * diagnostic for benchmarks that count launches. */
+unsigned long long topk_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOPK_GB300_TOPK_H */

@@ -1,0 +1,118 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/*.h declares, and rejects bad arguments on the host before any CUDA
+call (so these run on a machine without a GPU)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+
+    __graft_entry__._load_build_module().build()
+    import topk_selection_gb300 as tk
+
+    return tk._lib
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(topk_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("topk_i32", "topk_rows_f32", "topk_status_string", "topk_release_workspace",
+                     "topk_last_cuda_error", "topk_launch_count"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libtopk.so does not export {name}"
+
+
+def test_status_strings(lib):
+    import topk_selection_gb300 as tk
+
+    assert tk.status_string(0) == "ok"
+    assert tk.status_string(1) == "invalid argument"
+    assert tk.status_string(2) == "unsupported size"
+    assert tk.status_string(99) == "unknown status"
+
+
+# Fake, never-dereferenced addresses: the argument checks return before any
+# pointer is used or any CUDA call is made.
+A, B, C = 0x10000000, 0x20000000, 0x30000000
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 100, 5, B), 1),          # null input
+    ((A, 100, 5, 0), 1),          # null output
+    ((A, 0, 1, B), 1),            # n == 0
+    ((A, 100, 0, B), 1),          # k < 1
+    ((A, 100, -3, B), 1),         # k < 1
+    ((A, 100, 101, B), 1),        # k > n
+    ((A + 2, 100, 5, B), 1),      # misaligned input
+    ((A, 100, 5, B + 1), 1),      # misaligned output
+    ((A, 100, 5, A + 40), 1),     # output overlaps input
+    ((A, 5000, 1025, B), 2),      # k above the maximum
+    ((B, (1 << 40) + 4, 5, A), 2),  # n above the maximum
+])
+def test_topk_i32_argument_errors(lib, args, status):
+    import topk_selection_gb300 as tk
+
+    assert tk.topk_i32_ptr(*args) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 4, 8, 2, B, C), 1),        # null input
+    ((A, 4, 8, 2, 0, C), 1),        # null vals
+    ((A, 4, 8, 2, B, 0), 1),        # null idx
+    ((A, 0, 8, 2, B, C), 1),        # rows < 1
+    ((A, 4, 0, 1, B, C), 1),        # cols < 1
+    ((A, 4, 8, 0, B, C), 1),        # k < 1
+    ((A, 4, 8, 9, B, C), 1),        # k > cols
+    ((A, 4, 8, 2, B, B + 8), 1),    # vals and idx overlap
+    ((A, 4, 8, 2, A + 4, C), 1),    # vals overlaps the input
+    ((A, 4, 2048, 1025, B, C), 2),  # k above the maximum
+])
+def test_topk_rows_argument_errors(lib, args, status):
+    import topk_selection_gb300 as tk
+
+    assert tk.topk_rows_f32_ptr(*args) == status
+
+
+def test_python_binding_rejects_wrong_types(lib):
+    import torch
+
+    import topk_selection_gb300 as tk
+
+    with pytest.raises(TypeError):
+        tk.topk_i32(torch.zeros(10, dtype=torch.int64), 3)
+    with pytest.raises(TypeError):
+        tk.topk_rows_f32(torch.zeros(2, 10, dtype=torch.float64), 3)
+    with pytest.raises(ValueError):
+        tk.topk_rows_f32(torch.zeros(10, dtype=torch.float32), 3)
+    with pytest.raises(ValueError):
+        tk.topk_i32(torch.zeros(20, dtype=torch.int32)[::2], 3)
+    with pytest.raises(tk.TopKError) as e:
+        tk.topk_i32(torch.zeros(10, dtype=torch.int32), 11)
+    assert e.value.status == 1
+
+
+def test_launch_counter_starts_at_zero_without_gpu(lib):
+    import topk_selection_gb300 as tk
+
+    assert tk.launch_count() >= 0

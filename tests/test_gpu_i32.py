@@ -1,0 +1,174 @@
+"""int32 TopK on the GPU, through the C ABI, against the CPU oracle.
+
+Bit-exact: the output is an int32 multiset sorted descending, so the GPU's
+k values must equal the oracle's element by element.  Small and medium sizes
+are compared with the full oracle (std::sort); the 1e8 and 1e9 workloads are
+checked with the oracle's exact one-pass checker (which the CPU tests pin
+against the full oracle), and the 1e8 one also with the full oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+INT_MIN, INT_MAX = -(2**31), 2**31 - 1
+
+
+@pytest.fixture(scope="module")
+def tk():
+    import topk_selection_gb300
+
+    return topk_selection_gb300
+
+
+def gpu_topk(tk, x_np, k, offset=0, stream=None):
+    """Copy x to the device at an element offset (so the base pointer can be
+    misaligned to 16 bytes) and run topk_i32 there."""
+    buf = torch.empty(x_np.size + offset, dtype=torch.int32, device="cuda")
+    view = buf[offset:]
+    view.copy_(torch.from_numpy(x_np))
+    out = tk.topk_i32(view, k, stream=stream)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def make(kind, n, seed):
+    rng = np.random.default_rng(seed)
+    if kind == "uniform":
+        return synth.i32_uniform(n, seed)
+    if kind == "ascending":
+        return np.arange(n, dtype=np.int64).astype(np.int32)
+    if kind == "descending":
+        return np.arange(n, 0, -1, dtype=np.int64).astype(np.int32)
+    if kind == "equal":
+        return np.full(n, 7, dtype=np.int32)
+    if kind == "int_min":
+        return np.full(n, INT_MIN, dtype=np.int32)
+    if kind == "negative":
+        return rng.integers(INT_MIN, 0, size=n, dtype=np.int64).astype(np.int32)
+    if kind == "dups":
+        return rng.integers(0, 1000, size=n).astype(np.int32)
+    if kind == "few":
+        return rng.choice(np.array([INT_MIN, -1, 0, 1, INT_MAX], dtype=np.int32), size=n)
+    if kind == "int_max_heavy":
+        x = rng.integers(INT_MIN, INT_MAX, size=n, dtype=np.int64).astype(np.int32)
+        x[rng.random(n) < 0.3] = INT_MAX
+        return x
+    if kind == "sawtooth":
+        return (np.arange(n, dtype=np.int64) % 1009).astype(np.int32)
+    raise KeyError(kind)
+
+
+KINDS = ["uniform", "ascending", "descending", "equal", "int_min", "negative", "dups", "few",
+         "int_max_heavy", "sawtooth"]
+SIZES = [1, 2, 3, 4, 5, 7, 31, 33, 127, 129, 1023, 1025, 4095, 4097, 65537, 300_007]
+KS = [1, 2, 20, 32, 33, 64, 65, 100, 128, 129, 1000, 1024]
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_edge_sizes_and_ks(tk, kind):
+    for i, n in enumerate(SIZES):
+        x = make(kind, n, seed=n)
+        for k in KS:
+            if k > n:
+                continue
+            got = gpu_topk(tk, x, k)
+            exp = oracle.topk_i32(x, k)
+            assert np.array_equal(got, exp), (kind, n, k, got[:8], exp[:8])
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_misaligned_base(tk, offset):
+    for n in (5, 6, 7, 1029, 262_147):
+        x = make("uniform", n, seed=offset)
+        for k in (1, 20, 100):
+            if k <= n:
+                assert np.array_equal(gpu_topk(tk, x, k, offset=offset), oracle.topk_i32(x, k))
+
+
+def test_many_tiles_ragged_tail(tk):
+    # Several tiles per warp and a last tile that is only partly filled.
+    for n in (2_000_003, 4_194_305):
+        x = make("uniform", n, seed=n)
+        for k in (1, 20, 64, 100, 128):
+            assert np.array_equal(gpu_topk(tk, x, k), oracle.topk_i32(x, k)), (n, k)
+
+
+def test_back_to_back_calls_reset_state(tk):
+    # The control words are reset by each launch: a large threshold left by a
+    # call must not leak into the next call on the same stream.
+    big = np.full(500_000, INT_MAX, dtype=np.int32)
+    small = make("negative", 400_000, seed=3)
+    s = torch.cuda.Stream()
+    for _ in range(3):
+        with torch.cuda.stream(s):
+            a = gpu_topk(tk, big, 20, stream=s)
+            b = gpu_topk(tk, small, 20, stream=s)
+        assert np.array_equal(a, oracle.topk_i32(big, 20))
+        assert np.array_equal(b, oracle.topk_i32(small, 20))
+
+
+def test_non_default_stream_in_flight(tk):
+    x = synth.i32_uniform(3_000_000, 11)
+    d = torch.from_numpy(x).cuda()
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for k in (1, 20, 100):
+            outs.append((k, tk.topk_i32(d, k)))
+    s.synchronize()
+    for k, o in outs:
+        assert np.array_equal(o.cpu().numpy(), oracle.topk_i32(x, k))
+
+
+def test_host_buffers(tk):
+    # CPU tensors: the library stages them through device memory itself.
+    x = synth.i32_uniform(1_000_003, 21)
+    xt = torch.from_numpy(x)
+    for pin in (False, True):
+        src = xt.pin_memory() if pin else xt
+        out = torch.empty(20, dtype=torch.int32, pin_memory=pin)
+        tk.topk_i32(src, 20, out=out)
+        assert np.array_equal(out.numpy(), oracle.topk_i32(x, 20))
+
+
+def test_workload_2p20(tk):
+    x = synth.i32_workload("i32_uniform_2p20")
+    assert np.array_equal(gpu_topk(tk, x, 20), oracle.topk_i32(x, 20))
+
+
+def test_workload_1e7(tk):
+    x = synth.i32_workload("i32_uniform_1e7")
+    for k in (20, 100):
+        assert np.array_equal(gpu_topk(tk, x, k), oracle.topk_i32(x, k))
+
+
+def test_workload_1e8(tk):
+    x = synth.i32_workload("i32_uniform_1e8")
+    d = torch.from_numpy(x).cuda()
+    for k in (20, 1):
+        got = tk.topk_i32(d, k).cpu().numpy()
+        assert oracle.check_topk_i32(x, k, got)
+        if k == 20:
+            assert np.array_equal(got, oracle.topk_i32(x, k))
+        else:
+            assert got[0] == x.max()
+    del d
+
+
+@pytest.mark.parametrize("name", ["i32_uniform_1e9", "i32_ascending_1e9", "i32_dup1000_1e9"])
+def test_workload_1e9(tk, name):
+    x = synth.i32_workload(name)
+    d = torch.from_numpy(x).cuda()
+    got = tk.topk_i32(d, 20).cpu().numpy()
+    del d
+    torch.cuda.empty_cache()
+    assert oracle.check_topk_i32(x, 20, got), (name, got)
+    if name == "i32_ascending_1e9":
+        assert got.tolist() == list(range(10**9 - 1, 10**9 - 21, -1))
+    if name == "i32_dup1000_1e9":
+        assert got.tolist() == [999] * 20

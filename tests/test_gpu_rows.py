@@ -1,0 +1,140 @@
+"""Row TopK with indices on the GPU, through the C ABI, against the oracle.
+
+Bit-exact: column indices must equal the oracle's (value descending, lower
+column first among equal values) and the values must carry the input's bits.
+The 4096 x 32768 workload is compared with the oracle on a spread of sampled
+rows, and every row is checked for the properties that pin the answer (the
+k-th entry is beaten by exactly k-1 elements of its row, values are the
+input's bits at the returned columns, columns are distinct and ordered).
+"""
+import math
+import struct
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tk():
+    import topk_selection_gb300
+
+    return topk_selection_gb300
+
+
+def bits(a):
+    return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+
+
+def gpu_rows(tk, x, k, col_offset=0):
+    rows, cols = x.shape
+    if col_offset:
+        # Rows placed at an element offset so row starts are not 16-byte aligned.
+        buf = torch.empty(rows * cols + col_offset, dtype=torch.float32, device="cuda")
+        dx = buf[col_offset:].view(rows, cols)
+        dx.copy_(torch.from_numpy(x))
+    else:
+        dx = torch.from_numpy(x).cuda()
+    v, i = tk.topk_rows_f32(dx, k)
+    torch.cuda.synchronize()
+    return v.cpu().numpy(), i.cpu().numpy()
+
+
+def assert_rows_equal(tk, x, k, col_offset=0):
+    v, i = gpu_rows(tk, x, k, col_offset)
+    ev, ei = oracle.topk_rows_f32(x, k)
+    bad = np.nonzero(~np.all(i == ei, axis=1))[0]
+    assert bad.size == 0, (k, x.shape, bad[:5], i[bad[0]][:8], ei[bad[0]][:8])
+    assert np.array_equal(bits(v), bits(ev)), (k, x.shape)
+
+
+SPECIAL = np.array([math.nan, -math.inf, math.inf, -0.0, 0.0, 1.0, -1.0, 3.5e38, -3.5e38, 1e-45, -1e-45],
+                   dtype=np.float32)
+
+
+@pytest.mark.parametrize("cols", [1, 2, 3, 4, 5, 31, 33, 127, 1024, 1025, 4099, 32768])
+def test_shapes_and_ks(tk, cols):
+    rng = np.random.default_rng(cols)
+    rows = 37
+    x = rng.standard_normal((rows, cols)).astype(np.float32)
+    x[1] = 2.0                              # a row of equal values
+    x[2] = np.round(x[2] * 2) / 2           # many ties
+    x[3] = SPECIAL[rng.integers(0, SPECIAL.size, cols)]
+    x[4] = -np.abs(x[4])                    # all negative
+    for k in (1, 2, 7, 32, 33, 64, 100, 128, 129, 500, 1024):
+        if k <= cols:
+            assert_rows_equal(tk, x, k)
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_misaligned_rows(tk, offset):
+    rng = np.random.default_rng(offset)
+    x = rng.standard_normal((19, 2051)).astype(np.float32)
+    for k in (1, 64, 129):
+        assert_rows_equal(tk, x, k, col_offset=offset)
+
+
+def test_signed_zero_and_nan_payload(tk):
+    neg_nan = struct.unpack("<f", struct.pack("<I", 0xFFC12345))[0]
+    x = np.zeros((4, 64), dtype=np.float32)
+    x[0, ::2] = -0.0
+    x[1, 5] = neg_nan
+    x[1, 9] = math.nan
+    x[2, :] = -math.inf
+    x[3, 40:] = math.inf
+    for k in (1, 3, 64):
+        assert_rows_equal(tk, x, k)
+    v, i = gpu_rows(tk, x, 2)
+    assert i[1].tolist() == [5, 9]
+    assert bits(v[1])[0] == 0xFFC12345
+
+
+def test_tied_rows_small(tk):
+    x = synth.f32_rows_tied(128, 4096, 5)
+    for k in (1, 40, 41, 64, 128):
+        assert_rows_equal(tk, x, k)
+
+
+def test_host_buffers(tk):
+    x = synth.f32_rows_tied(33, 1000, 7)
+    ev, ei = oracle.topk_rows_f32(x, 64)
+    v, i = tk.topk_rows_f32(torch.from_numpy(x), 64)
+    assert np.array_equal(i.numpy(), ei)
+    assert np.array_equal(bits(v.numpy()), bits(ev))
+
+
+def check_all_rows(x, k, v, i):
+    rows, cols = x.shape
+    # values are the input's bits at the returned columns
+    assert np.array_equal(bits(v), bits(np.take_along_axis(x, i.astype(np.int64), axis=1)))
+    # columns are distinct per row
+    s = np.sort(i, axis=1)
+    assert np.all(s[:, 1:] != s[:, :-1])
+    # order: value descending, lower column first among equal values (no NaN here)
+    a, b = v[:, :-1], v[:, 1:]
+    assert np.all((a > b) | ((a == b) & (i[:, :-1] < i[:, 1:])))
+    # exactly k-1 elements of the row beat the k-th entry
+    kv, ki = v[:, -1:], i[:, -1:]
+    col = np.arange(cols)[None, :]
+    beat = (x > kv) | ((x == kv) & (col < ki))
+    assert np.all(beat.sum(axis=1) == k - 1)
+
+
+@pytest.mark.parametrize("tied", [True, False])
+def test_workload_4096x32768(tk, tied):
+    w = synth.ROWS_WORKLOAD
+    rows, cols, k = w["rows"], w["cols"], w["k"]
+    x = synth.f32_rows_tied(rows, cols, w["seed"], w["tie_frac"]) if tied else \
+        synth.f32_rows_normal(rows, cols, w["seed"])
+    v, i = gpu_rows(tk, x, k)
+    sample = np.unique(np.linspace(0, rows - 1, 256).astype(np.int64))
+    ev, ei = oracle.topk_rows_f32(x[sample], k)
+    assert np.array_equal(i[sample], ei)
+    assert np.array_equal(bits(v[sample]), bits(ev))
+    for lo in range(0, rows, 512):
+        check_all_rows(x[lo:lo + 512], k, v[lo:lo + 512], i[lo:lo + 512])

@@ -1,0 +1,157 @@
+"""TopK selection on one GB300 (sm_103a): thin Python binding of libtopk.so.
+
+Argument marshalling only -- every step of the selection runs in the CUDA
+kernels behind the C ABI declared in include/topk.h.  PyTorch supplies device
+memory and the current stream.  There is no CPU fallback: if the library has
+not been built, importing the binding raises.
+
+    topk_i32(x, k)          -> int32 tensor [k], the k largest values, descending
+    topk_rows_f32(x, k)     -> (float32 [rows, k], int32 [rows, k]) per-row best
+                               values and their columns; lower column wins ties
+
+Both accept CUDA tensors (asynchronous on the current stream) or CPU tensors
+(the library stages them through device memory and returns when done).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = ["topk_i32", "topk_rows_f32", "topk_i32_ptr", "topk_rows_f32_ptr", "TopKError", "MAX_K",
+           "status_string", "release_workspace", "launch_count", "last_cuda_error", "library_path"]
+
+MAX_K = 1024
+TOPK_OK, TOPK_ERR_INVALID_ARG, TOPK_ERR_UNSUPPORTED, TOPK_ERR_NO_MEMORY, TOPK_ERR_CUDA = range(5)
+
+
+class TopKError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def _load():
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, sz, ci = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    lib.topk_i32.argtypes = [vp, sz, ci, vp, vp]
+    lib.topk_i32.restype = ci
+    lib.topk_rows_f32.argtypes = [vp, ci, ci, ci, vp, vp, vp]
+    lib.topk_rows_f32.restype = ci
+    lib.topk_status_string.argtypes = [ci]
+    lib.topk_status_string.restype = ctypes.c_char_p
+    lib.topk_last_cuda_error.argtypes = []
+    lib.topk_last_cuda_error.restype = ci
+    lib.topk_release_workspace.argtypes = []
+    lib.topk_release_workspace.restype = ci
+    lib.topk_launch_count.argtypes = []
+    lib.topk_launch_count.restype = ctypes.c_ulonglong
+    return lib
+
+
+_lib = _load()
+
+
+def status_string(status: int) -> str:
+    return _lib.topk_status_string(int(status)).decode()
+
+
+def last_cuda_error() -> int:
+    return int(_lib.topk_last_cuda_error())
+
+
+def release_workspace() -> None:
+    rc = _lib.topk_release_workspace()
+    if rc != TOPK_OK:
+        raise TopKError(rc, "topk_release_workspace")
+
+
+def launch_count() -> int:
+    return int(_lib.topk_launch_count())
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        if device is None:
+            return 0
+        stream = torch.cuda.current_stream(device)
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def topk_i32_ptr(in_ptr: int, n: int, k: int, out_ptr: int, stream: int = 0) -> int:
+    """Raw C-ABI call; returns the status code."""
+    return int(_lib.topk_i32(ctypes.c_void_p(in_ptr), n, k, ctypes.c_void_p(out_ptr), ctypes.c_void_p(stream)))
+
+
+def topk_rows_f32_ptr(in_ptr: int, rows: int, cols: int, k: int, vals_ptr: int, idx_ptr: int,
+                      stream: int = 0) -> int:
+    """Raw C-ABI call; returns the status code."""
+    return int(_lib.topk_rows_f32(ctypes.c_void_p(in_ptr), rows, cols, k, ctypes.c_void_p(vals_ptr),
+                                  ctypes.c_void_p(idx_ptr), ctypes.c_void_p(stream)))
+
+
+def _check_input(x: torch.Tensor, dtype, name):
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if x.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {x.dtype}")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def topk_i32(x: torch.Tensor, k: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The k largest values of int32 tensor x (flattened), sorted descending."""
+    _check_input(x, torch.int32, "x")
+    if out is None:
+        out = torch.empty(max(int(k), 0), dtype=torch.int32, device=x.device)
+    _check_input(out, torch.int32, "out")
+    if out.numel() != k:
+        raise ValueError("out must have k elements")
+    dev = x.device if x.is_cuda else (out.device if out.is_cuda else None)
+    with torch.cuda.device(dev) if dev is not None else _null():
+        rc = topk_i32_ptr(x.data_ptr(), x.numel(), int(k), out.data_ptr(), _stream_handle(stream, dev))
+    if rc != TOPK_OK:
+        raise TopKError(rc, "topk_i32")
+    return out
+
+
+def topk_rows_f32(x: torch.Tensor, k: int, vals: torch.Tensor | None = None, idx: torch.Tensor | None = None,
+                  stream=None):
+    """Per-row TopK of a 2-D float32 tensor: (values [rows, k], columns [rows, k])."""
+    _check_input(x, torch.float32, "x")
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (rows, cols)")
+    rows, cols = x.shape
+    if vals is None:
+        vals = torch.empty((rows, max(int(k), 0)), dtype=torch.float32, device=x.device)
+    if idx is None:
+        idx = torch.empty((rows, max(int(k), 0)), dtype=torch.int32, device=x.device)
+    _check_input(vals, torch.float32, "vals")
+    _check_input(idx, torch.int32, "idx")
+    if vals.numel() != rows * k or idx.numel() != rows * k:
+        raise ValueError("vals and idx must have rows*k elements")
+    dev = x.device if x.is_cuda else None
+    with torch.cuda.device(dev) if dev is not None else _null():
+        rc = topk_rows_f32_ptr(x.data_ptr(), rows, cols, int(k), vals.data_ptr(), idx.data_ptr(),
+                               _stream_handle(stream, dev))
+    if rc != TOPK_OK:
+        raise TopKError(rc, "topk_rows_f32")
+    return vals, idx
+
+
+class _null:
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *a):
+        return False

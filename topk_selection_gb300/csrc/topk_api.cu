@@ -1,0 +1,246 @@
+// C ABI of libtopk.so: argument checks, workspace, host-buffer staging and
+// dispatch to the kernels.  The contract of every entry point is in
+// include/topk.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/topk.h"
+#include "topk_internal.h"
+
+namespace {
+
+std::atomic<unsigned long long> g_launches{0};
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return TOPK_ERR_CUDA;
+}
+
+// Cached device memory for one (device, stream) pair.
+struct Workspace {
+    void* ctrl_cand = nullptr;  // I32Ctrl followed by the candidate array
+    size_t ctrl_cand_bytes = 0;
+    void* stage_in = nullptr;   // device copy of a host input
+    size_t stage_in_bytes = 0;
+    void* stage_out = nullptr;  // device buffer for host outputs
+    size_t stage_out_bytes = 0;
+};
+
+std::mutex g_ws_mutex;
+std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+
+int grow(void** p, size_t* have, size_t need) {
+    if (*have >= need) return TOPK_OK;
+    if (*p) {
+        cudaError_t e = cudaFree(*p);
+        *p = nullptr;
+        *have = 0;
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    cudaError_t e = cudaMalloc(p, need);
+    if (e != cudaSuccess) {
+        *p = nullptr;
+        cudaGetLastError();
+        t_last_cuda_error = (int)e;
+        return TOPK_ERR_NO_MEMORY;
+    }
+    *have = need;
+    return TOPK_OK;
+}
+
+// Workspace for (current device, stream); sizes grow monotonically.
+int workspace(cudaStream_t s, int device, size_t ctrl_cand, size_t in_bytes, size_t out_bytes, Workspace** out) {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    Workspace& w = g_ws[{device, reinterpret_cast<uintptr_t>(s)}];
+    if (ctrl_cand && w.ctrl_cand_bytes < ctrl_cand) {
+        int rc = grow(&w.ctrl_cand, &w.ctrl_cand_bytes, ctrl_cand);
+        if (rc != TOPK_OK) return rc;
+        // The control words must start at zero; the kernels keep them so.
+        cudaError_t e = cudaMemsetAsync(w.ctrl_cand, 0, sizeof(topk::I32Ctrl), s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (in_bytes) {
+        int rc = grow(&w.stage_in, &w.stage_in_bytes, in_bytes);
+        if (rc != TOPK_OK) return rc;
+    }
+    if (out_bytes) {
+        int rc = grow(&w.stage_out, &w.stage_out_bytes, out_bytes);
+        if (rc != TOPK_OK) return rc;
+    }
+    *out = &w;
+    return TOPK_OK;
+}
+
+// True when p is host memory (pageable or pinned) rather than device or
+// managed memory.
+int is_host_pointer(const void* p, bool* host) {
+    cudaPointerAttributes a;
+    std::memset(&a, 0, sizeof(a));
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e == cudaErrorInvalidValue) {  // unregistered host memory on some drivers
+        cudaGetLastError();
+        *host = true;
+        return TOPK_OK;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    *host = a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeUnregistered;
+    return TOPK_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_st* stream) {
+    if (!in || !out || n == 0 || k < 1 || (size_t)k > n) return TOPK_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 3u) return TOPK_ERR_INVALID_ARG;
+    if (overlaps(in, n * sizeof(int32_t), out, (size_t)k * sizeof(int32_t))) return TOPK_ERR_INVALID_ARG;
+    if (k > TOPK_MAX_K) return TOPK_ERR_UNSUPPORTED;
+    if (n > (size_t(1) << 40)) return TOPK_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e);
+    bool in_host = false, out_host = false;
+    int rc = is_host_pointer(in, &in_host);
+    if (rc != TOPK_OK) return rc;
+    rc = is_host_pointer(out, &out_host);
+    if (rc != TOPK_OK) return rc;
+
+    topk::I32Plan plan;
+    e = topk::i32_plan(device, n, k, &plan);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const size_t ctrl_cand = sizeof(topk::I32Ctrl) + (size_t)plan.max_grid * TOPK_MAX_K * sizeof(int32_t);
+    Workspace* w = nullptr;
+    rc = workspace(s, device, ctrl_cand, in_host ? n * sizeof(int32_t) : 0,
+                   out_host ? (size_t)k * sizeof(int32_t) : 0, &w);
+    if (rc != TOPK_OK) return rc;
+
+    const int32_t* din = in;
+    int32_t* dout = out;
+    if (in_host) {
+        e = cudaMemcpyAsync(w->stage_in, in, n * sizeof(int32_t), cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        din = static_cast<const int32_t*>(w->stage_in);
+    }
+    if (out_host) dout = static_cast<int32_t*>(w->stage_out);
+
+    auto* ctrl = static_cast<topk::I32Ctrl*>(w->ctrl_cand);
+    auto* cand = reinterpret_cast<int32_t*>(static_cast<char*>(w->ctrl_cand) + sizeof(topk::I32Ctrl));
+    e = topk::i32_launch(plan, s, din, n, k, dout, cand, ctrl);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+
+    if (out_host) {
+        e = cudaMemcpyAsync(out, dout, (size_t)k * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (in_host || out_host) {
+        e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return TOPK_OK;
+}
+
+int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
+                  struct CUstream_st* stream) {
+    if (!in || !vals || !idx || rows < 1 || cols < 1 || k < 1 || k > cols) return TOPK_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(vals) | reinterpret_cast<uintptr_t>(idx)) &
+        3u)
+        return TOPK_ERR_INVALID_ARG;
+    const size_t nin = (size_t)rows * (size_t)cols * sizeof(float);
+    const size_t nout = (size_t)rows * (size_t)k * sizeof(float);
+    if (overlaps(in, nin, vals, nout) || overlaps(in, nin, idx, nout) || overlaps(vals, nout, idx, nout))
+        return TOPK_ERR_INVALID_ARG;
+    if (k > TOPK_MAX_K) return TOPK_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e);
+    bool in_host = false, vals_host = false, idx_host = false;
+    int rc = is_host_pointer(in, &in_host);
+    if (rc == TOPK_OK) rc = is_host_pointer(vals, &vals_host);
+    if (rc == TOPK_OK) rc = is_host_pointer(idx, &idx_host);
+    if (rc != TOPK_OK) return rc;
+
+    Workspace* w = nullptr;
+    const size_t out_stage = (vals_host || idx_host) ? 2 * nout : 0;
+    rc = workspace(s, device, 0, in_host ? nin : 0, out_stage, &w);
+    if (rc != TOPK_OK) return rc;
+
+    const float* din = in;
+    float* dvals = vals;
+    int32_t* didx = idx;
+    if (in_host) {
+        e = cudaMemcpyAsync(w->stage_in, in, nin, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        din = static_cast<const float*>(w->stage_in);
+    }
+    if (vals_host) dvals = static_cast<float*>(w->stage_out);
+    if (idx_host) didx = reinterpret_cast<int32_t*>(static_cast<char*>(w->stage_out) + nout);
+
+    e = topk::rows_launch(s, din, rows, cols, k, dvals, didx);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+
+    if (vals_host) {
+        e = cudaMemcpyAsync(vals, dvals, nout, cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (idx_host) {
+        e = cudaMemcpyAsync(idx, didx, nout, cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (in_host || vals_host || idx_host) {
+        e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return TOPK_OK;
+}
+
+const char* topk_status_string(int status) {
+    switch (status) {
+        case TOPK_OK: return "ok";
+        case TOPK_ERR_INVALID_ARG: return "invalid argument";
+        case TOPK_ERR_UNSUPPORTED: return "unsupported size";
+        case TOPK_ERR_NO_MEMORY: return "out of device memory";
+        case TOPK_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+int topk_last_cuda_error(void) { return t_last_cuda_error; }
+
+int topk_release_workspace(void) {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    int rc = TOPK_OK;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    for (auto& kv : g_ws) {
+        Workspace& w = kv.second;
+        cudaSetDevice(kv.first.first);
+        for (void* p : {w.ctrl_cand, w.stage_in, w.stage_out})
+            if (p && cudaFree(p) != cudaSuccess) rc = TOPK_ERR_CUDA;
+    }
+    g_ws.clear();
+    if (prev >= 0) cudaSetDevice(prev);
+    return rc;
+}
+
+unsigned long long topk_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

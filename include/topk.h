@@ -97,6 +97,37 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
 int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
                   struct CUstream_st* stream);
 
+/* Bytes of the device array that topk_i32_noalloc uses as scratch. */
+#define TOPK_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/*
+ * topk_i32_noalloc -- topk_i32 without any allocation.  The pages have no
+ * counterpart; it exists for callers that cannot call cudaMalloc: the
+ * enqueue hook of a framework plugin that is not allowed to allocate, a
+ * process whose device memory is already claimed by another allocator's
+ * pool, or a latency-bound loop that cannot take the implicit
+ * synchronisation of cudaMalloc/cudaFree.
+ *
+ * Same arguments, result and errors as topk_i32, except:
+ *   - in and out must be device (or managed) memory; host pointers are
+ *     rejected with TOPK_ERR_INVALID_ARG (staging them would allocate).
+ *   - The scratch is one file-scope device array of
+ *     TOPK_NOALLOC_SCRATCH_BYTES (1 MiB): control words plus per-block
+ *     candidates.  Every GPU that loads the library holds it until the
+ *     process exits.  k above TOPK_MAX_K is rejected with
+ *     TOPK_ERR_UNSUPPORTED; for large k the grid is cut so that its
+ *     candidates fit (1 MiB holds 255 blocks' worth at k = 1024).
+ *   - Every call uses the same array.  Each call clears the control words
+ *     on `stream` before its launch, but calls whose work overlaps on the
+ *     GPU (different streams, or different host threads without ordering)
+ *     race on the array and may return wrong results.  Order them.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.
+ */
+int topk_i32_noalloc(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_st* stream);
+
 /* A static, human-readable name for a status code. */
 const char* topk_status_string(int status);
 

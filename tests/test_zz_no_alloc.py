@@ -1,0 +1,73 @@
+"""topk_i32_noalloc: the int32 TopK whose scratch is a fixed device array.
+
+It serves callers that cannot allocate device memory (a plugin enqueue hook
+that must not allocate, a process whose memory another allocator's pool has
+already claimed, a loop that cannot take cudaMalloc's implicit
+synchronisation).  Its results must equal topk_i32's exactly (int32 output,
+bit-exact as in every other int32 test), call after call, since every call
+reuses the same array.
+
+This file is collected last on purpose, so a run that stops at its first
+failure has run every other test before it.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def entry():
+    import topk_selection_gb300 as tk
+
+    f = tk._lib.topk_i32_noalloc
+    f.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    return tk, f
+
+
+def run_noalloc(f, x, k, stream):
+    out = torch.empty(k, dtype=torch.int32, device=x.device)
+    rc = f(x.data_ptr(), x.numel(), k, out.data_ptr(), stream.cuda_stream)
+    assert rc == 0, rc
+    return out
+
+
+def test_noalloc_matches_topk_i32_on_two_calls_in_a_row(entry):
+    tk, f = entry
+    stream = torch.cuda.current_stream()
+    # Two different inputs back to back: a call that leaves a high threshold
+    # behind, then one whose answer lies far below it.
+    a = torch.from_numpy(synth.i32_uniform(3_000_017, 41)).cuda()
+    b = torch.from_numpy(synth.i32_mod(2_500_003, 42, 1000) - np.int32(5000)).cuda()
+    for x, k in ((a, 20), (b, 100)):
+        got = run_noalloc(f, x, k, stream)
+        exp = tk.topk_i32(x, k)
+        torch.cuda.synchronize()
+        assert torch.equal(got.cpu(), exp.cpu()), (k, got[:5], exp[:5])
+
+
+def test_noalloc_large_k_and_small_input(entry):
+    tk, f = entry
+    stream = torch.cuda.current_stream()
+    for n, k in ((5, 3), (100_003, 1024), (4_194_311, 1000)):
+        x = torch.from_numpy(synth.i32_uniform(n, n)).cuda()
+        for _ in range(2):
+            got = run_noalloc(f, x, k, stream)
+            exp = tk.topk_i32(x, k)
+            torch.cuda.synchronize()
+            assert torch.equal(got.cpu(), exp.cpu()), (n, k)
+
+
+def test_noalloc_rejects_what_it_cannot_take(entry):
+    tk, f = entry
+    x = torch.zeros(5000, dtype=torch.int32, device="cuda")
+    out = torch.empty(1025, dtype=torch.int32, device="cuda")
+    assert f(x.data_ptr(), 5000, 1025, out.data_ptr(), None) == 2  # k above the maximum
+    xh = torch.zeros(5000, dtype=torch.int32)
+    assert f(xh.data_ptr(), 5000, 20, out.data_ptr(), None) == 1   # host input: would need staging

@@ -101,6 +101,11 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 }  // namespace
 
+namespace topk {
+void note_cuda_error(int err) { t_last_cuda_error = err; }
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace topk
+
 extern "C" {
 
 int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_st* stream) {

@@ -35,4 +35,9 @@ cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, s
 // Enqueue the row TopK (one block per row).
 cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx);
 
+// Bookkeeping of the C ABI layer, for entry points defined in other files:
+// record the cudaError_t behind a TOPK_ERR_CUDA, and count a kernel launch.
+void note_cuda_error(int err);
+void note_launch();
+
 }  // namespace topk

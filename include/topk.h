@@ -50,7 +50,8 @@ enum topk_status {
     TOPK_ERR_INVALID_ARG = 1, /* null pointer, n == 0, k < 1, k > n, rows < 1, cols < k, overlap */
     TOPK_ERR_UNSUPPORTED = 2, /* k > TOPK_MAX_K, or a size the kernels do not take */
     TOPK_ERR_NO_MEMORY = 3,   /* workspace or staging allocation failed */
-    TOPK_ERR_CUDA = 4         /* a CUDA runtime call or launch failed; see topk_last_cuda_error() */
+    TOPK_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed; see topk_last_cuda_error() */
+    TOPK_ERR_DEVICE_TIMEOUT = 5 /* a kernel's bounded wait gave up; its results are not valid */
 };
 
 /* Largest k accepted by either operation. */
@@ -112,11 +113,11 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
  *   - in and out must be device (or managed) memory; host pointers are
  *     rejected with TOPK_ERR_INVALID_ARG (staging them would allocate).
  *   - The scratch is one file-scope device array of
- *     TOPK_NOALLOC_SCRATCH_BYTES (1 MiB): control words plus per-block
- *     candidates.  Every GPU that loads the library holds it until the
- *     process exits.  k above TOPK_MAX_K is rejected with
+ *     TOPK_NOALLOC_SCRATCH_BYTES (1 MiB): control words, per-block maxima
+ *     and per-block candidates.  Every GPU that loads the library holds it
+ *     until the process exits.  k above TOPK_MAX_K is rejected with
  *     TOPK_ERR_UNSUPPORTED; for large k the grid is cut so that its
- *     candidates fit (1 MiB holds 255 blocks' worth at k = 1024).
+ *     candidates fit (1 MiB holds 254 blocks' worth at k = 1024).
  *   - Every call uses the same array.  Each call clears the control words
  *     on `stream` before its launch, but calls whose work overlaps on the
  *     GPU (different streams, or different host threads without ordering)
@@ -127,6 +128,32 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
  *   - No cudaMalloc, cudaFree or other allocating call is made.
  */
 int topk_i32_noalloc(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_st* stream);
+
+/*
+ * topk_check_stream -- wait for `stream`, then report whether any TopK
+ * kernel that ran on it (through that stream's workspace, or through
+ * topk_i32_noalloc on the current device) gave up on a device-side wait.
+ * The kernels never spin without limit: each wait on another warp's
+ * progress stops after a fixed number of tries, sets a sticky status word
+ * and lets the launch finish, leaving invalid results.  This call reads and
+ * clears that word.  Returns TOPK_OK, TOPK_ERR_DEVICE_TIMEOUT or
+ * TOPK_ERR_CUDA.
+ */
+int topk_check_stream(struct CUstream_st* stream);
+
+/* Options for topk_set_option. */
+enum topk_option {
+    /* Upper bound on the number of candidates the int32 second stage sorts
+     * in shared memory (a power of two >= 2; 0 restores the default, which
+     * is what fits).  When more candidates exceed the final threshold, the
+     * second stage first finds the exact k-th value by radix select.  Lower
+     * it only to exercise that path; results are the same either way. */
+    TOPK_OPT_STAGE2_CAP = 1
+};
+
+/* Set a process-wide option; takes effect for calls made afterwards.
+ * Returns TOPK_OK or TOPK_ERR_INVALID_ARG. */
+int topk_set_option(int option, int value);
 
 /* A static, human-readable name for a status code. */
 const char* topk_status_string(int status);

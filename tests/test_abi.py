@@ -49,6 +49,7 @@ def test_status_strings(lib):
     assert tk.status_string(0) == "ok"
     assert tk.status_string(1) == "invalid argument"
     assert tk.status_string(2) == "unsupported size"
+    assert tk.status_string(5) == "a device-side wait gave up"
     assert tk.status_string(99) == "unknown status"
 
 
@@ -116,3 +117,13 @@ def test_launch_counter_starts_at_zero_without_gpu(lib):
     import topk_selection_gb300 as tk
 
     assert tk.launch_count() >= 0
+
+
+def test_set_option_validation(lib):
+    import topk_selection_gb300 as tk
+
+    for bad in (-1, 1, 3, 100):
+        assert tk._lib.topk_set_option(tk.OPT_STAGE2_CAP, bad) == 1
+    assert tk._lib.topk_set_option(99, 0) == 1
+    assert tk._lib.topk_set_option(tk.OPT_STAGE2_CAP, 64) == 0
+    assert tk._lib.topk_set_option(tk.OPT_STAGE2_CAP, 0) == 0

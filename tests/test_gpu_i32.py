@@ -22,7 +22,9 @@ INT_MIN, INT_MAX = -(2**31), 2**31 - 1
 def tk():
     import topk_selection_gb300
 
-    return topk_selection_gb300
+    yield topk_selection_gb300
+    # No kernel of this module gave up on a bounded device-side wait.
+    topk_selection_gb300.check_stream()
 
 
 def gpu_topk(tk, x_np, k, offset=0, stream=None):
@@ -96,6 +98,22 @@ def test_many_tiles_ragged_tail(tk):
         x = make("uniform", n, seed=n)
         for k in (1, 20, 64, 100, 128):
             assert np.array_equal(gpu_topk(tk, x, k), oracle.topk_i32(x, k)), (n, k)
+
+
+@pytest.mark.parametrize("cap", [2, 64])
+def test_second_stage_radix_select_path(tk, cap):
+    # With the second stage's shared list capped, more candidates exceed the
+    # final threshold than fit, and the exact k-th value is found by radix
+    # select over the candidates first.
+    tk.set_option(tk.OPT_STAGE2_CAP, cap)
+    try:
+        for kind, n in (("uniform", 2_000_003), ("dups", 1_000_001), ("negative", 700_001), ("few", 90_001),
+                        ("int_max_heavy", 500_009), ("sawtooth", 3_000_017)):
+            x = make(kind, n, seed=n)
+            for k in (1, 20, 64, 100, 128, 500):
+                assert np.array_equal(gpu_topk(tk, x, k), oracle.topk_i32(x, k)), (kind, n, k, cap)
+    finally:
+        tk.set_option(tk.OPT_STAGE2_CAP, 0)
 
 
 def test_back_to_back_calls_reset_state(tk):

@@ -24,7 +24,8 @@ pytestmark = pytest.mark.gpu
 def tk():
     import topk_selection_gb300
 
-    return topk_selection_gb300
+    yield topk_selection_gb300
+    topk_selection_gb300.check_stream()
 
 
 def bits(a):

@@ -22,10 +22,12 @@ import torch
 from . import build as _build
 
 __all__ = ["topk_i32", "topk_rows_f32", "topk_i32_ptr", "topk_rows_f32_ptr", "TopKError", "MAX_K",
-           "status_string", "release_workspace", "launch_count", "last_cuda_error", "library_path"]
+           "status_string", "release_workspace", "launch_count", "last_cuda_error", "library_path",
+           "check_stream", "set_option", "OPT_STAGE2_CAP"]
 
 MAX_K = 1024
-TOPK_OK, TOPK_ERR_INVALID_ARG, TOPK_ERR_UNSUPPORTED, TOPK_ERR_NO_MEMORY, TOPK_ERR_CUDA = range(5)
+(TOPK_OK, TOPK_ERR_INVALID_ARG, TOPK_ERR_UNSUPPORTED, TOPK_ERR_NO_MEMORY, TOPK_ERR_CUDA,
+ TOPK_ERR_DEVICE_TIMEOUT) = range(6)
 
 
 class TopKError(RuntimeError):
@@ -56,6 +58,10 @@ def _load():
     lib.topk_release_workspace.restype = ci
     lib.topk_launch_count.argtypes = []
     lib.topk_launch_count.restype = ctypes.c_ulonglong
+    lib.topk_check_stream.argtypes = [vp]
+    lib.topk_check_stream.restype = ci
+    lib.topk_set_option.argtypes = [ci, ci]
+    lib.topk_set_option.restype = ci
     return lib
 
 
@@ -78,6 +84,26 @@ def release_workspace() -> None:
 
 def launch_count() -> int:
     return int(_lib.topk_launch_count())
+
+
+OPT_STAGE2_CAP = 1
+
+
+def set_option(option: int, value: int) -> None:
+    """Process-wide option (see topk_set_option in include/topk.h)."""
+    rc = _lib.topk_set_option(int(option), int(value))
+    if rc != TOPK_OK:
+        raise TopKError(rc, "topk_set_option")
+
+
+def check_stream(stream=None, device=None) -> None:
+    """Wait for the stream and raise TopKError if a kernel's bounded
+    device-side wait gave up there (its results would not be valid)."""
+    if device is None and torch.cuda.is_available():
+        device = torch.cuda.current_device()
+    rc = _lib.topk_check_stream(ctypes.c_void_p(_stream_handle(stream, device)))
+    if rc != TOPK_OK:
+        raise TopKError(rc, "topk_check_stream")
 
 
 def _stream_handle(stream, device) -> int:

@@ -16,6 +16,7 @@
 namespace {
 
 std::atomic<unsigned long long> g_launches{0};
+std::atomic<int> g_stage2_cap{0};
 thread_local int t_last_cuda_error = 0;
 
 int cuda_fail(cudaError_t e) {
@@ -25,7 +26,7 @@ int cuda_fail(cudaError_t e) {
 
 // Cached device memory for one (device, stream) pair.
 struct Workspace {
-    void* ctrl_cand = nullptr;  // I32Ctrl followed by the candidate array
+    void* ctrl_cand = nullptr;  // int32 TopK scratch: control words, block maxima, candidates
     size_t ctrl_cand_bytes = 0;
     void* stage_in = nullptr;   // device copy of a host input
     size_t stage_in_bytes = 0;
@@ -62,8 +63,9 @@ int workspace(cudaStream_t s, int device, size_t ctrl_cand, size_t in_bytes, siz
     if (ctrl_cand && w.ctrl_cand_bytes < ctrl_cand) {
         int rc = grow(&w.ctrl_cand, &w.ctrl_cand_bytes, ctrl_cand);
         if (rc != TOPK_OK) return rc;
-        // The control words must start at zero; the kernels keep them so.
-        cudaError_t e = cudaMemsetAsync(w.ctrl_cand, 0, sizeof(topk::I32Ctrl), s);
+        // The control words and block-maximum slots must start at zero; the
+        // kernels leave them so.
+        cudaError_t e = cudaMemsetAsync(w.ctrl_cand, 0, topk::kI32CandOffset, s);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (in_bytes) {
@@ -102,6 +104,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }  // namespace
 
 namespace topk {
+int stage2_cap_option() { return g_stage2_cap.load(std::memory_order_relaxed); }
 void note_cuda_error(int err) { t_last_cuda_error = err; }
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 }  // namespace topk
@@ -128,7 +131,7 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
     topk::I32Plan plan;
     e = topk::i32_plan(device, n, k, &plan);
     if (e != cudaSuccess) return cuda_fail(e);
-    const size_t ctrl_cand = sizeof(topk::I32Ctrl) + (size_t)plan.max_grid * TOPK_MAX_K * sizeof(int32_t);
+    const size_t ctrl_cand = topk::i32_scratch_bytes(plan.max_grid, TOPK_MAX_K);
     Workspace* w = nullptr;
     rc = workspace(s, device, ctrl_cand, in_host ? n * sizeof(int32_t) : 0,
                    out_host ? (size_t)k * sizeof(int32_t) : 0, &w);
@@ -143,9 +146,7 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
     }
     if (out_host) dout = static_cast<int32_t*>(w->stage_out);
 
-    auto* ctrl = static_cast<topk::I32Ctrl*>(w->ctrl_cand);
-    auto* cand = reinterpret_cast<int32_t*>(static_cast<char*>(w->ctrl_cand) + sizeof(topk::I32Ctrl));
-    e = topk::i32_launch(plan, s, din, n, k, dout, cand, ctrl);
+    e = topk::i32_launch(plan, s, din, n, k, dout, w->ctrl_cand);
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
 
@@ -217,6 +218,47 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
     return TOPK_OK;
 }
 
+int topk_check_stream(struct CUstream_st* stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    void* words[2] = {nullptr, nullptr};
+    {
+        std::lock_guard<std::mutex> lock(g_ws_mutex);
+        auto it = g_ws.find({device, reinterpret_cast<uintptr_t>(s)});
+        if (it != g_ws.end() && it->second.ctrl_cand)
+            words[0] = static_cast<char*>(it->second.ctrl_cand) + topk::kI32StatusOffset;
+    }
+    if (void* na = topk::noalloc_scratch_if_ready(device)) words[1] = static_cast<char*>(na) + topk::kI32StatusOffset;
+    int rc = TOPK_OK;
+    for (void* w : words) {
+        if (!w) continue;
+        unsigned v = 0;
+        e = cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (v != 0) {
+            rc = TOPK_ERR_DEVICE_TIMEOUT;
+            e = cudaMemset(w, 0, sizeof(v));
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+    }
+    return rc;
+}
+
+int topk_set_option(int option, int value) {
+    switch (option) {
+        case TOPK_OPT_STAGE2_CAP:
+            if (value != 0 && (value < 2 || (value & (value - 1)) != 0)) return TOPK_ERR_INVALID_ARG;
+            g_stage2_cap.store(value, std::memory_order_relaxed);
+            return TOPK_OK;
+        default:
+            return TOPK_ERR_INVALID_ARG;
+    }
+}
+
 const char* topk_status_string(int status) {
     switch (status) {
         case TOPK_OK: return "ok";
@@ -224,6 +266,7 @@ const char* topk_status_string(int status) {
         case TOPK_ERR_UNSUPPORTED: return "unsupported size";
         case TOPK_ERR_NO_MEMORY: return "out of device memory";
         case TOPK_ERR_CUDA: return "CUDA error";
+        case TOPK_ERR_DEVICE_TIMEOUT: return "a device-side wait gave up";
         default: return "unknown status";
     }
 }

@@ -9,29 +9,38 @@
 // What is kept and what differs on sm_103a:
 //   * Stage 1 streams 128-bit coalesced loads (8 in flight per lane) in a
 //     persistent grid of 2 blocks/SM.  Instead of an insertion sort per
-//     element, each warp compares every element once against a running k-th
-//     value threshold; the rare survivors are compacted (ballot + popc) into
-//     a per-warp shared-memory buffer, which is bitonic-sorted and cut back
-//     to k when it fills, raising the threshold.
-//   * Thresholds are shared: through shared memory inside the block and one
-//     global word (atomicMax) across blocks.  Any threshold t used to
-//     discard an element is one with at least k input elements >= t, and
-//     every such t is published to the global word before the block
-//     finishes.  Start values come from a sample: the k-th largest of group
-//     maxima of the warp's first tile and of the array's last elements (the
-//     latter keeps sorted-ascending input cheap).
-//   * The block merge (section 2.1's tree) is a pairwise bitonic merge of
-//     the warps' sorted lists.
+//     element, each warp compares every element once against a running
+//     threshold t; the rare survivors are compacted (ballot + popc) into a
+//     per-warp shared-memory queue and merged 32 at a time into the warp's
+//     sorted top-K list, which it keeps in registers (bitonic sort of the 32,
+//     then a bitonic merge; the warp-shuffle technique of "Complete guide to
+//     CUDA reduction optimisation").
+//   * Thresholds.  Any t used to discard is a value with at least k input
+//     elements >= t, and every such t is published (atomicMax) to one global
+//     word before the block finishes.  Sources of t:
+//       - the warp's own k-th largest once its list holds k values;
+//       - a start value: the k-th largest of 32*G group maxima of the warp's
+//         first tile, and of the array's last 256 elements (so that sorted
+//         ascending input stays cheap);
+//       - each block keeps its running maximum in a global slot; the k-th
+//         largest of all blocks' maxima is a valid t (k distinct blocks each
+//         hold an element that large), and once every block has streamed a
+//         little it sits close to the true k-th value of the whole input.
+//         One warp per block refreshes it each round, in turn.
+//   * The block merge (section 2.1's tree) is warp 0 merging the other
+//     warps' sorted lists into its own, bitonically.
 //   * The second pass (section 2.2) runs in the same launch: the last block
 //     to finish (atomic ticket, no waiting) selects the answer from the
 //     grid*k candidates.  With t_g the final global threshold, the answer is
 //     the candidates greater than t_g, sorted, padded with copies of t_g
-//     when there are fewer than k of them.  If more candidates exceed t_g
-//     than fit in shared memory, an 8-bit-digit radix select (the per-digit
-//     histogram of "GPU radix sort", histogram section) finds the exact
-//     k-th value first.
-//   * The last block resets the two control words, so the next call on the
-//     same workspace starts clean.  No block ever waits on another.
+//     when fewer than k exceed it.  If more candidates exceed t_g than fit in
+//     shared memory, an 8-bit-digit radix select (the per-digit histogram of
+//     "GPU radix sort", histogram section) finds the exact k-th value first.
+//   * The last block zeroes the control words and the block-maximum slots,
+//     so the next launch on the same scratch starts clean.  No block ever
+//     waits on another.
+//   * k > 128 uses per-warp shared-memory buffers of 2048 entries sorted in
+//     place instead of register lists.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -44,9 +53,11 @@ namespace topk {
 
 namespace {
 
-constexpr int kU = 8;                 // 16-byte loads in flight per lane
-constexpr int kTileVec = 32 * kU;     // int4 vectors per warp-tile (4 KiB)
-constexpr int kTailVec = 64;          // int4 vectors in the tail sample (256 elements)
+constexpr int kU = 8;              // 16-byte loads in flight per lane
+constexpr int kTileVec = 32 * kU;  // int4 vectors per warp-tile (4 KiB)
+constexpr int kTailVec = 64;       // int4 vectors in the tail sample (256 elements)
+constexpr int kWarps = 16;         // warps per block
+constexpr int kQueue = 256;        // per-warp survivor queue (>= 31 + 128)
 
 __device__ __forceinline__ unsigned bias(int v) { return (unsigned)v ^ 0x80000000u; }
 __device__ __forceinline__ int unbias(unsigned u) { return (int)(u ^ 0x80000000u); }
@@ -57,9 +68,38 @@ __device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
     return v;
 }
 
-__device__ __forceinline__ int ld_cg(const int* p) { return __ldcg(p); }
-
 __device__ __forceinline__ int max4(int4 v) { return kmax(kmax(v.x, v.y), kmax(v.z, v.w)); }
+
+struct Scratch {
+    unsigned* status;  // sticky error bits (kStatusWaitTimeout)
+    I32Ctrl* ctrl;
+    unsigned* bmax;    // per-block running maxima, biased
+    int32_t* cand;
+};
+
+__device__ __forceinline__ Scratch scratch_view(unsigned char* base) {
+    return Scratch{reinterpret_cast<unsigned*>(base + kI32StatusOffset), reinterpret_cast<I32Ctrl*>(base + kI32CtrlOffset),
+                   reinterpret_cast<unsigned*>(base + kI32BmaxOffset), reinterpret_cast<int32_t*>(base + kI32CandOffset)};
+}
+
+// Input split: an unaligned head (< 4 elements), a 16-byte aligned body of
+// int4 vectors, a scalar tail (< 4 elements).
+struct Split {
+    size_t head, nvec, tail0, ntiles;
+    const int4* body;
+};
+
+__device__ __forceinline__ Split split_input(const int32_t* in, size_t n) {
+    Split s;
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(in);
+    s.head = ((16u - (unsigned)(addr & 15u)) & 15u) >> 2;
+    if (s.head > n) s.head = n;
+    s.body = reinterpret_cast<const int4*>(in + s.head);
+    s.nvec = (n - s.head) >> 2;
+    s.tail0 = s.head + s.nvec * 4;
+    s.ntiles = (s.nvec + kTileVec - 1) / kTileVec;
+    return s;
+}
 
 // One warp-tile: kU int4 per lane, lane-interleaved so that every load
 // instruction covers 512 contiguous bytes.  Vectors past nvec read as INT_MIN,
@@ -97,215 +137,61 @@ __device__ __forceinline__ int seed_from_groups(const int4 (&r)[NV], int k, int 
     return warp_sorted_at<GL>(g, k - 1);
 }
 
-// Per-warp candidate buffer of capacity B in shared memory.
-template <int B>
-struct WarpBuf {
-    int* buf;
-    int cnt;   // warp-uniform number of entries
-    int t;     // warp-uniform threshold: only values > t are admitted
-
-    // Append the lanes' values that exceed t (order of arrival, compacted).
-    __device__ __forceinline__ void admit(int v, int lane) {
-        const bool p = v > t;
-        const unsigned m = __ballot_sync(kFullMask, p);
-        if (p) buf[cnt + __popc(m & lanemask_lt())] = v;
-        cnt += __popc(m);
-    }
-
-    // Sort the buffer, keep its k largest, raise t to the k-th when there are
-    // k of them.  Returns true when t was raised.
-    __device__ bool flush(int k, int lane) {
-        __syncwarp();
-        bool raised = false;
-        if constexpr (B == 256) {
-            int v[8];
+// Start threshold of a warp from its first tile and the array's tail.
+template <int GL>
+__device__ __forceinline__ int start_threshold(const int4 (&r)[kU], const Split& sp, int k, int lane) {
+    int4 s[2];
+    const long long tv = (long long)sp.nvec - kTailVec + 2 * lane;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int p = j * 32 + lane;
-                v[j] = p < cnt ? buf[p] : INT_MIN;
-            }
-            warp_sort_desc<8>(v, lane);
-            const int keep = cnt < k ? cnt : k;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int p = j * 32 + lane;
-                if (p < keep) buf[p] = v[j];
-            }
-            if (cnt >= k) {
-                const int kth = warp_sorted_at<8>(v, k - 1);
-                if (kth > t) {
-                    t = kth;
-                    raised = true;
-                }
-            }
-            cnt = keep;
-        } else {
-            for (int p = cnt + lane; p < B; p += 32) buf[p] = INT_MIN;
-            __syncwarp();
-            warp_sort_smem_desc(buf, B, lane);
-            if (cnt >= k) {
-                const int kth = buf[k - 1];
-                if (kth > t) {
-                    t = kth;
-                    raised = true;
-                }
-            }
-            cnt = cnt < k ? cnt : k;
-        }
-        __syncwarp();
-        return raised;
-    }
-};
+    for (int q = 0; q < 2; ++q)
+        s[q] = tv + q >= 0 ? __ldg(sp.body + tv + q) : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
+    int seed = seed_from_groups<GL>(r, k, lane);
+    if constexpr (GL <= 2) seed = kmax(seed, seed_from_groups<GL>(s, k, lane));
+    return seed;
+}
 
-template <int B, int GL, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32, (WARPS <= 8 ? 4 : 2) * (B <= 256 ? 1 : 0) + (B > 256 ? 1 : 0))
-topk_i32_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* __restrict__ out,
-                int32_t* __restrict__ cand, I32Ctrl* __restrict__ ctrl) {
-    extern __shared__ __align__(16) int smem[];
-    __shared__ int s_thresh;
-    __shared__ int s_last;
-    __shared__ int s_count;
+// Append the lanes' values that exceed t to q[*nq...] (warp-uniform count).
+__device__ __forceinline__ void enqueue(int* q, int& nq, int v, int t, int lane) {
+    const bool p = v > t;
+    const unsigned m = __ballot_sync(kFullMask, p);
+    if (p) q[nq + __popc(m & lanemask_lt())] = v;
+    nq += __popc(m);
+}
 
+// ---------------------------------------------------------------- stage 2 --
+
+// Run by the last block to finish.  `room` ints of shared memory at `list`;
+// cap_limit > 0 lowers the list capacity (to exercise the radix-select path).
+__device__ void second_stage(const Scratch& sc, int k, int32_t* __restrict__ out, int* list, int room,
+                             int cap_limit, int* s_count) {
     const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) s_thresh = INT_MIN;
-    __syncthreads();
-
-    // Split the array into an unaligned head (< 4 elements), a 16-byte
-    // aligned body of int4 vectors and a scalar tail (< 4 elements).
-    const uintptr_t addr = reinterpret_cast<uintptr_t>(in);
-    size_t head = ((16u - (unsigned)(addr & 15u)) & 15u) >> 2;
-    if (head > n) head = n;
-    const int4* body = reinterpret_cast<const int4*>(in + head);
-    const size_t nvec = (n - head) >> 2;
-    const size_t tail0 = head + nvec * 4;
-    const size_t ntiles = (nvec + kTileVec - 1) / kTileVec;
-    const size_t gw = (size_t)blockIdx.x * WARPS + warp;
-    const size_t nw = (size_t)gridDim.x * WARPS;
-
-    WarpBuf<B> wb{smem + warp * B, 0, INT_MIN};
-    int published = INT_MIN;  // the largest value this warp has sent to the global word
-
-    auto publish = [&](int v) {
-        if (lane == 0) {
-            atomicMax(&s_thresh, v);
-            if (v > published) atomicMax(&ctrl->thresh, bias(v));
-        }
-        published = kmax(published, v);
-    };
-
-    // Scalars outside the aligned body: at most 3 + 3 elements, taken by the
-    // first warp of the grid.
-    if (gw == 0) {
-        const size_t ns = head + (n - tail0);
-        const size_t pos = (size_t)lane < head ? (size_t)lane : tail0 + (lane - head);
-        const int v = (size_t)lane < ns ? in[pos] : INT_MIN;
-        wb.admit(v, lane);
-    }
-
-    bool first = true;
-    for (size_t tile = gw; tile < ntiles; tile += nw) {
-        const unsigned g = ld_relaxed_gpu(&ctrl->thresh);
-        int4 r[kU];
-        load_tile(r, body, nvec, tile, lane);
-
-        if constexpr (GL > 0) {
-          if (first) {
-            first = false;
-            // Start threshold: k-th largest group maximum of this tile and of
-            // the array's last kTailVec vectors.
-            int4 s[2];
-            const long long tv = (long long)nvec - kTailVec + 2 * lane;
-#pragma unroll
-            for (int q = 0; q < 2; ++q)
-                s[q] = tv + q >= 0 ? __ldg(body + tv + q) : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
-            int seed = seed_from_groups<GL>(r, k, lane);
-            if constexpr (GL <= 2) seed = kmax(seed, seed_from_groups<GL>(s, k, lane));
-            if (seed > wb.t) {
-                wb.t = seed;
-                publish(seed);
-            }
-          }
-        }
-
-        wb.t = kmax(wb.t, kmax(unbias(g), *(volatile int*)&s_thresh));
-
-        int m = INT_MIN;
-#pragma unroll
-        for (int u = 0; u < kU; ++u) m = kmax(m, max4(r[u]));
-        if (__any_sync(kFullMask, m > wb.t)) {
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                if (wb.cnt > B - 128) {
-                    if (wb.flush(k, lane)) publish(wb.t);
-                }
-                wb.admit(r[u].x, lane);
-                wb.admit(r[u].y, lane);
-                wb.admit(r[u].z, lane);
-                wb.admit(r[u].w, lane);
-            }
-        }
-    }
-
-    // Final per-warp list: sorted, k largest, padded with INT_MIN to K.
-    if (wb.flush(k, lane)) publish(wb.t);
-    const int K = next_pow2(k < 32 ? 32 : k);
-    for (int p = wb.cnt + lane; p < K; p += 32) wb.buf[p] = INT_MIN;
-
-    // Block merge: pairwise bitonic merges of sorted K-lists (section 2.1's
-    // tree, with warps in place of threads).
-#pragma unroll 1
-    for (int s = 1; s < WARPS; s <<= 1) {
-        __syncthreads();
-        if ((warp & (2 * s - 1)) == 0) {
-            int* a = smem + warp * B;
-            const int* b = smem + (warp + s) * B;
-            for (int i = lane; i < K; i += 32) a[i] = kmax(a[i], b[K - 1 - i]);
-            __syncwarp();
-            warp_merge_smem_desc(a, K, lane);
-        }
-    }
-    __syncthreads();
-
-    // Candidates of this block, and its k-th value as a threshold.
-    for (int i = threadIdx.x; i < k; i += blockDim.x) cand[(size_t)blockIdx.x * k + i] = smem[i];
-    if (threadIdx.x == 0) {
-        const int kth = smem[k - 1];
-        if (kth != INT_MIN) atomicMax(&ctrl->thresh, bias(kth));
-    }
+    // The list is bitonic-sorted in place at a power-of-two length, so its
+    // capacity is the largest power of two that fits.
+    int cap = 1;
+    while (2 * cap <= room) cap *= 2;
+    if (cap_limit > 0 && cap_limit < cap) cap = cap_limit;
+    if (cap < k) cap = k;  // the sorted list must be able to hold the answer
     __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned ticket = atomicAdd(&ctrl->ticket, 1u);
-        s_last = ticket == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!s_last) return;
-
-    // ---- second stage, in the last block to finish ----------------------
-    __threadfence();
-    const int tg = unbias(ld_relaxed_gpu(&ctrl->thresh));
-    const int cap = WARPS * B;
-    int* list = smem;
+    const int tg = unbias(ld_relaxed_gpu(&sc.ctrl->thresh));
     const size_t M = (size_t)gridDim.x * k;
     const size_t Mr = (M + blockDim.x - 1) / blockDim.x * blockDim.x;
-    if (threadIdx.x == 0) s_count = 0;
+    if (threadIdx.x == 0) *s_count = 0;
     __syncthreads();
     for (size_t i = threadIdx.x; i < Mr; i += blockDim.x) {
-        const int v = i < M ? ld_cg(cand + i) : INT_MIN;
+        const int v = i < M ? __ldcg(sc.cand + i) : INT_MIN;
         const bool p = v > tg;
         const unsigned m = __ballot_sync(kFullMask, p);
         int base = 0;
-        if (lane == 0 && m) base = atomicAdd(&s_count, __popc(m));
+        if (lane == 0 && m) base = atomicAdd(s_count, __popc(m));
         base = __shfl_sync(kFullMask, base, 0);
         const int pos = base + __popc(m & lanemask_lt());
         if (p && pos < cap) list[pos] = v;
     }
     __syncthreads();
-    const int above = s_count;
+    const int above = *s_count;
 
-    int T = tg;       // value that fills the places after the sorted list
-    int nlist = above; // sorted entries that come first
+    int T = tg;         // value that fills the places after the sorted list
+    int nlist = above;  // sorted entries that come first
     if (above > cap) {
         // Radix select over the candidates above tg: the exact k-th largest
         // value T, most significant 8-bit digit first.
@@ -316,7 +202,7 @@ topk_i32_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* __rest
             for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
             __syncthreads();
             for (size_t i = threadIdx.x; i < M; i += blockDim.x) {
-                const int v = ld_cg(cand + i);
+                const int v = __ldcg(sc.cand + i);
                 const unsigned u = bias(v);
                 if (v > tg && (u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
             }
@@ -339,46 +225,487 @@ topk_i32_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* __rest
         }
         T = unbias(prefix);
         // Values strictly above T: fewer than k of them.
-        if (threadIdx.x == 0) s_count = 0;
+        if (threadIdx.x == 0) *s_count = 0;
         __syncthreads();
         for (size_t i = threadIdx.x; i < Mr; i += blockDim.x) {
-            const int v = i < M ? ld_cg(cand + i) : INT_MIN;
+            const int v = i < M ? __ldcg(sc.cand + i) : INT_MIN;
             const bool p = v > T;
             const unsigned m = __ballot_sync(kFullMask, p);
             int base = 0;
-            if (lane == 0 && m) base = atomicAdd(&s_count, __popc(m));
+            if (lane == 0 && m) base = atomicAdd(s_count, __popc(m));
             base = __shfl_sync(kFullMask, base, 0);
             if (p) list[base + __popc(m & lanemask_lt())] = v;
         }
         __syncthreads();
-        nlist = s_count;
+        nlist = *s_count;
     }
 
     const int L = next_pow2(nlist < 2 ? 2 : nlist);
     for (int i = nlist + threadIdx.x; i < L; i += blockDim.x) list[i] = INT_MIN;
     block_sort_smem_desc(list, L);
     for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < nlist ? list[i] : T;
+    // Leave the scratch as the next launch expects it.
+    for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) sc.bmax[i] = 0u;
     if (threadIdx.x == 0) {
-        ctrl->thresh = 0u;
-        ctrl->ticket = 0u;
+        sc.ctrl->thresh = 0u;
+        sc.ctrl->ticket = 0u;
     }
 }
 
-template <int B, int GL, int WARPS>
-struct I32Variant {
-    static constexpr int kWarps = WARPS;
-    static size_t smem_bytes() { return (size_t)WARPS * B * sizeof(int); }
-    static const void* fn() { return reinterpret_cast<const void*>(&topk_i32_kernel<B, GL, WARPS>); }
-    static void launch(int grid, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
-                       int32_t* cand, I32Ctrl* ctrl) {
-        topk_i32_kernel<B, GL, WARPS><<<grid, WARPS * 32, smem_bytes(), s>>>(in, n, k, out, cand, ctrl);
+// Publish this block's candidates (k, sorted, INT_MIN-padded) and its k-th
+// value, take a ticket; returns true in the last block to finish.
+__device__ __forceinline__ bool finish_block(const Scratch& sc, int k, const int* list, int* s_last) {
+    for (int i = threadIdx.x; i < k; i += blockDim.x) sc.cand[(size_t)blockIdx.x * k + i] = list[i];
+    if (threadIdx.x == 0) {
+        const int kth = list[k - 1];
+        if (kth != INT_MIN) atomicMax(&sc.ctrl->thresh, bias(kth));
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned ticket = atomicAdd(&sc.ctrl->ticket, 1u);
+        *s_last = ticket == gridDim.x - 1;
+    }
+    __syncthreads();
+    return *s_last != 0;
+}
+
+// ------------------------------------------------- k <= 128: register lists --
+
+// A warp's sorted top-K list, K = 32*L, position p = j*32 + lane in lst[j].
+template <int L>
+struct WarpList {
+    int lst[L];
+    int have;  // real entries in lst (the rest are INT_MIN)
+
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int j = 0; j < L; ++j) lst[j] = INT_MIN;
+        have = 0;
+    }
+
+    // Sort a bitonic list descending (the merge half of a bitonic sort).
+    __device__ __forceinline__ void bitonic_merge(int lane) {
+#pragma unroll
+        for (int stride = 16 * L; stride > 0; stride >>= 1) {
+            if (stride >= 32) {
+                const int js = stride >> 5;
+#pragma unroll
+                for (int j = 0; j < L; ++j) {
+                    if ((j & js) == 0) {
+                        const int a = lst[j], b = lst[j | js];
+                        lst[j] = kmax(a, b);
+                        lst[j | js] = kmin(a, b);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < L; ++j) {
+                    const int o = __shfl_xor_sync(kFullMask, lst[j], stride);
+                    lst[j] = (lane & stride) == 0 ? kmax(lst[j], o) : kmin(lst[j], o);
+                }
+            }
+        }
+    }
+
+    // Merge a sorted-descending 32-chunk (one value per lane, position =
+    // lane) into the list, keeping the K largest.
+    __device__ __forceinline__ void merge_sorted32(int c, int cnt, int lane) {
+        const int rc = __shfl_sync(kFullMask, c, 31 - lane);
+        lst[L - 1] = kmax(lst[L - 1], rc);  // half-cleaner against the reversed chunk
+        bitonic_merge(lane);
+        have = kmin(have + cnt, 32 * L);
     }
 };
 
-using VarK32 = I32Variant<256, 1, 16>;
-using VarK64 = I32Variant<256, 2, 16>;
-using VarK128 = I32Variant<256, 4, 16>;
-using VarK1024 = I32Variant<2048, 0, 16>;
+// Streaming ring: one producer warp issues bulk copies of 4 KiB tiles into
+// kStages shared-memory stages; kCons consumer warps each take every kCons-th
+// tile of the block (stage s is always consumed by warp s % kCons, so a
+// consumer never runs a full ring ahead of the producer).
+constexpr int kCons = 8;                    // consumer warps per block
+constexpr int kStages = 24;                 // ring depth (a multiple of kCons)
+constexpr int kRingBytes = kStages * kTileVec * 16;
+static_assert(kStages % kCons == 0, "stage s must always go to the same consumer warp");
+
+template <int L, int GL>
+__global__ void __launch_bounds__((kCons + 1) * 32, 2)
+topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* __restrict__ out,
+                       unsigned char* __restrict__ scratch, int cap_limit) {
+    constexpr int K = 32 * L;
+    extern __shared__ __align__(128) int4 ring[];             // kStages tiles; later the stage-2 list
+    __shared__ __align__(16) int s_queue[kCons * kQueue];      // survivor queues, then the merge area
+    __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
+    __shared__ int s_thresh, s_cmax, s_last, s_count;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const Scratch sc = scratch_view(scratch);
+    if (threadIdx.x == 0) {
+        s_thresh = INT_MIN;
+        s_cmax = INT_MIN;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    const Split sp = split_input(in, n);
+    const size_t G = gridDim.x;
+    const size_t b = blockIdx.x;
+    const size_t J = b < sp.ntiles ? (sp.ntiles - b + G - 1) / G : 0;  // tiles of this block: b + j*G
+    // The block-maxima threshold needs at least k blocks.
+    const bool use_bmax = (int)G >= k;
+
+    WarpList<L> wl;
+    wl.init();
+
+    if (warp == kCons) {
+        // ---- producer ----
+        if (lane == 0) {
+            size_t j = 0;
+            for (; j < J; ++j) {
+                const int s = (int)(j % kStages);
+                if (j >= (size_t)kStages && !mbar_wait(&empty_bar[s], (uint32_t)((j / kStages - 1) & 1))) {
+                    atomicOr(sc.status, kStatusWaitTimeout);
+                    break;
+                }
+                const size_t base = (b + j * G) * kTileVec;
+                const size_t cnt = sp.nvec - base < (size_t)kTileVec ? sp.nvec - base : (size_t)kTileVec;
+                mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(cnt * 16));
+                bulk_copy_g2s(ring + (size_t)s * kTileVec, sp.body + base, (uint32_t)(cnt * 16), &full_bar[s]);
+            }
+            // Leave no copy in flight: the last kStages issued must have landed.
+            for (size_t q = j > (size_t)kStages ? j - kStages : 0; q < j; ++q)
+                if (!mbar_wait(&full_bar[q % kStages], (uint32_t)((q / kStages) & 1))) {
+                    atomicOr(sc.status, kStatusWaitTimeout);
+                    break;
+                }
+        }
+    } else {
+        // ---- consumers ----
+        int* q = s_queue + warp * kQueue;
+        int nq = 0;
+        int t = INT_MIN;
+        int published = INT_MIN;   // largest value this warp sent to the global word
+        int pushed_max = INT_MIN;  // largest tile maximum this warp sent to s_cmax
+        int bmax_pub = INT_MIN;    // largest block maximum this warp wrote to the global slot
+
+        auto publish = [&](int v) {
+            if (lane == 0) {
+                atomicMax(&s_thresh, v);
+                if (v > published) atomicMax(&sc.ctrl->thresh, bias(v));
+            }
+            published = kmax(published, v);
+        };
+
+        // Merge every full 32-chunk of the queue (with all_of_it, the rest
+        // too) into the list; raise t to the list's k-th value.
+        auto drain = [&](bool all_of_it) {
+            while (nq >= 32 || (all_of_it && nq > 0)) {
+                const int cnt = nq >= 32 ? 32 : nq;
+                __syncwarp();
+                const int c = lane < cnt ? q[nq - cnt + lane] : INT_MIN;
+                __syncwarp();
+                nq -= cnt;
+                int one[1] = {c};
+                warp_sort_desc<1>(one, lane);
+                wl.merge_sorted32(one[0], cnt, lane);
+            }
+            if (wl.have >= k) {
+                const int kth = warp_sorted_at<L>(wl.lst, k - 1);
+                if (kth > t) {
+                    t = kth;
+                    publish(kth);
+                }
+            }
+        };
+
+        // Scalars outside the aligned body: at most 3 + 3, taken by consumer
+        // warp 0 of block 0.
+        if (b == 0 && warp == 0) {
+            const size_t ns = sp.head + (n - sp.tail0);
+            const size_t pos = (size_t)lane < sp.head ? (size_t)lane : sp.tail0 + (lane - sp.head);
+            enqueue(q, nq, (size_t)lane < ns ? in[pos] : INT_MIN, INT_MIN, lane);
+        }
+
+        int iter = 0;
+        for (size_t j = warp; j < J; j += kCons, ++iter) {
+            // Block-maxima threshold: refreshed by one consumer warp of the
+            // block per round, from (up to) the first 256 blocks' maxima.
+            const bool refresh = use_bmax && ((iter + warp) & (kCons - 1)) == kCons - 1;
+            unsigned bv[8];
+            if (refresh) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int x = i * 32 + lane;
+                    bv[i] = x < (int)G ? ld_relaxed_gpu(&sc.bmax[x]) : 0u;
+                }
+            }
+            const unsigned g = ld_relaxed_gpu(&sc.ctrl->thresh);
+
+            const int s = (int)(j % kStages);
+            if (!mbar_wait(&full_bar[s], (uint32_t)((j / kStages) & 1))) {
+                if (lane == 0) atomicOr(sc.status, kStatusWaitTimeout);
+                break;
+            }
+            const size_t base = (b + j * G) * kTileVec;
+            const size_t cnt = sp.nvec - base < (size_t)kTileVec ? sp.nvec - base : (size_t)kTileVec;
+            const int4* st = ring + (size_t)s * kTileVec;
+            int4 r[kU];
+            if (cnt == (size_t)kTileVec) {
+#pragma unroll
+                for (int u = 0; u < kU; ++u) r[u] = st[u * 32 + lane];
+            } else {
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+                    r[u] = (size_t)(u * 32 + lane) < cnt ? st[u * 32 + lane]
+                                                         : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[s]);  // the tile is in registers: release the stage
+
+            if (iter == 0) {
+                const int seed = start_threshold<GL>(r, sp, k, lane);
+                if (seed > t) {
+                    t = seed;
+                    publish(seed);
+                }
+            }
+            t = kmax(t, kmax(unbias(g), *(volatile int*)&s_thresh));
+
+            int m = INT_MIN;
+#pragma unroll
+            for (int u = 0; u < kU; ++u) m = kmax(m, max4(r[u]));
+            const int wm = __reduce_max_sync(kFullMask, m);
+            if (wm > pushed_max) {
+                if (lane == 0) atomicMax(&s_cmax, wm);
+                pushed_max = wm;
+            }
+            if (wm > t) {
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    if (__any_sync(kFullMask, max4(r[u]) > t)) {
+                        enqueue(q, nq, r[u].x, t, lane);
+                        enqueue(q, nq, r[u].y, t, lane);
+                        enqueue(q, nq, r[u].z, t, lane);
+                        enqueue(q, nq, r[u].w, t, lane);
+                        if (nq >= 32) drain(false);
+                    }
+                }
+            }
+
+            if (refresh) {
+                const int cm = *(volatile int*)&s_cmax;
+                if (cm > bmax_pub) {
+                    if (lane == 0) atomicMax(&sc.bmax[b], bias(cm));
+                    bmax_pub = cm;
+                }
+                // Block maxima above t, compacted behind the (< 32 entry) queue.
+                int* sel = q + 32;
+                int ns = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int x = unbias(bv[i]);
+                    const bool p = x > t;
+                    const unsigned bb = __ballot_sync(kFullMask, p);
+                    const int pos = ns + __popc(bb & lanemask_lt());
+                    if (p && pos < kQueue - 32) sel[pos] = x;
+                    ns += __popc(bb);
+                }
+                __syncwarp();
+                if (ns >= k && ns <= 128) {
+                    int sv[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int p = i * 32 + lane;
+                        sv[i] = p < ns ? sel[p] : INT_MIN;
+                    }
+                    warp_sort_desc<4>(sv, lane);
+                    const int theta = warp_sorted_at<4>(sv, k - 1);
+                    if (theta > t) {
+                        t = theta;
+                        publish(theta);
+                    }
+                }
+                __syncwarp();
+            }
+        }
+
+        drain(true);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < L; ++i) q[i * 32 + lane] = wl.lst[i];
+    }
+
+    // Block merge: consumer warp 0 merges the other consumers' lists.
+    __syncthreads();
+    if (warp == 0) {
+        for (int w = 1; w < kCons; ++w) {
+            const int* o = s_queue + w * kQueue;
+            // The other list reversed against ours: the half-cleaner of a
+            // bitonic merge, then the merge network.
+#pragma unroll
+            for (int i = 0; i < L; ++i) wl.lst[i] = kmax(wl.lst[i], o[K - 1 - (i * 32 + lane)]);
+            wl.bitonic_merge(lane);
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int i = 0; i < L; ++i) s_queue[i * 32 + lane] = wl.lst[i];
+    }
+    __syncthreads();
+
+    if (finish_block(sc, k, s_queue, &s_last))
+        second_stage(sc, k, out, reinterpret_cast<int*>(ring), kRingBytes / (int)sizeof(int), cap_limit, &s_count);
+}
+
+// ---------------------------------------- k > 128: shared-memory buffers --
+
+constexpr int kBigBuf = 2048;
+
+template <int B>
+struct WarpBuf {
+    int* buf;
+    int cnt;  // warp-uniform number of entries
+    int t;    // warp-uniform threshold: only values > t are admitted
+
+    __device__ __forceinline__ void admit(int v, int lane) {
+        const bool p = v > t;
+        const unsigned m = __ballot_sync(kFullMask, p);
+        if (p) buf[cnt + __popc(m & lanemask_lt())] = v;
+        cnt += __popc(m);
+    }
+
+    // Sort the buffer, keep its k largest, raise t to the k-th when there are
+    // k of them.  Returns true when t was raised.
+    __device__ bool flush(int k, int lane) {
+        __syncwarp();
+        for (int p = cnt + lane; p < B; p += 32) buf[p] = INT_MIN;
+        __syncwarp();
+        warp_sort_smem_desc(buf, B, lane);
+        bool raised = false;
+        if (cnt >= k) {
+            const int kth = buf[k - 1];
+            if (kth > t) {
+                t = kth;
+                raised = true;
+            }
+        }
+        cnt = cnt < k ? cnt : k;
+        __syncwarp();
+        return raised;
+    }
+};
+
+__global__ void __launch_bounds__(kWarps * 32, 1)
+topk_i32_smem_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* __restrict__ out,
+                     unsigned char* __restrict__ scratch, int cap_limit) {
+    extern __shared__ __align__(16) int smem[];
+    __shared__ int s_thresh;
+    __shared__ int s_last;
+    __shared__ int s_count;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const Scratch sc = scratch_view(scratch);
+    if (threadIdx.x == 0) s_thresh = INT_MIN;
+    __syncthreads();
+
+    const Split sp = split_input(in, n);
+    const size_t gw = (size_t)blockIdx.x * kWarps + warp;
+    const size_t nw = (size_t)gridDim.x * kWarps;
+
+    WarpBuf<kBigBuf> wb{smem + warp * kBigBuf, 0, INT_MIN};
+    int published = INT_MIN;
+    auto publish = [&](int v) {
+        if (lane == 0) {
+            atomicMax(&s_thresh, v);
+            if (v > published) atomicMax(&sc.ctrl->thresh, bias(v));
+        }
+        published = kmax(published, v);
+    };
+
+    if (gw == 0) {
+        const size_t ns = sp.head + (n - sp.tail0);
+        const size_t pos = (size_t)lane < sp.head ? (size_t)lane : sp.tail0 + (lane - sp.head);
+        wb.admit((size_t)lane < ns ? in[pos] : INT_MIN, lane);
+    }
+
+    for (size_t tile = gw; tile < sp.ntiles; tile += nw) {
+        const unsigned g = ld_relaxed_gpu(&sc.ctrl->thresh);
+        int4 r[kU];
+        load_tile(r, sp.body, sp.nvec, tile, lane);
+        wb.t = kmax(wb.t, kmax(unbias(g), *(volatile int*)&s_thresh));
+        int m = INT_MIN;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) m = kmax(m, max4(r[u]));
+        if (__any_sync(kFullMask, m > wb.t)) {
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                if (wb.cnt > kBigBuf - 128) {
+                    if (wb.flush(k, lane)) publish(wb.t);
+                }
+                wb.admit(r[u].x, lane);
+                wb.admit(r[u].y, lane);
+                wb.admit(r[u].z, lane);
+                wb.admit(r[u].w, lane);
+            }
+        }
+    }
+
+    if (wb.flush(k, lane)) publish(wb.t);
+    const int K = next_pow2(k);
+    for (int p = wb.cnt + lane; p < K; p += 32) wb.buf[p] = INT_MIN;
+
+    // Block merge: pairwise bitonic merges of sorted K-lists.
+#pragma unroll 1
+    for (int s = 1; s < kWarps; s <<= 1) {
+        __syncthreads();
+        if ((warp & (2 * s - 1)) == 0) {
+            int* a = smem + warp * kBigBuf;
+            const int* b = smem + (warp + s) * kBigBuf;
+            for (int i = lane; i < K; i += 32) a[i] = kmax(a[i], b[K - 1 - i]);
+            __syncwarp();
+            warp_merge_smem_desc(a, K, lane);
+        }
+    }
+    __syncthreads();
+
+    if (finish_block(sc, k, smem, &s_last))
+        second_stage(sc, k, out, smem, kWarps * kBigBuf, cap_limit, &s_count);
+}
+
+// ------------------------------------------------------------ host side --
+
+template <int L, int GL>
+struct StreamVariant {
+    static constexpr int kThreads = (kCons + 1) * 32;
+    static size_t smem_bytes() { return kRingBytes; }
+    static const void* fn() { return reinterpret_cast<const void*>(&topk_i32_stream_kernel<L, GL>); }
+    static void launch(int grid, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
+                       unsigned char* scratch, int cap_limit) {
+        topk_i32_stream_kernel<L, GL><<<grid, kThreads, smem_bytes(), s>>>(in, n, k, out, scratch, cap_limit);
+    }
+    static size_t units_per_block() { return kCons; }
+};
+
+struct SmemVariant {
+    static constexpr int kThreads = kWarps * 32;
+    static size_t units_per_block() { return kWarps; }
+    static size_t smem_bytes() { return (size_t)kWarps * kBigBuf * sizeof(int); }
+    static const void* fn() { return reinterpret_cast<const void*>(&topk_i32_smem_kernel); }
+    static void launch(int grid, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
+                       unsigned char* scratch, int cap_limit) {
+        topk_i32_smem_kernel<<<grid, kWarps * 32, smem_bytes(), s>>>(in, n, k, out, scratch, cap_limit);
+    }
+};
+
+using VarK32 = StreamVariant<1, 1>;
+using VarK64 = StreamVariant<2, 2>;
+using VarK128 = StreamVariant<4, 4>;
 
 template <class V>
 cudaError_t plan_for(int device, size_t n, I32Plan* plan) {
@@ -390,17 +717,20 @@ cudaError_t plan_for(int device, size_t n, I32Plan* plan) {
         e = cudaFuncSetAttribute(V::fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, V::fn(), V::kWarps * 32, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, V::fn(), V::kThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
+    size_t full = (size_t)sms * per_sm;
+    if (full > (size_t)kI32MaxGrid) full = kI32MaxGrid;
     const size_t nvec = n / 4;
     const size_t tiles = (nvec + kTileVec - 1) / kTileVec;
-    const size_t want = (tiles + V::kWarps - 1) / V::kWarps;
-    size_t grid = (size_t)sms * per_sm;
+    const size_t want = (tiles + V::units_per_block() - 1) / V::units_per_block();
+    size_t grid = full;
     if (want < grid) grid = want;
     if (grid < 1) grid = 1;
     plan->grid = (int)grid;
-    plan->max_grid = sms * per_sm;
+    plan->max_grid = (int)full;
+    plan->stage2_cap = stage2_cap_option();
     return cudaSuccess;
 }
 
@@ -410,19 +740,21 @@ cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan) {
     if (k <= 32) return plan_for<VarK32>(device, n, plan);
     if (k <= 64) return plan_for<VarK64>(device, n, plan);
     if (k <= 128) return plan_for<VarK128>(device, n, plan);
-    return plan_for<VarK1024>(device, n, plan);
+    return plan_for<SmemVariant>(device, n, plan);
 }
 
 cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
-                       int32_t* cand, I32Ctrl* ctrl) {
+                       void* scratch) {
+    auto* sc = static_cast<unsigned char*>(scratch);
+    const int cap = plan.stage2_cap;
     if (k <= 32)
-        VarK32::launch(plan.grid, s, in, n, k, out, cand, ctrl);
+        VarK32::launch(plan.grid, s, in, n, k, out, sc, cap);
     else if (k <= 64)
-        VarK64::launch(plan.grid, s, in, n, k, out, cand, ctrl);
+        VarK64::launch(plan.grid, s, in, n, k, out, sc, cap);
     else if (k <= 128)
-        VarK128::launch(plan.grid, s, in, n, k, out, cand, ctrl);
+        VarK128::launch(plan.grid, s, in, n, k, out, sc, cap);
     else
-        VarK1024::launch(plan.grid, s, in, n, k, out, cand, ctrl);
+        SmemVariant::launch(plan.grid, s, in, n, k, out, sc, cap);
     return cudaGetLastError();
 }
 

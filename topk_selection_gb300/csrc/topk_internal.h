@@ -19,18 +19,42 @@ struct I32Ctrl {
     unsigned pad[62];  // one 256-byte line to itself
 };
 
+// Scratch of one int32 TopK launch, in this order:
+//   [0, 256)                 status word: nonzero after a bounded wait gave up
+//                            (sticky; read and cleared by the host)
+//   [256, 512)               I32Ctrl
+//   [512, 512 + 4*1024)      per-block running maxima (biased like thresh)
+//   [kI32CandOffset, ...)    grid * k candidates
+// [kI32ResetBegin, kI32CandOffset) is zero between launches.
+constexpr int kI32MaxGrid = 1024;
+constexpr size_t kI32StatusOffset = 0;
+constexpr size_t kI32CtrlOffset = 256;
+constexpr size_t kI32BmaxOffset = 512;
+constexpr size_t kI32CandOffset = kI32BmaxOffset + (size_t)kI32MaxGrid * sizeof(unsigned);
+constexpr size_t kI32ResetBegin = kI32CtrlOffset;
+
+// Status bits a kernel may set in the status word.
+constexpr unsigned kStatusWaitTimeout = 1u;
+
+inline size_t i32_scratch_bytes(int grid, int k) { return kI32CandOffset + (size_t)grid * (size_t)k * sizeof(int32_t); }
+
 struct I32Plan {
-    int grid;      // blocks launched
-    int max_grid;  // persistent grid size for this device (blocks per SM x SMs)
+    int grid;        // blocks launched (<= kI32MaxGrid)
+    int max_grid;    // persistent grid size for this device (blocks per SM x SMs), <= kI32MaxGrid
+    int stage2_cap;  // 0, or a lower capacity for the second stage's shared list (TOPK_OPT_STAGE2_CAP)
 };
+
+// Current value of TOPK_OPT_STAGE2_CAP (0 = default).
+int stage2_cap_option();
 
 // Grid for an n-element, k-wide selection on `device`.
 cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan);
 
-// Enqueue the single-launch int32 TopK.  cand holds plan.grid * k ints;
-// ctrl must be zero (it is again when the launch completes).
+// Enqueue the single-launch int32 TopK.  scratch holds i32_scratch_bytes(plan.grid, k)
+// bytes, 256-byte aligned, whose first kI32CandOffset bytes are zero (they are
+// zero again when the launch completes).
 cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
-                       int32_t* cand, I32Ctrl* ctrl);
+                       void* scratch);
 
 // Enqueue the row TopK (one block per row).
 cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx);
@@ -39,5 +63,9 @@ cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int
 // record the cudaError_t behind a TOPK_ERR_CUDA, and count a kernel launch.
 void note_cuda_error(int err);
 void note_launch();
+
+// Device address of topk_i32_noalloc's scratch on `device`, or null if that
+// entry point has not run there yet.
+void* noalloc_scratch_if_ready(int device);
 
 }  // namespace topk

@@ -5,7 +5,7 @@
 // been claimed up front by another allocator's pool, or a latency-bound loop
 // that cannot afford the implicit synchronisation of cudaMalloc/cudaFree.
 // This entry point runs the same kernel as topk_i32, but its scratch (the
-// two control words and the per-block candidates) lives in the file-scope
+// control words, the block maxima and the per-block candidates) lives in the file-scope
 // device array below instead of the library's cudaMalloc'd workspace.
 //
 // The array is part of the module image: every GPU that loads the library
@@ -24,8 +24,8 @@
 namespace {
 
 constexpr size_t kNoallocScratchBytes = TOPK_NOALLOC_SCRATCH_BYTES;
-static_assert(kNoallocScratchBytes >= sizeof(topk::I32Ctrl) + TOPK_MAX_K * sizeof(int32_t),
-              "the scratch must hold the control words and one block's candidates");
+static_assert(kNoallocScratchBytes >= topk::kI32CandOffset + TOPK_MAX_K * sizeof(int32_t),
+              "the scratch must hold the control words, block maxima and one block's candidates");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -62,6 +62,16 @@ bool is_device_memory(const void* p) {
 
 }  // namespace
 
+namespace topk {
+// Device address of the no-alloc scratch on `device`, or null if no call
+// has set it up yet.
+void* noalloc_scratch_if_ready(int device) {
+    if (device < 0 || device >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    return g_scratch_ptr[device];
+}
+}  // namespace topk
+
 extern "C" int topk_i32_noalloc(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_st* stream) {
     if (!in || !out || n == 0 || k < 1 || (size_t)k > n) return TOPK_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 3u) return TOPK_ERR_INVALID_ARG;
@@ -91,16 +101,16 @@ extern "C" int topk_i32_noalloc(const int32_t* in, size_t n, int k, int32_t* out
     }
     // Fewer blocks when the candidates of a full grid would not fit; the
     // kernel's grid-stride loop covers the input with any grid size.
-    const size_t slots = (kNoallocScratchBytes - sizeof(topk::I32Ctrl)) / sizeof(int32_t);
+    const size_t slots = (kNoallocScratchBytes - topk::kI32CandOffset) / sizeof(int32_t);
     const size_t fit = slots / (size_t)k;
     if ((size_t)plan.grid > fit) plan.grid = (int)fit;
 
-    auto* ctrl = static_cast<topk::I32Ctrl*>(scratch);
-    auto* cand = reinterpret_cast<int32_t*>(static_cast<char*>(scratch) + sizeof(topk::I32Ctrl));
-    // The array keeps the last call's contents; the control words must start
-    // at zero, so clear them on the stream before the launch.
-    e = cudaMemsetAsync(ctrl, 0, sizeof(topk::I32Ctrl), s);
-    if (e == cudaSuccess) e = topk::i32_launch(plan, s, in, n, k, out, cand, ctrl);
+    // The array keeps the last call's contents; the control words and the
+    // block-maximum slots must start at zero, so clear them on the stream
+    // before the launch (the sticky status word is left alone).
+    e = cudaMemsetAsync(static_cast<char*>(scratch) + topk::kI32ResetBegin, 0,
+                        topk::kI32CandOffset - topk::kI32ResetBegin, s);
+    if (e == cudaSuccess) e = topk::i32_launch(plan, s, in, n, k, out, scratch);
     if (e != cudaSuccess) {
         topk::note_cuda_error((int)e);
         return TOPK_ERR_CUDA;

@@ -254,10 +254,11 @@ __device__ void second_stage(const Scratch& sc, int k, int32_t* __restrict__ out
 
 // Publish this block's candidates (k, sorted, INT_MIN-padded) and its k-th
 // value, take a ticket; returns true in the last block to finish.
-__device__ __forceinline__ bool finish_block(const Scratch& sc, int k, const int* list, int* s_last) {
+__device__ __forceinline__ bool finish_block(const Scratch& sc, int k, const int* list, int block_thresh,
+                                             int* s_last) {
     for (int i = threadIdx.x; i < k; i += blockDim.x) sc.cand[(size_t)blockIdx.x * k + i] = list[i];
     if (threadIdx.x == 0) {
-        const int kth = list[k - 1];
+        const int kth = kmax(list[k - 1], block_thresh);
         if (kth != INT_MIN) atomicMax(&sc.ctrl->thresh, bias(kth));
     }
     __threadfence();
@@ -321,21 +322,28 @@ struct WarpList {
 // Streaming ring: one producer warp issues bulk copies of 4 KiB tiles into
 // kStages shared-memory stages; kCons consumer warps each take every kCons-th
 // tile of the block (stage s is always consumed by warp s % kCons, so a
-// consumer never runs a full ring ahead of the producer).
+// consumer never runs a full ring ahead of the producer).  Consumers touch
+// only shared memory; a monitor warp carries thresholds between the block
+// and the grid.
 constexpr int kCons = 8;                    // consumer warps per block
+constexpr int kProducer = kCons;            // warp index of the producer
+constexpr int kMonitor = kCons + 1;         // warp index of the monitor
+constexpr int kStreamThreads = (kCons + 2) * 32;
 constexpr int kStages = 24;                 // ring depth (a multiple of kCons)
 constexpr int kRingBytes = kStages * kTileVec * 16;
+constexpr int kMonitorRounds = 1 << 20;     // bound on the monitor's polling rounds
 static_assert(kStages % kCons == 0, "stage s must always go to the same consumer warp");
 
 template <int L, int GL>
-__global__ void __launch_bounds__((kCons + 1) * 32, 2)
+__global__ void __launch_bounds__(kStreamThreads, 2)
 topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* __restrict__ out,
                        unsigned char* __restrict__ scratch, int cap_limit) {
     constexpr int K = 32 * L;
     extern __shared__ __align__(128) int4 ring[];             // kStages tiles; later the stage-2 list
     __shared__ __align__(16) int s_queue[kCons * kQueue];      // survivor queues, then the merge area
+    __shared__ int s_sel[256];                                 // monitor: block maxima above t
     __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
-    __shared__ int s_thresh, s_cmax, s_last, s_count;
+    __shared__ int s_thresh, s_cmax, s_done, s_last, s_count;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -343,6 +351,7 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
     if (threadIdx.x == 0) {
         s_thresh = INT_MIN;
         s_cmax = INT_MIN;
+        s_done = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
@@ -361,8 +370,7 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
     WarpList<L> wl;
     wl.init();
 
-    if (warp == kCons) {
-        // ---- producer ----
+    if (warp == kProducer) {
         if (lane == 0) {
             size_t j = 0;
             for (; j < J; ++j) {
@@ -383,22 +391,77 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
                     break;
                 }
         }
+    } else if (warp == kMonitor) {
+        // Start value from the array's last 256 elements (keeps sorted
+        // ascending input cheap), then poll: publish the block's threshold
+        // and maximum, pull the grid's threshold and the k-th largest block
+        // maximum.  Every value it puts in s_thresh is a valid threshold.
+        if constexpr (GL <= 2) {
+            if (sp.nvec > 0) {
+                int4 s[2];
+                const long long tv = (long long)sp.nvec - kTailVec + 2 * lane;
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    s[q] = tv + q >= 0 ? __ldg(sp.body + tv + q) : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
+                const int tseed = seed_from_groups<GL>(s, k, lane);
+                if (lane == 0) atomicMax(&s_thresh, tseed);
+            }
+        }
+        int pub_t = INT_MIN, pub_cmax = INT_MIN;
+        for (int round = 0; round < kMonitorRounds; ++round) {
+            const bool last = *(volatile int*)&s_done == kCons;
+            const int st = *(volatile int*)&s_thresh;
+            if (st > pub_t) {
+                if (lane == 0) atomicMax(&sc.ctrl->thresh, bias(st));
+                pub_t = st;
+            }
+            const int cm = *(volatile int*)&s_cmax;
+            if (use_bmax && cm > pub_cmax) {
+                if (lane == 0) atomicMax(&sc.bmax[b], bias(cm));
+                pub_cmax = cm;
+            }
+            if (last) break;
+            unsigned bv[8];
+            if (use_bmax) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int x = i * 32 + lane;
+                    bv[i] = x < (int)G ? ld_relaxed_gpu(&sc.bmax[x]) : 0u;
+                }
+            }
+            int t = kmax(st, unbias(ld_relaxed_gpu(&sc.ctrl->thresh)));
+            if (use_bmax) {
+                int ns = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int x = unbias(bv[i]);
+                    const bool p = x > t;
+                    const unsigned bb = __ballot_sync(kFullMask, p);
+                    if (p) s_sel[ns + __popc(bb & lanemask_lt())] = x;
+                    ns += __popc(bb);
+                }
+                __syncwarp();
+                if (ns >= k && ns <= 128) {
+                    int sv[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int p = i * 32 + lane;
+                        sv[i] = p < ns ? s_sel[p] : INT_MIN;
+                    }
+                    warp_sort_desc<4>(sv, lane);
+                    t = kmax(t, warp_sorted_at<4>(sv, k - 1));
+                }
+                __syncwarp();
+            }
+            if (t > st && lane == 0) atomicMax(&s_thresh, t);
+            __nanosleep(256);
+        }
     } else {
         // ---- consumers ----
         int* q = s_queue + warp * kQueue;
         int nq = 0;
         int t = INT_MIN;
-        int published = INT_MIN;   // largest value this warp sent to the global word
         int pushed_max = INT_MIN;  // largest tile maximum this warp sent to s_cmax
-        int bmax_pub = INT_MIN;    // largest block maximum this warp wrote to the global slot
-
-        auto publish = [&](int v) {
-            if (lane == 0) {
-                atomicMax(&s_thresh, v);
-                if (v > published) atomicMax(&sc.ctrl->thresh, bias(v));
-            }
-            published = kmax(published, v);
-        };
 
         // Merge every full 32-chunk of the queue (with all_of_it, the rest
         // too) into the list; raise t to the list's k-th value.
@@ -417,7 +480,7 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
                 const int kth = warp_sorted_at<L>(wl.lst, k - 1);
                 if (kth > t) {
                     t = kth;
-                    publish(kth);
+                    if (lane == 0) atomicMax(&s_thresh, kth);
                 }
             }
         };
@@ -430,21 +493,8 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
             enqueue(q, nq, (size_t)lane < ns ? in[pos] : INT_MIN, INT_MIN, lane);
         }
 
-        int iter = 0;
-        for (size_t j = warp; j < J; j += kCons, ++iter) {
-            // Block-maxima threshold: refreshed by one consumer warp of the
-            // block per round, from (up to) the first 256 blocks' maxima.
-            const bool refresh = use_bmax && ((iter + warp) & (kCons - 1)) == kCons - 1;
-            unsigned bv[8];
-            if (refresh) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int x = i * 32 + lane;
-                    bv[i] = x < (int)G ? ld_relaxed_gpu(&sc.bmax[x]) : 0u;
-                }
-            }
-            const unsigned g = ld_relaxed_gpu(&sc.ctrl->thresh);
-
+        bool first = true;
+        for (size_t j = warp; j < J; j += kCons) {
             const int s = (int)(j % kStages);
             if (!mbar_wait(&full_bar[s], (uint32_t)((j / kStages) & 1))) {
                 if (lane == 0) atomicOr(sc.status, kStatusWaitTimeout);
@@ -466,14 +516,16 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[s]);  // the tile is in registers: release the stage
 
-            if (iter == 0) {
-                const int seed = start_threshold<GL>(r, sp, k, lane);
+            if (first) {
+                // Start value: k-th largest of the tile's 32*GL group maxima.
+                first = false;
+                const int seed = seed_from_groups<GL>(r, k, lane);
                 if (seed > t) {
                     t = seed;
-                    publish(seed);
+                    if (lane == 0) atomicMax(&s_thresh, seed);
                 }
             }
-            t = kmax(t, kmax(unbias(g), *(volatile int*)&s_thresh));
+            t = kmax(t, *(volatile int*)&s_thresh);
 
             int m = INT_MIN;
 #pragma unroll
@@ -495,48 +547,13 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
                     }
                 }
             }
-
-            if (refresh) {
-                const int cm = *(volatile int*)&s_cmax;
-                if (cm > bmax_pub) {
-                    if (lane == 0) atomicMax(&sc.bmax[b], bias(cm));
-                    bmax_pub = cm;
-                }
-                // Block maxima above t, compacted behind the (< 32 entry) queue.
-                int* sel = q + 32;
-                int ns = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int x = unbias(bv[i]);
-                    const bool p = x > t;
-                    const unsigned bb = __ballot_sync(kFullMask, p);
-                    const int pos = ns + __popc(bb & lanemask_lt());
-                    if (p && pos < kQueue - 32) sel[pos] = x;
-                    ns += __popc(bb);
-                }
-                __syncwarp();
-                if (ns >= k && ns <= 128) {
-                    int sv[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int p = i * 32 + lane;
-                        sv[i] = p < ns ? sel[p] : INT_MIN;
-                    }
-                    warp_sort_desc<4>(sv, lane);
-                    const int theta = warp_sorted_at<4>(sv, k - 1);
-                    if (theta > t) {
-                        t = theta;
-                        publish(theta);
-                    }
-                }
-                __syncwarp();
-            }
         }
 
         drain(true);
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < L; ++i) q[i * 32 + lane] = wl.lst[i];
+        if (lane == 0) atomicAdd(&s_done, 1);
     }
 
     // Block merge: consumer warp 0 merges the other consumers' lists.
@@ -558,7 +575,9 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
     }
     __syncthreads();
 
-    if (finish_block(sc, k, s_queue, &s_last))
+    // Every threshold this block's warps used went through s_thresh: publish
+    // it before the ticket, whatever the monitor managed to do.
+    if (finish_block(sc, k, s_queue, s_thresh, &s_last))
         second_stage(sc, k, out, reinterpret_cast<int*>(ring), kRingBytes / (int)sizeof(int), cap_limit, &s_count);
 }
 
@@ -674,7 +693,7 @@ topk_i32_smem_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* _
     }
     __syncthreads();
 
-    if (finish_block(sc, k, smem, &s_last))
+    if (finish_block(sc, k, smem, s_thresh, &s_last))
         second_stage(sc, k, out, smem, kWarps * kBigBuf, cap_limit, &s_count);
 }
 
@@ -682,7 +701,7 @@ topk_i32_smem_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* _
 
 template <int L, int GL>
 struct StreamVariant {
-    static constexpr int kThreads = (kCons + 1) * 32;
+    static constexpr int kThreads = kStreamThreads;
     static size_t smem_bytes() { return kRingBytes; }
     static const void* fn() { return reinterpret_cast<const void*>(&topk_i32_stream_kernel<L, GL>); }
     static void launch(int grid, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,

@@ -211,3 +211,12 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 }
 
 }  // namespace topk
+
+namespace topk {
+// Order this thread's earlier generic-proxy accesses to shared memory before
+// its later async-proxy (bulk copy) accesses, e.g. before re-filling a stage
+// whose contents the warp has just read.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+}  // namespace topk

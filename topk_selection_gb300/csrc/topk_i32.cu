@@ -45,6 +45,7 @@
 
 #include <climits>
 #include <cstdint>
+#include <mutex>
 
 #include "topk_device.cuh"
 #include "topk_internal.h"
@@ -319,30 +320,28 @@ struct WarpList {
     }
 };
 
-// Streaming ring: one producer warp issues bulk copies of 4 KiB tiles into
-// kStages shared-memory stages; kCons consumer warps each take every kCons-th
-// tile of the block (stage s is always consumed by warp s % kCons, so a
-// consumer never runs a full ring ahead of the producer).  Consumers touch
-// only shared memory; a monitor warp carries thresholds between the block
-// and the grid.
-constexpr int kCons = 8;                    // consumer warps per block
-constexpr int kProducer = kCons;            // warp index of the producer
-constexpr int kMonitor = kCons + 1;         // warp index of the monitor
-constexpr int kStreamThreads = (kCons + 2) * 32;
-constexpr int kStages = 24;                 // ring depth (a multiple of kCons)
-constexpr int kRingBytes = kStages * kTileVec * 16;
-constexpr int kMonitorRounds = 1 << 20;     // bound on the monitor's polling rounds
-static_assert(kStages % kCons == 0, "stage s must always go to the same consumer warp");
+// Streaming: every consumer warp owns a ring of kWarpStages shared-memory
+// stages of one 4 KiB tile each and keeps bulk copies of its own next tiles
+// in flight; as soon as a tile is in registers the warp re-arms that stage
+// with the copy of its tile kWarpStages steps ahead.  No warp ever waits for
+// another warp's progress.  Consumers touch only shared memory; a monitor
+// warp carries thresholds between the block and the grid.
+constexpr int kCons = 8;                     // consumer warps per block
+constexpr int kMonitor = kCons;              // warp index of the monitor
+constexpr int kStreamThreads = (kCons + 1) * 32;
+constexpr int kWarpStages = 3;               // tiles in flight per consumer warp
+constexpr int kRingBytes = kCons * kWarpStages * kTileVec * 16;
+constexpr int kMonitorRounds = 1 << 20;      // bound on the monitor's polling rounds
 
 template <int L, int GL>
 __global__ void __launch_bounds__(kStreamThreads, 2)
 topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* __restrict__ out,
                        unsigned char* __restrict__ scratch, int cap_limit) {
     constexpr int K = 32 * L;
-    extern __shared__ __align__(128) int4 ring[];             // kStages tiles; later the stage-2 list
+    extern __shared__ __align__(128) int4 ring[];             // per-warp stages; later the stage-2 list
     __shared__ __align__(16) int s_queue[kCons * kQueue];      // survivor queues, then the merge area
     __shared__ int s_sel[256];                                 // monitor: block maxima above t
-    __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
+    __shared__ __align__(8) uint64_t full_bar[kCons * kWarpStages];
     __shared__ int s_thresh, s_cmax, s_done, s_last, s_count;
 
     const int lane = threadIdx.x & 31;
@@ -352,10 +351,7 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
         s_thresh = INT_MIN;
         s_cmax = INT_MIN;
         s_done = 0;
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);
-        }
+        for (int s = 0; s < kCons * kWarpStages; ++s) mbar_init(&full_bar[s], 1);
         mbar_init_fence();
     }
     __syncthreads();
@@ -370,28 +366,7 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
     WarpList<L> wl;
     wl.init();
 
-    if (warp == kProducer) {
-        if (lane == 0) {
-            size_t j = 0;
-            for (; j < J; ++j) {
-                const int s = (int)(j % kStages);
-                if (j >= (size_t)kStages && !mbar_wait(&empty_bar[s], (uint32_t)((j / kStages - 1) & 1))) {
-                    atomicOr(sc.status, kStatusWaitTimeout);
-                    break;
-                }
-                const size_t base = (b + j * G) * kTileVec;
-                const size_t cnt = sp.nvec - base < (size_t)kTileVec ? sp.nvec - base : (size_t)kTileVec;
-                mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(cnt * 16));
-                bulk_copy_g2s(ring + (size_t)s * kTileVec, sp.body + base, (uint32_t)(cnt * 16), &full_bar[s]);
-            }
-            // Leave no copy in flight: the last kStages issued must have landed.
-            for (size_t q = j > (size_t)kStages ? j - kStages : 0; q < j; ++q)
-                if (!mbar_wait(&full_bar[q % kStages], (uint32_t)((q / kStages) & 1))) {
-                    atomicOr(sc.status, kStatusWaitTimeout);
-                    break;
-                }
-        }
-    } else if (warp == kMonitor) {
+    if (warp == kMonitor) {
         // Start value from the array's last 256 elements (keeps sorted
         // ascending input cheap), then poll: publish the block's threshold
         // and maximum, pull the grid's threshold and the k-th largest block
@@ -493,16 +468,32 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
             enqueue(q, nq, (size_t)lane < ns ? in[pos] : INT_MIN, INT_MIN, lane);
         }
 
+        // This warp's tiles are j = warp + i*kCons (i = 0, 1, ...), tile
+        // b + j*G; tile i goes through stage i % kWarpStages.
+        int4* my_ring = ring + (size_t)warp * kWarpStages * kTileVec;
+        uint64_t* my_bar = full_bar + warp * kWarpStages;
+        const size_t my_tiles = (size_t)warp < J ? (J - warp + kCons - 1) / kCons : 0;
+        auto issue = [&](size_t i) {  // lane 0 only
+            const size_t base = (b + (warp + i * kCons) * G) * kTileVec;
+            const size_t cnt = sp.nvec - base < (size_t)kTileVec ? sp.nvec - base : (size_t)kTileVec;
+            const int st = (int)(i % kWarpStages);
+            mbar_arrive_expect_tx(&my_bar[st], (uint32_t)(cnt * 16));
+            bulk_copy_g2s(my_ring + (size_t)st * kTileVec, sp.body + base, (uint32_t)(cnt * 16), &my_bar[st]);
+        };
+        if (lane == 0)
+            for (size_t i = 0; i < my_tiles && i < (size_t)kWarpStages; ++i) issue(i);
+
         bool first = true;
-        for (size_t j = warp; j < J; j += kCons) {
-            const int s = (int)(j % kStages);
-            if (!mbar_wait(&full_bar[s], (uint32_t)((j / kStages) & 1))) {
+        size_t i = 0;
+        for (; i < my_tiles; ++i) {
+            const int stg = (int)(i % kWarpStages);
+            if (!mbar_wait(&my_bar[stg], (uint32_t)((i / kWarpStages) & 1))) {
                 if (lane == 0) atomicOr(sc.status, kStatusWaitTimeout);
                 break;
             }
-            const size_t base = (b + j * G) * kTileVec;
+            const size_t base = (b + (warp + i * kCons) * G) * kTileVec;
             const size_t cnt = sp.nvec - base < (size_t)kTileVec ? sp.nvec - base : (size_t)kTileVec;
-            const int4* st = ring + (size_t)s * kTileVec;
+            const int4* st = my_ring + (size_t)stg * kTileVec;
             int4 r[kU];
             if (cnt == (size_t)kTileVec) {
 #pragma unroll
@@ -514,7 +505,11 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
                                                          : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[s]);  // the tile is in registers: release the stage
+            // The tile is in registers: re-arm its stage with tile i + kWarpStages.
+            if (lane == 0 && i + kWarpStages < my_tiles) {
+                fence_proxy_async_smem();
+                issue(i + kWarpStages);
+            }
 
             if (first) {
                 // Start value: k-th largest of the tile's 32*GL group maxima.
@@ -549,10 +544,14 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
             }
         }
 
+        // After an early exit, let the copies this warp issued land before
+        // the block moves on.
+        for (size_t w2 = i + 1; w2 < my_tiles && w2 < i + kWarpStages; ++w2)
+            if (!mbar_wait(&my_bar[w2 % kWarpStages], (uint32_t)((w2 / kWarpStages) & 1))) break;
         drain(true);
         __syncwarp();
 #pragma unroll
-        for (int i = 0; i < L; ++i) q[i * 32 + lane] = wl.lst[i];
+        for (int x = 0; x < L; ++x) q[x * 32 + lane] = wl.lst[x];
         if (lane == 0) atomicAdd(&s_done, 1);
     }
 
@@ -726,20 +725,44 @@ using VarK32 = StreamVariant<1, 1>;
 using VarK64 = StreamVariant<2, 2>;
 using VarK128 = StreamVariant<4, 4>;
 
+// Blocks per SM and SM count of a kernel variant on a device, found once
+// (the shared-memory opt-in is set at the same time) and cached.
+struct DeviceFit {
+    int sms = 0;
+    int per_sm = 0;
+};
+
+template <class V>
+cudaError_t device_fit(int device, DeviceFit* out) {
+    constexpr int kMaxDev = 64;
+    static std::mutex mu;
+    static DeviceFit cache[kMaxDev];
+    if (device < 0 || device >= kMaxDev) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[device].sms == 0) {
+        DeviceFit f;
+        cudaError_t e = cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, device);
+        if (e != cudaSuccess) return e;
+        const size_t smem = V::smem_bytes();
+        if (smem > 48 * 1024) {
+            e = cudaFuncSetAttribute(V::fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f.per_sm, V::fn(), V::kThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (f.per_sm < 1) f.per_sm = 1;
+        cache[device] = f;
+    }
+    *out = cache[device];
+    return cudaSuccess;
+}
+
 template <class V>
 cudaError_t plan_for(int device, size_t n, I32Plan* plan) {
-    int sms = 0, per_sm = 0;
-    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    DeviceFit f;
+    cudaError_t e = device_fit<V>(device, &f);
     if (e != cudaSuccess) return e;
-    const size_t smem = V::smem_bytes();
-    if (smem > 48 * 1024) {
-        e = cudaFuncSetAttribute(V::fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, V::fn(), V::kThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    size_t full = (size_t)sms * per_sm;
+    size_t full = (size_t)f.sms * f.per_sm;
     if (full > (size_t)kI32MaxGrid) full = kI32MaxGrid;
     const size_t nvec = n / 4;
     const size_t tiles = (nvec + kTileVec - 1) / kTileVec;

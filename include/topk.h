@@ -116,8 +116,9 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
  *     TOPK_NOALLOC_SCRATCH_BYTES (1 MiB): control words, per-block maxima
  *     and per-block candidates.  Every GPU that loads the library holds it
  *     until the process exits.  k above TOPK_MAX_K is rejected with
- *     TOPK_ERR_UNSUPPORTED; for large k the grid is cut so that its
- *     candidates fit (1 MiB holds 254 blocks' worth at k = 1024).
+ *     TOPK_ERR_UNSUPPORTED.  The grid is cut so that every block's
+ *     candidate lists fit (1 MiB holds 246 blocks' worth), so on GPUs with
+ *     more SMs this entry point runs fewer blocks than topk_i32.
  *   - Every call uses the same array.  Each call clears the control words
  *     on `stream` before its launch, but calls whose work overlaps on the
  *     GPU (different streams, or different host threads without ordering)

@@ -65,7 +65,7 @@ int workspace(cudaStream_t s, int device, size_t ctrl_cand, size_t in_bytes, siz
         if (rc != TOPK_OK) return rc;
         // The control words and block-maximum slots must start at zero; the
         // kernels leave them so.
-        cudaError_t e = cudaMemsetAsync(w.ctrl_cand, 0, topk::kI32CandOffset, s);
+        cudaError_t e = cudaMemsetAsync(w.ctrl_cand, 0, topk::kI32ResetEnd, s);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (in_bytes) {
@@ -131,7 +131,7 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
     topk::I32Plan plan;
     e = topk::i32_plan(device, n, k, &plan);
     if (e != cudaSuccess) return cuda_fail(e);
-    const size_t ctrl_cand = topk::i32_scratch_bytes(plan.max_grid, TOPK_MAX_K);
+    const size_t ctrl_cand = topk::i32_scratch_bytes(plan.max_grid);
     Workspace* w = nullptr;
     rc = workspace(s, device, ctrl_cand, in_host ? n * sizeof(int32_t) : 0,
                    out_host ? (size_t)k * sizeof(int32_t) : 0, &w);

@@ -75,12 +75,14 @@ struct Scratch {
     unsigned* status;  // sticky error bits (kStatusWaitTimeout)
     I32Ctrl* ctrl;
     unsigned* bmax;    // per-block running maxima, biased
-    int32_t* cand;
+    int32_t* counts;   // per list: entries above the grid threshold at the block's end
+    int32_t* cand;     // per block: its sorted candidate lists
 };
 
 __device__ __forceinline__ Scratch scratch_view(unsigned char* base) {
     return Scratch{reinterpret_cast<unsigned*>(base + kI32StatusOffset), reinterpret_cast<I32Ctrl*>(base + kI32CtrlOffset),
-                   reinterpret_cast<unsigned*>(base + kI32BmaxOffset), reinterpret_cast<int32_t*>(base + kI32CandOffset)};
+                   reinterpret_cast<unsigned*>(base + kI32BmaxOffset), reinterpret_cast<int32_t*>(base + kI32CountOffset),
+                   reinterpret_cast<int32_t*>(base + kI32CandOffset)};
 }
 
 // Input split: an unaligned head (< 4 elements), a 16-byte aligned body of
@@ -160,33 +162,49 @@ __device__ __forceinline__ void enqueue(int* q, int& nq, int v, int t, int lane)
 }
 
 // ---------------------------------------------------------------- stage 2 --
+//
+// Every block leaves `lists_per_block` sorted lists of K entries (INT_MIN
+// padded) in its candidate area, and for each list the number of leading
+// entries that exceed the grid threshold it read when it finished.  The
+// entries after that count are at most a published threshold, so they can
+// never be needed: only the counted prefixes are gathered.
 
 // Run by the last block to finish.  `room` ints of shared memory at `list`;
 // cap_limit > 0 lowers the list capacity (to exercise the radix-select path).
-__device__ void second_stage(const Scratch& sc, int k, int32_t* __restrict__ out, int* list, int room,
-                             int cap_limit, int* s_count) {
+__device__ void second_stage(const Scratch& sc, int k, int lists_per_block, int K, int32_t* __restrict__ out,
+                             int* list, int room, int cap_limit, int* s_count) {
     const int lane = threadIdx.x & 31;
+    __threadfence();
+    const int tg = unbias(ld_relaxed_gpu(&sc.ctrl->thresh));
     // The list is bitonic-sorted in place at a power-of-two length, so its
     // capacity is the largest power of two that fits.
     int cap = 1;
     while (2 * cap <= room) cap *= 2;
     if (cap_limit > 0 && cap_limit < cap) cap = cap_limit;
     if (cap < k) cap = k;  // the sorted list must be able to hold the answer
-    __threadfence();
-    const int tg = unbias(ld_relaxed_gpu(&sc.ctrl->thresh));
-    const size_t M = (size_t)gridDim.x * k;
-    const size_t Mr = (M + blockDim.x - 1) / blockDim.x * blockDim.x;
+    const int nlists = (int)gridDim.x * lists_per_block;
+
     if (threadIdx.x == 0) *s_count = 0;
     __syncthreads();
-    for (size_t i = threadIdx.x; i < Mr; i += blockDim.x) {
-        const int v = i < M ? __ldcg(sc.cand + i) : INT_MIN;
-        const bool p = v > tg;
-        const unsigned m = __ballot_sync(kFullMask, p);
-        int base = 0;
-        if (lane == 0 && m) base = atomicAdd(s_count, __popc(m));
-        base = __shfl_sync(kFullMask, base, 0);
-        const int pos = base + __popc(m & lanemask_lt());
-        if (p && pos < cap) list[pos] = v;
+    constexpr int kBatch = 8;
+    for (int base = 0; base < nlists; base += kBatch * (int)blockDim.x) {
+        int c[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            const int l = base + q * (int)blockDim.x + (int)threadIdx.x;
+            c[q] = l < nlists ? __ldcg(sc.counts + l) : 0;
+        }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            const int l = base + q * (int)blockDim.x + (int)threadIdx.x;
+            const int32_t* src = sc.cand + (size_t)l * K;
+            for (int p = 0; p < c[q]; ++p) {
+                const int v = __ldcg(src + p);
+                if (v <= tg) break;  // the list is sorted: nothing after this exceeds tg
+                const int pos = atomicAdd(s_count, 1);
+                if (pos < cap) list[pos] = v;
+            }
+        }
     }
     __syncthreads();
     const int above = *s_count;
@@ -194,10 +212,12 @@ __device__ void second_stage(const Scratch& sc, int k, int32_t* __restrict__ out
     int T = tg;         // value that fills the places after the sorted list
     int nlist = above;  // sorted entries that come first
     if (above > cap) {
-        // Radix select over the candidates above tg: the exact k-th largest
+        // Radix select over every candidate above tg: the exact k-th largest
         // value T, most significant 8-bit digit first.
         __shared__ unsigned hist[256];
         __shared__ unsigned s_prefix, s_need;
+        const size_t M = (size_t)nlists * K;
+        const size_t Mr = (M + blockDim.x - 1) / blockDim.x * blockDim.x;
         unsigned prefix = 0, pmask = 0, need = (unsigned)k;
         for (int shift = 24; shift >= 0; shift -= 8) {
             for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
@@ -241,10 +261,29 @@ __device__ void second_stage(const Scratch& sc, int k, int32_t* __restrict__ out
         nlist = *s_count;
     }
 
-    const int L = next_pow2(nlist < 2 ? 2 : nlist);
-    for (int i = nlist + threadIdx.x; i < L; i += blockDim.x) list[i] = INT_MIN;
-    block_sort_smem_desc(list, L);
-    for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < nlist ? list[i] : T;
+    if (nlist <= 256) {
+        // Small list: one warp sorts it in registers.
+        if (threadIdx.x < 32) {
+            int v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int p = j * 32 + lane;
+                v[j] = p < nlist ? list[p] : INT_MIN;
+            }
+            warp_sort_desc<8>(v, lane);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int p = j * 32 + lane;
+                if (p < k) out[p] = p < nlist ? v[j] : T;
+            }
+            for (int p = 256 + lane; p < k; p += 32) out[p] = T;
+        }
+    } else {
+        const int L = next_pow2(nlist);
+        for (int i = nlist + threadIdx.x; i < L; i += blockDim.x) list[i] = INT_MIN;
+        block_sort_smem_desc(list, L);
+        for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < nlist ? list[i] : T;
+    }
     // Leave the scratch as the next launch expects it.
     for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) sc.bmax[i] = 0u;
     if (threadIdx.x == 0) {
@@ -253,23 +292,33 @@ __device__ void second_stage(const Scratch& sc, int k, int32_t* __restrict__ out
     }
 }
 
-// Publish this block's candidates (k, sorted, INT_MIN-padded) and its k-th
-// value, take a ticket; returns true in the last block to finish.
-__device__ __forceinline__ bool finish_block(const Scratch& sc, int k, const int* list, int block_thresh,
-                                             int* s_last) {
-    for (int i = threadIdx.x; i < k; i += blockDim.x) sc.cand[(size_t)blockIdx.x * k + i] = list[i];
-    if (threadIdx.x == 0) {
-        const int kth = kmax(list[k - 1], block_thresh);
-        if (kth != INT_MIN) atomicMax(&sc.ctrl->thresh, bias(kth));
-    }
+// Publish this block's threshold and take a ticket (after every thread has
+// written its candidates); returns true in the last block to finish.
+__device__ __forceinline__ bool block_done(const Scratch& sc, int block_thresh, int* s_last) {
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
+        if (block_thresh != INT_MIN) atomicMax(&sc.ctrl->thresh, bias(block_thresh));
+        __threadfence();
         const unsigned ticket = atomicAdd(&sc.ctrl->ticket, 1u);
         *s_last = ticket == gridDim.x - 1;
     }
     __syncthreads();
     return *s_last != 0;
+}
+
+// Write a warp's sorted K-list (lst[j] at position j*32 + lane) and the
+// number of its leading entries above t_now.
+template <int L>
+__device__ __forceinline__ void write_list(const Scratch& sc, int list_id, const int (&lst)[L], int t_now, int lane) {
+    int32_t* dst = sc.cand + (size_t)list_id * (32 * L);
+    int count = 0;
+#pragma unroll
+    for (int j = 0; j < L; ++j) {
+        dst[j * 32 + lane] = lst[j];
+        count += __popc(__ballot_sync(kFullMask, lst[j] > t_now));
+    }
+    if (lane == 0) sc.counts[list_id] = count;
 }
 
 // ------------------------------------------------- k <= 128: register lists --
@@ -416,15 +465,15 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
                     ns += __popc(bb);
                 }
                 __syncwarp();
-                if (ns >= k && ns <= 128) {
-                    int sv[4];
+                if (ns >= k) {
+                    int sv[8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < 8; ++i) {
                         const int p = i * 32 + lane;
                         sv[i] = p < ns ? s_sel[p] : INT_MIN;
                     }
-                    warp_sort_desc<4>(sv, lane);
-                    t = kmax(t, warp_sorted_at<4>(sv, k - 1));
+                    warp_sort_desc<8>(sv, lane);
+                    t = kmax(t, warp_sorted_at<8>(sv, k - 1));
                 }
                 __syncwarp();
             }
@@ -549,35 +598,45 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
         for (size_t w2 = i + 1; w2 < my_tiles && w2 < i + kWarpStages; ++w2)
             if (!mbar_wait(&my_bar[w2 % kWarpStages], (uint32_t)((w2 / kWarpStages) & 1))) break;
         drain(true);
-        __syncwarp();
-#pragma unroll
-        for (int x = 0; x < L; ++x) q[x * 32 + lane] = wl.lst[x];
         if (lane == 0) atomicAdd(&s_done, 1);
     }
 
-    // Block merge: consumer warp 0 merges the other consumers' lists.
+    // Block combine (section 2.1's tree, with warps in place of threads):
+    // three levels of pairwise bitonic merges of the consumers' register
+    // lists through shared memory.
+    if (warp < kCons) {
+#pragma unroll
+        for (int i = 0; i < L; ++i) s_queue[warp * kQueue + i * 32 + lane] = wl.lst[i];
+    }
     __syncthreads();
-    if (warp == 0) {
-        for (int w = 1; w < kCons; ++w) {
-            const int* o = s_queue + w * kQueue;
+#pragma unroll
+    for (int step = 1; step < kCons; step <<= 1) {
+        if (warp < kCons && (warp & (2 * step - 1)) == 0) {
+            const int* o = s_queue + (warp + step) * kQueue;
             // The other list reversed against ours: the half-cleaner of a
             // bitonic merge, then the merge network.
 #pragma unroll
             for (int i = 0; i < L; ++i) wl.lst[i] = kmax(wl.lst[i], o[K - 1 - (i * 32 + lane)]);
             wl.bitonic_merge(lane);
-        }
-    }
-    __syncthreads();
-    if (warp == 0) {
 #pragma unroll
-        for (int i = 0; i < L; ++i) s_queue[i * 32 + lane] = wl.lst[i];
+            for (int i = 0; i < L; ++i) s_queue[warp * kQueue + i * 32 + lane] = wl.lst[i];
+        }
+        __syncthreads();
     }
+    // The block's list, and how many of its entries exceed the grid
+    // threshold now (only those can matter).
+    if (threadIdx.x == 0) s_count = kmax(s_thresh, unbias(ld_relaxed_gpu(&sc.ctrl->thresh)));
     __syncthreads();
+    const int t_now = s_count;
+    if (warp == 0) write_list<L>(sc, (int)b, wl.lst, t_now, lane);
+    const int block_kth = s_queue[k - 1];
 
     // Every threshold this block's warps used went through s_thresh: publish
-    // it before the ticket, whatever the monitor managed to do.
-    if (finish_block(sc, k, s_queue, s_thresh, &s_last))
-        second_stage(sc, k, out, reinterpret_cast<int*>(ring), kRingBytes / (int)sizeof(int), cap_limit, &s_count);
+    // it (and the block's k-th value) before the ticket, whatever the
+    // monitor managed to do.
+    if (block_done(sc, kmax(s_thresh, block_kth), &s_last))
+        second_stage(sc, k, 1, K, out, reinterpret_cast<int*>(ring), kRingBytes / (int)sizeof(int), cap_limit,
+                     &s_count);
 }
 
 // ---------------------------------------- k > 128: shared-memory buffers --
@@ -692,8 +751,23 @@ topk_i32_smem_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* _
     }
     __syncthreads();
 
-    if (finish_block(sc, k, smem, s_thresh, &s_last))
-        second_stage(sc, k, out, smem, kWarps * kBigBuf, cap_limit, &s_count);
+    // The block's sorted list (K entries) and the count above the grid threshold.
+    __shared__ int s_tnow;
+    if (threadIdx.x == 0) s_tnow = kmax(s_thresh, unbias(ld_relaxed_gpu(&sc.ctrl->thresh)));
+    __syncthreads();
+    if (warp == 0) {
+        int32_t* dst = sc.cand + (size_t)blockIdx.x * K;
+        int count = 0;
+        for (int p0 = 0; p0 < K; p0 += 32) {
+            const int v = smem[p0 + lane];
+            dst[p0 + lane] = v;
+            count += __popc(__ballot_sync(kFullMask, v > s_tnow));
+        }
+        if (lane == 0) sc.counts[blockIdx.x] = count;
+    }
+    const int block_kth = smem[k - 1];
+    if (block_done(sc, kmax(s_thresh, block_kth), &s_last))
+        second_stage(sc, k, 1, K, out, smem, kWarps * kBigBuf, cap_limit, &s_count);
 }
 
 // ------------------------------------------------------------ host side --

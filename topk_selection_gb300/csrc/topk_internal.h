@@ -20,23 +20,33 @@ struct I32Ctrl {
 };
 
 // Scratch of one int32 TopK launch, in this order:
-//   [0, 256)                 status word: nonzero after a bounded wait gave up
-//                            (sticky; read and cleared by the host)
-//   [256, 512)               I32Ctrl
-//   [512, 512 + 4*1024)      per-block running maxima (biased like thresh)
-//   [kI32CandOffset, ...)    grid * k candidates
-// [kI32ResetBegin, kI32CandOffset) is zero between launches.
+//   [0, 256)                     status word: nonzero after a bounded wait gave
+//                                up (sticky; read and cleared by the host)
+//   [256, 512)                   I32Ctrl
+//   [512, 512 + 4*1024)          per-block running maxima (biased like thresh)
+//   [kI32CountOffset, +4*8192)   per-list survivor counts (up to 8 lists per block)
+//   [kI32CandOffset, ...)        per block, its candidate lists: up to
+//                                kI32CandPerBlock ints
+// [kI32ResetBegin, kI32CountOffset) is zero between launches.
 constexpr int kI32MaxGrid = 1024;
+constexpr int kI32MaxListsPerBlock = 8;
+constexpr int kI32CandPerBlock = 1024;
 constexpr size_t kI32StatusOffset = 0;
 constexpr size_t kI32CtrlOffset = 256;
 constexpr size_t kI32BmaxOffset = 512;
-constexpr size_t kI32CandOffset = kI32BmaxOffset + (size_t)kI32MaxGrid * sizeof(unsigned);
+constexpr size_t kI32CountOffset = kI32BmaxOffset + (size_t)kI32MaxGrid * sizeof(unsigned);
+constexpr size_t kI32CandOffset =
+    kI32CountOffset + (size_t)kI32MaxGrid * kI32MaxListsPerBlock * sizeof(int32_t);
 constexpr size_t kI32ResetBegin = kI32CtrlOffset;
+constexpr size_t kI32ResetEnd = kI32CountOffset;
+static_assert(kI32CandOffset % 256 == 0, "candidate area alignment");
 
 // Status bits a kernel may set in the status word.
 constexpr unsigned kStatusWaitTimeout = 1u;
 
-inline size_t i32_scratch_bytes(int grid, int k) { return kI32CandOffset + (size_t)grid * (size_t)k * sizeof(int32_t); }
+constexpr size_t i32_scratch_bytes(int grid) {
+    return kI32CandOffset + (size_t)grid * kI32CandPerBlock * sizeof(int32_t);
+}
 
 struct I32Plan {
     int grid;        // blocks launched (<= kI32MaxGrid)
@@ -50,9 +60,9 @@ int stage2_cap_option();
 // Grid for an n-element, k-wide selection on `device`.
 cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan);
 
-// Enqueue the single-launch int32 TopK.  scratch holds i32_scratch_bytes(plan.grid, k)
-// bytes, 256-byte aligned, whose first kI32CandOffset bytes are zero (they are
-// zero again when the launch completes).
+// Enqueue the single-launch int32 TopK.  scratch holds i32_scratch_bytes(plan.grid)
+// bytes, 256-byte aligned, whose [kI32ResetBegin, kI32ResetEnd) bytes are zero
+// (they are zero again when the launch completes).
 cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
                        void* scratch);
 

@@ -24,8 +24,8 @@
 namespace {
 
 constexpr size_t kNoallocScratchBytes = TOPK_NOALLOC_SCRATCH_BYTES;
-static_assert(kNoallocScratchBytes >= topk::kI32CandOffset + TOPK_MAX_K * sizeof(int32_t),
-              "the scratch must hold the control words, block maxima and one block's candidates");
+static_assert(kNoallocScratchBytes >= topk::i32_scratch_bytes(1),
+              "the scratch must hold the control words, block maxima, counts and one block's candidates");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -101,15 +101,14 @@ extern "C" int topk_i32_noalloc(const int32_t* in, size_t n, int k, int32_t* out
     }
     // Fewer blocks when the candidates of a full grid would not fit; the
     // kernel's grid-stride loop covers the input with any grid size.
-    const size_t slots = (kNoallocScratchBytes - topk::kI32CandOffset) / sizeof(int32_t);
-    const size_t fit = slots / (size_t)k;
+    const size_t fit = (kNoallocScratchBytes - topk::kI32CandOffset) / (topk::kI32CandPerBlock * sizeof(int32_t));
     if ((size_t)plan.grid > fit) plan.grid = (int)fit;
 
     // The array keeps the last call's contents; the control words and the
     // block-maximum slots must start at zero, so clear them on the stream
     // before the launch (the sticky status word is left alone).
     e = cudaMemsetAsync(static_cast<char*>(scratch) + topk::kI32ResetBegin, 0,
-                        topk::kI32CandOffset - topk::kI32ResetBegin, s);
+                        topk::kI32ResetEnd - topk::kI32ResetBegin, s);
     if (e == cudaSuccess) e = topk::i32_launch(plan, s, in, n, k, out, scratch);
     if (e != cudaSuccess) {
         topk::note_cuda_error((int)e);

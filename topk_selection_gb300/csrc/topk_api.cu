@@ -185,8 +185,10 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
 
     Workspace* w = nullptr;
     const size_t out_stage = (vals_host || idx_host) ? 2 * nout : 0;
-    rc = workspace(s, device, 0, in_host ? nin : 0, out_stage, &w);
+    // The row kernels use only the workspace's status word.
+    rc = workspace(s, device, topk::kI32CandOffset, in_host ? nin : 0, out_stage, &w);
     if (rc != TOPK_OK) return rc;
+    auto* status = reinterpret_cast<unsigned*>(static_cast<char*>(w->ctrl_cand) + topk::kI32StatusOffset);
 
     const float* din = in;
     float* dvals = vals;
@@ -199,7 +201,7 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
     if (vals_host) dvals = static_cast<float*>(w->stage_out);
     if (idx_host) didx = reinterpret_cast<int32_t*>(static_cast<char*>(w->stage_out) + nout);
 
-    e = topk::rows_launch(s, din, rows, cols, k, dvals, didx);
+    e = topk::rows_launch(s, din, rows, cols, k, dvals, didx, status);
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
 

@@ -142,6 +142,61 @@ __device__ void block_sort_smem_desc(T* a, int L) {
     }
 }
 
+// A warp's sorted (descending) top-K list of keys, K = 32*L, held in
+// registers: position p = j*32 + lane is lst[j] of lane `lane`.
+template <int L, typename T>
+struct RegList {
+    T lst[L];
+    int have;  // real entries (the rest hold the sentinel)
+
+    __device__ __forceinline__ void init(T sentinel) {
+#pragma unroll
+        for (int j = 0; j < L; ++j) lst[j] = sentinel;
+        have = 0;
+    }
+
+    // Sort a bitonic list descending (the merge half of a bitonic sort).
+    __device__ __forceinline__ void bitonic_merge(int lane) {
+#pragma unroll
+        for (int stride = 16 * L; stride > 0; stride >>= 1) {
+            if (stride >= 32) {
+                const int js = stride >> 5;
+#pragma unroll
+                for (int j = 0; j < L; ++j) {
+                    if ((j & js) == 0) {
+                        const T a = lst[j], b = lst[j | js];
+                        lst[j] = kmax(a, b);
+                        lst[j | js] = kmin(a, b);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < L; ++j) {
+                    const T o = __shfl_xor_sync(kFullMask, lst[j], stride);
+                    lst[j] = (lane & stride) == 0 ? kmax(lst[j], o) : kmin(lst[j], o);
+                }
+            }
+        }
+    }
+
+    // Merge a sorted-descending 32-chunk (one key per lane, position = lane)
+    // into the list, keeping the K largest: the half-cleaner against the
+    // reversed chunk, then the merge network.
+    __device__ __forceinline__ void merge_sorted32(T c, int cnt, int lane) {
+        const T rc = __shfl_sync(kFullMask, c, 31 - lane);
+        lst[L - 1] = kmax(lst[L - 1], rc);
+        bitonic_merge(lane);
+        have = have + cnt < 32 * L ? have + cnt : 32 * L;
+    }
+
+    // Merge another sorted K-list stored at o[0..K) into this one.
+    __device__ __forceinline__ void merge_list(const T* o, int lane) {
+#pragma unroll
+        for (int j = 0; j < L; ++j) lst[j] = kmax(lst[j], o[32 * L - 1 - (j * 32 + lane)]);
+        bitonic_merge(lane);
+    }
+};
+
 __host__ __device__ __forceinline__ int next_pow2(int x) {
     int p = 1;
     while (p < x) p <<= 1;

@@ -323,51 +323,8 @@ __device__ __forceinline__ void write_list(const Scratch& sc, int list_id, const
 
 // ------------------------------------------------- k <= 128: register lists --
 
-// A warp's sorted top-K list, K = 32*L, position p = j*32 + lane in lst[j].
 template <int L>
-struct WarpList {
-    int lst[L];
-    int have;  // real entries in lst (the rest are INT_MIN)
-
-    __device__ __forceinline__ void init() {
-#pragma unroll
-        for (int j = 0; j < L; ++j) lst[j] = INT_MIN;
-        have = 0;
-    }
-
-    // Sort a bitonic list descending (the merge half of a bitonic sort).
-    __device__ __forceinline__ void bitonic_merge(int lane) {
-#pragma unroll
-        for (int stride = 16 * L; stride > 0; stride >>= 1) {
-            if (stride >= 32) {
-                const int js = stride >> 5;
-#pragma unroll
-                for (int j = 0; j < L; ++j) {
-                    if ((j & js) == 0) {
-                        const int a = lst[j], b = lst[j | js];
-                        lst[j] = kmax(a, b);
-                        lst[j | js] = kmin(a, b);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < L; ++j) {
-                    const int o = __shfl_xor_sync(kFullMask, lst[j], stride);
-                    lst[j] = (lane & stride) == 0 ? kmax(lst[j], o) : kmin(lst[j], o);
-                }
-            }
-        }
-    }
-
-    // Merge a sorted-descending 32-chunk (one value per lane, position =
-    // lane) into the list, keeping the K largest.
-    __device__ __forceinline__ void merge_sorted32(int c, int cnt, int lane) {
-        const int rc = __shfl_sync(kFullMask, c, 31 - lane);
-        lst[L - 1] = kmax(lst[L - 1], rc);  // half-cleaner against the reversed chunk
-        bitonic_merge(lane);
-        have = kmin(have + cnt, 32 * L);
-    }
-};
+using WarpList = RegList<L, int>;
 
 // Streaming: every consumer warp owns a ring of kWarpStages shared-memory
 // stages of one 4 KiB tile each and keeps bulk copies of its own next tiles
@@ -413,7 +370,7 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
     const bool use_bmax = (int)G >= k;
 
     WarpList<L> wl;
-    wl.init();
+    wl.init(INT_MIN);
 
     if (warp == kMonitor) {
         // Start value from the array's last 256 elements (keeps sorted

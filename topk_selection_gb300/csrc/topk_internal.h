@@ -66,8 +66,10 @@ cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan);
 cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
                        void* scratch);
 
-// Enqueue the row TopK (one block per row).
-cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx);
+// Enqueue the row TopK.  status: a device word that bounded waits set to
+// kStatusWaitTimeout when they give up (sticky).
+cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
+                        unsigned* status);
 
 // Bookkeeping of the C ABI layer, for entry points defined in other files:
 // record the cudaError_t behind a TOPK_ERR_CUDA, and count a kernel launch.

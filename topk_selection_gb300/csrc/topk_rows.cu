@@ -31,6 +31,7 @@
 
 #include <climits>
 #include <cstdint>
+#include <mutex>
 
 #include "topk_device.cuh"
 #include "topk_internal.h"
@@ -133,8 +134,8 @@ __device__ bool rows_flush(RowBufT& w, int k, int lane) {
 
 template <int B>
 __global__ void __launch_bounds__(kWarps * 32, (B <= 256 ? 4 : 1))
-topk_rows_kernel(const float* __restrict__ in, int cols, int k, float* __restrict__ vals,
-                 int32_t* __restrict__ idx) {
+topk_rows_smem_kernel(const float* __restrict__ in, int cols, int k, float* __restrict__ vals,
+                      int32_t* __restrict__ idx) {
     extern __shared__ __align__(16) u64 smem64[];
     __shared__ u64 s_T;
     __shared__ unsigned s_gmax[kWarps * 32];
@@ -268,18 +269,311 @@ topk_rows_kernel(const float* __restrict__ in, int cols, int k, float* __restric
     }
 }
 
+
+// ------------------------------------------ k <= 128: streamed rows --
+//
+// A persistent grid; every warp takes whole rows (rows gw, gw + W, ... for
+// global warp gw of W) and needs no other warp.  Each warp owns a ring of
+// kRowStages shared-memory stages and keeps bulk copies of its next 4 KiB
+// tiles in flight; its tile stream runs on from one row to the next.
+// Per row:
+//   * start threshold: the k-th largest of 32*GL group maxima of the row's
+//     first tile (disjoint groups of real elements, so at least k elements
+//     of the row reach it);
+//   * every element is compared once, as a float, against the threshold's
+//     score; those that may pass get their exact 64-bit key, and keys above
+//     the warp's threshold are queued and merged 32 at a time into the
+//     warp's sorted register list, whose k-th key raises the threshold;
+//   * the warp writes the row's k best (value, column) pairs.
+constexpr int kRowThreads = kWarps * 32;
+constexpr int kRowStages = 3;                        // tiles in flight per warp
+constexpr int kRowQueue = 160;                       // per-warp key queue (>= 31 + 128)
+constexpr int kRowRingBytes = kWarps * kRowStages * kTileVec * 16;
+
+struct RowGeom {
+    const float* rp;
+    const float4* body;
+    int head, nvec, tail0, ns, tiles;
+};
+
+__device__ __forceinline__ RowGeom row_geom(const float* in, int row, int cols) {
+    RowGeom g;
+    g.rp = in + (size_t)row * (size_t)cols;
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(g.rp);
+    g.head = (int)(((16u - (unsigned)(addr & 15u)) & 15u) >> 2);
+    if (g.head > cols) g.head = cols;
+    g.body = reinterpret_cast<const float4*>(g.rp + g.head);
+    g.nvec = (cols - g.head) >> 2;
+    g.tail0 = g.head + g.nvec * 4;
+    g.ns = g.head + (cols - g.tail0);
+    g.tiles = (g.nvec + kTileVec - 1) / kTileVec;
+    return g;
+}
+
+// Score keys of the largest element of each of a lane's GL groups of kU/GL
+// float4s (0 for a group with no valid vector; vectors u >= nvalid are not
+// valid).
+template <int GL>
+__device__ __forceinline__ void group_max_keys(const float4 (&r)[kU], int nvalid, unsigned (&gk)[GL]) {
+#pragma unroll
+    for (int j = 0; j < GL; ++j) {
+        float fm = -INFINITY;
+        bool nan = false, any = false;
+#pragma unroll
+        for (int u = j * (kU / GL); u < (j + 1) * (kU / GL); ++u) {
+            if (u < nvalid) {
+                fm = fmaxf(fmaxf(fm, r[u].x), fmaxf(r[u].y, fmaxf(r[u].z, r[u].w)));
+                nan |= (r[u].x != r[u].x) | (r[u].y != r[u].y) | (r[u].z != r[u].z) | (r[u].w != r[u].w);
+                any = true;
+            }
+        }
+        gk[j] = !any ? 0u : (nan ? 0xFFFFFFFFu : score_key(__float_as_uint(fm)));
+    }
+}
+
+template <int L>
+__global__ void __launch_bounds__(kRowThreads, 2)
+topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k, float* __restrict__ vals,
+                        int32_t* __restrict__ idx, unsigned* __restrict__ status) {
+    constexpr int GL = L;  // groups per lane for the start threshold: 32*GL >= k
+    extern __shared__ __align__(128) float4 rring[];       // per-warp stages
+    __shared__ __align__(16) u64 s_q[kWarps * kRowQueue];  // key queues
+    __shared__ __align__(8) uint64_t s_bar[kWarps * kRowStages];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kWarps * kRowStages; ++i) mbar_init(&s_bar[i], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    float4* my_ring = rring + (size_t)warp * kRowStages * kTileVec;
+    uint64_t* my_bar = s_bar + warp * kRowStages;
+    u64* q = s_q + warp * kRowQueue;
+    const int W = gridDim.x * kWarps;
+    const int gw = blockIdx.x * kWarps + warp;
+
+    // Issue side of this warp's tile stream (lane 0): the next (row, tile).
+    int it_row = gw, it_t = 0;
+    size_t issued = 0;
+    auto issue_next = [&]() {  // lane 0 only; false when the stream is over
+        while (it_row < rows && it_t >= row_geom(in, it_row, cols).tiles) {
+            it_row += W;
+            it_t = 0;
+        }
+        if (it_row >= rows) return false;
+        const RowGeom g = row_geom(in, it_row, cols);
+        const int base = it_t * kTileVec;
+        const int cnt = g.nvec - base < kTileVec ? g.nvec - base : kTileVec;
+        const int st = (int)(issued % kRowStages);
+        mbar_arrive_expect_tx(&my_bar[st], (uint32_t)cnt * 16u);
+        bulk_copy_g2s(my_ring + (size_t)st * kTileVec, g.body + base, (uint32_t)cnt * 16u, &my_bar[st]);
+        ++issued;
+        ++it_t;
+        return true;
+    };
+    if (lane == 0)
+        for (int i = 0; i < kRowStages; ++i)
+            if (!issue_next()) break;
+    size_t consumed = 0;
+    bool failed = false;
+
+    for (int row = gw; row < rows; row += W) {
+        const RowGeom g = row_geom(in, row, cols);
+        RegList<L, u64> wl;
+        wl.init(0ull);
+        u64 T = 0ull;  // only keys above T are kept
+        int nq = 0;
+        auto drain = [&](bool all_of_it) {
+            while (nq >= 32 || (all_of_it && nq > 0)) {
+                const int c = nq >= 32 ? 32 : nq;
+                __syncwarp();
+                const u64 x = lane < c ? q[nq - c + lane] : 0ull;
+                __syncwarp();
+                nq -= c;
+                u64 one[1] = {x};
+                warp_sort_desc<1>(one, lane);
+                wl.merge_sorted32(one[0], c, lane);
+            }
+            if (wl.have >= k) T = kmax(T, warp_sorted_at<L>(wl.lst, k - 1));
+        };
+        auto admit = [&](bool has, float v, unsigned col, float tf) {
+            bool p = false;
+            u64 key = 0ull;
+            if (has && maybe(v, tf)) {
+                key = full_key(v, col);
+                p = key > T;
+            }
+            const unsigned m = __ballot_sync(kFullMask, p);
+            if (p) q[nq + __popc(m & lanemask_lt())] = key;
+            nq += __popc(m);
+        };
+
+        // Scalars outside the aligned body (fewer than 8).
+        {
+            const int col = lane < g.head ? lane : g.tail0 + (lane - g.head);
+            const bool has = lane < g.ns;
+            admit(has, has ? g.rp[col] : 0.f, (unsigned)col, -INFINITY);
+        }
+
+        for (int t = 0; t < g.tiles; ++t) {
+            const int stg = (int)(consumed % kRowStages);
+            if (!failed && !mbar_wait(&my_bar[stg], (uint32_t)((consumed / kRowStages) & 1))) {
+                if (lane == 0) atomicOr(status, kStatusWaitTimeout);
+                failed = true;
+            }
+            const int base = t * kTileVec;
+            const int cnt = g.nvec - base < kTileVec ? g.nvec - base : kTileVec;
+            const float4* st = my_ring + (size_t)stg * kTileVec;
+            const int nvalid = cnt > lane ? (cnt - lane + 31) / 32 : 0;  // valid vectors u < nvalid
+
+            if (t == 0) {
+                // Start threshold: k-th largest group maximum of the first tile.
+                float4 r[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+                    r[u] = u < nvalid ? st[u * 32 + lane] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                unsigned gk[GL];
+                group_max_keys<GL>(r, nvalid, gk);
+                warp_sort_desc<GL>(gk, lane);
+                const unsigned seed = warp_sorted_at<GL>(gk, k - 1);
+                T = kmax(T, (u64)seed << 32);  // keeps every key with score >= seed
+            }
+
+            // Fast pass: which of the lane's vectors hold an element that may
+            // beat the threshold (float compare; NaN always may).
+            const float tf = key_float((unsigned)(T >> 32));
+            unsigned slots = 0u;
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                if (u < nvalid) {
+                    const float4 v = st[u * 32 + lane];
+                    if (maybe(v.x, tf) | maybe(v.y, tf) | maybe(v.z, tf) | maybe(v.w, tf)) slots |= 1u << u;
+                }
+            }
+            // Slow pass over the flagged vectors, read again from the stage.
+            unsigned todo = __reduce_or_sync(kFullMask, slots);
+#pragma unroll 1
+            while (todo) {
+                const int u = __ffs(todo) - 1;
+                todo &= todo - 1;
+                // Pass bits of the lane's 4 elements of vector u.
+                unsigned bits = 0u;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                const unsigned c0 = (unsigned)(g.head + (base + u * 32 + lane) * 4);
+                if (slots & (1u << u)) {
+                    v = st[u * 32 + lane];
+                    if (maybe(v.x, tf) && full_key(v.x, c0 + 0) > T) bits |= 1u;
+                    if (maybe(v.y, tf) && full_key(v.y, c0 + 1) > T) bits |= 2u;
+                    if (maybe(v.z, tf) && full_key(v.z, c0 + 2) > T) bits |= 4u;
+                    if (maybe(v.w, tf) && full_key(v.w, c0 + 3) > T) bits |= 8u;
+                }
+                const int c = __popc(bits);
+                // Warp-wide exclusive prefix of the per-lane counts (0..4),
+                // from one ballot per bit of the count.
+                const unsigned b0 = __ballot_sync(kFullMask, c & 1), b1 = __ballot_sync(kFullMask, c & 2),
+                               b2 = __ballot_sync(kFullMask, c & 4);
+                const unsigned lt = lanemask_lt();
+                const int off = __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
+                const int total = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
+                if (bits) {
+                    int o = nq + off;
+                    if (bits & 1u) q[o++] = full_key(v.x, c0 + 0);
+                    if (bits & 2u) q[o++] = full_key(v.y, c0 + 1);
+                    if (bits & 4u) q[o++] = full_key(v.z, c0 + 2);
+                    if (bits & 8u) q[o++] = full_key(v.w, c0 + 3);
+                }
+                nq += total;
+                if (nq >= 32) drain(false);
+            }
+            __syncwarp();
+            ++consumed;
+            if (lane == 0 && !failed) {
+                fence_proxy_async_smem();
+                issue_next();
+            }
+        }
+        drain(true);
+
+        // The row's k best.  The key gives the value back exactly except for
+        // -0.0 (keyed as +0.0) and NaN payloads: those are read from the row.
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+            const int p = j * 32 + lane;
+            if (p < k) {
+                const u64 key = wl.lst[j];
+                const unsigned col = 0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull);
+                const unsigned u = (unsigned)(key >> 32);
+                float v;
+                if (col >= (unsigned)cols)
+                    v = __int_as_float(0x7fc00000);  // unreachable: every list entry is a real element
+                else if (u == 0x80000000u || u == 0xFFFFFFFFu)
+                    v = g.rp[col];
+                else
+                    v = key_float(u);
+                vals[(size_t)row * k + p] = v;
+                idx[(size_t)row * k + p] = (int32_t)col;
+            }
+        }
+    }
+    // After a wait gave up, let the copies still in flight land before exit.
+    if (lane == 0)
+        for (size_t c = consumed; c < issued; ++c)
+            if (!mbar_wait(&my_bar[c % kRowStages], (uint32_t)((c / kRowStages) & 1))) break;
+}
+
 }  // namespace
 
-cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx) {
+template <int L>
+cudaError_t launch_stream(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
+                          unsigned* status) {
+    constexpr int kMaxDev = 64;
+    static std::mutex mu;
+    static int grid_cache[kMaxDev] = {};
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return e;
+    if (device < 0 || device >= kMaxDev) return cudaErrorInvalidDevice;
+    const void* fn = reinterpret_cast<const void*>(&topk_rows_stream_kernel<L>);
+    int full;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (grid_cache[device] == 0) {
+            int sms = 0, per_sm = 0;
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowRingBytes);
+            if (e != cudaSuccess) return e;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kRowThreads, kRowRingBytes);
+            if (e != cudaSuccess) return e;
+            grid_cache[device] = sms * (per_sm < 1 ? 1 : per_sm);
+        }
+        full = grid_cache[device];
+    }
+    const int want = (rows + kWarps - 1) / kWarps;
+    const int grid = want < full ? want : full;
+    topk_rows_stream_kernel<L><<<grid, kRowThreads, kRowRingBytes, s>>>(in, rows, cols, k, vals, idx, status);
+    return cudaGetLastError();
+}
+
+cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
+                        unsigned* status) {
+    // k <= 128 streams (one warp per row); k > 128 uses one block per row
+    // with shared-memory buffers.
+    const bool stream = k <= 128;
+    if (stream && k <= 32) return launch_stream<1>(s, in, rows, cols, k, vals, idx, status);
+    if (stream && k <= 64) return launch_stream<2>(s, in, rows, cols, k, vals, idx, status);
+    if (stream) return launch_stream<4>(s, in, rows, cols, k, vals, idx, status);
+    const size_t smem = (size_t)kWarps * 2048 * sizeof(u64);
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&topk_rows_smem_kernel<2048>),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     if (k <= 128) {
-        const size_t smem = (size_t)kWarps * 256 * sizeof(u64);
-        topk_rows_kernel<256><<<rows, kWarps * 32, smem, s>>>(in, cols, k, vals, idx);
+        const size_t smem256 = (size_t)kWarps * 256 * sizeof(u64);
+        topk_rows_smem_kernel<256><<<rows, kWarps * 32, smem256, s>>>(in, cols, k, vals, idx);
     } else {
-        const size_t smem = (size_t)kWarps * 2048 * sizeof(u64);
-        cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&topk_rows_kernel<2048>),
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        topk_rows_kernel<2048><<<rows, kWarps * 32, smem, s>>>(in, cols, k, vals, idx);
+        topk_rows_smem_kernel<2048><<<rows, kWarps * 32, smem, s>>>(in, cols, k, vals, idx);
     }
     return cudaGetLastError();
 }

@@ -385,36 +385,62 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
         wl.init(0ull);
         u64 T = 0ull;  // only keys above T are kept
         int nq = 0;
+        // The queue holds raw (value bits << 32 | column) entries that beat
+        // the threshold when they were queued.  A drain turns 32 of them into
+        // exact keys, drops those no longer above T, and merges the rest.
         auto drain = [&](bool all_of_it) {
             while (nq >= 32 || (all_of_it && nq > 0)) {
                 const int c = nq >= 32 ? 32 : nq;
                 __syncwarp();
-                const u64 x = lane < c ? q[nq - c + lane] : 0ull;
+                const u64 raw = lane < c ? q[nq - c + lane] : 0ull;
                 __syncwarp();
                 nq -= c;
-                u64 one[1] = {x};
-                warp_sort_desc<1>(one, lane);
-                wl.merge_sorted32(one[0], c, lane);
+                u64 key = 0ull;
+                if (lane < c) key = full_key(__uint_as_float((unsigned)(raw >> 32)), (unsigned)raw);
+                if (key <= T) key = 0ull;
+                const unsigned m = __ballot_sync(kFullMask, key != 0ull);
+                if (m) {
+                    u64 one[1] = {key};
+                    warp_sort_desc<1>(one, lane);
+                    wl.merge_sorted32(one[0], __popc(m), lane);
+                    if (wl.have >= k) T = kmax(T, warp_sorted_at<L>(wl.lst, k - 1));
+                }
             }
-            if (wl.have >= k) T = kmax(T, warp_sorted_at<L>(wl.lst, k - 1));
         };
-        auto admit = [&](bool has, float v, unsigned col, float tf) {
-            bool p = false;
-            u64 key = 0ull;
-            if (has && maybe(v, tf)) {
-                key = full_key(v, col);
-                p = key > T;
+        // Queue a lane's elements that may beat T, given T's score as a
+        // float (tf) and T's column (tc): greater than tf (or NaN), or equal
+        // to it with a lower column.
+        auto queue4 = [&](bool has, float4 v, unsigned c0, float tf, unsigned tc) {
+            unsigned bits = 0u;
+            if (has) {
+                if (!(v.x <= tf) || (v.x == tf && c0 + 0 < tc)) bits |= 1u;
+                if (!(v.y <= tf) || (v.y == tf && c0 + 1 < tc)) bits |= 2u;
+                if (!(v.z <= tf) || (v.z == tf && c0 + 2 < tc)) bits |= 4u;
+                if (!(v.w <= tf) || (v.w == tf && c0 + 3 < tc)) bits |= 8u;
             }
-            const unsigned m = __ballot_sync(kFullMask, p);
-            if (p) q[nq + __popc(m & lanemask_lt())] = key;
-            nq += __popc(m);
+            const int c = __popc(bits);
+            // Warp-wide exclusive prefix of the counts (0..4): one ballot per bit.
+            const unsigned b0 = __ballot_sync(kFullMask, c & 1), b1 = __ballot_sync(kFullMask, c & 2),
+                           b2 = __ballot_sync(kFullMask, c & 4);
+            if (bits) {
+                const unsigned lt = lanemask_lt();
+                int o = nq + __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
+                if (bits & 1u) q[o++] = ((u64)__float_as_uint(v.x) << 32) | (c0 + 0);
+                if (bits & 2u) q[o++] = ((u64)__float_as_uint(v.y) << 32) | (c0 + 1);
+                if (bits & 4u) q[o++] = ((u64)__float_as_uint(v.z) << 32) | (c0 + 2);
+                if (bits & 8u) q[o++] = ((u64)__float_as_uint(v.w) << 32) | (c0 + 3);
+            }
+            nq += __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
+            if (nq >= 32) drain(false);
         };
 
-        // Scalars outside the aligned body (fewer than 8).
+        // Scalars outside the aligned body (fewer than 8): queued raw.
         {
             const int col = lane < g.head ? lane : g.tail0 + (lane - g.head);
             const bool has = lane < g.ns;
-            admit(has, has ? g.rp[col] : 0.f, (unsigned)col, -INFINITY);
+            const unsigned m = __ballot_sync(kFullMask, has);
+            if (has) q[nq + __popc(m & lanemask_lt())] = ((u64)__float_as_uint(g.rp[col]) << 32) | (unsigned)col;
+            nq += __popc(m);
         }
 
         for (int t = 0; t < g.tiles; ++t) {
@@ -442,14 +468,18 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
             }
 
             // Fast pass: which of the lane's vectors hold an element that may
-            // beat the threshold (float compare; NaN always may).
+            // beat T (by value, or a tie with a lower column).
             const float tf = key_float((unsigned)(T >> 32));
+            const unsigned tc = 0xFFFFFFFFu - (unsigned)T;  // T's column (all columns when T is a bare score)
             unsigned slots = 0u;
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 if (u < nvalid) {
                     const float4 v = st[u * 32 + lane];
-                    if (maybe(v.x, tf) | maybe(v.y, tf) | maybe(v.z, tf) | maybe(v.w, tf)) slots |= 1u << u;
+                    const bool gt = !(v.x <= tf) | !(v.y <= tf) | !(v.z <= tf) | !(v.w <= tf);
+                    const bool eq = (v.x == tf) | (v.y == tf) | (v.z == tf) | (v.w == tf);
+                    const unsigned c0 = (unsigned)(g.head + (base + u * 32 + lane) * 4);
+                    if (gt | (eq & (c0 < tc))) slots |= 1u << u;
                 }
             }
             // Slow pass over the flagged vectors, read again from the stage.
@@ -458,34 +488,11 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
             while (todo) {
                 const int u = __ffs(todo) - 1;
                 todo &= todo - 1;
-                // Pass bits of the lane's 4 elements of vector u.
-                unsigned bits = 0u;
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                const unsigned c0 = (unsigned)(g.head + (base + u * 32 + lane) * 4);
-                if (slots & (1u << u)) {
-                    v = st[u * 32 + lane];
-                    if (maybe(v.x, tf) && full_key(v.x, c0 + 0) > T) bits |= 1u;
-                    if (maybe(v.y, tf) && full_key(v.y, c0 + 1) > T) bits |= 2u;
-                    if (maybe(v.z, tf) && full_key(v.z, c0 + 2) > T) bits |= 4u;
-                    if (maybe(v.w, tf) && full_key(v.w, c0 + 3) > T) bits |= 8u;
-                }
-                const int c = __popc(bits);
-                // Warp-wide exclusive prefix of the per-lane counts (0..4),
-                // from one ballot per bit of the count.
-                const unsigned b0 = __ballot_sync(kFullMask, c & 1), b1 = __ballot_sync(kFullMask, c & 2),
-                               b2 = __ballot_sync(kFullMask, c & 4);
-                const unsigned lt = lanemask_lt();
-                const int off = __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
-                const int total = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
-                if (bits) {
-                    int o = nq + off;
-                    if (bits & 1u) q[o++] = full_key(v.x, c0 + 0);
-                    if (bits & 2u) q[o++] = full_key(v.y, c0 + 1);
-                    if (bits & 4u) q[o++] = full_key(v.z, c0 + 2);
-                    if (bits & 8u) q[o++] = full_key(v.w, c0 + 3);
-                }
-                nq += total;
-                if (nq >= 32) drain(false);
+                const bool has = (slots >> u) & 1u;
+                const float4 v = has ? st[u * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+                // T may have risen in a drain above: queue against the current one.
+                queue4(has, v, (unsigned)(g.head + (base + u * 32 + lane) * 4), key_float((unsigned)(T >> 32)),
+                       0xFFFFFFFFu - (unsigned)T);
             }
             __syncwarp();
             ++consumed;

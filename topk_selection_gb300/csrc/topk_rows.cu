@@ -286,7 +286,7 @@ topk_rows_smem_kernel(const float* __restrict__ in, int cols, int k, float* __re
 //     warp's sorted register list, whose k-th key raises the threshold;
 //   * the warp writes the row's k best (value, column) pairs.
 constexpr int kRowThreads = kWarps * 32;
-constexpr int kRowStages = 3;                        // tiles in flight per warp
+constexpr int kRowStages = 2;                        // tiles in flight per warp
 constexpr int kRowQueue = 160;                       // per-warp key queue (>= 31 + 128)
 constexpr int kRowRingBytes = kWarps * kRowStages * kTileVec * 16;
 
@@ -332,7 +332,7 @@ __device__ __forceinline__ void group_max_keys(const float4 (&r)[kU], int nvalid
 }
 
 template <int L>
-__global__ void __launch_bounds__(kRowThreads, 2)
+__global__ void __launch_bounds__(kRowThreads, 3)
 topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k, float* __restrict__ vals,
                         int32_t* __restrict__ idx, unsigned* __restrict__ status) {
     constexpr int GL = L;  // groups per lane for the start threshold: 32*GL >= k

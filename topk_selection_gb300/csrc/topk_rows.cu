@@ -63,6 +63,13 @@ __device__ __forceinline__ u64 full_key(float v, unsigned col) {
     return ((u64)score_key(__float_as_uint(v)) << 32) | (u64)(0xFFFFFFFFu - col);
 }
 
+// max(a, b) that returns NaN when either is NaN (PTX max.NaN).
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
 // Elements that may beat threshold score tf: v >= tf, or v is NaN.
 __device__ __forceinline__ bool maybe(float v, float tf) { return !(v < tf); }
 
@@ -335,7 +342,7 @@ template <int L>
 __global__ void __launch_bounds__(kRowThreads, 3)
 topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k, float* __restrict__ vals,
                         int32_t* __restrict__ idx, unsigned* __restrict__ status) {
-    constexpr int GL = L;  // groups per lane for the start threshold: 32*GL >= k
+    constexpr int GL = 8;  // groups of 4 elements per lane for the start threshold: 32*GL >= k
     extern __shared__ __align__(128) float4 rring[];       // per-warp stages
     __shared__ __align__(16) u64 s_q[kWarps * kRowQueue];  // key queues
     __shared__ __align__(8) uint64_t s_bar[kWarps * kRowStages];
@@ -354,21 +361,23 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
     const int W = gridDim.x * kWarps;
     const int gw = blockIdx.x * kWarps + warp;
 
-    // Issue side of this warp's tile stream (lane 0): the next (row, tile).
+    // Issue side of this warp's tile stream (lane 0): the next (row, tile),
+    // with the geometry of that row cached.
     int it_row = gw, it_t = 0;
+    RowGeom it_g = row_geom(in, it_row < rows ? it_row : 0, cols);
     size_t issued = 0;
     auto issue_next = [&]() {  // lane 0 only; false when the stream is over
-        while (it_row < rows && it_t >= row_geom(in, it_row, cols).tiles) {
+        while (it_row < rows && it_t >= it_g.tiles) {
             it_row += W;
             it_t = 0;
+            if (it_row < rows) it_g = row_geom(in, it_row, cols);
         }
         if (it_row >= rows) return false;
-        const RowGeom g = row_geom(in, it_row, cols);
         const int base = it_t * kTileVec;
-        const int cnt = g.nvec - base < kTileVec ? g.nvec - base : kTileVec;
+        const int cnt = it_g.nvec - base < kTileVec ? it_g.nvec - base : kTileVec;
         const int st = (int)(issued % kRowStages);
         mbar_arrive_expect_tx(&my_bar[st], (uint32_t)cnt * 16u);
-        bulk_copy_g2s(my_ring + (size_t)st * kTileVec, g.body + base, (uint32_t)cnt * 16u, &my_bar[st]);
+        bulk_copy_g2s(my_ring + (size_t)st * kTileVec, it_g.body + base, (uint32_t)cnt * 16u, &my_bar[st]);
         ++issued;
         ++it_t;
         return true;
@@ -476,10 +485,10 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
             for (int u = 0; u < kU; ++u) {
                 if (u < nvalid) {
                     const float4 v = st[u * 32 + lane];
-                    const bool gt = !(v.x <= tf) | !(v.y <= tf) | !(v.z <= tf) | !(v.w <= tf);
-                    const bool eq = (v.x == tf) | (v.y == tf) | (v.z == tf) | (v.w == tf);
+                    // Largest of the 4, NaN if any is NaN.
+                    const float m = max_nan(max_nan(v.x, v.y), max_nan(v.z, v.w));
                     const unsigned c0 = (unsigned)(g.head + (base + u * 32 + lane) * 4);
-                    if (gt | (eq & (c0 < tc))) slots |= 1u << u;
+                    if (!(m <= tf) || (m == tf && c0 < tc)) slots |= 1u << u;
                 }
             }
             // Slow pass over the flagged vectors, read again from the stage.

@@ -86,26 +86,32 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {
+    "topk_i32_stream_kernel": ("topk_i32.cu", "topk_device.cuh", "topk_internal.h"),
+    "topk_rows_stream_kernel": ("topk_rows.cu", "topk_device.cuh", "topk_internal.h"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources a kernel is built from (its .cu and shared headers)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "topk_selection_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources."""
+    """DRAM bytes (read + write) per launch from the committed ncu summary,
+    if it was taken on the current sources of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
         e = rec[f"{kernel}@{workload}"]
-        if e.get("source_hash") == kernel_source_hash():
+        if e.get("source_hash") == kernel_source_hash(kernel):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -256,8 +262,9 @@ def run_ours(args, world, rank, local):
         "gbs": round(achieved, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                     "traffic": recorded_traffic("topk_i32_kernel", WORKLOAD),
-                     "kernel": "topk_i32_kernel<256,1,16>", "algorithmic_bytes_per_launch": 4 * n},
+                     "traffic": recorded_traffic("topk_i32_stream_kernel", WORKLOAD),
+                     "kernel": "topk_i32_stream_kernel<1,1> (k<=32)", "algorithmic_bytes_per_launch": 4 * n,
+                     "timing": "CUDA events on the launching stream around the timed steps; one launch per step"},
         "e2e": {"value": round(total * e2e_steps / e2e_s / 1e9, 4), "unit": UNIT,
                 "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 4 * K_TOP,
                 "steps": e2e_steps, "matches_device_result": e2e_ok},
@@ -302,7 +309,10 @@ def run_rows(tk, dev, stream, args):
     return {"workload": "fp32 rows 4096x32768 N(0,1) seed 5, 1% ties to row max, k=64",
             "steps": steps, "ms_per_step": round(ms, 5),
             "value": round(rows * cols / (ms / 1e3) / 1e9, 3), "unit": UNIT,
-            "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "kernel": "topk_rows_stream_kernel<2> (k<=64)",
+                         "algorithmic_bytes_per_launch": rows * cols * 4 + rows * k * 8,
+                         "traffic": recorded_traffic("topk_rows_stream_kernel", "rows_4096x32768_k64_tied")}}
 
 
 def cpu_baseline_leg(x: np.ndarray, gpu_result: np.ndarray):
@@ -331,7 +341,7 @@ def run_reference(args, world, rank):
     t0 = time.perf_counter()
     oracle.topk_i32(probe, K_TOP)
     rate = probe.size / (time.perf_counter() - t0)
-    budget = min(10.0, 120.0 / max(1, args.steps + args.warmup))
+    budget = min(10.0, args.ref_budget_s / max(1, args.steps + args.warmup))
     m = int(min(n, max(10_000, rate * budget)))
     x = synth.i32_uniform(m, 2)  # the first m elements of the workload's input
     for _ in range(args.warmup):
@@ -363,6 +373,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-cpu", action="store_true", help="leave out the CPU-baseline leg")
     ap.add_argument("--skip-rows", action="store_true", help="leave out the row-TopK measurement")
+    ap.add_argument("--ref-budget-s", type=float, default=120.0,
+                    help="--impl reference: seconds of oracle work for the whole run (sets the sample size)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

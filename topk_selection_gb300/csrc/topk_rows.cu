@@ -279,9 +279,10 @@ topk_rows_smem_kernel(const float* __restrict__ in, int cols, int k, float* __re
 
 // ------------------------------------------ k <= 128: streamed rows --
 //
-// A persistent grid; every warp takes whole rows (rows gw, gw + W, ... for
+// A persistent grid of 3 blocks of 9 warps per SM, so that 4096 rows get one
+// warp each on 152 SMs; every warp takes whole rows (rows gw, gw + W, ... for
 // global warp gw of W) and needs no other warp.  Each warp owns a ring of
-// kRowStages shared-memory stages and keeps bulk copies of its next 4 KiB
+// kRowStages shared-memory stages and keeps bulk copies of its next 3 KiB
 // tiles in flight; its tile stream runs on from one row to the next.
 // Per row:
 //   * start threshold: the k-th largest of 32*GL group maxima of the row's
@@ -292,10 +293,13 @@ topk_rows_smem_kernel(const float* __restrict__ in, int cols, int k, float* __re
 //     the warp's threshold are queued and merged 32 at a time into the
 //     warp's sorted register list, whose k-th key raises the threshold;
 //   * the warp writes the row's k best (value, column) pairs.
-constexpr int kRowThreads = kWarps * 32;
+constexpr int kRowWarps = 9;                         // 3 blocks x 9 warps = 27 warps per SM
+constexpr int kRowThreads = kRowWarps * 32;
+constexpr int kRowU = 6;                             // 16-byte vectors per lane per tile
+constexpr int kRowTileVec = 32 * kRowU;              // 3 KiB tiles
 constexpr int kRowStages = 2;                        // tiles in flight per warp
 constexpr int kRowQueue = 160;                       // per-warp key queue (>= 31 + 128)
-constexpr int kRowRingBytes = kWarps * kRowStages * kTileVec * 16;
+constexpr int kRowRingBytes = kRowWarps * kRowStages * kRowTileVec * 16;
 
 struct RowGeom {
     const float* rp;
@@ -313,21 +317,21 @@ __device__ __forceinline__ RowGeom row_geom(const float* in, int row, int cols) 
     g.nvec = (cols - g.head) >> 2;
     g.tail0 = g.head + g.nvec * 4;
     g.ns = g.head + (cols - g.tail0);
-    g.tiles = (g.nvec + kTileVec - 1) / kTileVec;
+    g.tiles = (g.nvec + kRowTileVec - 1) / kRowTileVec;
     return g;
 }
 
-// Score keys of the largest element of each of a lane's GL groups of kU/GL
+// Score keys of the largest element of each of a lane's GL groups of kRowU/GL
 // float4s (0 for a group with no valid vector; vectors u >= nvalid are not
 // valid).
 template <int GL>
-__device__ __forceinline__ void group_max_keys(const float4 (&r)[kU], int nvalid, unsigned (&gk)[GL]) {
+__device__ __forceinline__ void group_max_keys(const float4 (&r)[kRowU], int nvalid, unsigned (&gk)[GL]) {
 #pragma unroll
     for (int j = 0; j < GL; ++j) {
         float fm = -INFINITY;
         bool nan = false, any = false;
 #pragma unroll
-        for (int u = j * (kU / GL); u < (j + 1) * (kU / GL); ++u) {
+        for (int u = j * (kRowU / GL); u < (j + 1) * (kRowU / GL); ++u) {
             if (u < nvalid) {
                 fm = fmaxf(fmaxf(fm, r[u].x), fmaxf(r[u].y, fmaxf(r[u].z, r[u].w)));
                 nan |= (r[u].x != r[u].x) | (r[u].y != r[u].y) | (r[u].z != r[u].z) | (r[u].w != r[u].w);
@@ -342,24 +346,24 @@ template <int L>
 __global__ void __launch_bounds__(kRowThreads, 3)
 topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k, float* __restrict__ vals,
                         int32_t* __restrict__ idx, unsigned* __restrict__ status) {
-    constexpr int GL = 8;  // groups of 4 elements per lane for the start threshold: 32*GL >= k
+    constexpr int GL = kRowU;  // groups of 4 elements per lane for the start threshold: 32*GL >= k
     extern __shared__ __align__(128) float4 rring[];       // per-warp stages
-    __shared__ __align__(16) u64 s_q[kWarps * kRowQueue];  // key queues
-    __shared__ __align__(8) uint64_t s_bar[kWarps * kRowStages];
+    __shared__ __align__(16) u64 s_q[kRowWarps * kRowQueue];  // key queues
+    __shared__ __align__(8) uint64_t s_bar[kRowWarps * kRowStages];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kWarps * kRowStages; ++i) mbar_init(&s_bar[i], 1);
+        for (int i = 0; i < kRowWarps * kRowStages; ++i) mbar_init(&s_bar[i], 1);
         mbar_init_fence();
     }
     __syncthreads();
 
-    float4* my_ring = rring + (size_t)warp * kRowStages * kTileVec;
+    float4* my_ring = rring + (size_t)warp * kRowStages * kRowTileVec;
     uint64_t* my_bar = s_bar + warp * kRowStages;
     u64* q = s_q + warp * kRowQueue;
-    const int W = gridDim.x * kWarps;
-    const int gw = blockIdx.x * kWarps + warp;
+    const int W = gridDim.x * kRowWarps;
+    const int gw = blockIdx.x * kRowWarps + warp;
 
     // Issue side of this warp's tile stream (lane 0): the next (row, tile),
     // with the geometry of that row cached.
@@ -373,11 +377,11 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
             if (it_row < rows) it_g = row_geom(in, it_row, cols);
         }
         if (it_row >= rows) return false;
-        const int base = it_t * kTileVec;
-        const int cnt = it_g.nvec - base < kTileVec ? it_g.nvec - base : kTileVec;
+        const int base = it_t * kRowTileVec;
+        const int cnt = it_g.nvec - base < kRowTileVec ? it_g.nvec - base : kRowTileVec;
         const int st = (int)(issued % kRowStages);
         mbar_arrive_expect_tx(&my_bar[st], (uint32_t)cnt * 16u);
-        bulk_copy_g2s(my_ring + (size_t)st * kTileVec, it_g.body + base, (uint32_t)cnt * 16u, &my_bar[st]);
+        bulk_copy_g2s(my_ring + (size_t)st * kRowTileVec, it_g.body + base, (uint32_t)cnt * 16u, &my_bar[st]);
         ++issued;
         ++it_t;
         return true;
@@ -458,16 +462,16 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
                 if (lane == 0) atomicOr(status, kStatusWaitTimeout);
                 failed = true;
             }
-            const int base = t * kTileVec;
-            const int cnt = g.nvec - base < kTileVec ? g.nvec - base : kTileVec;
-            const float4* st = my_ring + (size_t)stg * kTileVec;
+            const int base = t * kRowTileVec;
+            const int cnt = g.nvec - base < kRowTileVec ? g.nvec - base : kRowTileVec;
+            const float4* st = my_ring + (size_t)stg * kRowTileVec;
             const int nvalid = cnt > lane ? (cnt - lane + 31) / 32 : 0;  // valid vectors u < nvalid
 
             if (t == 0) {
                 // Start threshold: k-th largest group maximum of the first tile.
-                float4 r[kU];
+                float4 r[kRowU];
 #pragma unroll
-                for (int u = 0; u < kU; ++u)
+                for (int u = 0; u < kRowU; ++u)
                     r[u] = u < nvalid ? st[u * 32 + lane] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
                 unsigned gk[GL];
                 group_max_keys<GL>(r, nvalid, gk);
@@ -482,7 +486,7 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
             const unsigned tc = 0xFFFFFFFFu - (unsigned)T;  // T's column (all columns when T is a bare score)
             unsigned slots = 0u;
 #pragma unroll
-            for (int u = 0; u < kU; ++u) {
+            for (int u = 0; u < kRowU; ++u) {
                 if (u < nvalid) {
                     const float4 v = st[u * 32 + lane];
                     // Largest of the 4, NaN if any is NaN.
@@ -567,7 +571,7 @@ cudaError_t launch_stream(cudaStream_t s, const float* in, int rows, int cols, i
         }
         full = grid_cache[device];
     }
-    const int want = (rows + kWarps - 1) / kWarps;
+    const int want = (rows + kRowWarps - 1) / kRowWarps;
     const int grid = want < full ? want : full;
     topk_rows_stream_kernel<L><<<grid, kRowThreads, kRowRingBytes, s>>>(in, rows, cols, k, vals, idx, status);
     return cudaGetLastError();

@@ -495,17 +495,68 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
                     if (!(m <= tf) || (m == tf && c0 < tc)) slots |= 1u << u;
                 }
             }
-            // Slow pass over the flagged vectors, read again from the stage.
-            unsigned todo = __reduce_or_sync(kFullMask, slots);
+            // Slow pass: each lane checks its flagged vectors (read again from
+            // the stage) exactly against T, one warp-wide prefix of the
+            // per-lane counts (0..4*kRowU, one ballot per bit) places every
+            // candidate of the tile in the queue at once.
+            if (__any_sync(kFullMask, slots != 0u)) {
+                const float tf2 = key_float((unsigned)(T >> 32));
+                const unsigned tc2 = 0xFFFFFFFFu - (unsigned)T;
+                unsigned pass[kRowU];
+                int c = 0;
+#pragma unroll
+                for (int u = 0; u < kRowU; ++u) {
+                    pass[u] = 0u;
+                    if ((slots >> u) & 1u) {
+                        const float4 v = st[u * 32 + lane];
+                        const unsigned c0 = (unsigned)(g.head + (base + u * 32 + lane) * 4);
+                        unsigned bits = 0u;
+                        if (!(v.x <= tf2) || (v.x == tf2 && c0 + 0 < tc2)) bits |= 1u;
+                        if (!(v.y <= tf2) || (v.y == tf2 && c0 + 1 < tc2)) bits |= 2u;
+                        if (!(v.z <= tf2) || (v.z == tf2 && c0 + 2 < tc2)) bits |= 4u;
+                        if (!(v.w <= tf2) || (v.w == tf2 && c0 + 3 < tc2)) bits |= 8u;
+                        pass[u] = bits;
+                        c += __popc(bits);
+                    }
+                }
+                const unsigned lt = lanemask_lt();
+                int off = 0, total = 0;
+#pragma unroll
+                for (int bit = 0; bit < 5; ++bit) {
+                    const unsigned bb = __ballot_sync(kFullMask, (c >> bit) & 1);
+                    off += __popc(bb & lt) << bit;
+                    total += __popc(bb) << bit;
+                }
+                if (nq + total <= kRowQueue) {
+                    int o = nq + off;
+#pragma unroll
+                    for (int u = 0; u < kRowU; ++u) {
+                        if (pass[u]) {
+                            const float4 v = st[u * 32 + lane];
+                            const unsigned c0 = (unsigned)(g.head + (base + u * 32 + lane) * 4);
+                            if (pass[u] & 1u) q[o++] = ((u64)__float_as_uint(v.x) << 32) | (c0 + 0);
+                            if (pass[u] & 2u) q[o++] = ((u64)__float_as_uint(v.y) << 32) | (c0 + 1);
+                            if (pass[u] & 4u) q[o++] = ((u64)__float_as_uint(v.z) << 32) | (c0 + 2);
+                            if (pass[u] & 8u) q[o++] = ((u64)__float_as_uint(v.w) << 32) | (c0 + 3);
+                        }
+                    }
+                    nq += total;
+                    if (nq >= 32) drain(false);
+                } else {
+                    // Too many for the queue at once (a weak threshold early in
+                    // a row): one flagged vector at a time, draining between.
+                    unsigned todo = __reduce_or_sync(kFullMask, slots);
 #pragma unroll 1
-            while (todo) {
-                const int u = __ffs(todo) - 1;
-                todo &= todo - 1;
-                const bool has = (slots >> u) & 1u;
-                const float4 v = has ? st[u * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-                // T may have risen in a drain above: queue against the current one.
-                queue4(has, v, (unsigned)(g.head + (base + u * 32 + lane) * 4), key_float((unsigned)(T >> 32)),
-                       0xFFFFFFFFu - (unsigned)T);
+                    while (todo) {
+                        const int u = __ffs(todo) - 1;
+                        todo &= todo - 1;
+                        const bool has = (slots >> u) & 1u;
+                        const float4 v = has ? st[u * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        // T may have risen in a drain above: queue against the current one.
+                        queue4(has, v, (unsigned)(g.head + (base + u * 32 + lane) * 4),
+                               key_float((unsigned)(T >> 32)), 0xFFFFFFFFu - (unsigned)T);
+                    }
+                }
             }
             __syncwarp();
             ++consumed;

@@ -48,14 +48,17 @@ struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
 enum topk_status {
     TOPK_OK = 0,
     TOPK_ERR_INVALID_ARG = 1, /* null pointer, n == 0, k < 1, k > n, rows < 1, cols < k, overlap */
-    TOPK_ERR_UNSUPPORTED = 2, /* k > TOPK_MAX_K, or a size the kernels do not take */
+    TOPK_ERR_UNSUPPORTED = 2, /* k above TOPK_MAX_K / TOPK_MAX_K_ROWS, or a size the kernels do not take */
     TOPK_ERR_NO_MEMORY = 3,   /* workspace or staging allocation failed */
     TOPK_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed; see topk_last_cuda_error() */
     TOPK_ERR_DEVICE_TIMEOUT = 5 /* a kernel's bounded wait gave up; its results are not valid */
 };
 
-/* Largest k accepted by either operation. */
-#define TOPK_MAX_K 1024
+/* Largest k accepted by topk_i32 (and topk_i32_noalloc). */
+#define TOPK_MAX_K 32768
+
+/* Largest k accepted by topk_rows_f32. */
+#define TOPK_MAX_K_ROWS 1024
 
 /*
  * topk_i32 -- the k largest values of in[0..n), written to out[0..k) in
@@ -67,10 +70,11 @@ enum topk_status {
  *   k      1 <= k <= min(n, TOPK_MAX_K).
  *   out    int32[k], written.
  *
- * Work is two passes over the data on the GPU: every block filters its share
- * of the input against a running k-th-value threshold and leaves k
- * candidates; the last block to finish merges the candidates (section 2.2's
- * second pass, fused into the same launch).
+ * k <= 128: one launch.  Every block filters its share of the input against
+ * a running k-th-value threshold and leaves k candidates; the last block to
+ * finish merges the candidates (section 2.2's second pass, fused into the
+ * same launch).  k > 128: radix select in four launches (two or three
+ * passes over the input, then one block that sorts the answer).
  *
  * Returns TOPK_OK or an error code; on error nothing is written to out.
  */
@@ -89,7 +93,7 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
  *   in     float32[rows * cols], row-major, read-only.
  *   rows   1 <= rows <= 2^31 - 1.
  *   cols   k <= cols <= 2^31 - 1.
- *   k      1 <= k <= min(cols, TOPK_MAX_K).
+ *   k      1 <= k <= min(cols, TOPK_MAX_K_ROWS).
  *   vals   float32[rows * k], written.
  *   idx    int32[rows * k], written.
  *
@@ -116,9 +120,12 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
  *     TOPK_NOALLOC_SCRATCH_BYTES (1 MiB): control words, per-block maxima
  *     and per-block candidates.  Every GPU that loads the library holds it
  *     until the process exits.  k above TOPK_MAX_K is rejected with
- *     TOPK_ERR_UNSUPPORTED.  The grid is cut so that every block's
- *     candidate lists fit (1 MiB holds 246 blocks' worth), so on GPUs with
- *     more SMs this entry point runs fewer blocks than topk_i32.
+ *     TOPK_ERR_UNSUPPORTED.  For k <= 128 the grid is cut so that every
+ *     block's candidate lists fit (1 MiB holds 243 blocks' worth), so on
+ *     GPUs with more SMs this entry point runs fewer blocks than topk_i32;
+ *     for larger k the radix select's boundary buffer is what the array has
+ *     left (about 225K keys at k = 32768), so inputs whose k-th value shares
+ *     its top 12 bits with more keys than that take one more pass.
  *   - Every call uses the same array.  Each call clears the control words
  *     on `stream` before its launch, but calls whose work overlaps on the
  *     GPU (different streams, or different host threads without ordering)

@@ -68,7 +68,7 @@ A, B, C = 0x10000000, 0x20000000, 0x30000000
     ((A + 2, 100, 5, B), 1),      # misaligned input
     ((A, 100, 5, B + 1), 1),      # misaligned output
     ((A, 100, 5, A + 40), 1),     # output overlaps input
-    ((A, 5000, 1025, B), 2),      # k above the maximum
+    ((A, 40000, 32769, B), 2),    # k above the maximum
     ((B, (1 << 40) + 4, 5, A), 2),  # n above the maximum
 ])
 def test_topk_i32_argument_errors(lib, args, status):
@@ -87,7 +87,7 @@ def test_topk_i32_argument_errors(lib, args, status):
     ((A, 4, 8, 9, B, C), 1),        # k > cols
     ((A, 4, 8, 2, B, B + 8), 1),    # vals and idx overlap
     ((A, 4, 8, 2, A + 4, C), 1),    # vals overlaps the input
-    ((A, 4, 2048, 1025, B, C), 2),  # k above the maximum
+    ((A, 4, 2048, 1025, B, C), 2),  # k above the row maximum
 ])
 def test_topk_rows_argument_errors(lib, args, status):
     import topk_selection_gb300 as tk
@@ -127,3 +127,11 @@ def test_set_option_validation(lib):
     assert tk._lib.topk_set_option(99, 0) == 1
     assert tk._lib.topk_set_option(tk.OPT_STAGE2_CAP, 64) == 0
     assert tk._lib.topk_set_option(tk.OPT_STAGE2_CAP, 0) == 0
+
+
+def test_header_limits_match_binding(lib):
+    import topk_selection_gb300 as tk
+
+    text = open(os.path.join(ROOT, "include", "topk.h")).read()
+    assert re.search(r"#define TOPK_MAX_K\s+%d\b" % tk.MAX_K, text)
+    assert re.search(r"#define TOPK_MAX_K_ROWS\s+%d\b" % tk.MAX_K_ROWS, text)

@@ -116,6 +116,37 @@ def test_second_stage_radix_select_path(tk, cap):
         tk.set_option(tk.OPT_STAGE2_CAP, 0)
 
 
+@pytest.mark.parametrize("kind,n", [("uniform", 1_000_003), ("dups", 2_000_003), ("few", 2_000_003),
+                                    ("ascending", 3_000_000), ("descending", 999_999), ("equal", 400_000),
+                                    ("int_min", 300_007), ("negative", 1_500_001), ("sawtooth", 1_234_567),
+                                    ("int_max_heavy", 700_001)])
+def test_large_k_radix_select(tk, kind, n):
+    # k > 128: radix select.  "dups" and "few" put more than the boundary
+    # buffer holds into one top-12-bit bucket, so they take the 3-pass path.
+    x = make(kind, n, seed=n)
+    for k in (129, 1000, 4096, 32768):
+        assert np.array_equal(gpu_topk(tk, x, k), oracle.topk_i32(x, k)), (kind, n, k)
+
+
+def test_large_k_full_sort_and_edges(tk):
+    for n, k in ((129, 129), (32768, 32768), (40000, 32768), (1025, 1000), (5000, 4097)):
+        x = make("uniform", n, seed=n + k)
+        assert np.array_equal(gpu_topk(tk, x, k), oracle.topk_i32(x, k)), (n, k)
+    x = make("uniform", 300_007, seed=5)
+    for offset in (1, 2, 3):
+        assert np.array_equal(gpu_topk(tk, x, 777, offset=offset), oracle.topk_i32(x, 777))
+
+
+def test_plans_alternate_on_one_workspace(tk):
+    # The streaming plan (k <= 128) and the radix plan (k > 128) share the
+    # workspace of a stream; each must leave it as the other expects.
+    x = make("uniform", 2_000_003, seed=9)
+    y = make("dups", 1_000_003, seed=10)
+    for k in (20, 500, 64, 2000, 1, 129, 128):
+        for v in (x, y):
+            assert np.array_equal(gpu_topk(tk, v, k), oracle.topk_i32(v, k)), k
+
+
 def test_back_to_back_calls_reset_state(tk):
     # The control words are reset by each launch: a large threshold left by a
     # call must not leak into the next call on the same stream.

@@ -55,7 +55,7 @@ def test_noalloc_matches_topk_i32_on_two_calls_in_a_row(entry):
 def test_noalloc_large_k_and_small_input(entry):
     tk, f = entry
     stream = torch.cuda.current_stream()
-    for n, k in ((5, 3), (100_003, 1024), (4_194_311, 1000)):
+    for n, k in ((5, 3), (100_003, 1024), (4_194_311, 1000), (3_000_017, 32768)):
         x = torch.from_numpy(synth.i32_uniform(n, n)).cuda()
         for _ in range(2):
             got = run_noalloc(f, x, k, stream)
@@ -67,7 +67,8 @@ def test_noalloc_large_k_and_small_input(entry):
 def test_noalloc_rejects_what_it_cannot_take(entry):
     tk, f = entry
     x = torch.zeros(5000, dtype=torch.int32, device="cuda")
-    out = torch.empty(1025, dtype=torch.int32, device="cuda")
-    assert f(x.data_ptr(), 5000, 1025, out.data_ptr(), None) == 2  # k above the maximum
+    x2 = torch.zeros(40000, dtype=torch.int32, device="cuda")
+    out = torch.empty(32769, dtype=torch.int32, device="cuda")
+    assert f(x2.data_ptr(), 40000, 32769, out.data_ptr(), None) == 2  # k above the maximum
     xh = torch.zeros(5000, dtype=torch.int32)
     assert f(xh.data_ptr(), 5000, 20, out.data_ptr(), None) == 1   # host input: would need staging

@@ -21,11 +21,12 @@ import torch
 
 from . import build as _build
 
-__all__ = ["topk_i32", "topk_rows_f32", "topk_i32_ptr", "topk_rows_f32_ptr", "TopKError", "MAX_K",
+__all__ = ["topk_i32", "topk_rows_f32", "topk_i32_ptr", "topk_rows_f32_ptr", "TopKError", "MAX_K", "MAX_K_ROWS",
            "status_string", "release_workspace", "launch_count", "last_cuda_error", "library_path",
            "check_stream", "set_option", "OPT_STAGE2_CAP"]
 
-MAX_K = 1024
+MAX_K = 32768       # topk_i32
+MAX_K_ROWS = 1024   # topk_rows_f32
 (TOPK_OK, TOPK_ERR_INVALID_ARG, TOPK_ERR_UNSUPPORTED, TOPK_ERR_NO_MEMORY, TOPK_ERR_CUDA,
  TOPK_ERR_DEVICE_TIMEOUT) = range(6)
 

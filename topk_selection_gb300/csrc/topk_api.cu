@@ -65,7 +65,7 @@ int workspace(cudaStream_t s, int device, size_t ctrl_cand, size_t in_bytes, siz
         if (rc != TOPK_OK) return rc;
         // The control words and block-maximum slots must start at zero; the
         // kernels leave them so.
-        cudaError_t e = cudaMemsetAsync(w.ctrl_cand, 0, topk::kI32ResetEnd, s);
+        cudaError_t e = cudaMemsetAsync(w.ctrl_cand, 0, topk::kI32ResetEnd, s);  // status word included
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (in_bytes) {
@@ -129,9 +129,12 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
     if (rc != TOPK_OK) return rc;
 
     topk::I32Plan plan;
-    e = topk::i32_plan(device, n, k, &plan);
+    e = topk::i32_plan(device, n, k <= 128 ? k : 128, &plan);
     if (e != cudaSuccess) return cuda_fail(e);
-    const size_t ctrl_cand = topk::i32_scratch_bytes(plan.max_grid);
+    // One workspace serves both plans (k <= 128 streams; larger k use radix select).
+    size_t ctrl_cand = topk::i32_scratch_bytes(plan.max_grid);
+    const size_t radix_bytes = topk::radix_scratch_bytes(topk::kRadixMaxK, topk::kRadixCap);
+    if (radix_bytes > ctrl_cand) ctrl_cand = radix_bytes;
     Workspace* w = nullptr;
     rc = workspace(s, device, ctrl_cand, in_host ? n * sizeof(int32_t) : 0,
                    out_host ? (size_t)k * sizeof(int32_t) : 0, &w);
@@ -146,9 +149,12 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
     }
     if (out_host) dout = static_cast<int32_t*>(w->stage_out);
 
-    e = topk::i32_launch(plan, s, din, n, k, dout, w->ctrl_cand);
+    if (k <= 128)
+        e = topk::i32_launch(plan, s, din, n, k, dout, w->ctrl_cand);
+    else
+        e = topk::radix_launch(s, din, n, k, dout, w->ctrl_cand, topk::kRadixCap);
     if (e != cudaSuccess) return cuda_fail(e);
-    g_launches.fetch_add(1, std::memory_order_relaxed);
+    g_launches.fetch_add(k <= 128 ? 1 : 4, std::memory_order_relaxed);
 
     if (out_host) {
         e = cudaMemcpyAsync(out, dout, (size_t)k * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
@@ -171,7 +177,7 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
     const size_t nout = (size_t)rows * (size_t)k * sizeof(float);
     if (overlaps(in, nin, vals, nout) || overlaps(in, nin, idx, nout) || overlaps(vals, nout, idx, nout))
         return TOPK_ERR_INVALID_ARG;
-    if (k > TOPK_MAX_K) return TOPK_ERR_UNSUPPORTED;
+    if (k > TOPK_MAX_K_ROWS) return TOPK_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     int device = 0;

@@ -39,8 +39,7 @@
 //   * The last block zeroes the control words and the block-maximum slots,
 //     so the next launch on the same scratch starts clean.  No block ever
 //     waits on another.
-//   * k > 128 uses per-warp shared-memory buffers of 2048 entries sorted in
-//     place instead of register lists.
+//   * k > 128 uses the radix select of topk_radix.cu instead.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -596,137 +595,6 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
                      &s_count);
 }
 
-// ---------------------------------------- k > 128: shared-memory buffers --
-
-constexpr int kBigBuf = 2048;
-
-template <int B>
-struct WarpBuf {
-    int* buf;
-    int cnt;  // warp-uniform number of entries
-    int t;    // warp-uniform threshold: only values > t are admitted
-
-    __device__ __forceinline__ void admit(int v, int lane) {
-        const bool p = v > t;
-        const unsigned m = __ballot_sync(kFullMask, p);
-        if (p) buf[cnt + __popc(m & lanemask_lt())] = v;
-        cnt += __popc(m);
-    }
-
-    // Sort the buffer, keep its k largest, raise t to the k-th when there are
-    // k of them.  Returns true when t was raised.
-    __device__ bool flush(int k, int lane) {
-        __syncwarp();
-        for (int p = cnt + lane; p < B; p += 32) buf[p] = INT_MIN;
-        __syncwarp();
-        warp_sort_smem_desc(buf, B, lane);
-        bool raised = false;
-        if (cnt >= k) {
-            const int kth = buf[k - 1];
-            if (kth > t) {
-                t = kth;
-                raised = true;
-            }
-        }
-        cnt = cnt < k ? cnt : k;
-        __syncwarp();
-        return raised;
-    }
-};
-
-__global__ void __launch_bounds__(kWarps * 32, 1)
-topk_i32_smem_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* __restrict__ out,
-                     unsigned char* __restrict__ scratch, int cap_limit) {
-    extern __shared__ __align__(16) int smem[];
-    __shared__ int s_thresh;
-    __shared__ int s_last;
-    __shared__ int s_count;
-
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const Scratch sc = scratch_view(scratch);
-    if (threadIdx.x == 0) s_thresh = INT_MIN;
-    __syncthreads();
-
-    const Split sp = split_input(in, n);
-    const size_t gw = (size_t)blockIdx.x * kWarps + warp;
-    const size_t nw = (size_t)gridDim.x * kWarps;
-
-    WarpBuf<kBigBuf> wb{smem + warp * kBigBuf, 0, INT_MIN};
-    int published = INT_MIN;
-    auto publish = [&](int v) {
-        if (lane == 0) {
-            atomicMax(&s_thresh, v);
-            if (v > published) atomicMax(&sc.ctrl->thresh, bias(v));
-        }
-        published = kmax(published, v);
-    };
-
-    if (gw == 0) {
-        const size_t ns = sp.head + (n - sp.tail0);
-        const size_t pos = (size_t)lane < sp.head ? (size_t)lane : sp.tail0 + (lane - sp.head);
-        wb.admit((size_t)lane < ns ? in[pos] : INT_MIN, lane);
-    }
-
-    for (size_t tile = gw; tile < sp.ntiles; tile += nw) {
-        const unsigned g = ld_relaxed_gpu(&sc.ctrl->thresh);
-        int4 r[kU];
-        load_tile(r, sp.body, sp.nvec, tile, lane);
-        wb.t = kmax(wb.t, kmax(unbias(g), *(volatile int*)&s_thresh));
-        int m = INT_MIN;
-#pragma unroll
-        for (int u = 0; u < kU; ++u) m = kmax(m, max4(r[u]));
-        if (__any_sync(kFullMask, m > wb.t)) {
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                if (wb.cnt > kBigBuf - 128) {
-                    if (wb.flush(k, lane)) publish(wb.t);
-                }
-                wb.admit(r[u].x, lane);
-                wb.admit(r[u].y, lane);
-                wb.admit(r[u].z, lane);
-                wb.admit(r[u].w, lane);
-            }
-        }
-    }
-
-    if (wb.flush(k, lane)) publish(wb.t);
-    const int K = next_pow2(k);
-    for (int p = wb.cnt + lane; p < K; p += 32) wb.buf[p] = INT_MIN;
-
-    // Block merge: pairwise bitonic merges of sorted K-lists.
-#pragma unroll 1
-    for (int s = 1; s < kWarps; s <<= 1) {
-        __syncthreads();
-        if ((warp & (2 * s - 1)) == 0) {
-            int* a = smem + warp * kBigBuf;
-            const int* b = smem + (warp + s) * kBigBuf;
-            for (int i = lane; i < K; i += 32) a[i] = kmax(a[i], b[K - 1 - i]);
-            __syncwarp();
-            warp_merge_smem_desc(a, K, lane);
-        }
-    }
-    __syncthreads();
-
-    // The block's sorted list (K entries) and the count above the grid threshold.
-    __shared__ int s_tnow;
-    if (threadIdx.x == 0) s_tnow = kmax(s_thresh, unbias(ld_relaxed_gpu(&sc.ctrl->thresh)));
-    __syncthreads();
-    if (warp == 0) {
-        int32_t* dst = sc.cand + (size_t)blockIdx.x * K;
-        int count = 0;
-        for (int p0 = 0; p0 < K; p0 += 32) {
-            const int v = smem[p0 + lane];
-            dst[p0 + lane] = v;
-            count += __popc(__ballot_sync(kFullMask, v > s_tnow));
-        }
-        if (lane == 0) sc.counts[blockIdx.x] = count;
-    }
-    const int block_kth = smem[k - 1];
-    if (block_done(sc, kmax(s_thresh, block_kth), &s_last))
-        second_stage(sc, k, 1, K, out, smem, kWarps * kBigBuf, cap_limit, &s_count);
-}
-
 // ------------------------------------------------------------ host side --
 
 template <int L, int GL>
@@ -739,17 +607,6 @@ struct StreamVariant {
         topk_i32_stream_kernel<L, GL><<<grid, kThreads, smem_bytes(), s>>>(in, n, k, out, scratch, cap_limit);
     }
     static size_t units_per_block() { return kCons; }
-};
-
-struct SmemVariant {
-    static constexpr int kThreads = kWarps * 32;
-    static size_t units_per_block() { return kWarps; }
-    static size_t smem_bytes() { return (size_t)kWarps * kBigBuf * sizeof(int); }
-    static const void* fn() { return reinterpret_cast<const void*>(&topk_i32_smem_kernel); }
-    static void launch(int grid, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
-                       unsigned char* scratch, int cap_limit) {
-        topk_i32_smem_kernel<<<grid, kWarps * 32, smem_bytes(), s>>>(in, n, k, out, scratch, cap_limit);
-    }
 };
 
 using VarK32 = StreamVariant<1, 1>;
@@ -812,8 +669,7 @@ cudaError_t plan_for(int device, size_t n, I32Plan* plan) {
 cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan) {
     if (k <= 32) return plan_for<VarK32>(device, n, plan);
     if (k <= 64) return plan_for<VarK64>(device, n, plan);
-    if (k <= 128) return plan_for<VarK128>(device, n, plan);
-    return plan_for<SmemVariant>(device, n, plan);
+    return plan_for<VarK128>(device, n, plan);
 }
 
 cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
@@ -824,10 +680,8 @@ cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, s
         VarK32::launch(plan.grid, s, in, n, k, out, sc, cap);
     else if (k <= 64)
         VarK64::launch(plan.grid, s, in, n, k, out, sc, cap);
-    else if (k <= 128)
-        VarK128::launch(plan.grid, s, in, n, k, out, sc, cap);
     else
-        SmemVariant::launch(plan.grid, s, in, n, k, out, sc, cap);
+        VarK128::launch(plan.grid, s, in, n, k, out, sc, cap);
     return cudaGetLastError();
 }
 

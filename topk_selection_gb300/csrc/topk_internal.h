@@ -19,27 +19,54 @@ struct I32Ctrl {
     unsigned pad[62];  // one 256-byte line to itself
 };
 
-// Scratch of one int32 TopK launch, in this order:
+// Scratch of an int32 TopK launch.  Both plans (streaming, k <= 128; radix
+// select, larger k) use the same workspace, laid out so that every byte one
+// of them needs zero at its start is one that both leave zero at their end:
 //   [0, 256)                     status word: nonzero after a bounded wait gave
 //                                up (sticky; read and cleared by the host)
-//   [256, 512)                   I32Ctrl
-//   [512, 512 + 4*1024)          per-block running maxima (biased like thresh)
-//   [kI32CountOffset, +4*8192)   per-list survivor counts (up to 8 lists per block)
-//   [kI32CandOffset, ...)        per block, its candidate lists: up to
-//                                kI32CandPerBlock ints
-// [kI32ResetBegin, kI32CountOffset) is zero between launches.
+//   [256, 512)                   control words: I32Ctrl (streaming) or the
+//                                radix control words
+//   [512, 512 + 4*4096)          streaming: per-block running maxima (first
+//                                4 KiB); radix: the global digit histogram
+//   -- everything above is zero between launches: [kI32ResetBegin, kI32ResetEnd) --
+//   [kRadixCandOffset, ...)      radix: collected keys (k rounded up to 64),
+//                                then the boundary buffer (cap keys)
+//   [kI32CountOffset, +4*8192)   streaming: per-list survivor counts
+//   [kI32CandOffset, ...)        streaming: per block, its candidate lists
+//                                (up to kI32CandPerBlock ints)
+// The last two areas overlap the radix area; none of them needs any value
+// at the start of a launch.
 constexpr int kI32MaxGrid = 1024;
 constexpr int kI32MaxListsPerBlock = 8;
 constexpr int kI32CandPerBlock = 1024;
 constexpr size_t kI32StatusOffset = 0;
 constexpr size_t kI32CtrlOffset = 256;
 constexpr size_t kI32BmaxOffset = 512;
-constexpr size_t kI32CountOffset = kI32BmaxOffset + (size_t)kI32MaxGrid * sizeof(unsigned);
+constexpr size_t kRadixCtrlOffset = kI32CtrlOffset;
+constexpr size_t kRadixHistOffset = kI32BmaxOffset;
+constexpr size_t kRadixCandOffset = kRadixHistOffset + 4096 * sizeof(unsigned);
+constexpr size_t kI32ResetBegin = kI32CtrlOffset;
+constexpr size_t kI32ResetEnd = kRadixCandOffset;
+constexpr size_t kI32CountOffset = kRadixCandOffset;
 constexpr size_t kI32CandOffset =
     kI32CountOffset + (size_t)kI32MaxGrid * kI32MaxListsPerBlock * sizeof(int32_t);
-constexpr size_t kI32ResetBegin = kI32CtrlOffset;
-constexpr size_t kI32ResetEnd = kI32CountOffset;
-static_assert(kI32CandOffset % 256 == 0, "candidate area alignment");
+constexpr int kRadixMaxK = 32768;
+static_assert(kI32BmaxOffset + kI32MaxGrid * sizeof(unsigned) <= kI32ResetEnd, "block maxima are reset");
+static_assert(kI32CountOffset % 256 == 0 && kI32CandOffset % 256 == 0, "area alignment");
+
+// Boundary buffer of the radix plan in the cached workspace, in keys.
+constexpr size_t kRadixCap = size_t(1) << 18;
+
+constexpr size_t radix_scratch_bytes(int k, size_t cap) {
+    return kRadixCandOffset + ((size_t)k + 63) / 64 * 64 * sizeof(unsigned) + cap * sizeof(unsigned);
+}
+
+// Enqueue the radix-select int32 TopK (four launches; any k up to
+// kRadixMaxK).  scratch holds radix_scratch_bytes(k, cap) bytes whose
+// control words and histogram are zero (they are again afterwards); cap is
+// the boundary buffer's capacity in keys.
+cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out, void* scratch,
+                         size_t cap);
 
 // Status bits a kernel may set in the status word.
 constexpr unsigned kStatusWaitTimeout = 1u;
@@ -57,7 +84,8 @@ struct I32Plan {
 // Current value of TOPK_OPT_STAGE2_CAP (0 = default).
 int stage2_cap_option();
 
-// Grid for an n-element, k-wide selection on `device`.
+// Grid for an n-element, k-wide selection on `device` (k <= 128: the
+// streaming plan; larger k use radix_launch).
 cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan);
 
 // Enqueue the single-launch int32 TopK.  scratch holds i32_scratch_bytes(plan.grid)

@@ -73,8 +73,13 @@ enum topk_status {
  * k <= 128: one launch.  Every block filters its share of the input against
  * a running k-th-value threshold and leaves k candidates; the last block to
  * finish merges the candidates (section 2.2's second pass, fused into the
- * same launch).  k > 128: radix select in four launches (two or three
- * passes over the input, then one block that sorts the answer).
+ * same launch).  k > 128: a radix select on order-preserving keys ("GPU
+ * radix sort", histogram section).  When n exceeds 2^18, a threshold is
+ * taken from a 2^18-key sample, one pass over the input keeps the keys above
+ * it, and one 8-CTA cluster selects the k-th key among them and sorts the
+ * answer (six launches, one input pass; two more input passes run only when
+ * the sample misled the filter).  When n <= 2^18 the cluster does it all in
+ * one launch.
  *
  * Returns TOPK_OK or an error code; on error nothing is written to out.
  */
@@ -121,11 +126,11 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
  *     and per-block candidates.  Every GPU that loads the library holds it
  *     until the process exits.  k above TOPK_MAX_K is rejected with
  *     TOPK_ERR_UNSUPPORTED.  For k <= 128 the grid is cut so that every
- *     block's candidate lists fit (1 MiB holds 243 blocks' worth), so on
+ *     block's candidate lists fit (1 MiB holds 239 blocks' worth), so on
  *     GPUs with more SMs this entry point runs fewer blocks than topk_i32;
- *     for larger k the radix select's boundary buffer is what the array has
- *     left (about 225K keys at k = 32768), so inputs whose k-th value shares
- *     its top 12 bits with more keys than that take one more pass.
+ *     for larger k the radix select's candidate buffer is what the array
+ *     has left (253,824 keys instead of 262,144), so slightly fewer inputs
+ *     avoid the exact passes.
  *   - Every call uses the same array.  Each call clears the control words
  *     on `stream` before its launch, but calls whose work overlaps on the
  *     GPU (different streams, or different host threads without ordering)
@@ -156,7 +161,17 @@ enum topk_option {
      * is what fits).  When more candidates exceed the final threshold, the
      * second stage first finds the exact k-th value by radix select.  Lower
      * it only to exercise that path; results are the same either way. */
-    TOPK_OPT_STAGE2_CAP = 1
+    TOPK_OPT_STAGE2_CAP = 1,
+    /* Upper bound, in keys, on the candidate buffer of the large-k plan
+     * (k > 128; 0 restores the default; values below k act as k).  Inputs
+     * whose candidates overflow it take the exact radix passes.  Lower it
+     * only to exercise those passes; results are the same either way. */
+    TOPK_OPT_RADIX_CAP = 2,
+    /* Rank, within the large-k plan's 2^18-key sample, of the key used as
+     * the filter threshold (0 restores the automatic choice).  A rank that
+     * is too small makes the filter keep fewer than k keys, and the plan
+     * takes the exact radix passes.  For tests of that path only. */
+    TOPK_OPT_RADIX_SAMPLE_RANK = 3
 };
 
 /* Set a process-wide option; takes effect for calls made afterwards.

@@ -127,6 +127,14 @@ def test_set_option_validation(lib):
     assert tk._lib.topk_set_option(99, 0) == 1
     assert tk._lib.topk_set_option(tk.OPT_STAGE2_CAP, 64) == 0
     assert tk._lib.topk_set_option(tk.OPT_STAGE2_CAP, 0) == 0
+    for opt in (tk.OPT_RADIX_CAP, tk.OPT_RADIX_SAMPLE_RANK):
+        assert tk._lib.topk_set_option(opt, -1) == 1
+        assert tk._lib.topk_set_option(opt, 5) == 0
+        assert tk._lib.topk_set_option(opt, 0) == 0
+    text = open(os.path.join(ROOT, "include", "topk.h")).read()
+    for name, value in (("TOPK_OPT_STAGE2_CAP", tk.OPT_STAGE2_CAP), ("TOPK_OPT_RADIX_CAP", tk.OPT_RADIX_CAP),
+                        ("TOPK_OPT_RADIX_SAMPLE_RANK", tk.OPT_RADIX_SAMPLE_RANK)):
+        assert re.search(r"%s = %d\b" % (name, value), text), name
 
 
 def test_header_limits_match_binding(lib):

@@ -121,11 +121,39 @@ def test_second_stage_radix_select_path(tk, cap):
                                     ("int_min", 300_007), ("negative", 1_500_001), ("sawtooth", 1_234_567),
                                     ("int_max_heavy", 700_001)])
 def test_large_k_radix_select(tk, kind, n):
-    # k > 128: radix select.  "dups" and "few" put more than the boundary
-    # buffer holds into one top-12-bit bucket, so they take the 3-pass path.
+    # k > 128: sampled threshold, one filter pass, cluster select and sort.
     x = make(kind, n, seed=n)
     for k in (129, 1000, 4096, 32768):
         assert np.array_equal(gpu_topk(tk, x, k), oracle.topk_i32(x, k)), (kind, n, k)
+
+
+@pytest.mark.parametrize("kind,n", [("uniform", 1_000_003), ("dups", 2_000_003), ("few", 700_001),
+                                    ("ascending", 3_000_000), ("negative", 1_500_001), ("sawtooth", 1_234_567),
+                                    ("int_max_heavy", 700_001), ("equal", 400_000)])
+def test_large_k_exact_passes(tk, kind, n):
+    # The sampled threshold is only a shortcut: when it misleads the filter,
+    # exact radix passes take over.  Sample rank 1 puts the threshold at the
+    # sample's maximum, so the filter keeps fewer than k keys; a buffer capped
+    # at k (option value 1) makes the filter overflow and makes the second
+    # exact pass histogram instead of collect.
+    x = make(kind, n, seed=n + 1)
+    try:
+        for rank, cap in ((1, 0), (1, 1), (0, 1), (0, 6000)):
+            tk.set_option(tk.OPT_RADIX_SAMPLE_RANK, rank)
+            tk.set_option(tk.OPT_RADIX_CAP, cap)
+            for k in (129, 1000, 5000):
+                assert np.array_equal(gpu_topk(tk, x, k), oracle.topk_i32(x, k)), (kind, n, k, rank, cap)
+    finally:
+        tk.set_option(tk.OPT_RADIX_SAMPLE_RANK, 0)
+        tk.set_option(tk.OPT_RADIX_CAP, 0)
+
+
+def test_large_k_cluster_only_sizes(tk):
+    # n up to 2^18 runs the single cluster launch on the input itself.
+    for n, k in ((262_144, 32_768), (262_144, 129), (262_145, 32_768), (200_000, 200_000 // 7), (4096, 4096)):
+        for kind in ("uniform", "ascending", "dups", "equal"):
+            x = make(kind, n, seed=n + k)
+            assert np.array_equal(gpu_topk(tk, x, k), oracle.topk_i32(x, k)), (kind, n, k)
 
 
 def test_large_k_full_sort_and_edges(tk):

@@ -23,7 +23,7 @@ from . import build as _build
 
 __all__ = ["topk_i32", "topk_rows_f32", "topk_i32_ptr", "topk_rows_f32_ptr", "TopKError", "MAX_K", "MAX_K_ROWS",
            "status_string", "release_workspace", "launch_count", "last_cuda_error", "library_path",
-           "check_stream", "set_option", "OPT_STAGE2_CAP"]
+           "check_stream", "set_option", "OPT_STAGE2_CAP", "OPT_RADIX_CAP", "OPT_RADIX_SAMPLE_RANK"]
 
 MAX_K = 32768       # topk_i32
 MAX_K_ROWS = 1024   # topk_rows_f32
@@ -88,6 +88,8 @@ def launch_count() -> int:
 
 
 OPT_STAGE2_CAP = 1
+OPT_RADIX_CAP = 2
+OPT_RADIX_SAMPLE_RANK = 3
 
 
 def set_option(option: int, value: int) -> None:

@@ -17,6 +17,8 @@ namespace {
 
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<int> g_stage2_cap{0};
+std::atomic<int> g_radix_cap{0};
+std::atomic<int> g_radix_sample_rank{0};
 thread_local int t_last_cuda_error = 0;
 
 int cuda_fail(cudaError_t e) {
@@ -105,6 +107,8 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 namespace topk {
 int stage2_cap_option() { return g_stage2_cap.load(std::memory_order_relaxed); }
+int radix_cap_option() { return g_radix_cap.load(std::memory_order_relaxed); }
+int radix_sample_rank_option() { return g_radix_sample_rank.load(std::memory_order_relaxed); }
 void note_cuda_error(int err) { t_last_cuda_error = err; }
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 }  // namespace topk
@@ -133,7 +137,7 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
     if (e != cudaSuccess) return cuda_fail(e);
     // One workspace serves both plans (k <= 128 streams; larger k use radix select).
     size_t ctrl_cand = topk::i32_scratch_bytes(plan.max_grid);
-    const size_t radix_bytes = topk::radix_scratch_bytes(topk::kRadixMaxK, topk::kRadixCap);
+    const size_t radix_bytes = topk::radix_scratch_bytes(topk::kRadixCap);
     if (radix_bytes > ctrl_cand) ctrl_cand = radix_bytes;
     Workspace* w = nullptr;
     rc = workspace(s, device, ctrl_cand, in_host ? n * sizeof(int32_t) : 0,
@@ -149,12 +153,13 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
     }
     if (out_host) dout = static_cast<int32_t*>(w->stage_out);
 
+    int launches = 1;
     if (k <= 128)
         e = topk::i32_launch(plan, s, din, n, k, dout, w->ctrl_cand);
     else
-        e = topk::radix_launch(s, din, n, k, dout, w->ctrl_cand, topk::kRadixCap);
+        e = topk::radix_launch(s, din, n, k, dout, w->ctrl_cand, topk::kRadixCap, &launches);
+    g_launches.fetch_add((unsigned long long)launches, std::memory_order_relaxed);
     if (e != cudaSuccess) return cuda_fail(e);
-    g_launches.fetch_add(k <= 128 ? 1 : 4, std::memory_order_relaxed);
 
     if (out_host) {
         e = cudaMemcpyAsync(out, dout, (size_t)k * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
@@ -261,6 +266,14 @@ int topk_set_option(int option, int value) {
         case TOPK_OPT_STAGE2_CAP:
             if (value != 0 && (value < 2 || (value & (value - 1)) != 0)) return TOPK_ERR_INVALID_ARG;
             g_stage2_cap.store(value, std::memory_order_relaxed);
+            return TOPK_OK;
+        case TOPK_OPT_RADIX_CAP:
+            if (value < 0) return TOPK_ERR_INVALID_ARG;
+            g_radix_cap.store(value, std::memory_order_relaxed);
+            return TOPK_OK;
+        case TOPK_OPT_RADIX_SAMPLE_RANK:
+            if (value < 0) return TOPK_ERR_INVALID_ARG;
+            g_radix_sample_rank.store(value, std::memory_order_relaxed);
             return TOPK_OK;
         default:
             return TOPK_ERR_INVALID_ARG;

@@ -26,15 +26,17 @@ struct I32Ctrl {
 //                                up (sticky; read and cleared by the host)
 //   [256, 512)                   control words: I32Ctrl (streaming) or the
 //                                radix control words
-//   [512, 512 + 4*4096)          streaming: per-block running maxima (first
-//                                4 KiB); radix: the global digit histogram
+//   [512, 512 + 8*4096)          streaming: per-block running maxima (first
+//                                4 KiB); radix: the global 12-bit digit
+//                                histogram (64-bit counts)
 //   -- everything above is zero between launches: [kI32ResetBegin, kI32ResetEnd) --
-//   [kRadixCandOffset, ...)      radix: collected keys (k rounded up to 64),
-//                                then the boundary buffer (cap keys)
+//   [kRadixCandOffset, +2048)    radix: the sort plan (range table) the
+//                                cluster kernel leaves for the sort kernel
+//   [kRadixBufOffset, ...)       radix: the candidate buffer (cap keys)
 //   [kI32CountOffset, +4*8192)   streaming: per-list survivor counts
 //   [kI32CandOffset, ...)        streaming: per block, its candidate lists
 //                                (up to kI32CandPerBlock ints)
-// The last two areas overlap the radix area; none of them needs any value
+// The last two areas overlap the radix buffer; none of them needs any value
 // at the start of a launch.
 constexpr int kI32MaxGrid = 1024;
 constexpr int kI32MaxListsPerBlock = 8;
@@ -44,7 +46,9 @@ constexpr size_t kI32CtrlOffset = 256;
 constexpr size_t kI32BmaxOffset = 512;
 constexpr size_t kRadixCtrlOffset = kI32CtrlOffset;
 constexpr size_t kRadixHistOffset = kI32BmaxOffset;
-constexpr size_t kRadixCandOffset = kRadixHistOffset + 4096 * sizeof(unsigned);
+constexpr size_t kRadixCandOffset = kRadixHistOffset + 4096 * sizeof(unsigned long long);
+constexpr size_t kRadixPlanBytes = 2048;
+constexpr size_t kRadixBufOffset = kRadixCandOffset + kRadixPlanBytes;
 constexpr size_t kI32ResetBegin = kI32CtrlOffset;
 constexpr size_t kI32ResetEnd = kRadixCandOffset;
 constexpr size_t kI32CountOffset = kRadixCandOffset;
@@ -52,21 +56,29 @@ constexpr size_t kI32CandOffset =
     kI32CountOffset + (size_t)kI32MaxGrid * kI32MaxListsPerBlock * sizeof(int32_t);
 constexpr int kRadixMaxK = 32768;
 static_assert(kI32BmaxOffset + kI32MaxGrid * sizeof(unsigned) <= kI32ResetEnd, "block maxima are reset");
-static_assert(kI32CountOffset % 256 == 0 && kI32CandOffset % 256 == 0, "area alignment");
+static_assert(kRadixCandOffset % 256 == 0 && kRadixBufOffset % 256 == 0 && kI32CountOffset % 256 == 0 &&
+                  kI32CandOffset % 256 == 0,
+              "area alignment");
 
-// Boundary buffer of the radix plan in the cached workspace, in keys.
-constexpr size_t kRadixCap = size_t(1) << 18;
+// Keys one thread-block cluster of the radix plan holds in shared memory
+// (8 CTAs x 32768); the candidate buffer never exceeds it.
+constexpr size_t kRadixClusterCap = size_t(1) << 18;
+// Candidate buffer of the radix plan in the cached workspace, in keys.
+constexpr size_t kRadixCap = kRadixClusterCap;
 
-constexpr size_t radix_scratch_bytes(int k, size_t cap) {
-    return kRadixCandOffset + ((size_t)k + 63) / 64 * 64 * sizeof(unsigned) + cap * sizeof(unsigned);
-}
+constexpr size_t radix_scratch_bytes(size_t cap) { return kRadixBufOffset + cap * sizeof(unsigned); }
 
-// Enqueue the radix-select int32 TopK (four launches; any k up to
-// kRadixMaxK).  scratch holds radix_scratch_bytes(k, cap) bytes whose
-// control words and histogram are zero (they are again afterwards); cap is
-// the boundary buffer's capacity in keys.
+// Enqueue the radix-select int32 TopK (two launches when n fits one
+// cluster, else seven; any k up to kRadixMaxK).  scratch holds radix_scratch_bytes(cap)
+// bytes, 256-byte aligned, whose [kI32ResetBegin, kI32ResetEnd) bytes are
+// zero (they are zero again afterwards); cap is the candidate buffer's
+// capacity in keys, k <= cap <= kRadixClusterCap.
 cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out, void* scratch,
-                         size_t cap);
+                         size_t cap, int* launches);
+
+// Test options of the radix plan (TOPK_OPT_RADIX_CAP, TOPK_OPT_RADIX_SAMPLE_RANK; 0 = default).
+int radix_cap_option();
+int radix_sample_rank_option();
 
 // Status bits a kernel may set in the status word.
 constexpr unsigned kStatusWaitTimeout = 1u;

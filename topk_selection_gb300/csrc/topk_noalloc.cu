@@ -26,8 +26,8 @@ namespace {
 constexpr size_t kNoallocScratchBytes = TOPK_NOALLOC_SCRATCH_BYTES;
 static_assert(kNoallocScratchBytes >= topk::i32_scratch_bytes(1),
               "the scratch must hold the control words, block maxima, counts and one block's candidates");
-static_assert(kNoallocScratchBytes >= topk::radix_scratch_bytes(TOPK_MAX_K, 1 << 16),
-              "the scratch must hold the radix plan's keys and a useful boundary buffer at the largest k");
+static_assert(kNoallocScratchBytes >= topk::radix_scratch_bytes(TOPK_MAX_K),
+              "the radix plan's candidate buffer must hold at least the largest k keys");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -96,17 +96,18 @@ extern "C" int topk_i32_noalloc(const int32_t* in, size_t n, int k, int32_t* out
     if (rc != TOPK_OK) return rc;
 
     if (k > 128) {
-        // Large k: radix select, its boundary buffer sized to what the array
-        // leaves after the control words and the collected keys.
-        const size_t cap = (kNoallocScratchBytes - topk::radix_scratch_bytes(k, 0)) / sizeof(unsigned);
+        // Large k: radix select, its candidate buffer sized to what the
+        // array leaves after the control words and the histogram.
+        const size_t cap = (kNoallocScratchBytes - topk::radix_scratch_bytes(0)) / sizeof(unsigned);
+        int launches = 0;
         e = cudaMemsetAsync(static_cast<char*>(scratch) + topk::kI32ResetBegin, 0,
                             topk::kI32ResetEnd - topk::kI32ResetBegin, s);
-        if (e == cudaSuccess) e = topk::radix_launch(s, in, n, k, out, scratch, cap);
+        if (e == cudaSuccess) e = topk::radix_launch(s, in, n, k, out, scratch, cap, &launches);
+        for (int i = 0; i < launches; ++i) topk::note_launch();
         if (e != cudaSuccess) {
             topk::note_cuda_error((int)e);
             return TOPK_ERR_CUDA;
         }
-        for (int i = 0; i < 4; ++i) topk::note_launch();
         return TOPK_OK;
     }
 

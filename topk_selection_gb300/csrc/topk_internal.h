@@ -30,8 +30,8 @@ struct I32Ctrl {
 //                                4 KiB); radix: the global 12-bit digit
 //                                histogram (64-bit counts)
 //   -- everything above is zero between launches: [kI32ResetBegin, kI32ResetEnd) --
-//   [kRadixCandOffset, +2048)    radix: the sort plan (range table) the
-//                                cluster kernel leaves for the sort kernel
+//   [kRadixCandOffset, +4096)    radix: the range table the cluster kernel
+//                                leaves for the sort kernel
 //   [kRadixBufOffset, ...)       radix: the candidate buffer (cap keys)
 //   [kI32CountOffset, +4*8192)   streaming: per-list survivor counts
 //   [kI32CandOffset, ...)        streaming: per block, its candidate lists
@@ -47,7 +47,7 @@ constexpr size_t kI32BmaxOffset = 512;
 constexpr size_t kRadixCtrlOffset = kI32CtrlOffset;
 constexpr size_t kRadixHistOffset = kI32BmaxOffset;
 constexpr size_t kRadixCandOffset = kRadixHistOffset + 4096 * sizeof(unsigned long long);
-constexpr size_t kRadixPlanBytes = 2048;
+constexpr size_t kRadixPlanBytes = 4096;
 constexpr size_t kRadixBufOffset = kRadixCandOffset + kRadixPlanBytes;
 constexpr size_t kI32ResetBegin = kI32CtrlOffset;
 constexpr size_t kI32ResetEnd = kRadixCandOffset;

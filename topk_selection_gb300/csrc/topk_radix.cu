@@ -32,15 +32,14 @@
 //                       prefix's top are written from the histogram
 //   final    one cluster loads the buffer into its 8 CTAs' shared memory and
 //            selects the k-th key with four cluster-wide 8-bit digit
-//            histograms (summed through distributed shared memory).  Each CTA
-//            keeps its keys above the k-th; rank 0 cuts their value range into
-//            about 768-key ranges from a sample weighted by each CTA's share
-//            (a value that dominates the sample gets a range of its own).
-//   sort     one CTA per range: it counts the keys in higher ranges for its
-//            output offset, gathers its own and sorts them in shared memory.
-//            The cluster writes the copies of the k-th key after them.
-// When n fits one cluster, the cluster kernel and the sort alone run, on the
-// input itself.
+//            histograms (summed through distributed shared memory).  Rank 0
+//            cuts the value range of the keys above it into ranges of about
+//            256 keys, from a sample weighted by each CTA's share (a value
+//            that dominates the sample gets a range of its own).  Every CTA
+//            counts its keys per range, writes them straight to their range
+//            of the output, and each range is then sorted in place by one
+//            warp.  Copies of the k-th key fill the rest of the output.
+// When n fits one cluster, the cluster kernel alone runs, on the input itself.
 // Every decision stays on the device, so a call only enqueues work.  No
 // kernel here waits on another block or CTA except through hardware
 // barriers (__syncthreads, the cluster barrier), so none can hang.
@@ -472,7 +471,7 @@ radix_exact3_kernel(const int32_t* __restrict__ in, size_t n, unsigned char* __r
 }
 
 // ---------------------------------------------------------------------------
-// Cluster kernel: select in 8 CTAs' shared memory, then plan the sort.
+// Cluster kernel: select, partition and sort in 8 CTAs' shared memory.
 
 __device__ __forceinline__ unsigned cluster_rank() {
     unsigned r;
@@ -510,44 +509,126 @@ __device__ __forceinline__ uint4 ld_cluster_v4(const unsigned* p, unsigned rank)
 
 enum : int { kClFull = 0, kClSample = 1, kClFinal = 2 };
 
-constexpr int kMaxRanges = 128;        // sort ranges (one sort CTA each)
-constexpr unsigned kRangeKeys = 768;   // keys a sort range aims at
-constexpr unsigned kMaxPlanned = 48;   // ranges planned from the sample (heavy values add more)
-constexpr unsigned kPlanSamples = 256; // splitter sample, at most
-constexpr int kSortThreads = 1024;
-constexpr int kSortCap = kRadixMaxK;   // keys one sort CTA holds: a range has fewer than k
+constexpr int kMaxRanges = 256;          // output ranges (one sorting warp each)
+constexpr unsigned kMaxPlanned = 128;    // ranges cut from the sample; repeated values add up to as many
+constexpr unsigned kRangeKeys = 256;     // keys a range aims at
+constexpr unsigned kPlanSamples = 512;   // splitter sample, at most
+static_assert(2 * kMaxPlanned <= (unsigned)kMaxRanges, "range table");
+static_assert(kClCtas * kMaxRanges == 2 * kClThreads, "two (CTA, range) counts per thread");
+constexpr int kSortWarps = 4;            // warps per CTA of the sort kernel
+constexpr int kSortRegCap = 512;         // a warp sorts ranges up to this in registers
+constexpr int kSortCap = kRadixMaxK;     // a larger range is sorted by its CTA in shared memory
 
 // What the cluster leaves for the sort kernel (at kRadixCandOffset).
 struct RadixPlan {
-    unsigned nranges;           // ranges to sort (0: no key above the k-th)
-    unsigned seg_off[kClCtas];  // keys above the k-th: buf[seg_off[r] .. + seg_cnt[r]) per CTA r
-    unsigned seg_cnt[kClCtas];
-    unsigned lb[kMaxRanges];    // range q: keys u with lb[q] <= u < lb[q-1] (range 0: u >= lb[0])
+    unsigned nranges;
+    unsigned rstart[kMaxRanges + 1];  // range q: out[rstart[q] .. rstart[q+1])
+    unsigned lb[kMaxRanges];          // range q holds keys u with lb[q] <= u < lb[q-1]
 };
 static_assert(sizeof(RadixPlan) <= kRadixPlanBytes, "plan area");
 
 struct ClSmem {
-    unsigned keys[kClSlice];              // the CTA's keys, then the ones above the k-th
+    unsigned keys[kClSlice];              // the CTA's keys
     unsigned hist[2][256];                // digit histograms (read by the other CTAs)
-    unsigned samp[kPlanSamples];          // rank 0: the gathered sample, sorted
+    unsigned part[kClCtas][kMaxRanges];   // the cluster's histograms of a level; later the range counts
+    unsigned samp[kPlanSamples];          // rank 0: the gathered sample
     unsigned mysamp[kPlanSamples];        // this CTA's part of it (read by rank 0)
+    unsigned lb[kMaxRanges];              // range bounds (rank 0 builds them; the others copy)
+    unsigned rcnt[kMaxRanges];            // this CTA's keys per range (read by the others)
+    unsigned rstart[kMaxRanges + 1];      // output offset of each range
+    unsigned rpos[kMaxRanges];            // this CTA's next output slot in each range
     unsigned ccount[kClCtas];             // every CTA's count of keys above the k-th
     unsigned wcnt[kClWarps];
     unsigned woff[kClWarps];
-    unsigned lb[kMaxRanges];              // rank 0: the range table being built
-    unsigned mine_count;                  // this CTA's count (read by rank 0)
+    unsigned mine_count;                  // this CTA's count (read by the others)
+    unsigned nranges;                     // (rank 0's is read by the others)
     unsigned pick_digit;
     unsigned pick_above;
 };
+static_assert(kMaxRanges == 256, "a level's histogram fits a row of part");
 
-// mode kClFull:   select among the n input values (n <= cap) and plan the
-//                 sort of the TopK.
+// Sort a[0..m) descending in place, m <= 32 N, by one warp in registers.
+template <int N>
+__device__ __forceinline__ void warp_sort_smem_list(unsigned* a, unsigned m, unsigned lane) {
+    unsigned v[N];
+#pragma unroll
+    for (int jj = 0; jj < N; ++jj) {
+        const unsigned p = jj * 32 + lane;
+        v[jj] = p < m ? a[p] : 0u;
+    }
+    warp_sort_desc(v, (int)lane);
+#pragma unroll
+    for (int jj = 0; jj < N; ++jj) {
+        const unsigned p = jj * 32 + lane;
+        if (p < m) a[p] = v[jj];
+    }
+}
+
+// After the cluster barrier that completes every CTA's histogram H: sum the
+// 8 histograms (warp r reads CTA r's with 16-byte remote loads) and find the
+// bucket holding the need-th largest key.  Every CTA finds the same one.
+__device__ __forceinline__ void cluster_pick(ClSmem& S, const unsigned* H, unsigned need) {
+    const unsigned lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (w < (unsigned)kClCtas) {
+        const uint4 a = ld_cluster_v4(&H[lane * 8], w);
+        const uint4 b = ld_cluster_v4(&H[lane * 8 + 4], w);
+        *reinterpret_cast<uint4*>(&S.part[w][lane * 8]) = a;
+        *reinterpret_cast<uint4*>(&S.part[w][lane * 8 + 4]) = b;
+    }
+    __syncthreads();
+    if (w == 0) {
+        unsigned c[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int r = 0; r < kClCtas; ++r) {
+            const uint4 a = *reinterpret_cast<const uint4*>(&S.part[r][lane * 8]);
+            const uint4 b = *reinterpret_cast<const uint4*>(&S.part[r][lane * 8 + 4]);
+            c[0] += a.x, c[1] += a.y, c[2] += a.z, c[3] += a.w;
+            c[4] += b.x, c[5] += b.y, c[6] += b.z, c[7] += b.w;
+        }
+        unsigned tot = 0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) tot += c[b];
+        unsigned x = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_down_sync(kFullMask, x, o);
+            if ((int)lane + o < 32) x += y;
+        }
+        const unsigned above = x - tot;
+        if (above < need && need <= above + tot) {
+            unsigned acc = above;
+#pragma unroll
+            for (int b = 7; b >= 0; --b) {
+                if (acc + c[b] >= need) {
+                    S.pick_digit = lane * 8 + b;
+                    S.pick_above = acc;
+                    break;
+                }
+                acc += c[b];
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// Range of key u: the first q with u >= lb[q] (lb descending, lb[nr-1] <= u).
+__device__ __forceinline__ unsigned range_of(const unsigned* lb, unsigned nr, unsigned u) {
+    unsigned lo = 0, hi = nr - 1;
+    while (lo < hi) {
+        const unsigned mid = (lo + hi) >> 1;
+        if (u >= lb[mid])
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return lo;
+}
+
+// mode kClFull:   the TopK of the n input values (n <= cap).
 // mode kClSample: select the j-th largest of 2^18 sampled keys; write it to
 //                 the control words as the filter threshold.
-// mode kClFinal:  select among the buffered keys as the control words say,
-//                 plan the sort and zero the control words.
-// In the first and last modes the copies of the k-th key are written here;
-// the keys above it are left, per CTA, in the buffer for the sort kernel.
+// mode kClFinal:  the TopK from the buffered keys, as the control words say;
+//                 zero the control words.
 __global__ void __cluster_dims__(kClCtas, 1, 1) __launch_bounds__(kClThreads, 1)
 radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j_sample, int32_t* __restrict__ out,
                      unsigned char* __restrict__ scratch, unsigned cap, int mode) {
@@ -586,106 +667,94 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
     const unsigned lo = min(C, rank * per);
     const unsigned mine = min(C, lo + per) - lo;
 
-    // Load the CTA's slice, 16 loads in flight per thread (indices past the
-    // slice load its last key again and are not stored).
-    constexpr int kLd = 16;
-    for (unsigned base = 0; base < mine; base += kLd * kClThreads) {
-        unsigned v[kLd];
-        if (mode == kClFinal) {
+    // Load the CTA's keys, histogramming their top digit on the way (level 0
+    // of the select).
+    if (tid < 256) S.hist[0][tid] = 0u;
+    __syncthreads();
+    if (mode == kClSample) {
+        // Segment g of the sample: 16 keys from the 16-byte-aligned body,
+        // four vector loads; this CTA's 2048 segments, 8 vectors per thread.
+        const unsigned head = (unsigned)(((16u - (unsigned)(reinterpret_cast<uintptr_t>(in) & 15u)) & 15u) >> 2);
+        const int4* body = reinterpret_cast<const int4*>(in + head);
+        const size_t nvec = (n - head) >> 2;
+        int4 v[8];
 #pragma unroll
-            for (int u = 0; u < kLd; ++u) v[u] = __ldcg(rv.buf + lo + min(base + u * kClThreads + tid, mine - 1));
-        } else if (mode == kClFull) {
-#pragma unroll
-            for (int u = 0; u < kLd; ++u) v[u] = key_of(__ldg(in + lo + min(base + u * kClThreads + tid, mine - 1)));
-        } else {
-#pragma unroll
-            for (int u = 0; u < kLd; ++u) {
-                const unsigned x = lo + min(base + u * kClThreads + tid, mine - 1);
-                const size_t pos = (size_t)(x / kSegLen) * (n - kSegLen) / (kSegments - 1) + (x % kSegLen);
-                v[u] = key_of(__ldg(in + pos));
-            }
+        for (int m = 0; m < 8; ++m) {
+            const unsigned x = lo / 4 + m * kClThreads + tid;
+            const size_t vi = (size_t)(x >> 2) * (nvec - 4) / (kSegments - 1) + (x & 3);
+            v[m] = __ldg(body + vi);
         }
 #pragma unroll
-        for (int u = 0; u < kLd; ++u) {
-            const unsigned i = base + u * kClThreads + tid;
-            if (i < mine) S.keys[i] = v[u];
+        for (int m = 0; m < 8; ++m) {
+            const uint4 u = make_uint4(key_of(v[m].x), key_of(v[m].y), key_of(v[m].z), key_of(v[m].w));
+            *reinterpret_cast<uint4*>(&S.keys[(m * kClThreads + tid) * 4]) = u;
+            hist_add(S.hist[0], u.x >> 24, true);
+            hist_add(S.hist[0], u.y >> 24, true);
+            hist_add(S.hist[0], u.z >> 24, true);
+            hist_add(S.hist[0], u.w >> 24, true);
+        }
+    } else {
+        // 16 loads in flight per thread; indices past the slice load its
+        // last key again and are not stored.
+        constexpr int kLd = 16;
+        for (unsigned base = 0; base < mine; base += kLd * kClThreads) {
+            unsigned v[kLd];
+            if (mode == kClFinal) {
+#pragma unroll
+                for (int u = 0; u < kLd; ++u) v[u] = __ldcg(rv.buf + lo + min(base + u * kClThreads + tid, mine - 1));
+            } else {
+#pragma unroll
+                for (int u = 0; u < kLd; ++u)
+                    v[u] = key_of(__ldg(in + lo + min(base + u * kClThreads + tid, mine - 1)));
+            }
+#pragma unroll
+            for (int u = 0; u < kLd; ++u) {
+                const unsigned i = base + u * kClThreads + tid;
+                if (i < mine) S.keys[i] = v[u];
+                hist_add(S.hist[0], v[u] >> 24, i < mine);
+            }
         }
     }
     __syncthreads();
 
-    // Warp w owns the run S.keys[w0 .. w0 + cnt) of its 1024-key sub-slice;
+    // Warp w owns the run S.keys[w0 .. w0 + cnt) of its 1/32 of the slice;
     // each pass below compacts the run in place (order kept).
-    const unsigned w0 = w * 1024u;
-    unsigned cnt = mine > w0 ? min(1024u, mine - w0) : 0u;
+    const unsigned share = (mine + kClWarps - 1) / kClWarps;
+    const unsigned w0 = w * share;
+    unsigned cnt = mine > w0 ? min(share, mine - w0) : 0u;
 
-    // Select: four 8-bit digit levels.  Each level drops the keys below the
-    // bucket chosen so far (keys above it stay: they are in the answer) and
-    // histograms the next digit of the keys in it; the 256-bin histogram is
-    // summed over the cluster's CTAs by one warp (16-byte remote loads), and
-    // every CTA finds the same bucket.
-    unsigned need;
+    // Select: four 8-bit digit levels.  Each level after the first drops the
+    // keys below the bucket chosen so far (keys above it stay: they are in
+    // the answer) and histograms the next digit of the keys in it.
     if (select) {
-        unsigned prefix = 0;
-        need = j;
+        unsigned prefix = 0, need = j;
         for (int level = 0; level < 4; ++level) {
             const int shift = 24 - 8 * level;
-            const unsigned fixed = level == 0 ? 0u : (0xFFFFFFFFu << (32 - 8 * level));
             unsigned* H = S.hist[level & 1];
-            if (tid < 256) H[tid] = 0u;
-            __syncthreads();
-            unsigned kept = 0;
-            for (unsigned m = 0; m < cnt; m += 32) {
-                const unsigned i = m + lane;
-                const bool valid = i < cnt;
-                const unsigned u = valid ? S.keys[w0 + i] : 0u;
-                hist_add(H, (u >> shift) & 0xFFu, valid && (u & fixed) == prefix);
-                const bool keep = valid && (u & fixed) >= prefix;
-                const unsigned b = __ballot_sync(kFullMask, keep);
-                if (keep) S.keys[w0 + kept + __popc(b & lanemask_lt())] = u;
-                kept += __popc(b);
+            if (level > 0) {
+                const unsigned fixed = 0xFFFFFFFFu << (32 - 8 * level);
+                if (tid < 256) H[tid] = 0u;
+                __syncthreads();
+                unsigned kept = 0;
+                for (unsigned m = 0; m < cnt; m += 32) {
+                    const unsigned i = m + lane;
+                    const bool valid = i < cnt;
+                    const unsigned u = valid ? S.keys[w0 + i] : 0u;
+                    hist_add(H, (u >> shift) & 0xFFu, valid && (u & fixed) == prefix);
+                    const bool keep = valid && (u & fixed) >= prefix;
+                    const unsigned b = __ballot_sync(kFullMask, keep);
+                    if (keep) S.keys[w0 + kept + __popc(b & lanemask_lt())] = u;
+                    kept += __popc(b);
+                }
+                cnt = kept;
             }
-            cnt = kept;
             cluster_barrier();
-            if (w == 0) {
-                unsigned c[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-#pragma unroll
-                for (unsigned r = 0; r < (unsigned)kClCtas; ++r) {
-                    const uint4 a = ld_cluster_v4(&H[lane * 8], r);
-                    const uint4 b = ld_cluster_v4(&H[lane * 8 + 4], r);
-                    c[0] += a.x, c[1] += a.y, c[2] += a.z, c[3] += a.w;
-                    c[4] += b.x, c[5] += b.y, c[6] += b.z, c[7] += b.w;
-                }
-                unsigned tot = 0;
-#pragma unroll
-                for (int b = 0; b < 8; ++b) tot += c[b];
-                unsigned x = tot;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned y = __shfl_down_sync(kFullMask, x, o);
-                    if ((int)lane + o < 32) x += y;
-                }
-                const unsigned above = x - tot;
-                if (above < need && need <= above + tot) {
-                    unsigned acc = above;
-#pragma unroll
-                    for (int b = 7; b >= 0; --b) {
-                        if (acc + c[b] >= need) {
-                            S.pick_digit = lane * 8 + b;
-                            S.pick_above = acc;
-                            break;
-                        }
-                        acc += c[b];
-                    }
-                }
-            }
-            __syncthreads();
+            cluster_pick(S, H, need);
             prefix |= S.pick_digit << shift;
             need -= S.pick_above;
-            __syncthreads();
+            __syncthreads();  // the pick and part are rewritten at the next level
         }
         T = prefix;
-    } else {
-        need = (unsigned)k - C;
     }
 
     if (mode == kClSample) {
@@ -694,8 +763,7 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
         return;
     }
 
-    // Keys above T: compact the runs once more, then the CTA's survivors go
-    // out contiguously to its own part of the buffer.
+    // Keys above T, compacted in each warp's run.
     unsigned cw = 0;
     for (unsigned m = 0; m < cnt; m += 32) {
         const unsigned i = m + lane;
@@ -719,73 +787,94 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
         if (lane == 31) S.mine_count = x;
     }
     __syncthreads();
-    unsigned* X = rv.buf + lo;
-    for (unsigned i = lane; i < cw; i += 32) X[S.woff[w] + i] = S.keys[w0 + i];
-    __threadfence();
-    cluster_barrier();  // every CTA's survivors and their count are out
+    cluster_barrier();  // every CTA's count is out
 
-    // Sample for the sort plan.
+    // Splitter sample: a CTA's share of kPlanSamples follows its share of the
+    // keys above T.
     if (tid < (unsigned)kClCtas) S.ccount[tid] = ld_cluster(&S.mine_count, tid);
     __syncthreads();
     unsigned total = 0;
 #pragma unroll
     for (int r = 0; r < kClCtas; ++r) total += S.ccount[r];
-    // About kPlanSamples in all (never more): a CTA's share of them follows
-    // its share of the keys above T.
     auto samples_of = [&](unsigned c) -> unsigned {
         return total ? (unsigned)(((unsigned long long)c * kPlanSamples) / total) : 0u;
     };
     {
         const unsigned my_c = S.mine_count, my_s = samples_of(my_c);
-        for (unsigned i = tid; i < my_s; i += kClThreads) S.mysamp[i] = X[(unsigned long long)i * my_c / my_s];
-    }
-    cluster_barrier();  // samples out
-    unsigned ns = 0;
-    if (rank == 0 && total) {
-        unsigned soff[kClCtas + 1];
-#pragma unroll
-        for (int r = 0; r < kClCtas; ++r) {
-            soff[r] = ns;
-            ns += samples_of(S.ccount[r]);
-        }
-        soff[kClCtas] = ns;
-        for (unsigned i = tid; i < kPlanSamples; i += kClThreads) {
-            unsigned v = 0u;
-            if (i < ns) {
-                unsigned r = 0;
-                while (r + 1 < (unsigned)kClCtas && soff[r + 1] <= i) ++r;
-                v = ld_cluster(&S.mysamp[i - soff[r]], r);
+        for (unsigned i = tid; i < my_s; i += kClThreads) {
+            const unsigned g = (unsigned)((unsigned long long)i * my_c / my_s);
+            unsigned a = 0, b = kClWarps - 1;  // the last warp whose run starts at or before g
+            while (a < b) {
+                const unsigned mid = (a + b + 1) >> 1;
+                if (S.woff[mid] <= g)
+                    a = mid;
+                else
+                    b = mid - 1;
             }
-            S.samp[i] = v;
+            S.mysamp[i] = S.keys[a * share + (g - S.woff[a])];
         }
+        __syncthreads();
+        // This CTA's samples, sorted descending by one warp (zeros pad past
+        // my_s; every sample is above T, so nonzero).
+        if (w == 0 && my_s > 128) warp_sort_smem_list<kPlanSamples / 32>(S.mysamp, my_s, lane);
+        if (w == 0 && my_s <= 128) warp_sort_smem_list<4>(S.mysamp, my_s, lane);
     }
-    cluster_barrier();  // rank 0 has read every sample; no remote reads after this
+    cluster_barrier();  // sorted samples out
 
     if (rank == 0) {
-        RadixPlan* plan = reinterpret_cast<RadixPlan*>(scratch + kRadixCandOffset);
-        if (tid < (unsigned)kClCtas) {
-            plan->seg_off[tid] = min(C, tid * per);
-            plan->seg_cnt[tid] = S.ccount[tid];
-        }
-        if (w == 0) {
-            // One warp plans the ranges: R - 1 splitters at even positions of
-            // the sorted sample, about kRangeKeys keys apart; a splitter value
-            // that repeats at a neighbouring position (a value holding a
-            // range's worth of keys) also bounds a range holding only that
-            // value, which needs no sorting.  The last range ends at T + 1.
-            unsigned nr = 0;
-            if (total) {
-                unsigned v[kPlanSamples / 32];
+        if (total) {
+            unsigned soff[kClCtas + 1], ns = 0;
 #pragma unroll
-                for (int jj = 0; jj < (int)(kPlanSamples / 32); ++jj) v[jj] = S.samp[jj * 32 + lane];
-                warp_sort_desc(v, (int)lane);
+            for (int r = 0; r < kClCtas; ++r) {
+                soff[r] = ns;
+                ns += samples_of(S.ccount[r]);
+            }
+            soff[kClCtas] = ns;
+            // Gather the 8 sorted lists, then merge them by rank: an element's
+            // place is its index in its own list plus, in every other list,
+            // the count of greater keys (equal keys count from lower ranks).
+            unsigned* lists = &S.part[0][0];
+            for (unsigned i = tid; i < ns; i += kClThreads) {
+                unsigned r = 0;
+                while (r + 1 < (unsigned)kClCtas && soff[r + 1] <= i) ++r;
+                lists[i] = ld_cluster(&S.mysamp[i - soff[r]], r);
+            }
+            __syncthreads();
+            for (unsigned i = tid; i < ns; i += kClThreads) {
+                unsigned r = 0;
+                while (r + 1 < (unsigned)kClCtas && soff[r + 1] <= i) ++r;
+                const unsigned v = lists[i];
+                unsigned place = i - soff[r];
+                for (unsigned o = 0; o < (unsigned)kClCtas; ++o) {
+                    if (o == r) continue;
+                    // first index in list o whose key is below v (o < r) or not above v (o > r)
+                    unsigned a = soff[o], b = soff[o + 1];
+                    while (a < b) {
+                        const unsigned mid = (a + b) >> 1;
+                        const unsigned x = lists[mid];
+                        if (o < r ? x >= v : x > v)
+                            a = mid + 1;
+                        else
+                            b = mid;
+                    }
+                    place += a - soff[o];
+                }
+                S.samp[place] = v;
+            }
+            __syncthreads();
+            if (w == 0) {
+                // R - 1 splitters at even positions of the sorted sample,
+                // about kRangeKeys keys apart.  A splitter value that repeats
+                // at a neighbouring position (a value holding a range's worth
+                // of keys) also bounds a range holding only that value, which
+                // needs no sorting.  The last range ends at T + 1.
+                // At least 4 samples per range keep the ranges' sizes close
+                // to their mean.
+                const unsigned R =
+                    min(min(kMaxPlanned, max(1u, ns / 4)), max(1u, (total + kRangeKeys - 1) / kRangeKeys));
+                unsigned bnd[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // candidates at positions jj * 32 + lane
 #pragma unroll
-                for (int jj = 0; jj < (int)(kPlanSamples / 32); ++jj) S.samp[jj * 32 + lane] = v[jj];
-                __syncwarp();
-                const unsigned R = min(kMaxPlanned, max(1u, (total + kRangeKeys - 1) / kRangeKeys));
-                unsigned bnd[4] = {0u, 0u, 0u, 0u};  // candidate bounds at positions jj * 32 + lane; 0 = none
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < 4; ++h) {
                     const unsigned q = lane + 1 + 32 * h;  // splitter q of 1 .. R-1
                     if (q < R) {
                         const unsigned c = S.samp[q * ns / R];
@@ -795,111 +884,157 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
                         bnd[2 * h + 1] = (dup && c != 0xFFFFFFFFu) ? c + 1 : 0u;
                     }
                 }
-                if (lane == 31) bnd[3] = T + 1;  // position 127: no splitter lands there (R <= 48)
+                if (lane == 31) bnd[7] = T + 1;  // position 255: no splitter lands there (R <= 128)
                 warp_sort_desc(bnd, (int)lane);
-                // Keep the distinct nonzero bounds, in descending order.
+                // The distinct nonzero bounds, in descending order.
+                unsigned nr = 0;
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
+                for (int jj = 0; jj < 8; ++jj) {
                     const unsigned prev_in_warp = __shfl_up_sync(kFullMask, bnd[jj], 1);
                     const unsigned prev_last = __shfl_sync(kFullMask, jj ? bnd[jj - 1] : 0u, 31);
-                    const unsigned prev = lane ? prev_in_warp : (jj ? prev_last : 0xFFFFFFFFu);
-                    const bool keep = bnd[jj] != 0u && (bnd[jj] != prev || (jj == 0 && lane == 0));
+                    const bool first = jj == 0 && lane == 0;
+                    const unsigned prev = lane ? prev_in_warp : prev_last;
+                    const bool keep = bnd[jj] != 0u && (first || bnd[jj] != prev);
                     const unsigned b = __ballot_sync(kFullMask, keep);
                     if (keep) S.lb[nr + __popc(b & lanemask_lt())] = bnd[jj];
                     nr += __popc(b);
                 }
-                __syncwarp();
-                for (unsigned i = lane; i < nr; i += 32) plan->lb[i] = S.lb[i];
+                if (lane == 0) S.nranges = nr;
             }
-            if (lane == 0) plan->nranges = nr;
+        } else if (tid == 0) {
+            S.nranges = 0u;
         }
     }
-    // Copies of the k-th key fill the rest.
+    cluster_barrier();  // rank 0's range table is out
+
+    if (rank != 0 && tid <= (unsigned)kMaxRanges) {
+        if (tid < (unsigned)kMaxRanges)
+            S.lb[tid] = ld_cluster(&S.lb[tid], 0);
+        else
+            S.nranges = ld_cluster(&S.nranges, 0);
+    }
+    if (tid < (unsigned)kMaxRanges) S.rcnt[tid] = 0u;
+    __syncthreads();
+    const unsigned nr = S.nranges;
+    if (nr) {
+        for (unsigned m = lane; m < cw; m += 32) atomicAdd(&S.rcnt[range_of(S.lb, nr, S.keys[w0 + m])], 1u);
+    }
+    __syncthreads();
+    cluster_barrier();  // every CTA's range counts are out
+
+    // part[r][q]: CTA r's keys in range q.  Range q starts at the keys of
+    // all lower ranges; this CTA's keys in it follow those of lower ranks.
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const unsigned e = tid + h * kClThreads, r = e / kMaxRanges, q = e % kMaxRanges;
+        S.part[r][q] = q < nr ? ld_cluster(&S.rcnt[q], r) : 0u;
+    }
+    __syncthreads();
+    if (w == 0) {
+        unsigned c[8], tot = 0;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+            const unsigned q = lane * 8 + h;
+            c[h] = 0;
+#pragma unroll
+            for (int r = 0; r < kClCtas; ++r) c[h] += S.part[r][q];
+            tot += c[h];
+        }
+        unsigned x = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(kFullMask, x, o);
+            if ((int)lane >= o) x += y;
+        }
+        unsigned acc = x - tot;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+            S.rstart[lane * 8 + h] = acc;
+            acc += c[h];
+        }
+        if (lane == 31) S.rstart[kMaxRanges] = acc;
+    }
+    __syncthreads();
+    if (tid < (unsigned)kMaxRanges) {
+        unsigned below = 0;
+        for (unsigned r = 0; r < rank; ++r) below += S.part[r][tid];
+        S.rpos[tid] = S.rstart[tid] + below;
+    }
+    __syncthreads();
+    if (nr) {
+        for (unsigned m = lane; m < cw; m += 32) {
+            const unsigned u = S.keys[w0 + m];
+            out[atomicAdd(&S.rpos[range_of(S.lb, nr, u)], 1u)] = value_of(u);
+        }
+    }
+    // Copies of the k-th key after the keys above it.
     for (unsigned i = total + rank * kClThreads + tid; i < (unsigned)k; i += kClCtas * kClThreads)
         out[i] = value_of(T);
+    // The range table for the sort kernel.
+    if (rank == 0) {
+        RadixPlan* plan = reinterpret_cast<RadixPlan*>(scratch + kRadixCandOffset);
+        for (unsigned i = tid; i <= (unsigned)kMaxRanges; i += kClThreads) {
+            if (i < nr) plan->lb[i] = S.lb[i];
+            if (i <= nr) plan->rstart[i] = S.rstart[i];
+        }
+        if (tid == 0) plan->nranges = nr;
+    }
+    cluster_barrier();  // no CTA exits while another may read its shared memory
     if (mode == kClFinal && rank == 0 && tid < (unsigned)kCtrlWords) reinterpret_cast<unsigned*>(rv.ctrl)[tid] = 0u;
 }
 
-// Sort kernel: CTA q sorts range q of the plan.  It reads every key above
-// the k-th (fewer than k, from L2), counts those in higher ranges for its
-// output offset, and sorts its own in shared memory; a single-value range
-// is only counted and written.
-__global__ void __launch_bounds__(kSortThreads, 1)
+// Sort kernel: warp w of CTA b sorts range q = b * kSortWarps + w of the
+// plan in place, in registers (up to kSortRegCap keys); a range of one value
+// is already in order.  A larger range (the sample missed a dense value
+// range) is sorted by its CTA in shared memory.
+template <int N>
+__device__ __forceinline__ void warp_sort_range(int32_t* __restrict__ a, unsigned sz, int lane) {
+    unsigned v[N];
+#pragma unroll
+    for (int jj = 0; jj < N; ++jj) {
+        const unsigned p = jj * 32 + lane;
+        v[jj] = p < sz ? key_of(__ldcg(a + p)) : 0u;
+    }
+    warp_sort_desc(v, lane);
+#pragma unroll
+    for (int jj = 0; jj < N; ++jj) {
+        const unsigned p = jj * 32 + lane;
+        if (p < sz) a[p] = value_of(v[jj]);
+    }
+}
+
+__device__ __forceinline__ bool single_value_range(const RadixPlan* plan, unsigned q) {
+    const unsigned lbq = __ldcg(&plan->lb[q]);
+    return q ? __ldcg(&plan->lb[q - 1]) == lbq + 1 : lbq == 0xFFFFFFFFu;
+}
+
+__global__ void __launch_bounds__(kSortWarps * 32, 1)
 radix_sort_kernel(int32_t* __restrict__ out, const unsigned char* __restrict__ scratch) {
     extern __shared__ __align__(16) unsigned radix_sort_smem[];
-    __shared__ unsigned s_fill;
-    __shared__ unsigned s_red[2][32];
     const RadixPlan* plan = reinterpret_cast<const RadixPlan*>(scratch + kRadixCandOffset);
-    const unsigned* buf = reinterpret_cast<const unsigned*>(scratch + kRadixBufOffset);
-    const unsigned q = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    if (q >= __ldcg(&plan->nranges)) return;
-    const unsigned lb = __ldcg(&plan->lb[q]);
-    const bool has_ub = q > 0;
-    const unsigned ub = has_ub ? __ldcg(&plan->lb[q - 1]) : 0u;
-    const bool single = has_ub ? ub == lb + 1 : lb == 0xFFFFFFFFu;
-    if (tid == 0) s_fill = 0u;
-    __syncthreads();
-    // The keys above the k-th, as one index space over the CTAs' parts.
-    unsigned seg_off[kClCtas], seg_start[kClCtas], total = 0;
-#pragma unroll
-    for (int r = 0; r < kClCtas; ++r) {
-        seg_off[r] = __ldcg(&plan->seg_off[r]);
-        seg_start[r] = total;
-        total += __ldcg(&plan->seg_cnt[r]);
+    const unsigned nr = __ldcg(&plan->nranges);
+    const unsigned q0 = blockIdx.x * kSortWarps;
+    if (q0 >= nr) return;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const unsigned q = q0 + w;
+    if (q < nr && !single_value_range(plan, q)) {
+        const unsigned s0 = __ldcg(&plan->rstart[q]), sz = __ldcg(&plan->rstart[q + 1]) - s0;
+        if (sz >= 2 && sz <= 256)
+            warp_sort_range<8>(out + s0, sz, lane);
+        else if (sz > 256 && sz <= (unsigned)kSortRegCap)
+            warp_sort_range<16>(out + s0, sz, lane);
+
     }
-    unsigned above = 0, inr = 0;
-    constexpr int kLd = 8;
-    for (unsigned base = 0; base < total; base += kLd * kSortThreads) {
-        unsigned v[kLd];
-#pragma unroll
-        for (int u = 0; u < kLd; ++u) {
-            const unsigned g = min(base + u * kSortThreads + tid, total - 1);
-            unsigned off = seg_off[0] + g;
-#pragma unroll
-            for (int r = 1; r < kClCtas; ++r)
-                if (g >= seg_start[r]) off = seg_off[r] + (g - seg_start[r]);
-            v[u] = __ldcg(buf + off);
-        }
-#pragma unroll
-        for (int u = 0; u < kLd; ++u) {
-            const bool ok = base + u * kSortThreads + tid < total;
-            above += (ok && has_ub && v[u] >= ub) ? 1u : 0u;
-            const bool p = ok && v[u] >= lb && (!has_ub || v[u] < ub);
-            inr += p ? 1u : 0u;
-            if (!single) {
-                const unsigned b = __ballot_sync(kFullMask, p);
-                if (b) {
-                    const int leader = __ffs(b) - 1;
-                    unsigned pos = 0;
-                    if ((int)lane == leader) pos = atomicAdd(&s_fill, (unsigned)__popc(b));
-                    pos = __shfl_sync(kFullMask, pos, leader);
-                    if (p) radix_sort_smem[pos + __popc(b & lanemask_lt())] = v[u];
-                }
-            }
-        }
+    for (unsigned qq = q0; qq < q0 + kSortWarps && qq < nr; ++qq) {
+        const unsigned s0 = __ldcg(&plan->rstart[qq]), sz = __ldcg(&plan->rstart[qq + 1]) - s0;
+        if (sz <= (unsigned)kSortRegCap || single_value_range(plan, qq)) continue;
+        __syncthreads();
+        const int L = next_pow2((int)sz);
+        for (int i = threadIdx.x; i < L; i += blockDim.x)
+            radix_sort_smem[i] = (unsigned)i < sz ? key_of(__ldcg(out + s0 + i)) : 0u;
+        block_sort_smem_desc(radix_sort_smem, L);
+        for (unsigned i = threadIdx.x; i < sz; i += blockDim.x) out[s0 + i] = value_of(radix_sort_smem[i]);
     }
-    above = __reduce_add_sync(kFullMask, above);
-    inr = __reduce_add_sync(kFullMask, inr);
-    if (lane == 0) {
-        s_red[0][w] = above;
-        s_red[1][w] = inr;
-    }
-    __syncthreads();
-    above = 0;
-    inr = 0;
-#pragma unroll
-    for (int i = 0; i < kSortThreads / 32; ++i) {
-        above += s_red[0][i];
-        inr += s_red[1][i];
-    }
-    if (single) {
-        for (unsigned i = tid; i < inr; i += kSortThreads) out[above + i] = value_of(lb);
-        return;
-    }
-    const int L = next_pow2((int)max(inr, 2u));
-    for (unsigned i = inr + tid; i < (unsigned)L; i += kSortThreads) radix_sort_smem[i] = 0u;
-    block_sort_smem_desc(radix_sort_smem, L);
-    for (unsigned i = tid; i < inr; i += kSortThreads) out[above + i] = value_of(radix_sort_smem[i]);
 }
 
 struct RadixFit {
@@ -957,9 +1092,10 @@ cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int
     auto* sc = static_cast<unsigned char*>(scratch);
     const unsigned ucap = (unsigned)cap;
     const size_t cl_smem = sizeof(ClSmem), sort_smem = kSortCap * sizeof(unsigned);
+    constexpr int sort_grid = kMaxRanges / kSortWarps;
     if (n <= cap) {
         radix_cluster_kernel<<<kClCtas, kClThreads, cl_smem, s>>>(in, n, k, 0u, out, sc, ucap, kClFull);
-        radix_sort_kernel<<<kMaxRanges, kSortThreads, sort_smem, s>>>(out, sc);
+        radix_sort_kernel<<<sort_grid, kSortWarps * 32, sort_smem, s>>>(out, sc);
         *launches = 2;
         return cudaGetLastError();
     }
@@ -980,7 +1116,7 @@ cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int
     radix_exact2_kernel<<<(int)grid, kRThreads, 0, s>>>(in, n, sc, ucap);
     radix_exact3_kernel<<<(int)grid, kRThreads, 0, s>>>(in, n, sc, ucap);
     radix_cluster_kernel<<<kClCtas, kClThreads, cl_smem, s>>>(in, n, k, 0u, out, sc, ucap, kClFinal);
-    radix_sort_kernel<<<kMaxRanges, kSortThreads, sort_smem, s>>>(out, sc);
+    radix_sort_kernel<<<sort_grid, kSortWarps * 32, sort_smem, s>>>(out, sc);
     *launches = 7;
     return cudaGetLastError();
 }

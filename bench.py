@@ -89,6 +89,7 @@ def load_peaks():
 KERNEL_SOURCES = {
     "topk_i32_stream_kernel": ("topk_i32.cu", "topk_device.cuh", "topk_internal.h"),
     "topk_rows_stream_kernel": ("topk_rows.cu", "topk_device.cuh", "topk_internal.h"),
+    "radix_filter_kernel": ("topk_radix.cu", "topk_device.cuh", "topk_internal.h"),
 }
 
 
@@ -217,6 +218,8 @@ def run_ours(args, world, rank, local):
 
     # Rows workload (the batched float32 TopK with indices), same device.
     rows_line = run_rows(tk, dev, stream, args) if not args.skip_rows else None
+    # The large-k plan (radix select) on the same input.
+    large_k_line = run_large_k(tk, x, stream, args) if not args.skip_rows else None
 
     # End to end through the C ABI with host buffers: the library copies the
     # pinned input to the device, selects, and copies the k results back.
@@ -273,6 +276,8 @@ def run_ours(args, world, rank, local):
     }
     if rows_line is not None:
         line["rows_f32"] = rows_line
+    if large_k_line is not None:
+        line["large_k"] = large_k_line
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline_leg(x_host.numpy(), result)
     return line
@@ -313,6 +318,50 @@ def run_rows(tk, dev, stream, args):
                          "frac": round(gbs / peak, 4), "kernel": "topk_rows_stream_kernel<2> (k<=64)",
                          "algorithmic_bytes_per_launch": rows * cols * 4 + rows * k * 8,
                          "traffic": recorded_traffic("topk_rows_stream_kernel", "rows_4096x32768_k64_tied")}}
+
+
+LARGE_K = (1000, 32768)
+
+
+def run_large_k(tk, x, stream, args):
+    """topk_i32 with k above the streaming plan's limit (the radix-select
+    plan: sample, filter pass, cluster select, range sort) on the 1e8 input
+    already on the device.  The roofline counts one read of the input."""
+    n = x.numel()
+    peak, _ = load_peaks()
+    h = stream.cuda_stream
+    res = {}
+    for k in LARGE_K:
+        out = torch.empty(k, dtype=torch.int32, device=x.device)
+
+        def step():
+            rc = tk.topk_i32_ptr(x.data_ptr(), n, k, out.data_ptr(), h)
+            if rc != 0:
+                raise tk.TopKError(rc, "topk_i32 (large k)")
+
+        for _ in range(5):
+            step()
+        torch.cuda.synchronize()
+        steps = max(10, min(200, args.steps // 20))
+        l0 = tk.launch_count()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / steps
+        gbs = 4.0 * n / (ms / 1e3) / 1e9
+        res[f"k{k}"] = {"steps": steps, "ms_per_step": round(ms, 5),
+                        "value": round(n / (ms / 1e3) / 1e9, 3), "unit": UNIT,
+                        "launches_per_step": (tk.launch_count() - l0) // steps,
+                        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                                     "frac": round(gbs / peak, 4), "algorithmic_bytes_per_launch": 4 * n,
+                                     "kernel": "whole plan (dominant kernel: radix_filter_kernel)",
+                                     "traffic_dominant_kernel": recorded_traffic("radix_filter_kernel",
+                                                                                 "i32_uniform_1e8_k1000")}}
+    res["workload"] = "int32 TopK, N=1e8 uniform full range (seed 2), k in (1000, 32768), sorted descending"
+    return res
 
 
 def cpu_baseline_leg(x: np.ndarray, gpu_result: np.ndarray):
@@ -372,7 +421,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-cpu", action="store_true", help="leave out the CPU-baseline leg")
-    ap.add_argument("--skip-rows", action="store_true", help="leave out the row-TopK measurement")
+    ap.add_argument("--skip-rows", action="store_true", help="leave out the row-TopK and large-k measurements")
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="--impl reference: seconds of oracle work for the whole run (sets the sample size)")
     args = ap.parse_args()

@@ -29,7 +29,7 @@ _libs: dict = {}
 # Deliberately wrong variants, built only by the tests that show the pins
 # reject them.  The plain build defines none of these.
 PLANTED = ("ORACLE_PLANT_ASCENDING", "ORACLE_PLANT_DEDUP", "ORACLE_PLANT_UNSTABLE",
-           "ORACLE_PLANT_NAN_LOW", "ORACLE_PLANT_SIGNED_ZERO")
+           "ORACLE_PLANT_NAN_LOW", "ORACLE_PLANT_SIGNED_ZERO", "ORACLE_PLANT_SUM_WRAP", "ORACLE_PLANT_ZERO_ORDER")
 
 
 def _lib_path(plant):
@@ -65,6 +65,10 @@ def load(plant: str | None = None):
             lib.oracle_topk_rows_f32.restype = ci
             lib.oracle_check_topk_i32.argtypes = [vp, sz, ci, vp]
             lib.oracle_check_topk_i32.restype = ci
+            lib.oracle_reduce_i32.argtypes = [vp, sz, ci, vp]
+            lib.oracle_reduce_i32.restype = ci
+            lib.oracle_reduce_f32.argtypes = [vp, sz, ci, vp]
+            lib.oracle_reduce_f32.restype = ci
             _libs[plant] = lib
     return lib
 
@@ -107,3 +111,27 @@ def check_topk_i32(x, k: int, out) -> bool:
     if rc < 0:
         raise OracleError(f"oracle_check_topk_i32 rejected n={a.size} k={k}")
     return rc == 1
+
+
+REDUCE_OPS = {"sum": 0, "max": 1, "min": 2}
+
+
+def reduce_i32(x, op: str, plant: str | None = None) -> int:
+    """Sum (exact, int64), max or min of an int32 array."""
+    a = np.ascontiguousarray(x, dtype=np.int32).reshape(-1)
+    out = np.zeros(1, dtype=np.int64)
+    rc = load(plant).oracle_reduce_i32(a.ctypes.data, a.size, REDUCE_OPS[op], out.ctypes.data)
+    if rc != 0:
+        raise OracleError(f"oracle_reduce_i32 rejected n={a.size} op={op}")
+    return int(out[0])
+
+
+def reduce_f32(x, op: str, plant: str | None = None) -> float:
+    """Sum (left to right in double), max or min (NaN if any NaN; -0 below
+    +0) of a float32 array, as a Python float (a double)."""
+    a = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    out = np.zeros(1, dtype=np.float64)
+    rc = load(plant).oracle_reduce_f32(a.ctypes.data, a.size, REDUCE_OPS[op], out.ctypes.data)
+    if rc != 0:
+        raise OracleError(f"oracle_reduce_f32 rejected n={a.size} op={op}")
+    return float(out[0])

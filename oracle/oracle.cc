@@ -12,7 +12,10 @@
 //     descending.
 //   * section 6: update_candidates(candidates, k, item, score) -- the same
 //     selection keyed by a score that carries an item id; here a row of
-//     float32 scores whose item id is the column index.
+//     float32 scores whose item id is the column index.  The same section
+//     names the two-stage reduction pattern as a general tool (sums and
+//     other statistics); "CUDA reduction, complete guide" builds it for
+//     sums level by level.  oracle_reduce_* are the plain definitions.
 //
 // The method is exact, so the oracle is the plain definition:
 //   topk_i32:      copy, std::sort descending, take the first k.  The output
@@ -39,6 +42,7 @@
 #include <cstdint>
 #include <cstring>
 #include <functional>
+#include <limits>
 #include <numeric>
 #include <vector>
 
@@ -144,6 +148,75 @@ int oracle_check_topk_i32(const int32_t* in, size_t n, int k, const int32_t* out
     for (size_t j = above.size(); j < (size_t)k; ++j)
         if (out[j] != t) return 0;
     return 1;
+}
+
+// Reductions (sum, max, min) over int32 and float32 arrays.
+//
+// op 0 = sum, 1 = max, 2 = min.
+//   int32: the sum is exact in int64 (no wrap); max and min are the plain
+//          extremes, widened to int64.
+//   float32: the sum is accumulated left to right in double (so it differs
+//          from the exact sum by at most n * 2^-53 * sum|x|); NaN or
+//          +inf + -inf give NaN, as in IEEE arithmetic.  max and min use the
+//          IEEE 754-2019 maximum/minimum reading: any NaN gives NaN (written
+//          as the canonical quiet NaN), and -0 counts as below +0.  The
+//          result is widened to double, which is exact.
+// Returns 0, or -1 for invalid arguments.
+int oracle_reduce_i32(const int32_t* in, size_t n, int op, int64_t* out) {
+    if (!in || !out || n == 0 || op < 0 || op > 2) return -1;
+#if defined(ORACLE_PLANT_SUM_WRAP)
+    int32_t acc32 = 0;  // planted mistake: a 32-bit accumulator that wraps
+    for (size_t i = 0; i < n; ++i) acc32 = (int32_t)((uint32_t)acc32 + (uint32_t)in[i]);
+    if (op == 0) {
+        *out = acc32;
+        return 0;
+    }
+#endif
+    int64_t acc = op == 0 ? 0 : (int64_t)in[0];
+    for (size_t i = 0; i < n; ++i) {
+        const int64_t x = in[i];
+        if (op == 0)
+            acc += x;
+        else if (op == 1)
+            acc = x > acc ? x : acc;
+        else
+            acc = x < acc ? x : acc;
+    }
+    *out = acc;
+    return 0;
+}
+
+int oracle_reduce_f32(const float* in, size_t n, int op, double* out) {
+    if (!in || !out || n == 0 || op < 0 || op > 2) return -1;
+    if (op == 0) {
+        double acc = 0.0;
+        for (size_t i = 0; i < n; ++i) acc += (double)in[i];
+        *out = acc;
+        return 0;
+    }
+    bool any_nan = false;
+    float best = in[0];
+    for (size_t i = 0; i < n; ++i) {
+        const float x = in[i];
+        if (std::isnan(x)) {
+            any_nan = true;
+            continue;
+        }
+        if (std::isnan(best)) {
+            best = x;
+            continue;
+        }
+#if defined(ORACLE_PLANT_ZERO_ORDER)
+        const bool better = op == 1 ? x > best : x < best;  // planted mistake: +-0 ties keep the first
+#else
+        const bool zeros = x == 0.0f && best == 0.0f;
+        const bool better = op == 1 ? (x > best || (zeros && std::signbit(best) && !std::signbit(x)))
+                                    : (x < best || (zeros && !std::signbit(best) && std::signbit(x)));
+#endif
+        if (better) best = x;
+    }
+    *out = any_nan ? std::numeric_limits<double>::quiet_NaN() : (double)best;
+    return 0;
 }
 
 }  // extern "C"

@@ -28,6 +28,14 @@ def rows_cases():
                np.array([float(v) for v in vals.split()], dtype=np.float32))
 
 
+def reduce_cases():
+    for dtype, op, inp, exp in _lines("reduce_hand.txt"):
+        if dtype == "i32":
+            yield dtype, op, np.array([int(v) for v in inp.split()], dtype=np.int32), int(exp)
+        else:
+            yield dtype, op, np.array([float(v) for v in inp.split()], dtype=np.float32), float(exp)
+
+
 def bits(a):
     return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
 

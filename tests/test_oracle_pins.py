@@ -7,7 +7,10 @@
 * closed forms (ascending input, k = 1 is the maximum, k = n is a full
   descending sort done by numpy, all-equal input);
 * invariants on random inputs (sorted, sub-multiset, k-th value rank);
-* for rows, numpy's stable argsort on inputs without NaN.
+* for rows, numpy's stable argsort on inputs without NaN;
+* for reductions: Python's exact integers, math.fsum (the correctly rounded
+  sum of floats) within the double-precision bound, and an order written
+  out with Python keys for max/min over NaN and signed zeros.
 
 The planted-mistake test at the end rebuilds the oracle with one plausible
 bug at a time (on the CPU) and shows that at least one pin rejects it.
@@ -21,7 +24,7 @@ import numpy as np
 import pytest
 
 import oracle
-from _golden import bits, i32_cases, rows_cases
+from _golden import bits, i32_cases, reduce_cases, rows_cases
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
@@ -130,8 +133,65 @@ def pin_rows_numpy(plant=None):
         assert np.array_equal(bits(vals), bits(np.take_along_axis(x, exp_idx, axis=1)))
 
 
+def _same_double(a, b):
+    return (math.isnan(a) and math.isnan(b)) or (a == b and math.copysign(1.0, a) == math.copysign(1.0, b))
+
+
+def pin_golden_reduce(plant=None):
+    for dtype, op, x, exp in reduce_cases():
+        got = oracle.reduce_i32(x, op, plant=plant) if dtype == "i32" else oracle.reduce_f32(x, op, plant=plant)
+        assert got == exp if dtype == "i32" else _same_double(got, exp), (dtype, op, x.tolist(), got, exp)
+
+
+def _py_extreme(values, op):
+    # IEEE 754-2019 maximum/minimum: NaN wins; otherwise order by value, with
+    # -0.0 below +0.0 (the sign bit as a tie-break).
+    if any(math.isnan(v) for v in values):
+        return math.nan
+    key = lambda v: (v, math.copysign(1.0, v))
+    return max(values, key=key) if op == "max" else min(values, key=key)
+
+
+def pin_exhaustive_reduce(plant=None, max_n=4):
+    for n in range(1, max_n + 1):
+        for combo in itertools.product(I32_ALPHABET, repeat=n):
+            x = np.array(combo, dtype=np.int32)
+            assert oracle.reduce_i32(x, "sum", plant=plant) == sum(combo), combo
+            assert oracle.reduce_i32(x, "max", plant=plant) == max(combo), combo
+            assert oracle.reduce_i32(x, "min", plant=plant) == min(combo), combo
+        for combo in itertools.product(F32_ALPHABET, repeat=min(n, 3)):
+            x = np.array(combo, dtype=np.float32)
+            vals = [float(v) for v in x]
+            for op in ("max", "min"):
+                assert _same_double(oracle.reduce_f32(x, op, plant=plant), _py_extreme(vals, op)), (combo, op)
+            exact = math.fsum(vals) if not any(math.isnan(v) for v in vals) and not (
+                math.inf in vals and -math.inf in vals) else math.nan
+            assert _same_double(oracle.reduce_f32(x, "sum", plant=plant) + 0.0, exact + 0.0), combo
+
+
+def pin_closed_forms_reduce(plant=None):
+    n = 100_001
+    asc = np.arange(n, dtype=np.int32)
+    assert oracle.reduce_i32(asc, "sum", plant=plant) == n * (n - 1) // 2
+    big = np.full(70_000, INT_MAX, dtype=np.int32)  # a 32-bit running sum would wrap
+    assert oracle.reduce_i32(big, "sum", plant=plant) == 70_000 * INT_MAX
+    rng = np.random.default_rng(13)
+    x = rng.integers(INT_MIN, INT_MAX, size=200_000, endpoint=True, dtype=np.int64).astype(np.int32)
+    assert oracle.reduce_i32(x, "sum", plant=plant) == int(x.astype(np.int64).sum())
+    assert oracle.reduce_i32(x, "max", plant=plant) == int(x.max())
+    assert oracle.reduce_i32(x, "min", plant=plant) == int(x.min())
+    f = (rng.standard_normal(300_000) * 1e3).astype(np.float32)
+    s = oracle.reduce_f32(f, "sum", plant=plant)
+    vals = f.astype(np.float64)
+    bound = f.size * 2.0 ** -53 * float(np.abs(vals).sum())
+    assert abs(s - math.fsum(vals.tolist())) <= bound
+    assert oracle.reduce_f32(f, "max", plant=plant) == float(f.max())
+    assert oracle.reduce_f32(f, "min", plant=plant) == float(f.min())
+
+
 ALL_PINS = [pin_golden_i32, pin_golden_rows, pin_exhaustive_i32, pin_exhaustive_rows,
-            pin_closed_forms_i32, pin_rows_numpy]
+            pin_closed_forms_i32, pin_rows_numpy, pin_golden_reduce, pin_exhaustive_reduce,
+            pin_closed_forms_reduce]
 
 
 # ------------------------------------------------------------------ tests --
@@ -249,6 +309,25 @@ def test_checker_rejects_wrong_results():
     assert not oracle.check_topk_i32(y, 2, np.array([3, 3], dtype=np.int32))
 
 
+def test_golden_reduce():
+    pin_golden_reduce()
+
+
+def test_exhaustive_reduce():
+    pin_exhaustive_reduce()
+
+
+def test_closed_forms_reduce():
+    pin_closed_forms_reduce()
+
+
+def test_reduce_rejects_bad_arguments():
+    with pytest.raises(oracle.OracleError):
+        oracle.reduce_i32(np.zeros(0, dtype=np.int32), "sum")
+    with pytest.raises(KeyError):
+        oracle.reduce_f32(np.zeros(3, dtype=np.float32), "mean")
+
+
 # -------------------------------------------- planted mistakes (CPU only) --
 
 @pytest.mark.parametrize("plant", oracle.PLANTED)
@@ -260,6 +339,8 @@ def test_pins_reject_planted_mistake(plant):
                 pin(plant=plant, max_n=4)
             elif pin is pin_exhaustive_rows:
                 pin(plant=plant, max_cols=3)
+            elif pin is pin_exhaustive_reduce:
+                pin(plant=plant, max_n=3)
             else:
                 pin(plant=plant)
         except AssertionError:

@@ -220,6 +220,8 @@ def run_ours(args, world, rank, local):
     rows_line = run_rows(tk, dev, stream, args) if not args.skip_rows else None
     # The large-k plan (radix select) on the same input.
     large_k_line = run_large_k(tk, x, stream, args) if not args.skip_rows else None
+    # Two-stage reductions (sum of the int32 input; sum of a float32 copy).
+    reduce_line = run_reduce(tk, x, stream, args) if not args.skip_rows else None
 
     # End to end through the C ABI with host buffers: the library copies the
     # pinned input to the device, selects, and copies the k results back.
@@ -278,6 +280,8 @@ def run_ours(args, world, rank, local):
         line["rows_f32"] = rows_line
     if large_k_line is not None:
         line["large_k"] = large_k_line
+    if reduce_line is not None:
+        line["reduce"] = reduce_line
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline_leg(x_host.numpy(), result)
     return line
@@ -364,6 +368,45 @@ def run_large_k(tk, x, stream, args):
     return res
 
 
+def run_reduce(tk, x, stream, args):
+    """topk_reduce_i32 (sum) on the 1e8 int32 input and topk_reduce_f32 (sum)
+    on a float32 array of the same size; one launch per call, 4 bytes read
+    per element."""
+    n = x.numel()
+    peak, _ = load_peaks()
+    h = stream.cuda_stream
+    xf = (x.to(torch.float64) * 2.0 ** -31).to(torch.float32)
+    res = {}
+    for name, t, is_float, odt in (("i32_sum", x, False, torch.int64), ("f32_sum", xf, True, torch.float64)):
+        out = torch.empty(1, dtype=odt, device=x.device)
+
+        def step():
+            rc = tk.reduce_ptr(t.data_ptr(), n, is_float, 0, out.data_ptr(), h)
+            if rc != 0:
+                raise tk.TopKError(rc, "topk_reduce")
+
+        for _ in range(5):
+            step()
+        torch.cuda.synchronize()
+        steps = max(10, min(200, args.steps // 20))
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / steps
+        gbs = 4.0 * n / (ms / 1e3) / 1e9
+        res[name] = {"steps": steps, "ms_per_step": round(ms, 5), "value": round(n / (ms / 1e3) / 1e9, 3),
+                     "unit": UNIT,
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                                  "frac": round(gbs / peak, 4), "algorithmic_bytes_per_launch": 4 * n,
+                                  "kernel": "reduce_kernel (one launch per call)"}}
+    del xf
+    res["workload"] = "sum of N=1e8 int32 (seed 2) and of the same values scaled to float32"
+    return res
+
+
 def cpu_baseline_leg(x: np.ndarray, gpu_result: np.ndarray):
     """The oracle (single-threaded std::sort, untuned) on the host cores of
     this box, over the whole 1e8 input once; also confirms the GPU result."""
@@ -421,7 +464,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-cpu", action="store_true", help="leave out the CPU-baseline leg")
-    ap.add_argument("--skip-rows", action="store_true", help="leave out the row-TopK and large-k measurements")
+    ap.add_argument("--skip-rows", action="store_true", help="leave out the row-TopK, large-k and reduction measurements")
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="--impl reference: seconds of oracle work for the whole run (sets the sample size)")
     args = ap.parse_args()

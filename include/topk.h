@@ -107,6 +107,38 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
 int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
                   struct CUstream_st* stream);
 
+/* Operations of topk_reduce_i32 / topk_reduce_f32. */
+enum topk_reduce_op { TOPK_REDUCE_SUM = 0, TOPK_REDUCE_MAX = 1, TOPK_REDUCE_MIN = 2 };
+
+/*
+ * topk_reduce_i32 / topk_reduce_f32 -- the sum, maximum or minimum of
+ * in[0..n), in one launch: the two-stage block/warp reduction of "CUDA
+ * reduction, complete guide" (its warp-shuffle level and multi-level
+ * system), which the TopK page (section 6) names as the same pattern as the
+ * TopK.  Every block reduces its share to one partial; the last block to
+ * finish reduces the partials.
+ *
+ *   in     int32[n] or float32[n], read-only; any 4-byte-aligned address.
+ *   n      1 <= n <= 2^40.
+ *   op     TOPK_REDUCE_SUM, TOPK_REDUCE_MAX or TOPK_REDUCE_MIN.
+ *   out    one int64_t (int32 input) or one double (float32 input), written;
+ *          8-byte aligned.
+ *
+ * int32: the sum is exact (int64, no wrap); max and min are widened to int64.
+ * float32 max/min: IEEE 754-2019 maximum/minimum -- any NaN gives the
+ *   canonical quiet NaN, and -0.0 counts as below +0.0; exact.
+ * float32 sum: pairwise float32 sums of 4, added with compensation over
+ *   batches of 32 elements and folded into doubles; the result is within
+ *   2^-22 * sum|x| (plus double rounding) of the exact sum.  +inf, -inf and NaN propagate as in IEEE arithmetic.
+ *   A batch whose float partial sum passes FLT_MAX (inputs near 1e37 and
+ *   above) gives inf.
+ * Pointers may be device or host memory, as for topk_i32.
+ * Returns TOPK_OK or an error code (TOPK_ERR_INVALID_ARG for a null pointer,
+ * n == 0, an unknown op or misalignment); on error out is not written.
+ */
+int topk_reduce_i32(const int32_t* in, size_t n, int op, int64_t* out, struct CUstream_st* stream);
+int topk_reduce_f32(const float* in, size_t n, int op, double* out, struct CUstream_st* stream);
+
 /* Bytes of the device array that topk_i32_noalloc uses as scratch. */
 #define TOPK_NOALLOC_SCRATCH_BYTES (1u << 20)
 

@@ -23,7 +23,8 @@ from . import build as _build
 
 __all__ = ["topk_i32", "topk_rows_f32", "topk_i32_ptr", "topk_rows_f32_ptr", "TopKError", "MAX_K", "MAX_K_ROWS",
            "status_string", "release_workspace", "launch_count", "last_cuda_error", "library_path",
-           "check_stream", "set_option", "OPT_STAGE2_CAP", "OPT_RADIX_CAP", "OPT_RADIX_SAMPLE_RANK"]
+           "check_stream", "set_option", "OPT_STAGE2_CAP", "OPT_RADIX_CAP", "OPT_RADIX_SAMPLE_RANK",
+           "reduce", "reduce_ptr", "REDUCE_OPS"]
 
 MAX_K = 32768       # topk_i32
 MAX_K_ROWS = 1024   # topk_rows_f32
@@ -63,6 +64,10 @@ def _load():
     lib.topk_check_stream.restype = ci
     lib.topk_set_option.argtypes = [ci, ci]
     lib.topk_set_option.restype = ci
+    lib.topk_reduce_i32.argtypes = [vp, sz, ci, vp, vp]
+    lib.topk_reduce_i32.restype = ci
+    lib.topk_reduce_f32.argtypes = [vp, sz, ci, vp, vp]
+    lib.topk_reduce_f32.restype = ci
     return lib
 
 
@@ -176,6 +181,37 @@ def topk_rows_f32(x: torch.Tensor, k: int, vals: torch.Tensor | None = None, idx
     if rc != TOPK_OK:
         raise TopKError(rc, "topk_rows_f32")
     return vals, idx
+
+
+REDUCE_OPS = {"sum": 0, "max": 1, "min": 2}
+
+
+def reduce_ptr(in_ptr: int, n: int, is_float: bool, op: int, out_ptr: int, stream: int = 0) -> int:
+    """Raw C-ABI call (topk_reduce_f32 if is_float else topk_reduce_i32); returns the status code."""
+    fn = _lib.topk_reduce_f32 if is_float else _lib.topk_reduce_i32
+    return int(fn(ctypes.c_void_p(in_ptr), n, op, ctypes.c_void_p(out_ptr), ctypes.c_void_p(stream)))
+
+
+def reduce(x: torch.Tensor, op: str, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Sum, max or min of an int32 or float32 tensor (flattened).  Returns a
+    one-element tensor: int64 for int32 input (exact sum), float64 for
+    float32 input (see topk_reduce_f32 in include/topk.h for its rules)."""
+    if x.dtype not in (torch.int32, torch.float32):
+        raise TypeError("x must be int32 or float32")
+    _check_input(x, x.dtype, "x")
+    is_float = x.dtype == torch.float32
+    odt = torch.float64 if is_float else torch.int64
+    if out is None:
+        out = torch.empty(1, dtype=odt, device=x.device)
+    _check_input(out, odt, "out")
+    if out.numel() != 1:
+        raise ValueError("out must have one element")
+    dev = x.device if x.is_cuda else (out.device if out.is_cuda else None)
+    with torch.cuda.device(dev) if dev is not None else _null():
+        rc = reduce_ptr(x.data_ptr(), x.numel(), is_float, REDUCE_OPS[op], out.data_ptr(), _stream_handle(stream, dev))
+    if rc != TOPK_OK:
+        raise TopKError(rc, "topk_reduce_f32" if is_float else "topk_reduce_i32")
+    return out
 
 
 class _null:

@@ -172,6 +172,58 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
     return TOPK_OK;
 }
 
+namespace {
+
+// Shared body of topk_reduce_i32 / topk_reduce_f32: in holds n 4-byte
+// values, out one 8-byte result.
+int reduce_common(const void* in, size_t n, int op, void* out, bool is_float, struct CUstream_st* stream) {
+    if (!in || !out || n == 0 || op < TOPK_REDUCE_SUM || op > TOPK_REDUCE_MIN) return TOPK_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(in) & 3u) || (reinterpret_cast<uintptr_t>(out) & 7u)) return TOPK_ERR_INVALID_ARG;
+    if (overlaps(in, n * 4, out, 8)) return TOPK_ERR_INVALID_ARG;
+    if (n > (size_t(1) << 40)) return TOPK_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e);
+    bool in_host = false, out_host = false;
+    int rc = is_host_pointer(in, &in_host);
+    if (rc == TOPK_OK) rc = is_host_pointer(out, &out_host);
+    if (rc != TOPK_OK) return rc;
+    Workspace* w = nullptr;
+    rc = workspace(s, device, topk::kReduceScratchBytes, in_host ? n * 4 : 0, out_host ? 8 : 0, &w);
+    if (rc != TOPK_OK) return rc;
+    const void* din = in;
+    void* dout = out;
+    if (in_host) {
+        e = cudaMemcpyAsync(w->stage_in, in, n * 4, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        din = w->stage_in;
+    }
+    if (out_host) dout = w->stage_out;
+    e = topk::reduce_launch(s, din, n, is_float, op, dout, w->ctrl_cand);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (out_host) {
+        e = cudaMemcpyAsync(out, dout, 8, cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (in_host || out_host) {
+        e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return TOPK_OK;
+}
+
+}  // namespace
+
+int topk_reduce_i32(const int32_t* in, size_t n, int op, int64_t* out, struct CUstream_st* stream) {
+    return reduce_common(in, n, op, out, false, stream);
+}
+
+int topk_reduce_f32(const float* in, size_t n, int op, double* out, struct CUstream_st* stream) {
+    return reduce_common(in, n, op, out, true, stream);
+}
+
 int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
                   struct CUstream_st* stream) {
     if (!in || !vals || !idx || rows < 1 || cols < 1 || k < 1 || k > cols) return TOPK_ERR_INVALID_ARG;

@@ -111,6 +111,14 @@ cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, s
 cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
                         unsigned* status);
 
+// Enqueue a one-launch reduction (op 0 sum, 1 max, 2 min) of n int32 or
+// float32 values.  out: one int64 (int32 input) or one double (float32
+// input), in device memory.  scratch: the int32 workspace (its ticket word in
+// the control line is zero and is left zero; block partials go after the
+// control area, 32 bytes per block, at most kI32MaxGrid blocks).
+cudaError_t reduce_launch(cudaStream_t s, const void* in, size_t n, bool is_float, int op, void* out, void* scratch);
+constexpr size_t kReduceScratchBytes = kI32CandOffset + (size_t)kI32MaxGrid * 32;
+
 // Bookkeeping of the C ABI layer, for entry points defined in other files:
 // record the cudaError_t behind a TOPK_ERR_CUDA, and count a kernel launch.
 void note_cuda_error(int err);

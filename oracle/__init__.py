@@ -29,7 +29,8 @@ _libs: dict = {}
 # Deliberately wrong variants, built only by the tests that show the pins
 # reject them.  The plain build defines none of these.
 PLANTED = ("ORACLE_PLANT_ASCENDING", "ORACLE_PLANT_DEDUP", "ORACLE_PLANT_UNSTABLE",
-           "ORACLE_PLANT_NAN_LOW", "ORACLE_PLANT_SIGNED_ZERO", "ORACLE_PLANT_SUM_WRAP", "ORACLE_PLANT_ZERO_ORDER")
+           "ORACLE_PLANT_NAN_LOW", "ORACLE_PLANT_SIGNED_ZERO", "ORACLE_PLANT_SUM_WRAP", "ORACLE_PLANT_ZERO_ORDER",
+           "ORACLE_PLANT_KEEP_IGNORED")
 
 
 def _lib_path(plant):
@@ -69,6 +70,8 @@ def load(plant: str | None = None):
             lib.oracle_reduce_i32.restype = ci
             lib.oracle_reduce_f32.argtypes = [vp, sz, ci, vp]
             lib.oracle_reduce_f32.restype = ci
+            lib.oracle_topk_items_f32.argtypes = [vp, vp, vp, sz, ci, vp, vp, vp]
+            lib.oracle_topk_items_f32.restype = ci
             _libs[plant] = lib
     return lib
 
@@ -135,3 +138,22 @@ def reduce_f32(x, op: str, plant: str | None = None) -> float:
     if rc != 0:
         raise OracleError(f"oracle_reduce_f32 rejected n={a.size} op={op}")
     return float(out[0])
+
+
+def topk_items_f32(score, k: int, item=None, keep=None, plant: str | None = None):
+    """Score-keyed TopK with item ids and an optional filter: (scores, items,
+    count); see oracle_topk_items_f32."""
+    sc = np.ascontiguousarray(score, dtype=np.float32).reshape(-1)
+    it = None if item is None else np.ascontiguousarray(item, dtype=np.int64).reshape(-1)
+    kp = None if keep is None else np.ascontiguousarray(keep, dtype=np.uint8).reshape(-1)
+    if it is not None and it.size != sc.size or kp is not None and kp.size != sc.size:
+        raise OracleError("item and keep must match score in size")
+    os_ = np.empty(max(k, 0), dtype=np.float32)
+    oi = np.empty(max(k, 0), dtype=np.int64)
+    cnt = np.zeros(1, dtype=np.int64)
+    rc = load(plant).oracle_topk_items_f32(sc.ctypes.data, None if it is None else it.ctypes.data,
+                                           None if kp is None else kp.ctypes.data, sc.size, int(k),
+                                           os_.ctypes.data, oi.ctypes.data, cnt.ctypes.data)
+    if rc != 0:
+        raise OracleError(f"oracle_topk_items_f32 rejected n={sc.size} k={k}")
+    return os_, oi, int(cnt[0])

@@ -11,8 +11,10 @@
 //     (section 4.2 shifts smaller entries down), so the output order is
 //     descending.
 //   * section 6: update_candidates(candidates, k, item, score) -- the same
-//     selection keyed by a score that carries an item id; here a row of
-//     float32 scores whose item id is the column index.  The same section
+//     selection keyed by a score that carries an item id: a row of float32
+//     scores whose item id is the column index (topk_rows_f32), or one
+//     array of scores with item ids and an optional filter in front
+//     (topk_items_f32); the section suggests filtering first, then TopK.  The same section
 //     names the two-stage reduction pattern as a general tool (sums and
 //     other statistics); "CUDA reduction, complete guide" builds it for
 //     sums level by level.  oracle_reduce_* are the plain definitions.
@@ -114,6 +116,42 @@ int oracle_topk_rows_f32(const float* in, int rows, int cols, int k, float* vals
             std::memcpy(&vals[(size_t)r * k + j], &row[c], sizeof(float));
         }
     }
+    return 0;
+}
+
+// Score-keyed TopK with item ids over one array (section 6's
+// update_candidates(candidates, k, item, score), composed with a filter as
+// the same section suggests): among the positions i with keep[i] != 0 (all
+// positions when keep is null), the k best by score in the row order above
+// (NaN first, -0 equal to +0, the lower position first among equal scores).
+// out_score[j] is the j-th best score (the input's bits), out_item[j] its
+// item (item[i], or i when item is null).  When fewer than k positions are
+// kept, the rest of the outputs hold -inf and item -1; *out_count is the
+// number of real entries.  Returns 0, or -1 for invalid arguments.
+int oracle_topk_items_f32(const float* score, const int64_t* item, const uint8_t* keep, size_t n, int k,
+                          float* out_score, int64_t* out_item, int64_t* out_count) {
+    if (!score || !out_score || !out_item || !out_count || n == 0 || k < 1 || (size_t)k > n) return -1;
+    std::vector<int64_t> cand;
+    for (size_t i = 0; i < n; ++i)
+#if defined(ORACLE_PLANT_KEEP_IGNORED)
+        cand.push_back((int64_t)i);  // planted mistake: the filter is ignored
+#else
+        if (!keep || keep[i]) cand.push_back((int64_t)i);
+#endif
+    auto cmp = [score](int64_t a, int64_t b) { return ranks_above(score[a], score[b]); };
+    std::stable_sort(cand.begin(), cand.end(), cmp);
+    const size_t m = cand.size() < (size_t)k ? cand.size() : (size_t)k;
+    for (size_t j = 0; j < (size_t)k; ++j) {
+        if (j < m) {
+            const int64_t i = cand[j];
+            std::memcpy(&out_score[j], &score[i], sizeof(float));
+            out_item[j] = item ? item[i] : i;
+        } else {
+            out_score[j] = -std::numeric_limits<float>::infinity();
+            out_item[j] = -1;
+        }
+    }
+    *out_count = (int64_t)m;
     return 0;
 }
 

@@ -36,6 +36,15 @@ def reduce_cases():
             yield dtype, op, np.array([float(v) for v in inp.split()], dtype=np.float32), float(exp)
 
 
+def items_cases():
+    for sc, it, kp, k, es, ei, cnt in _lines("topk_items_hand.txt"):
+        yield (np.array([float(v) for v in sc.split()], dtype=np.float32),
+               None if it == "-" else np.array([int(v) for v in it.split()], dtype=np.int64),
+               None if kp == "-" else np.array([int(v) for v in kp.split()], dtype=np.uint8), int(k),
+               np.array([float(v) for v in es.split()], dtype=np.float32),
+               np.array([int(v) for v in ei.split()], dtype=np.int64), int(cnt))
+
+
 def bits(a):
     return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
 

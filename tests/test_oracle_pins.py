@@ -24,7 +24,7 @@ import numpy as np
 import pytest
 
 import oracle
-from _golden import bits, i32_cases, reduce_cases, rows_cases
+from _golden import bits, i32_cases, items_cases, reduce_cases, rows_cases
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
@@ -189,9 +189,64 @@ def pin_closed_forms_reduce(plant=None):
     assert oracle.reduce_f32(f, "min", plant=plant) == float(f.min())
 
 
+def pin_golden_items(plant=None):
+    for sc, it, kp, k, es, ei, cnt in items_cases():
+        s_, i_, c_ = oracle.topk_items_f32(sc, k, item=it, keep=kp, plant=plant)
+        assert c_ == cnt and i_.tolist() == ei.tolist(), (sc.tolist(), k, i_.tolist(), c_)
+        assert bits(s_).tolist() == bits(es).tolist(), (sc.tolist(), k)
+
+
+def brute_items(scores, items, keep, k):
+    """Pick the best remaining kept position k times (lowest position wins
+    ties), then pad."""
+    remaining = [i for i in range(len(scores)) if keep is None or keep[i]]
+    picked = []
+    for _ in range(min(k, len(remaining))):
+        best = remaining[0]
+        for c in remaining[1:]:
+            if _rank_key(scores[c]) > _rank_key(scores[best]):
+                best = c
+        remaining.remove(best)
+        picked.append(best)
+    got_items = [items[i] if items is not None else i for i in picked] + [-1] * (k - len(picked))
+    return picked, got_items
+
+
+def pin_exhaustive_items(plant=None, max_n=4):
+    for n in range(1, max_n + 1):
+        for combo in itertools.product(F32_ALPHABET[:5], repeat=n):
+            x = np.array(combo, dtype=np.float32)
+            for mask_bits in range(2 ** n):
+                keep = np.array([(mask_bits >> i) & 1 for i in range(n)], dtype=np.uint8)
+                items = np.arange(100, 100 + n, dtype=np.int64)[::-1].copy()
+                for k in range(1, n + 1):
+                    s_, i_, c_ = oracle.topk_items_f32(x, k, item=items, keep=keep, plant=plant)
+                    picked, exp_items = brute_items(x.tolist(), items.tolist(), keep.tolist(), k)
+                    assert c_ == len(picked) and i_.tolist() == exp_items, (combo, keep.tolist(), k)
+                    assert bits(s_[:c_]).tolist() == bits(x[picked]).tolist()
+                    assert all(math.isinf(v) and v < 0 for v in s_[c_:].tolist())
+
+
+def pin_items_numpy(plant=None):
+    # Without NaN, the kept positions in numpy's stable argsort of the negated
+    # scores, first k.
+    rng = np.random.default_rng(17)
+    x = (np.round(rng.standard_normal(20_000) * 8) / 8).astype(np.float32)  # many ties
+    keep = (rng.random(x.size) < 0.3).astype(np.uint8)
+    items = rng.integers(-2**62, 2**62, size=x.size, dtype=np.int64)
+    kept = np.nonzero(keep)[0]
+    order = kept[np.argsort(-x[kept], kind="stable")]
+    for k in (1, 50, 1000):
+        s_, i_, c_ = oracle.topk_items_f32(x, k, item=items, keep=keep, plant=plant)
+        assert c_ == k and i_.tolist() == items[order[:k]].tolist()
+        assert bits(s_).tolist() == bits(x[order[:k]]).tolist()
+    s_, i_, c_ = oracle.topk_items_f32(x, 64, plant=plant)
+    assert i_.tolist() == np.argsort(-x, kind="stable")[:64].tolist()
+
+
 ALL_PINS = [pin_golden_i32, pin_golden_rows, pin_exhaustive_i32, pin_exhaustive_rows,
             pin_closed_forms_i32, pin_rows_numpy, pin_golden_reduce, pin_exhaustive_reduce,
-            pin_closed_forms_reduce]
+            pin_closed_forms_reduce, pin_golden_items, pin_exhaustive_items, pin_items_numpy]
 
 
 # ------------------------------------------------------------------ tests --
@@ -321,6 +376,18 @@ def test_closed_forms_reduce():
     pin_closed_forms_reduce()
 
 
+def test_golden_items():
+    pin_golden_items()
+
+
+def test_exhaustive_items():
+    pin_exhaustive_items()
+
+
+def test_items_numpy():
+    pin_items_numpy()
+
+
 def test_reduce_rejects_bad_arguments():
     with pytest.raises(oracle.OracleError):
         oracle.reduce_i32(np.zeros(0, dtype=np.int32), "sum")
@@ -340,6 +407,8 @@ def test_pins_reject_planted_mistake(plant):
             elif pin is pin_exhaustive_rows:
                 pin(plant=plant, max_cols=3)
             elif pin is pin_exhaustive_reduce:
+                pin(plant=plant, max_n=3)
+            elif pin is pin_exhaustive_items:
                 pin(plant=plant, max_n=3)
             else:
                 pin(plant=plant)

@@ -222,6 +222,8 @@ def run_ours(args, world, rank, local):
     large_k_line = run_large_k(tk, x, stream, args) if not args.skip_rows else None
     # Two-stage reductions (sum of the int32 input; sum of a float32 copy).
     reduce_line = run_reduce(tk, x, stream, args) if not args.skip_rows else None
+    # Score-keyed TopK with item ids, without and with a keep filter.
+    items_line = run_items(tk, dev, stream, args) if not args.skip_rows else None
 
     # End to end through the C ABI with host buffers: the library copies the
     # pinned input to the device, selects, and copies the k results back.
@@ -282,6 +284,8 @@ def run_ours(args, world, rank, local):
         line["large_k"] = large_k_line
     if reduce_line is not None:
         line["reduce"] = reduce_line
+    if items_line is not None:
+        line["items"] = items_line
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline_leg(x_host.numpy(), result)
     return line
@@ -407,6 +411,51 @@ def run_reduce(tk, x, stream, args):
     return res
 
 
+def run_items(tk, dev, stream, args):
+    """topk_items_f32 on N=1e8 N(0,1) scores (seed 2), k=64, item = position:
+    without a filter (4 bytes read per element) and with a keep mask of about
+    half the positions (score + mask = 5 bytes per element at least)."""
+    n, k = 10**8, 64
+    peak, _ = load_peaks()
+    h = stream.cuda_stream
+    sh = torch.empty(n, dtype=torch.float32).pin_memory()
+    synth.f32_normal(n, 2, out=sh.numpy())
+    sc = sh.to(dev)
+    mh = torch.from_numpy((synth.i32_uniform(n, 3) & 1).astype(np.uint8))
+    keep = mh.to(dev)
+    out_s = torch.empty(k, dtype=torch.float32, device=dev)
+    out_i = torch.empty(k, dtype=torch.int64, device=dev)
+    res = {}
+    for name, kp, bytes_per in (("no_filter", None, 4), ("keep_half", keep, 5)):
+        def step():
+            rc = tk.topk_items_f32_ptr(sc.data_ptr(), 0, kp.data_ptr() if kp is not None else 0, n, k,
+                                       out_s.data_ptr(), out_i.data_ptr(), 0, h)
+            if rc != 0:
+                raise tk.TopKError(rc, "topk_items_f32")
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        steps = max(5, min(100, args.steps // 40))
+        l0 = tk.launch_count()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / steps
+        gbs = bytes_per * n / (ms / 1e3) / 1e9
+        res[name] = {"steps": steps, "ms_per_step": round(ms, 5), "value": round(n / (ms / 1e3) / 1e9, 3),
+                     "unit": UNIT, "launches_per_step": (tk.launch_count() - l0) // steps,
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                                  "frac": round(gbs / peak, 4), "algorithmic_bytes_per_launch": bytes_per * n,
+                                  "kernel": "whole call (dominant kernel: topk_rows_stream_kernel, level 1)"}}
+    del sc, keep
+    res["workload"] = "float32 N(0,1) scores N=1e8 (seed 2), k=64, items = positions; keep = low bit of a uniform int32 stream (seed 3)"
+    return res
+
+
 def cpu_baseline_leg(x: np.ndarray, gpu_result: np.ndarray):
     """The oracle (single-threaded std::sort, untuned) on the host cores of
     this box, over the whole 1e8 input once; also confirms the GPU result."""
@@ -464,7 +513,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-cpu", action="store_true", help="leave out the CPU-baseline leg")
-    ap.add_argument("--skip-rows", action="store_true", help="leave out the row-TopK, large-k and reduction measurements")
+    ap.add_argument("--skip-rows", action="store_true", help="leave out the row-TopK, large-k, reduction and item measurements")
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="--impl reference: seconds of oracle work for the whole run (sets the sample size)")
     args = ap.parse_args()

@@ -107,6 +107,41 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
 int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
                   struct CUstream_st* stream);
 
+/*
+ * topk_items_f32 -- score-keyed TopK with item ids, with an optional filter
+ * in front ("CUDA parallel optimisation: TopK ...", section 6:
+ * update_candidates(candidates, k, item, score), and its remark that stages
+ * compose: filter first, then TopK; merge several TopK results).
+ *
+ * Among the positions i of score[0..n) with keep[i] != 0 (every position
+ * when keep is null), the k best: score descending, NaN above +inf, -0.0
+ * equal to +0.0, the lower position first among equal scores -- the order
+ * of topk_rows_f32.  out_score[j] is the j-th best score (the input's bits),
+ * out_item[j] its item: item[i], or the position i when item is null.  When
+ * fewer than k positions are kept, the remaining entries hold -inf and item
+ * -1, and *out_count (if out_count is not null) is the number of real
+ * entries.  Merging several TopK results is this call on their
+ * concatenated scores and items.
+ *
+ *   score      float32[n], device memory.
+ *   item       int64[n] or null, device memory.
+ *   keep       uint8[n] or null, device memory (nonzero = candidate).
+ *   n          1 <= n <= 2^31 - 1.
+ *   k          1 <= k <= min(n, TOPK_MAX_K_ROWS).
+ *   out_score  float32[k]; out_item int64[k]; out_count one int64 or null.
+ *
+ * The selection runs the row TopK level by level (two-stage reduction):
+ * rows of at least 8k scores give their k best, whose winners, in order,
+ * are the next level's rows, until one row is left.  With keep, an ordered
+ * compaction of the kept scores runs first, and the call waits for the
+ * kept count (a 4-byte copy to the host) before it enqueues the levels;
+ * without keep it only enqueues.  Scratch: about 8n bytes with keep, plus
+ * 24 * 4097 * k bytes, in the library's per-stream workspace.
+ * Host pointers are rejected with TOPK_ERR_INVALID_ARG.
+ */
+int topk_items_f32(const float* score, const int64_t* item, const uint8_t* keep, size_t n, int k, float* out_score,
+                   int64_t* out_item, int64_t* out_count, struct CUstream_st* stream);
+
 /* Operations of topk_reduce_i32 / topk_reduce_f32. */
 enum topk_reduce_op { TOPK_REDUCE_SUM = 0, TOPK_REDUCE_MAX = 1, TOPK_REDUCE_MIN = 2 };
 

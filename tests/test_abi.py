@@ -113,6 +113,32 @@ def test_python_binding_rejects_wrong_types(lib):
     assert e.value.status == 1
 
 
+def test_reduce_and_items_argument_errors(lib):
+    import topk_selection_gb300 as tk
+
+    buf = (ctypes.c_int32 * 64)()
+    out = (ctypes.c_int64 * 64)()
+    p, o = ctypes.addressof(buf), ctypes.addressof(out)
+    f = lib.topk_reduce_i32
+    assert f(None, 10, 0, o, None) == 1              # null input
+    assert f(p, 10, 0, None, None) == 1              # null output
+    assert f(p, 0, 0, o, None) == 1                  # n == 0
+    assert f(p, 10, 3, o, None) == 1                 # unknown op
+    assert f(p, 10, -1, o, None) == 1
+    assert f(p + 1, 10, 0, o, None) == 1             # misaligned input
+    assert f(p, 10, 0, o + 4, None) == 1             # misaligned output
+    assert lib.topk_reduce_f32(p, 10, 1, p + 8, None) == 1  # output overlaps input
+    g = lib.topk_items_f32
+    assert g(None, None, None, 10, 1, p, o, None, None) == 1   # null score
+    assert g(p, None, None, 10, 1, None, o, None, None) == 1   # null out_score
+    assert g(p, None, None, 0, 1, p + 128, o, None, None) == 1  # n == 0
+    assert g(p, None, None, 10, 11, p + 128, o, None, None) == 1  # k > n
+    assert g(p, None, None, 10, 0, p + 128, o, None, None) == 1   # k < 1
+    assert g(p, None, None, 10, 2, p, o, None, None) == 1      # out_score overlaps score
+    assert g(p, o + 4, None, 10, 2, p + 128, o + 64, None, None) == 1  # misaligned item
+    assert tk.OPT_STAGE2_CAP == 1
+
+
 def test_launch_counter_starts_at_zero_without_gpu(lib):
     import topk_selection_gb300 as tk
 

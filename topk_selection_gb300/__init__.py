@@ -24,7 +24,7 @@ from . import build as _build
 __all__ = ["topk_i32", "topk_rows_f32", "topk_i32_ptr", "topk_rows_f32_ptr", "TopKError", "MAX_K", "MAX_K_ROWS",
            "status_string", "release_workspace", "launch_count", "last_cuda_error", "library_path",
            "check_stream", "set_option", "OPT_STAGE2_CAP", "OPT_RADIX_CAP", "OPT_RADIX_SAMPLE_RANK",
-           "reduce", "reduce_ptr", "REDUCE_OPS"]
+           "reduce", "reduce_ptr", "REDUCE_OPS", "topk_items_f32", "topk_items_f32_ptr"]
 
 MAX_K = 32768       # topk_i32
 MAX_K_ROWS = 1024   # topk_rows_f32
@@ -68,6 +68,8 @@ def _load():
     lib.topk_reduce_i32.restype = ci
     lib.topk_reduce_f32.argtypes = [vp, sz, ci, vp, vp]
     lib.topk_reduce_f32.restype = ci
+    lib.topk_items_f32.argtypes = [vp, vp, vp, sz, ci, vp, vp, vp, vp]
+    lib.topk_items_f32.restype = ci
     return lib
 
 
@@ -181,6 +183,45 @@ def topk_rows_f32(x: torch.Tensor, k: int, vals: torch.Tensor | None = None, idx
     if rc != TOPK_OK:
         raise TopKError(rc, "topk_rows_f32")
     return vals, idx
+
+
+def topk_items_f32_ptr(score_ptr: int, item_ptr: int, keep_ptr: int, n: int, k: int, out_score_ptr: int,
+                       out_item_ptr: int, out_count_ptr: int, stream: int = 0) -> int:
+    """Raw C-ABI call (0 for a null item, keep or out_count); returns the status code."""
+    vp = ctypes.c_void_p
+    return int(_lib.topk_items_f32(vp(score_ptr), vp(item_ptr or None), vp(keep_ptr or None), n, k,
+                                   vp(out_score_ptr), vp(out_item_ptr), vp(out_count_ptr or None), vp(stream)))
+
+
+def topk_items_f32(score: torch.Tensor, k: int, item: torch.Tensor | None = None, keep: torch.Tensor | None = None,
+                   stream=None):
+    """Score-keyed TopK with item ids over CUDA tensors: (scores [k] float32,
+    items [k] int64, count) -- see topk_items_f32 in include/topk.h."""
+    _check_input(score, torch.float32, "score")
+    if not score.is_cuda:
+        raise ValueError("score must be a CUDA tensor")
+    n = score.numel()
+    if item is not None:
+        _check_input(item, torch.int64, "item")
+        if item.numel() != n:
+            raise ValueError("item must match score")
+    if keep is not None:
+        if keep.dtype == torch.bool:
+            keep = keep.view(torch.uint8)
+        _check_input(keep, torch.uint8, "keep")
+        if keep.numel() != n:
+            raise ValueError("keep must match score")
+    dev = score.device
+    out_score = torch.empty(max(int(k), 0), dtype=torch.float32, device=dev)
+    out_item = torch.empty(max(int(k), 0), dtype=torch.int64, device=dev)
+    out_count = torch.empty(1, dtype=torch.int64, device=dev)
+    with torch.cuda.device(dev):
+        rc = topk_items_f32_ptr(score.data_ptr(), item.data_ptr() if item is not None else 0,
+                                keep.data_ptr() if keep is not None else 0, n, int(k), out_score.data_ptr(),
+                                out_item.data_ptr(), out_count.data_ptr(), _stream_handle(stream, dev))
+    if rc != TOPK_OK:
+        raise TopKError(rc, "topk_items_f32")
+    return out_score, out_item, out_count
 
 
 REDUCE_OPS = {"sum": 0, "max": 1, "min": 2}

@@ -34,6 +34,8 @@ struct Workspace {
     size_t stage_in_bytes = 0;
     void* stage_out = nullptr;  // device buffer for host outputs
     size_t stage_out_bytes = 0;
+    void* items = nullptr;      // topk_items_f32 scratch
+    size_t items_bytes = 0;
 };
 
 std::mutex g_ws_mutex;
@@ -224,6 +226,50 @@ int topk_reduce_f32(const float* in, size_t n, int op, double* out, struct CUstr
     return reduce_common(in, n, op, out, true, stream);
 }
 
+int topk_items_f32(const float* score, const int64_t* item, const uint8_t* keep, size_t n, int k, float* out_score,
+                   int64_t* out_item, int64_t* out_count, struct CUstream_st* stream) {
+    if (!score || !out_score || !out_item || n == 0 || k < 1 || (size_t)k > n) return TOPK_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(score) | reinterpret_cast<uintptr_t>(out_score)) & 3u)
+        return TOPK_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(item) | reinterpret_cast<uintptr_t>(out_item) |
+         reinterpret_cast<uintptr_t>(out_count)) & 7u)
+        return TOPK_ERR_INVALID_ARG;
+    const size_t ko = (size_t)k;
+    if (overlaps(score, n * 4, out_score, ko * 4) || overlaps(score, n * 4, out_item, ko * 8) ||
+        overlaps(out_score, ko * 4, out_item, ko * 8) || (item && overlaps(item, n * 8, out_item, ko * 8)))
+        return TOPK_ERR_INVALID_ARG;
+    if (k > TOPK_MAX_K_ROWS) return TOPK_ERR_UNSUPPORTED;
+    if (n > (size_t)INT32_MAX) return TOPK_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e);
+    for (const void* p : {(const void*)score, (const void*)item, (const void*)keep, (const void*)out_score,
+                          (const void*)out_item, (const void*)out_count}) {
+        if (!p) continue;
+        bool host = false;
+        const int rc = is_host_pointer(p, &host);
+        if (rc != TOPK_OK) return rc;
+        if (host) return TOPK_ERR_INVALID_ARG;  // device memory only
+    }
+    Workspace* w = nullptr;
+    int rc = workspace(s, device, topk::kI32CandOffset, 0, 0, &w);
+    if (rc != TOPK_OK) return rc;
+    const size_t need = topk::items_scratch_bytes(n, k, keep != nullptr);
+    {
+        std::lock_guard<std::mutex> lock(g_ws_mutex);
+        rc = grow(&w->items, &w->items_bytes, need);
+    }
+    if (rc != TOPK_OK) return rc;
+    auto* status = reinterpret_cast<unsigned*>(static_cast<char*>(w->ctrl_cand) + topk::kI32StatusOffset);
+    int launches = 0;
+    e = topk::items_launch(s, score, item, keep, n, k, out_score, out_item, out_count, w->items, w->items_bytes,
+                           status, &launches);
+    g_launches.fetch_add((unsigned long long)launches, std::memory_order_relaxed);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return TOPK_OK;
+}
+
 int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
                   struct CUstream_st* stream) {
     if (!in || !vals || !idx || rows < 1 || cols < 1 || k < 1 || k > cols) return TOPK_ERR_INVALID_ARG;
@@ -354,7 +400,7 @@ int topk_release_workspace(void) {
     for (auto& kv : g_ws) {
         Workspace& w = kv.second;
         cudaSetDevice(kv.first.first);
-        for (void* p : {w.ctrl_cand, w.stage_in, w.stage_out})
+        for (void* p : {w.ctrl_cand, w.stage_in, w.stage_out, w.items})
             if (p && cudaFree(p) != cudaSuccess) rc = TOPK_ERR_CUDA;
     }
     g_ws.clear();

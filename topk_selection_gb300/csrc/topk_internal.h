@@ -119,6 +119,15 @@ cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int
 cudaError_t reduce_launch(cudaStream_t s, const void* in, size_t n, bool is_float, int op, void* out, void* scratch);
 constexpr size_t kReduceScratchBytes = kI32CandOffset + (size_t)kI32MaxGrid * 32;
 
+// Score-keyed TopK with item ids and an optional keep filter (topk_items.cu).
+// scratch: items_scratch_bytes(n, k, keep != null) bytes of device memory
+// (no contents needed).  With a filter the call waits for the kept count (one
+// 4-byte copy to the host) before enqueueing the selection.
+size_t items_scratch_bytes(size_t n, int k, bool filtered);
+cudaError_t items_launch(cudaStream_t s, const float* score, const int64_t* item, const uint8_t* keep, size_t n,
+                         int k, float* out_score, int64_t* out_item, int64_t* out_count, void* scratch,
+                         size_t scratch_bytes, unsigned* status, int* launches);
+
 // Bookkeeping of the C ABI layer, for entry points defined in other files:
 // record the cudaError_t behind a TOPK_ERR_CUDA, and count a kernel launch.
 void note_cuda_error(int err);

@@ -1,0 +1,477 @@
+// Score-keyed TopK with item ids, with an optional filter in front
+// ("CUDA parallel optimisation: TopK, shared memory and two-stage
+// reduction", section 6: update_candidates(candidates, k, item, score); its
+// closing remark on composing stages -- filter first, then TopK; merge
+// several TopK results).
+//
+// Among the positions i with keep[i] != 0 (every position when keep is
+// null), the k best by score -- value descending, NaN above +inf, -0 equal
+// to +0, the lower position first among equal scores -- with their scores
+// (the input bits) and items (item[i], or i when item is null).
+//
+// Plan: the page's two-stage reduction, applied level by level with the row
+// kernel (topk_rows.cu) as the block-level TopK:
+//   filter   (keep given) an ordered compaction of the kept scores and their
+//            positions: per-block counts over contiguous ranges, then every
+//            block writes its kept elements at its offset, in order.
+//   level 1  the m candidates, as rows of C >= 8k scores plus one shorter
+//            tail row: the row kernel leaves each row's k best.
+//   level j  the previous level's winners, in row order, are the next
+//            level's candidates.  Equal scores stay in position order: rows
+//            are in position order, and a row's winners with equal scores
+//            come in column order.  Repeat until one row is left.
+//   final    the last row's winners map back to input positions, items and
+//            score bits.
+// Merging several TopK results is this call on their concatenation.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "topk_device.cuh"
+#include "topk_internal.h"
+
+namespace topk {
+
+namespace {
+
+constexpr int kFiltThreads = 512;
+constexpr int kFiltMaxGrid = 1024;
+
+// Per-block counts of kept positions over contiguous ranges.
+__global__ void __launch_bounds__(kFiltThreads)
+items_count_kernel(const uint8_t* __restrict__ keep, size_t n, size_t per, unsigned* __restrict__ counts) {
+    const size_t lo = (size_t)blockIdx.x * per, hi = lo + per < n ? lo + per : n;
+    unsigned c = 0;
+    for (size_t i = lo + threadIdx.x; i < hi; i += blockDim.x) c += keep[i] != 0;
+    c = __reduce_add_sync(kFullMask, c);
+    __shared__ unsigned s[kFiltThreads / 32];
+    if ((threadIdx.x & 31) == 0) s[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned t = 0;
+        for (int w = 0; w < kFiltThreads / 32; ++w) t += s[w];
+        counts[blockIdx.x] = t;
+    }
+}
+
+// Nonzero bytes of a 32-bit word.
+__device__ __forceinline__ unsigned nonzero_bytes(unsigned w) {
+    return (unsigned)__popc((((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | w) & 0x80808080u);
+}
+
+// Vector form of the two filter kernels, for 16-byte-aligned score and keep
+// arrays and ranges of whole 16-element groups: thread t of a chunk takes
+// the 16 consecutive elements of group t (one 16-byte keep load, four
+// 16-byte score loads), kVecChunks chunks of loads in flight.
+constexpr int kVecGroup = 16;
+constexpr int kStageBytes = kFiltThreads * kVecGroup * 8;  // one chunk's kept scores and positions
+
+__global__ void __launch_bounds__(kFiltThreads)
+items_count_vec_kernel(const uint8_t* __restrict__ keep, size_t n, size_t per, unsigned* __restrict__ counts) {
+    const size_t lo = (size_t)blockIdx.x * per, hi = lo + per < n ? lo + per : n;
+    const uint4* kv = reinterpret_cast<const uint4*>(keep);
+    unsigned c = 0;
+    constexpr int kIn = 4;
+    for (size_t g0 = lo / kVecGroup + threadIdx.x; g0 * kVecGroup < hi; g0 += (size_t)kIn * blockDim.x) {
+        uint4 v[kIn];
+#pragma unroll
+        for (int u = 0; u < kIn; ++u) {
+            const size_t g = g0 + (size_t)u * blockDim.x;
+            v[u] = g * kVecGroup < hi ? __ldg(kv + g) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kIn; ++u)
+            c += nonzero_bytes(v[u].x) + nonzero_bytes(v[u].y) + nonzero_bytes(v[u].z) + nonzero_bytes(v[u].w);
+    }
+    c = __reduce_add_sync(kFullMask, c);
+    __shared__ unsigned s[kFiltThreads / 32];
+    if ((threadIdx.x & 31) == 0) s[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned t = 0;
+        for (int w = 0; w < kFiltThreads / 32; ++w) t += s[w];
+        counts[blockIdx.x] = t;
+    }
+}
+
+// Ordered compaction: block b writes its kept (score, position) pairs at the
+// sum of the counts of the blocks before it, chunk by chunk in position
+// order.  Block 0 also writes the total.
+__global__ void __launch_bounds__(kFiltThreads)
+items_compact_kernel(const float* __restrict__ score, const uint8_t* __restrict__ keep, size_t n, size_t per,
+                     const unsigned* __restrict__ counts, float* __restrict__ cs, int32_t* __restrict__ cpos,
+                     unsigned* __restrict__ total) {
+    __shared__ unsigned s_warp[kFiltThreads / 32];
+    __shared__ unsigned s_before[kFiltThreads / 32], s_all[kFiltThreads / 32];
+    __shared__ unsigned s_base;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    // This block's offset (counts of the blocks before it) and, for block 0,
+    // the total: a block-wide sum over at most kFiltMaxGrid counts.
+    {
+        unsigned before = 0, all = 0;
+        for (unsigned j = threadIdx.x; j < gridDim.x; j += blockDim.x) {
+            const unsigned c = counts[j];
+            before += j < blockIdx.x ? c : 0u;
+            all += c;
+        }
+        before = __reduce_add_sync(kFullMask, before);
+        all = __reduce_add_sync(kFullMask, all);
+        if (lane == 0) {
+            s_before[w] = before;
+            s_all[w] = all;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            unsigned b = 0, t = 0;
+            for (int j = 0; j < kFiltThreads / 32; ++j) {
+                b += s_before[j];
+                t += s_all[j];
+            }
+            s_base = b;
+            if (blockIdx.x == 0) *total = t;
+        }
+    }
+    __syncthreads();
+    unsigned base = s_base;
+    const size_t lo = (size_t)blockIdx.x * per, hi = lo + per < n ? lo + per : n;
+    for (size_t c0 = lo; c0 < hi; c0 += blockDim.x) {
+        const size_t i = c0 + threadIdx.x;
+        const bool p = i < hi && keep[i] != 0;
+        const unsigned b = __ballot_sync(kFullMask, p);
+        if (lane == 0) s_warp[w] = __popc(b);
+        __syncthreads();
+        unsigned before = 0, all = 0;
+        for (int j = 0; j < kFiltThreads / 32; ++j) {
+            const unsigned v = s_warp[j];
+            before += j < w ? v : 0u;
+            all += v;
+        }
+        if (p) {
+            const unsigned slot = base + before + __popc(b & lanemask_lt());
+            cs[slot] = score[i];
+            cpos[slot] = (int32_t)i;
+        }
+        base += all;
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(kFiltThreads)
+items_compact_vec_kernel(const float* __restrict__ score, const uint8_t* __restrict__ keep, size_t n, size_t per,
+                         const unsigned* __restrict__ counts, float* __restrict__ cs, int32_t* __restrict__ cpos,
+                         unsigned* __restrict__ total) {
+    extern __shared__ __align__(16) unsigned char items_stage_smem[];
+    float* st_s = reinterpret_cast<float*>(items_stage_smem);                                  // one chunk's kept scores
+    int32_t* st_p = reinterpret_cast<int32_t*>(items_stage_smem + kFiltThreads * kVecGroup * 4);  // and positions
+    __shared__ unsigned s_warp[kFiltThreads / 32];
+    __shared__ unsigned s_before[kFiltThreads / 32], s_all[kFiltThreads / 32];
+    __shared__ unsigned s_base;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    {
+        unsigned before = 0, all = 0;
+        for (unsigned j = threadIdx.x; j < gridDim.x; j += blockDim.x) {
+            const unsigned c = counts[j];
+            before += j < blockIdx.x ? c : 0u;
+            all += c;
+        }
+        before = __reduce_add_sync(kFullMask, before);
+        all = __reduce_add_sync(kFullMask, all);
+        if (lane == 0) {
+            s_before[w] = before;
+            s_all[w] = all;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            unsigned b = 0, t = 0;
+            for (int j = 0; j < kFiltThreads / 32; ++j) {
+                b += s_before[j];
+                t += s_all[j];
+            }
+            s_base = b;
+            if (blockIdx.x == 0) *total = t;
+        }
+    }
+    __syncthreads();
+    unsigned base = s_base;
+    const size_t lo = (size_t)blockIdx.x * per, hi = lo + per < n ? lo + per : n;
+    const uint4* kv = reinterpret_cast<const uint4*>(keep);
+    const float4* sv = reinterpret_cast<const float4*>(score);
+    for (size_t c0 = lo; c0 < hi; c0 += (size_t)blockDim.x * kVecGroup) {
+        const size_t g = c0 / kVecGroup + threadIdx.x;  // this thread's group
+        const bool in = g * kVecGroup < hi;
+        const uint4 kb = in ? __ldg(kv + g) : make_uint4(0u, 0u, 0u, 0u);
+        const unsigned words[4] = {kb.x, kb.y, kb.z, kb.w};
+        unsigned mine = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mine += nonzero_bytes(words[q]);
+        // exclusive prefix of `mine` over the block (thread order = position order)
+        unsigned x = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(kFullMask, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_warp[w] = x;
+        __syncthreads();
+        unsigned before = 0, all = 0;
+        for (int j = 0; j < kFiltThreads / 32; ++j) {
+            const unsigned v = s_warp[j];
+            before += j < w ? v : 0u;
+            all += v;
+        }
+        // This chunk's kept elements go to shared memory in position order,
+        // then out to the compacted arrays with coalesced stores.
+        unsigned slot = before + x - mine;
+        if (mine) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 f = __ldg(sv + g * 4 + q);
+                const float fs[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    if ((words[q] >> (8 * b)) & 0xFFu) {
+                        st_s[slot] = fs[b];
+                        st_p[slot] = (int32_t)(g * kVecGroup + q * 4 + b);
+                        ++slot;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        for (unsigned i = threadIdx.x; i < all; i += blockDim.x) {
+            cs[base + i] = st_s[i];
+            cpos[base + i] = st_p[i];
+        }
+        base += all;
+        __syncthreads();
+    }
+}
+
+// Next level's candidates: this level's winners of its R full rows (R x ke,
+// row r's columns counting from r * C), then the tail the rows did not cover
+// (its candidates carried over as they are), then -inf pads up to `len`.
+// Positions map through pos (null: identity).  Pads only ever sit at the end
+// of an array, after every real candidate, so under the position tie-break
+// they never beat a real one, not even a real -inf.
+__global__ void items_gather_kernel(const float* __restrict__ wv, const int32_t* __restrict__ wx, int R, int C,
+                                    int ke, const float* __restrict__ cur, const int32_t* __restrict__ pos,
+                                    size_t tail_begin, size_t tail_len, size_t len, float* __restrict__ ns,
+                                    int32_t* __restrict__ npos) {
+    const size_t nw = (size_t)R * ke;
+    for (size_t j = (size_t)blockIdx.x * blockDim.x + threadIdx.x; j < len; j += (size_t)gridDim.x * blockDim.x) {
+        float v;
+        int32_t p;
+        if (j < nw) {
+            const size_t src = (j / ke) * C + wx[j];
+            v = wv[j];
+            p = pos ? pos[src] : (int32_t)src;
+        } else if (j < nw + tail_len) {
+            const size_t src = tail_begin + (j - nw);
+            v = cur[src];
+            p = pos ? pos[src] : (int32_t)src;
+        } else {
+            v = __int_as_float(0xFF800000);  // -inf
+            p = -1;
+        }
+        ns[j] = v;
+        npos[j] = p;
+    }
+}
+
+// Order key of a score: value descending with NaN on top and -0 equal to +0
+// (the row order), then the lower array index first.
+__device__ __forceinline__ unsigned long long items_key(float v, unsigned j) {
+    const unsigned b = __float_as_uint(v);
+    unsigned k;
+    if ((b & 0x7FFFFFFFu) > 0x7F800000u)
+        k = 0xFFFFFFFFu;  // NaN
+    else if ((b & 0x7FFFFFFFu) == 0u)
+        k = 0x80000000u;  // +-0
+    else
+        k = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)k << 32) | (0xFFFFFFFFu - j);
+}
+
+// The last level: at most kFinalCap candidates (their array order is their
+// position order among equal scores) sorted in one block; the best ke map
+// to items and score bits, the rest of the k outputs are padding.
+constexpr int kFinalCap = 4096;
+constexpr int kFinalThreads = 1024;
+__global__ void __launch_bounds__(kFinalThreads)
+items_final_sort_kernel(const float* __restrict__ cv, const int32_t* __restrict__ cp, int count, int ke, int k,
+                        const int64_t* __restrict__ item, float* __restrict__ out_score,
+                        int64_t* __restrict__ out_item, int64_t* __restrict__ out_count) {
+    __shared__ unsigned long long keys[kFinalCap];
+    const int L = next_pow2(count < 2 ? 2 : count);
+    for (int j = threadIdx.x; j < L; j += blockDim.x) keys[j] = j < count ? items_key(cv[j], (unsigned)j) : 0ull;
+    block_sort_smem_desc(keys, L);
+    for (int j = threadIdx.x; j < k; j += blockDim.x) {
+        const unsigned idx = 0xFFFFFFFFu - (unsigned)(keys[j] & 0xFFFFFFFFull);
+        const int32_t p = j < ke ? (cp ? cp[idx] : (int32_t)idx) : -1;
+        if (p >= 0) {  // a pad (p = -1) never ranks among the best ke; guarded all the same
+            out_score[j] = cv[idx];
+            out_item[j] = item ? item[p] : (int64_t)p;
+        } else {
+            out_score[j] = __int_as_float(0xFF800000);
+            out_item[j] = -1;
+        }
+    }
+    if (threadIdx.x == 0 && out_count) *out_count = ke;
+}
+
+// Pads the outputs when nothing is kept.
+__global__ void items_empty_kernel(int k, float* __restrict__ out_score, int64_t* __restrict__ out_item,
+                                   int64_t* __restrict__ out_count) {
+    for (int j = threadIdx.x; j < k; j += blockDim.x) {
+        out_score[j] = __int_as_float(0xFF800000);
+        out_item[j] = -1;
+    }
+    if (threadIdx.x == 0 && out_count) *out_count = 0;
+}
+
+// Rows of the first level aim at kTargetRows (one warp per row fills the
+// GPU); later levels, whose candidates are few, at kLaterRows.  A row holds
+// at least 8 ke candidates, so every level shrinks them at least eightfold.
+constexpr size_t kTargetRows = 4096;
+constexpr size_t kLaterRows = 256;
+inline size_t level_cols(size_t count, int ke, bool first) {
+    const size_t rows = first ? kTargetRows : kLaterRows;
+    size_t c = (count + rows - 1) / rows;
+    if (c < (size_t)8 * ke) c = (size_t)8 * ke;
+    return c;
+}
+
+// Largest number of candidates a later level holds, padding included.
+inline size_t next_cap(size_t n, int k) {
+    return (kTargetRows + 1) * (size_t)k + 4 * (n / kTargetRows + 32 * (size_t)k + 2);
+}
+
+}  // namespace
+
+size_t items_scratch_bytes(size_t n, int k, bool filtered) {
+    size_t b = 0;
+    if (filtered) b += kFiltMaxGrid * 4 + 256 + n * 8 + 512;  // counts, total, compacted scores and positions
+    const size_t winners = (kTargetRows + 1) * (size_t)k;
+    b += winners * 8 + 2 * next_cap(n, k) * 8 + 6 * 256;      // winners, two candidate arrays
+    return b;
+}
+
+namespace {
+std::mutex g_items_mu;
+bool g_items_ready[64];
+}  // namespace
+
+cudaError_t items_launch(cudaStream_t s, const float* score, const int64_t* item, const uint8_t* keep, size_t n,
+                         int k, float* out_score, int64_t* out_item, int64_t* out_count, void* scratch,
+                         size_t scratch_bytes, unsigned* status, int* launches) {
+    *launches = 0;
+    if (scratch_bytes < items_scratch_bytes(n, k, keep != nullptr)) return cudaErrorInvalidValue;
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return e;
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(g_items_mu);
+        if (!g_items_ready[device]) {
+            e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&items_compact_vec_kernel),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
+            if (e != cudaSuccess) return e;
+            g_items_ready[device] = true;
+        }
+    }
+    auto* base = static_cast<unsigned char*>(scratch);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        void* p = base + off;
+        off += (bytes + 255) / 256 * 256;
+        return p;
+    };
+
+    const float* cur = score;
+    const int32_t* cur_pos = nullptr;
+    size_t m = n;
+    if (keep) {
+        const size_t per0 = (n + kFiltMaxGrid - 1) / kFiltMaxGrid;
+        const size_t per = per0 < (size_t)kFiltThreads ? (size_t)kFiltThreads : (per0 + 511) / 512 * 512;
+        const int grid = (int)((n + per - 1) / per);
+        auto* counts = static_cast<unsigned*>(take(kFiltMaxGrid * 4));
+        auto* total = static_cast<unsigned*>(take(4));
+        auto* cs = static_cast<float*>(take(n * 4));
+        auto* cp = static_cast<int32_t*>(take(n * 4));
+        // The vector kernels need 16-byte-aligned arrays and ranges of whole
+        // 16-element groups: per is a multiple of 512, and n a multiple of 16.
+        const bool vec = ((reinterpret_cast<uintptr_t>(keep) | reinterpret_cast<uintptr_t>(score)) & 15u) == 0 &&
+                         n % kVecGroup == 0;
+        if (vec) {
+            items_count_vec_kernel<<<grid, kFiltThreads, 0, s>>>(keep, n, per, counts);
+            items_compact_vec_kernel<<<grid, kFiltThreads, kStageBytes, s>>>(score, keep, n, per, counts, cs, cp,
+                                                                            total);
+        } else {
+            items_count_kernel<<<grid, kFiltThreads, 0, s>>>(keep, n, per, counts);
+            items_compact_kernel<<<grid, kFiltThreads, 0, s>>>(score, keep, n, per, counts, cs, cp, total);
+        }
+        *launches += 2;
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        // The plan of the levels depends on how many are kept: read it.
+        unsigned h = 0;
+        e = cudaMemcpyAsync(&h, total, 4, cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return e;
+        m = h;
+        cur = cs;
+        cur_pos = cp;
+        if (m == 0) {
+            items_empty_kernel<<<1, 256, 0, s>>>(k, out_score, out_item, out_count);
+            *launches += 1;
+            return cudaGetLastError();
+        }
+    }
+    const int ke = m < (size_t)k ? (int)m : k;
+    const size_t winners = (kTargetRows + 1) * (size_t)k;
+    auto* wv = static_cast<float*>(take(winners * 4));
+    auto* wx = static_cast<int32_t*>(take(winners * 4));
+    const size_t cap = next_cap(n, k);
+    float* nb_s[2] = {static_cast<float*>(take(cap * 4)), nullptr};
+    int32_t* nb_p[2] = {static_cast<int32_t*>(take(cap * 4)), nullptr};
+    nb_s[1] = static_cast<float*>(take(cap * 4));
+    nb_p[1] = static_cast<int32_t*>(take(cap * 4));
+    int flip = 0;
+    size_t len = m;      // entries of cur, pads included
+    size_t real = m;     // entries of cur that are not pads (an upper bound after level 1)
+    bool first = true;
+    for (;;) {
+        if (real <= (size_t)kFinalCap) {
+            // cur holds real entries only here (a single-row level adds no pads)
+            items_final_sort_kernel<<<1, kFinalThreads, 0, s>>>(cur, cur_pos, (int)real, ke, k, item, out_score,
+                                                                out_item, out_count);
+            *launches += 1;
+            return cudaGetLastError();
+        }
+        size_t C = level_cols(real, ke, first);
+        if (C > len) C = len;  // fewer candidates than one row of 8 ke: a single row of all of them
+        const size_t R = len / C, tail = len - R * C;  // later levels: len is a multiple of C, tail 0
+        e = rows_launch(s, cur, (int)R, (int)C, ke, wv, wx, status);
+        if (e != cudaSuccess) return e;
+        *launches += 1;
+        const size_t next_real = R * ke + tail;
+        const size_t Cn = level_cols(next_real, ke, false);
+        const size_t next_len = next_real <= (size_t)kFinalCap ? next_real : (next_real + Cn - 1) / Cn * Cn;
+        const int gb = (int)((next_len + 255) / 256 < 1024 ? (next_len + 255) / 256 : 1024);
+        items_gather_kernel<<<gb, 256, 0, s>>>(wv, wx, (int)R, (int)C, ke, cur, cur_pos, R * C, tail, next_len,
+                                               nb_s[flip], nb_p[flip]);
+        *launches += 1;
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        cur = nb_s[flip];
+        cur_pos = nb_p[flip];
+        flip ^= 1;
+        len = next_len;
+        real = next_real;
+        first = false;
+    }
+}
+
+}  // namespace topk

@@ -30,7 +30,7 @@ _libs: dict = {}
 # reject them.  The plain build defines none of these.
 PLANTED = ("ORACLE_PLANT_ASCENDING", "ORACLE_PLANT_DEDUP", "ORACLE_PLANT_UNSTABLE",
            "ORACLE_PLANT_NAN_LOW", "ORACLE_PLANT_SIGNED_ZERO", "ORACLE_PLANT_SUM_WRAP", "ORACLE_PLANT_ZERO_ORDER",
-           "ORACLE_PLANT_KEEP_IGNORED")
+           "ORACLE_PLANT_KEEP_IGNORED", "ORACLE_PLANT_SORT_UNSTABLE")
 
 
 def _lib_path(plant):
@@ -72,6 +72,8 @@ def load(plant: str | None = None):
             lib.oracle_reduce_f32.restype = ci
             lib.oracle_topk_items_f32.argtypes = [vp, vp, vp, sz, ci, vp, vp, vp]
             lib.oracle_topk_items_f32.restype = ci
+            lib.oracle_sort_u32.argtypes = [vp, vp, sz, vp, vp]
+            lib.oracle_sort_u32.restype = ci
             _libs[plant] = lib
     return lib
 
@@ -157,3 +159,19 @@ def topk_items_f32(score, k: int, item=None, keep=None, plant: str | None = None
     if rc != 0:
         raise OracleError(f"oracle_topk_items_f32 rejected n={sc.size} k={k}")
     return os_, oi, int(cnt[0])
+
+
+def sort_u32(keys, vals=None, plant: str | None = None):
+    """Stable ascending sort of uint32 keys, carrying uint32 values if given:
+    (keys, values or None)."""
+    k = np.ascontiguousarray(keys, dtype=np.uint32).reshape(-1)
+    v = None if vals is None else np.ascontiguousarray(vals, dtype=np.uint32).reshape(-1)
+    if v is not None and v.size != k.size:
+        raise OracleError("vals must match keys")
+    ko = np.empty_like(k)
+    vo = None if v is None else np.empty_like(v)
+    rc = load(plant).oracle_sort_u32(k.ctypes.data, None if v is None else v.ctypes.data, k.size, ko.ctypes.data,
+                                     None if vo is None else vo.ctypes.data)
+    if rc != 0:
+        raise OracleError(f"oracle_sort_u32 rejected n={k.size}")
+    return ko, vo

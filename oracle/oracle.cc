@@ -155,6 +155,28 @@ int oracle_topk_items_f32(const float* score, const int64_t* item, const uint8_t
     return 0;
 }
 
+// Radix sort ("GPU radix sort": an LSD radix sort of uint32 keys; its
+// extensions section adds key-value pairs).  The result is the keys in
+// ascending order, stable: equal keys keep their input order, so each value
+// stays with its key and values of equal keys keep their input order.
+// vals (and vals_out) may be null for a keys-only sort.  Returns 0, or -1
+// for invalid arguments.
+int oracle_sort_u32(const uint32_t* keys, const uint32_t* vals, size_t n, uint32_t* keys_out, uint32_t* vals_out) {
+    if (!keys || !keys_out || n == 0 || (!vals) != (!vals_out)) return -1;
+    std::vector<size_t> order(n);
+    std::iota(order.begin(), order.end(), (size_t)0);
+#if defined(ORACLE_PLANT_SORT_UNSTABLE)
+    std::sort(order.begin(), order.end(), [keys](size_t a, size_t b) { return keys[a] < keys[b]; });  // planted
+#else
+    std::stable_sort(order.begin(), order.end(), [keys](size_t a, size_t b) { return keys[a] < keys[b]; });
+#endif
+    for (size_t i = 0; i < n; ++i) {
+        keys_out[i] = keys[order[i]];
+        if (vals) vals_out[i] = vals[order[i]];
+    }
+    return 0;
+}
+
 // Exact check of a claimed int32 TopK result at any size, in one pass.
 //
 // out[0..k) is the TopK of in[0..n) exactly when, with t = out[k-1]:

@@ -244,9 +244,49 @@ def pin_items_numpy(plant=None):
     assert i_.tolist() == np.argsort(-x, kind="stable")[:64].tolist()
 
 
+def pin_golden_sort(plant=None):
+    # Hand-worked: "GPU radix sort", sections 2.1 and 8 (key-value pairs):
+    # ascending keys, equal keys in input order, values travel with keys.
+    keys = np.array([5, 1, 4294967295, 1, 0, 5, 7], dtype=np.uint32)
+    vals = np.array([10, 11, 12, 13, 14, 15, 16], dtype=np.uint32)
+    ko, vo = oracle.sort_u32(keys, vals, plant=plant)
+    assert ko.tolist() == [0, 1, 1, 5, 5, 7, 4294967295]
+    assert vo.tolist() == [14, 11, 13, 10, 15, 16, 12]
+
+
+def pin_exhaustive_sort(plant=None, max_n=5):
+    alphabet = [0, 1, 2, 0xFFFFFFFF]
+    for n in range(1, max_n + 1):
+        for combo in itertools.product(alphabet, repeat=n):
+            keys = np.array(combo, dtype=np.uint32)
+            vals = np.arange(n, dtype=np.uint32)
+            ko, vo = oracle.sort_u32(keys, vals, plant=plant)
+            # brute force: take the smallest remaining key, the earliest first
+            pool = list(range(n))
+            order = []
+            while pool:
+                best = min(pool, key=lambda i: (combo[i], i))
+                pool.remove(best)
+                order.append(best)
+            assert vo.tolist() == order and ko.tolist() == [combo[i] for i in order], combo
+
+
+def pin_sort_numpy(plant=None):
+    rng = np.random.default_rng(23)
+    for n, hi in ((100_000, 2**32), (100_000, 50), (3, 2)):
+        keys = rng.integers(0, hi, size=n, dtype=np.uint64).astype(np.uint32)
+        vals = rng.integers(0, 2**32, size=n, dtype=np.uint64).astype(np.uint32)
+        order = np.argsort(keys, kind="stable")
+        ko, vo = oracle.sort_u32(keys, vals, plant=plant)
+        assert np.array_equal(ko, keys[order]) and np.array_equal(vo, vals[order])
+        ko2, vo2 = oracle.sort_u32(keys, plant=plant)
+        assert np.array_equal(ko2, keys[order]) and vo2 is None
+
+
 ALL_PINS = [pin_golden_i32, pin_golden_rows, pin_exhaustive_i32, pin_exhaustive_rows,
             pin_closed_forms_i32, pin_rows_numpy, pin_golden_reduce, pin_exhaustive_reduce,
-            pin_closed_forms_reduce, pin_golden_items, pin_exhaustive_items, pin_items_numpy]
+            pin_closed_forms_reduce, pin_golden_items, pin_exhaustive_items, pin_items_numpy,
+            pin_golden_sort, pin_exhaustive_sort, pin_sort_numpy]
 
 
 # ------------------------------------------------------------------ tests --
@@ -388,6 +428,18 @@ def test_items_numpy():
     pin_items_numpy()
 
 
+def test_golden_sort():
+    pin_golden_sort()
+
+
+def test_exhaustive_sort():
+    pin_exhaustive_sort()
+
+
+def test_sort_numpy():
+    pin_sort_numpy()
+
+
 def test_reduce_rejects_bad_arguments():
     with pytest.raises(oracle.OracleError):
         oracle.reduce_i32(np.zeros(0, dtype=np.int32), "sum")
@@ -410,6 +462,8 @@ def test_pins_reject_planted_mistake(plant):
                 pin(plant=plant, max_n=3)
             elif pin is pin_exhaustive_items:
                 pin(plant=plant, max_n=3)
+            elif pin is pin_exhaustive_sort:
+                pin(plant=plant, max_n=4)
             else:
                 pin(plant=plant)
         except AssertionError:

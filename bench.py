@@ -224,6 +224,8 @@ def run_ours(args, world, rank, local):
     reduce_line = run_reduce(tk, x, stream, args) if not args.skip_rows else None
     # Score-keyed TopK with item ids, without and with a keep filter.
     items_line = run_items(tk, dev, stream, args) if not args.skip_rows else None
+    # Radix sort of the 1e8 int32 input's bits as uint32 keys (with values).
+    sort_line = run_sort(tk, x, stream, args) if not args.skip_rows else None
 
     # End to end through the C ABI with host buffers: the library copies the
     # pinned input to the device, selects, and copies the k results back.
@@ -286,6 +288,8 @@ def run_ours(args, world, rank, local):
         line["reduce"] = reduce_line
     if items_line is not None:
         line["items"] = items_line
+    if sort_line is not None:
+        line["sort"] = sort_line
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline_leg(x_host.numpy(), result)
     return line
@@ -456,6 +460,47 @@ def run_items(tk, dev, stream, args):
     return res
 
 
+def run_sort(tk, x, stream, args):
+    """topk_sort_u32 on the 1e8 input's bits as uint32 keys, keys only and
+    with uint32 values (positions).  Algorithmic traffic: the histogram pass
+    reads 4 bytes per key and each of the four digit passes reads and writes
+    4 (keys) or 8 (pairs) bytes per key: 36 or 68 bytes per key."""
+    n = x.numel()
+    peak, _ = load_peaks()
+    h = stream.cuda_stream
+    vals = torch.arange(n, dtype=torch.int32, device=x.device)
+    ko = torch.empty_like(x)
+    vo = torch.empty_like(vals)
+    res = {}
+    for name, with_vals, bytes_per in (("keys", False, 36), ("pairs", True, 68)):
+        def step():
+            rc = tk.sort_u32_ptr(x.data_ptr(), vals.data_ptr() if with_vals else 0, n, ko.data_ptr(),
+                                 vo.data_ptr() if with_vals else 0, h)
+            if rc != 0:
+                raise tk.TopKError(rc, "topk_sort_u32")
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        steps = max(5, min(50, args.steps // 100))
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / steps
+        gbs = bytes_per * n / (ms / 1e3) / 1e9
+        res[name] = {"steps": steps, "ms_per_step": round(ms, 4), "value": round(n / (ms / 1e3) / 1e9, 3),
+                     "unit": "Gkeys/s",
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                                  "frac": round(gbs / peak, 4), "algorithmic_bytes_per_launch": bytes_per * n,
+                                  "kernel": "whole sort (5 launches; dominant: sort_pass_kernel)"}}
+    del vals, ko, vo
+    res["workload"] = "uint32 keys = bits of the N=1e8 uniform int32 input (seed 2); values = positions"
+    return res
+
+
 def cpu_baseline_leg(x: np.ndarray, gpu_result: np.ndarray):
     """The oracle (single-threaded std::sort, untuned) on the host cores of
     this box, over the whole 1e8 input once; also confirms the GPU result."""
@@ -513,7 +558,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-cpu", action="store_true", help="leave out the CPU-baseline leg")
-    ap.add_argument("--skip-rows", action="store_true", help="leave out the row-TopK, large-k, reduction and item measurements")
+    ap.add_argument("--skip-rows", action="store_true", help="leave out the row-TopK, large-k, reduction, item and sort measurements")
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="--impl reference: seconds of oracle work for the whole run (sets the sample size)")
     args = ap.parse_args()

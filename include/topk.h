@@ -142,6 +142,29 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
 int topk_items_f32(const float* score, const int64_t* item, const uint8_t* keep, size_t n, int k, float* out_score,
                    int64_t* out_item, int64_t* out_count, struct CUstream_st* stream);
 
+/*
+ * topk_sort_u32 -- sort n uint32 keys ascending, stably, carrying uint32
+ * values if given: an LSD radix sort with 8-bit digits, four passes ("GPU
+ * radix sort": sections 2-4; key-value pairs from its extensions section).
+ * Equal keys keep their input order, and each value travels with its key.
+ *
+ *   keys       uint32[n], device memory, read-only.
+ *   vals       uint32[n] or null (keys only), device memory, read-only.
+ *   n          1 <= n <= 2^32 - 1.
+ *   keys_out   uint32[n], device memory, written; must not overlap the inputs.
+ *   vals_out   uint32[n], written; null exactly when vals is null.
+ *
+ * Five launches: one histogram pass for all four digits, then one pass per
+ * digit in which every 4096-key tile ranks its keys, finds where its keys of
+ * each digit go from the tiles before it (decoupled look-back, bounded
+ * waits) and writes them in digit order.  Scratch (in the library's
+ * per-stream workspace): about 4n bytes (8n with values) plus 0.5 byte per
+ * key of look-back words.  The call only enqueues work.  Host pointers are
+ * rejected with TOPK_ERR_INVALID_ARG.
+ */
+int topk_sort_u32(const uint32_t* keys, const uint32_t* vals, size_t n, uint32_t* keys_out, uint32_t* vals_out,
+                  struct CUstream_st* stream);
+
 /* Operations of topk_reduce_i32 / topk_reduce_f32. */
 enum topk_reduce_op { TOPK_REDUCE_SUM = 0, TOPK_REDUCE_MAX = 1, TOPK_REDUCE_MIN = 2 };
 

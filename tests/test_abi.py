@@ -136,6 +136,12 @@ def test_reduce_and_items_argument_errors(lib):
     assert g(p, None, None, 10, 0, p + 128, o, None, None) == 1   # k < 1
     assert g(p, None, None, 10, 2, p, o, None, None) == 1      # out_score overlaps score
     assert g(p, o + 4, None, 10, 2, p + 128, o + 64, None, None) == 1  # misaligned item
+    h = lib.topk_sort_u32
+    assert h(None, None, 10, p, None, None) == 1            # null keys
+    assert h(p, None, 0, p + 128, None, None) == 1          # n == 0
+    assert h(p, p + 64, 10, p + 128, None, None) == 1       # values without an output for them
+    assert h(p, None, 10, p + 16, None, None) == 1          # output overlaps input
+    assert h(p + 2, None, 10, p + 128, None, None) == 1     # misaligned
     assert tk.OPT_STAGE2_CAP == 1
 
 

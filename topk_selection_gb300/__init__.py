@@ -24,7 +24,8 @@ from . import build as _build
 __all__ = ["topk_i32", "topk_rows_f32", "topk_i32_ptr", "topk_rows_f32_ptr", "TopKError", "MAX_K", "MAX_K_ROWS",
            "status_string", "release_workspace", "launch_count", "last_cuda_error", "library_path",
            "check_stream", "set_option", "OPT_STAGE2_CAP", "OPT_RADIX_CAP", "OPT_RADIX_SAMPLE_RANK",
-           "reduce", "reduce_ptr", "REDUCE_OPS", "topk_items_f32", "topk_items_f32_ptr"]
+           "reduce", "reduce_ptr", "REDUCE_OPS", "topk_items_f32", "topk_items_f32_ptr", "sort_u32",
+           "sort_u32_ptr"]
 
 MAX_K = 32768       # topk_i32
 MAX_K_ROWS = 1024   # topk_rows_f32
@@ -70,6 +71,8 @@ def _load():
     lib.topk_reduce_f32.restype = ci
     lib.topk_items_f32.argtypes = [vp, vp, vp, sz, ci, vp, vp, vp, vp]
     lib.topk_items_f32.restype = ci
+    lib.topk_sort_u32.argtypes = [vp, vp, sz, vp, vp, vp]
+    lib.topk_sort_u32.restype = ci
     return lib
 
 
@@ -222,6 +225,41 @@ def topk_items_f32(score: torch.Tensor, k: int, item: torch.Tensor | None = None
     if rc != TOPK_OK:
         raise TopKError(rc, "topk_items_f32")
     return out_score, out_item, out_count
+
+
+def sort_u32_ptr(keys_ptr: int, vals_ptr: int, n: int, keys_out_ptr: int, vals_out_ptr: int, stream: int = 0) -> int:
+    """Raw C-ABI call (0 for null value pointers); returns the status code."""
+    vp = ctypes.c_void_p
+    return int(_lib.topk_sort_u32(vp(keys_ptr), vp(vals_ptr or None), n, vp(keys_out_ptr), vp(vals_out_ptr or None),
+                                  vp(stream)))
+
+
+def sort_u32(keys: torch.Tensor, vals: torch.Tensor | None = None, stream=None):
+    """Stable ascending radix sort of uint32 keys (a CUDA tensor of dtype
+    torch.uint32, or int32 reinterpreted as uint32), carrying uint32 values:
+    (sorted keys, sorted values or None)."""
+    def as_u32(t, name):
+        if t.dtype == torch.int32:
+            return t
+        if t.dtype == getattr(torch, "uint32", None):
+            return t
+        raise TypeError(f"{name} must be uint32 (or int32 holding uint32 bits)")
+    keys = as_u32(keys, "keys")
+    if not keys.is_cuda or not keys.is_contiguous():
+        raise ValueError("keys must be a contiguous CUDA tensor")
+    if vals is not None:
+        vals = as_u32(vals, "vals")
+        if not vals.is_cuda or not vals.is_contiguous() or vals.numel() != keys.numel():
+            raise ValueError("vals must be a contiguous CUDA tensor matching keys")
+    ko = torch.empty_like(keys)
+    vo = torch.empty_like(vals) if vals is not None else None
+    dev = keys.device
+    with torch.cuda.device(dev):
+        rc = sort_u32_ptr(keys.data_ptr(), vals.data_ptr() if vals is not None else 0, keys.numel(), ko.data_ptr(),
+                          vo.data_ptr() if vo is not None else 0, _stream_handle(stream, dev))
+    if rc != TOPK_OK:
+        raise TopKError(rc, "topk_sort_u32")
+    return ko, vo
 
 
 REDUCE_OPS = {"sum": 0, "max": 1, "min": 2}

@@ -36,6 +36,9 @@ struct Workspace {
     size_t stage_out_bytes = 0;
     void* items = nullptr;      // topk_items_f32 scratch
     size_t items_bytes = 0;
+    void* sort = nullptr;       // topk_sort_u32 scratch (its header zero between calls)
+    size_t sort_bytes = 0;
+    unsigned sort_epoch = 0;    // tags the sort's look-back words, one per call
 };
 
 std::mutex g_ws_mutex;
@@ -226,6 +229,51 @@ int topk_reduce_f32(const float* in, size_t n, int op, double* out, struct CUstr
     return reduce_common(in, n, op, out, true, stream);
 }
 
+int topk_sort_u32(const uint32_t* keys, const uint32_t* vals, size_t n, uint32_t* keys_out, uint32_t* vals_out,
+                  struct CUstream_st* stream) {
+    if (!keys || !keys_out || n == 0 || (!vals) != (!vals_out)) return TOPK_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(keys) | reinterpret_cast<uintptr_t>(keys_out) |
+         reinterpret_cast<uintptr_t>(vals) | reinterpret_cast<uintptr_t>(vals_out)) & 3u)
+        return TOPK_ERR_INVALID_ARG;
+    const size_t b = n * 4;
+    if (overlaps(keys, b, keys_out, b) || (vals && (overlaps(vals, b, vals_out, b) || overlaps(keys, b, vals_out, b) ||
+                                                     overlaps(vals, b, keys_out, b) || overlaps(keys_out, b, vals_out, b))))
+        return TOPK_ERR_INVALID_ARG;
+    if (n > (size_t)0xFFFFFFFFu) return TOPK_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e);
+    for (const void* p : {(const void*)keys, (const void*)vals, (const void*)keys_out, (const void*)vals_out}) {
+        if (!p) continue;
+        bool host = false;
+        const int rc = is_host_pointer(p, &host);
+        if (rc != TOPK_OK) return rc;
+        if (host) return TOPK_ERR_INVALID_ARG;  // device memory only
+    }
+    Workspace* w = nullptr;
+    int rc = workspace(s, device, topk::kI32CandOffset, 0, 0, &w);
+    if (rc != TOPK_OK) return rc;
+    unsigned epoch = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_ws_mutex);
+        const size_t need = topk::sort_scratch_bytes(n, vals != nullptr);
+        if (w->sort_bytes < need) {
+            rc = grow(&w->sort, &w->sort_bytes, need);
+            if (rc != TOPK_OK) return rc;
+            e = cudaMemsetAsync(w->sort, 0, topk::kSortHeaderBytes, s);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        epoch = ++w->sort_epoch;
+    }
+    auto* status = reinterpret_cast<unsigned*>(static_cast<char*>(w->ctrl_cand) + topk::kI32StatusOffset);
+    int launches = 0;
+    e = topk::sort_launch(s, keys, vals, n, keys_out, vals_out, w->sort, epoch, status, &launches);
+    g_launches.fetch_add((unsigned long long)launches, std::memory_order_relaxed);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return TOPK_OK;
+}
+
 int topk_items_f32(const float* score, const int64_t* item, const uint8_t* keep, size_t n, int k, float* out_score,
                    int64_t* out_item, int64_t* out_count, struct CUstream_st* stream) {
     if (!score || !out_score || !out_item || n == 0 || k < 1 || (size_t)k > n) return TOPK_ERR_INVALID_ARG;
@@ -400,7 +448,7 @@ int topk_release_workspace(void) {
     for (auto& kv : g_ws) {
         Workspace& w = kv.second;
         cudaSetDevice(kv.first.first);
-        for (void* p : {w.ctrl_cand, w.stage_in, w.stage_out, w.items})
+        for (void* p : {w.ctrl_cand, w.stage_in, w.stage_out, w.items, w.sort})
             if (p && cudaFree(p) != cudaSuccess) rc = TOPK_ERR_CUDA;
     }
     g_ws.clear();

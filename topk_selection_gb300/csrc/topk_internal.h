@@ -128,6 +128,16 @@ cudaError_t items_launch(cudaStream_t s, const float* score, const int64_t* item
                          int k, float* out_score, int64_t* out_item, int64_t* out_count, void* scratch,
                          size_t scratch_bytes, unsigned* status, int* launches);
 
+// LSD radix sort of uint32 keys (optionally with uint32 values), stable,
+// ascending (topk_sort.cu).  scratch: sort_scratch_bytes(n, vals != null)
+// bytes whose first kSortHeaderBytes are zero before the first call on it
+// (the kernels leave them so); epoch: a number that differs between calls
+// on the same scratch (it tags the look-back words).  n < 2^32.
+constexpr size_t kSortHeaderBytes = 16384;
+size_t sort_scratch_bytes(size_t n, bool with_vals);
+cudaError_t sort_launch(cudaStream_t s, const uint32_t* keys, const uint32_t* vals, size_t n, uint32_t* keys_out,
+                        uint32_t* vals_out, void* scratch, unsigned epoch, unsigned* status, int* launches);
+
 // Bookkeeping of the C ABI layer, for entry points defined in other files:
 // record the cudaError_t behind a TOPK_ERR_CUDA, and count a kernel launch.
 void note_cuda_error(int err);

@@ -1,0 +1,381 @@
+// LSD radix sort of uint32 keys, optionally carrying uint32 values
+// ("GPU radix sort": 8-bit digits, four passes for 32-bit keys, per-block
+// shared-memory histograms; its extensions section adds key-value pairs).
+//
+// GB300 form: one histogram pass for all four digits, then one launch per
+// digit in which every tile of 4096 keys
+//   1. takes the next tile id from a counter (so a tile only ever waits for
+//      tiles whose blocks are already running),
+//   2. ranks its keys stably: per warp, keys go slot by slot (32
+//      consecutive keys per slot) and __match_any_sync groups the lanes
+//      with equal digits, so a key's rank among equal digits follows input
+//      order; warps then add the counts of the warps before them,
+//   3. publishes its per-digit counts and looks back over earlier tiles for
+//      the keys of each digit before it (decoupled look-back: a tile's word
+//      says "my count" or "count of every tile up to me"),
+//   4. places its keys in shared memory in digit order and writes them out,
+//      so that keys of one digit go to consecutive addresses.
+// The page's printed scatter increments shared counters without atomics;
+// only its plan (digits, passes, histograms) is kept.
+//
+// Look-back words are 64-bit: status (2 bits), epoch (30 bits: the call and
+// pass that wrote it), count (32 bits).  A word from another call or pass
+// reads as "not ready", so the array never needs clearing.  Every wait is
+// bounded: after kSpins polls the tile records kStatusWaitTimeout in the
+// status word and goes on with what it has (the result is then invalid, and
+// topk_check_stream reports it).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "topk_device.cuh"
+#include "topk_internal.h"
+
+namespace topk {
+
+namespace {
+
+constexpr int kST = 512;            // threads per tile
+constexpr int kSW = kST / 32;       // warps per tile
+constexpr int kSI = 8;              // keys per thread
+constexpr int kTile = kST * kSI;    // keys per tile
+constexpr int kRadix = 256;
+constexpr int kSpins = 1 << 22;     // polls of one look-back word before giving up
+constexpr int kHT = 512, kHU = 8;   // histogram pass: threads, 16-byte loads in flight
+
+constexpr unsigned long long kAgg = 1ull << 62;   // word holds this tile's count
+constexpr unsigned long long kIncl = 2ull << 62;  // word holds the count up to and including this tile
+
+struct SortHeader {
+    unsigned hist[4][kRadix];   // digit counts (zero between calls)
+    unsigned base[4][kRadix];   // where each digit's keys start, per pass
+    unsigned ticket;            // histogram pass blocks done (zero between calls)
+    unsigned tile_counter[4];   // next tile id, per pass (zero between calls)
+};
+static_assert(sizeof(SortHeader) <= kSortHeaderBytes, "sort header");
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// ---- pass 0: histograms of all four digits, then the digit bases ----
+
+__global__ void __launch_bounds__(kHT, 2)
+sort_hist_kernel(const uint32_t* __restrict__ keys, size_t n, SortHeader* __restrict__ h) {
+    __shared__ unsigned sh[4][kRadix];
+    __shared__ int s_last;
+    for (int i = threadIdx.x; i < 4 * kRadix; i += blockDim.x) (&sh[0][0])[i] = 0u;
+    __syncthreads();
+    auto add = [&](uint32_t k) {
+        atomicAdd(&sh[0][k & 0xFFu], 1u);
+        atomicAdd(&sh[1][(k >> 8) & 0xFFu], 1u);
+        atomicAdd(&sh[2][(k >> 16) & 0xFFu], 1u);
+        atomicAdd(&sh[3][k >> 24], 1u);
+    };
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(keys);
+    size_t head = ((16u - (unsigned)(addr & 15u)) & 15u) >> 2;
+    if (head > n) head = n;
+    const uint4* body = reinterpret_cast<const uint4*>(keys + head);
+    const size_t nvec = (n - head) >> 2, tail0 = head + nvec * 4;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t b = (size_t)blockIdx.x * blockDim.x * kHU; b < nvec; b += stride * kHU) {
+        uint4 r[kHU];
+#pragma unroll
+        for (int u = 0; u < kHU; ++u) {
+            const size_t i = b + (size_t)u * blockDim.x + threadIdx.x;
+            r[u] = i < nvec ? __ldg(body + i) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kHU; ++u)
+            if (b + (size_t)u * blockDim.x + threadIdx.x < nvec) {
+                add(r[u].x);
+                add(r[u].y);
+                add(r[u].z);
+                add(r[u].w);
+            }
+    }
+    if (blockIdx.x == 0 && threadIdx.x < 32) {
+        const size_t ns = head + (n - tail0), lane = threadIdx.x;
+        if (lane < ns) add(keys[lane < head ? lane : tail0 + (lane - head)]);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 4 * kRadix; i += blockDim.x) {
+        const unsigned v = (&sh[0][0])[i];
+        if (v) atomicAdd(&(&h->hist[0][0])[i], v);
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&h->ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // Last block: exclusive scans of the four histograms (one warp each).
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (w < 4) {
+        unsigned c[8], t = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            c[j] = __ldcg(&h->hist[w][lane * 8 + j]);
+            t += c[j];
+        }
+        unsigned x = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(kFullMask, x, o);
+            if (lane >= o) x += y;
+        }
+        unsigned acc = x - t;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            h->base[w][lane * 8 + j] = acc;
+            acc += c[j];
+            h->hist[w][lane * 8 + j] = 0u;
+        }
+    }
+    if (threadIdx.x == 0) h->ticket = 0u;
+}
+
+// ---- one digit pass ----
+
+template <bool kVals>
+__global__ void __launch_bounds__(kST, 2)
+sort_pass_kernel(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ vin, uint32_t* __restrict__ kout,
+                 uint32_t* __restrict__ vout, size_t n, int shift, SortHeader* __restrict__ h, int pass,
+                 unsigned long long* __restrict__ look, unsigned epoch, unsigned ntiles, unsigned* __restrict__ status) {
+    extern __shared__ __align__(16) uint32_t sort_smem[];
+    uint32_t* s_keys = sort_smem;                       // kTile
+    uint32_t* s_vals = sort_smem + kTile;               // kTile (with values)
+    __shared__ unsigned s_whist[kSW][kRadix];           // per-warp counts, then the warps' offsets
+    __shared__ unsigned s_tcount[kRadix];               // this tile's count per digit
+    __shared__ unsigned s_texcl[kRadix];                // where each digit starts in the tile
+    __shared__ unsigned s_goff[kRadix];                 // where this tile's keys of each digit go
+    __shared__ unsigned s_tile;
+    __shared__ unsigned s_scan[kSW];
+
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        const unsigned t = atomicAdd(&h->tile_counter[pass], 1u);
+        s_tile = t;
+        if (t == ntiles - 1) h->tile_counter[pass] = 0u;  // every block has its id: reset for the next call
+    }
+    for (int i = lane; i < kRadix; i += 32) s_whist[w][i] = 0u;
+    __syncthreads();
+    const unsigned tile = s_tile;
+    const size_t tbase = (size_t)tile * kTile;
+    const unsigned tcnt = (unsigned)(n - tbase < (size_t)kTile ? n - tbase : (size_t)kTile);
+
+    // Load: warp w owns tile keys [w*256, w*256 + 256), slot i = keys
+    // w*256 + i*32 .. +31 (lane order = input order).
+    uint32_t key[kSI], val[kSI];
+    unsigned rank[kSI];
+#pragma unroll
+    for (int i = 0; i < kSI; ++i) {
+        const unsigned p = (unsigned)(w * 32 * kSI + i * 32 + lane);
+        key[i] = p < tcnt ? kin[tbase + p] : 0xFFFFFFFFu;
+        if (kVals) val[i] = p < tcnt ? vin[tbase + p] : 0u;
+    }
+    // Stable rank within the warp among keys of the same digit: the lanes
+    // whose digit equals this lane's, from one ballot per digit bit (a warp
+    // multisplit); the lowest of them adds the group to the warp's count.
+#pragma unroll
+    for (int i = 0; i < kSI; ++i) {
+        const unsigned p = (unsigned)(w * 32 * kSI + i * 32 + lane);
+        const bool ok = p < tcnt;
+        const unsigned d = (key[i] >> shift) & 0xFFu;
+        unsigned peers = __ballot_sync(kFullMask, ok);
+#pragma unroll
+        for (int bit = 0; bit < 8; ++bit) {
+            const unsigned bb = __ballot_sync(kFullMask, (d >> bit) & 1u);
+            peers &= ((d >> bit) & 1u) ? bb : ~bb;
+        }
+        if (!ok) peers = 1u << lane;  // past the end: a group of its own, never counted
+        const int leader = __ffs(peers) - 1;
+        unsigned before = 0;
+        if (lane == leader && ok) {
+            before = s_whist[w][d];
+            s_whist[w][d] = before + __popc(peers);
+        }
+        before = __shfl_sync(kFullMask, before, leader);
+        rank[i] = before + __popc(peers & lanemask_lt());
+        __syncwarp();
+    }
+    __syncthreads();
+    // Per digit: the counts of the warps before each warp, and the tile's count.
+    if (threadIdx.x < kRadix) {
+        const int d = threadIdx.x;
+        unsigned acc = 0;
+#pragma unroll
+        for (int ww = 0; ww < kSW; ++ww) {
+            const unsigned c = s_whist[ww][d];
+            s_whist[ww][d] = acc;
+            acc += c;
+        }
+        s_tcount[d] = acc;
+    }
+    __syncthreads();
+    // Publish this tile's counts, then look back (one thread per digit).
+    if (threadIdx.x < kRadix) {
+        const int d = threadIdx.x;
+        const unsigned c = s_tcount[d];
+        const unsigned long long tag = (unsigned long long)(epoch & 0x3FFFFFFFu) << 32;
+        unsigned long long* mine = look + (size_t)tile * kRadix + d;
+        unsigned excl = 0;
+        if (tile == 0) {
+            st_relaxed_u64(mine, kIncl | tag | c);
+        } else {
+            st_relaxed_u64(mine, kAgg | tag | c);
+            // Walk back over the tiles before this one, four words per round
+            // trip: add counts until a word that already covers every tile
+            // before it.  A word not yet written is read again (bounded).
+            long long j = (long long)tile - 1;
+            int spins = 0;
+            bool done = false;
+            while (!done && j >= 0) {
+                unsigned long long v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[q] = j - q >= 0 ? ld_relaxed_u64(look + (size_t)(j - q) * kRadix + d) : 0ull;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (done || j < 0) break;
+                    if ((v[q] & 0x3FFFFFFF00000000ull) != tag || (v[q] >> 62) == 0) {
+                        if (++spins >= kSpins) {  // give up: go on with what has been summed
+                            atomicOr(status, kStatusWaitTimeout);
+                            done = true;
+                        }
+                        break;  // read again from j
+                    }
+                    excl += (unsigned)v[q];
+                    --j;
+                    if ((v[q] >> 62) == 2) done = true;
+                }
+            }
+            st_relaxed_u64(mine, kIncl | tag | (excl + c));
+        }
+        s_goff[d] = __ldcg(&h->base[pass][d]) + excl;
+    }
+    // Where each digit starts inside the tile: exclusive scan of s_tcount.
+    if (threadIdx.x < kRadix) {
+        const unsigned c = s_tcount[threadIdx.x];
+        unsigned x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(kFullMask, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_scan[w] = x;
+        __syncwarp();
+        s_texcl[threadIdx.x] = x - c;  // within the warp; warps added below
+    }
+    __syncthreads();
+    if (threadIdx.x < kRadix) {
+        unsigned add = 0;
+        for (int ww = 0; ww < w; ++ww) add += s_scan[ww];
+        s_texcl[threadIdx.x] += add;
+    }
+    __syncthreads();
+    // Keys to shared memory in digit order (stable), then out.
+#pragma unroll
+    for (int i = 0; i < kSI; ++i) {
+        const unsigned p = (unsigned)(w * 32 * kSI + i * 32 + lane);
+        if (p < tcnt) {
+            const unsigned d = (key[i] >> shift) & 0xFFu;
+            const unsigned slot = s_texcl[d] + s_whist[w][d] + rank[i];
+            s_keys[slot] = key[i];
+            if (kVals) s_vals[slot] = val[i];
+        }
+    }
+    __syncthreads();
+    for (unsigned i = threadIdx.x; i < tcnt; i += kST) {
+        const uint32_t k = s_keys[i];
+        const unsigned d = (k >> shift) & 0xFFu;
+        const size_t dst = (size_t)s_goff[d] + (i - s_texcl[d]);
+        kout[dst] = k;
+        if (kVals) vout[dst] = s_vals[i];
+    }
+}
+
+struct SortFit {
+    int hist_grid = 0;
+};
+
+cudaError_t sort_fit(int device, SortFit* out) {
+    constexpr int kMaxDev = 64;
+    static std::mutex mu;
+    static SortFit cache[kMaxDev];
+    if (device < 0 || device >= kMaxDev) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[device].hist_grid == 0) {
+        int sms = 0, b = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, reinterpret_cast<const void*>(&sort_hist_kernel), kHT, 0);
+        if (e != cudaSuccess) return e;
+        for (const void* f : {reinterpret_cast<const void*>(&sort_pass_kernel<true>),
+                              reinterpret_cast<const void*>(&sort_pass_kernel<false>)}) {
+            e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTile * 4);
+            if (e != cudaSuccess) return e;
+        }
+        cache[device].hist_grid = sms * (b < 1 ? 1 : b);
+    }
+    *out = cache[device];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t sort_scratch_bytes(size_t n, bool with_vals) {
+    const size_t tiles = (n + kTile - 1) / kTile;
+    const size_t look = tiles * kRadix * 8;
+    const size_t tmp = (n * 4 + 255) / 256 * 256;
+    return kSortHeaderBytes + (look + 255) / 256 * 256 + tmp * (with_vals ? 2 : 1);
+}
+
+cudaError_t sort_launch(cudaStream_t s, const uint32_t* keys, const uint32_t* vals, size_t n, uint32_t* keys_out,
+                        uint32_t* vals_out, void* scratch, unsigned epoch, unsigned* status, int* launches) {
+    *launches = 0;
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return e;
+    SortFit f;
+    e = sort_fit(device, &f);
+    if (e != cudaSuccess) return e;
+    auto* base = static_cast<unsigned char*>(scratch);
+    auto* h = reinterpret_cast<SortHeader*>(base);
+    const size_t tiles = (n + kTile - 1) / kTile;
+    auto* look = reinterpret_cast<unsigned long long*>(base + kSortHeaderBytes);
+    const size_t look_bytes = (tiles * kRadix * 8 + 255) / 256 * 256;
+    auto* tk = reinterpret_cast<uint32_t*>(base + kSortHeaderBytes + look_bytes);
+    const size_t tmp = (n * 4 + 255) / 256 * 256;
+    auto* tv = vals ? reinterpret_cast<uint32_t*>(base + kSortHeaderBytes + look_bytes + tmp) : nullptr;
+
+    size_t hgrid = (n + (size_t)kHT * kHU * 4 - 1) / ((size_t)kHT * kHU * 4);
+    if (hgrid > (size_t)f.hist_grid) hgrid = f.hist_grid;
+    if (hgrid < 1) hgrid = 1;
+    sort_hist_kernel<<<(int)hgrid, kHT, 0, s>>>(keys, n, h);
+    *launches += 1;
+    // pass 0: keys -> tmp, 1: tmp -> out, 2: out -> tmp, 3: tmp -> out
+    const uint32_t* ki[4] = {keys, tk, keys_out, tk};
+    uint32_t* ko[4] = {tk, keys_out, tk, keys_out};
+    const uint32_t* vi[4] = {vals, tv, vals_out, tv};
+    uint32_t* vo[4] = {tv, vals_out, tv, vals_out};
+    const size_t smem = (size_t)(vals ? 2 : 1) * kTile * 4;
+    for (int p = 0; p < 4; ++p) {
+        const unsigned ep = (epoch * 4u + (unsigned)p) & 0x3FFFFFFFu;
+        if (vals)
+            sort_pass_kernel<true><<<(unsigned)tiles, kST, smem, s>>>(ki[p], vi[p], ko[p], vo[p], n, 8 * p, h, p,
+                                                                     look, ep, (unsigned)tiles, status);
+        else
+            sort_pass_kernel<false><<<(unsigned)tiles, kST, smem, s>>>(ki[p], nullptr, ko[p], nullptr, n, 8 * p, h,
+                                                                      p, look, ep, (unsigned)tiles, status);
+        *launches += 1;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace topk

@@ -189,6 +189,43 @@ def test_back_to_back_calls_reset_state(tk):
         assert np.array_equal(b, oracle.topk_i32(small, 20))
 
 
+def test_chained_calls_read_the_previous_output(tk):
+    # Back-to-back launches on one stream may overlap (the next starts
+    # streaming while the previous finishes), except when the next call's
+    # input is the previous call's output: that chain must see the finished
+    # values.
+    x = synth.i32_uniform(5_000_000, 31)
+    d = torch.from_numpy(x).cuda()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(5):
+            a = tk.topk_i32(d, 128, stream=s)
+            b = tk.topk_i32(a, 20, stream=s)      # input = the previous output
+            c = tk.topk_i32(d, 64, stream=s)      # independent input: may overlap b
+            e = tk.topk_i32(c, 1, stream=s)
+    s.synchronize()
+    exp = oracle.topk_i32(x, 128)
+    assert np.array_equal(a.cpu().numpy(), exp)
+    assert np.array_equal(b.cpu().numpy(), exp[:20])
+    assert np.array_equal(c.cpu().numpy(), exp[:64])
+    assert e.cpu().numpy()[0] == exp[0]
+
+
+def test_many_back_to_back_calls(tk):
+    # A long run of overlapping launches on one stream, inputs and outputs
+    # distinct: every result must match.
+    xs = [synth.i32_uniform(3_000_000 + 17 * i, 40 + i) for i in range(4)]
+    ds = [torch.from_numpy(x).cuda() for x in xs]
+    outs = []
+    for rep in range(50):
+        for i, d in enumerate(ds):
+            outs.append((i, tk.topk_i32(d, (20, 1, 100, 64)[i])))
+    torch.cuda.synchronize()
+    exps = [oracle.topk_i32(x, k) for x, k in zip(xs, (20, 1, 100, 64))]
+    for i, o in outs:
+        assert np.array_equal(o.cpu().numpy(), exps[i])
+
+
 def test_non_default_stream_in_flight(tk):
     x = synth.i32_uniform(3_000_000, 11)
     d = torch.from_numpy(x).cuda()

@@ -36,6 +36,8 @@ struct Workspace {
     size_t stage_out_bytes = 0;
     void* items = nullptr;      // topk_items_f32 scratch
     size_t items_bytes = 0;
+    const void* stream_out = nullptr;  // output of the last streaming-plan launch on this stream
+    size_t stream_out_bytes = 0;
     void* sort = nullptr;       // topk_sort_u32 scratch (its header zero between calls)
     size_t sort_bytes = 0;
     unsigned sort_epoch = 0;    // tags the sort's look-back words, one per call
@@ -159,9 +161,19 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
     if (out_host) dout = static_cast<int32_t*>(w->stage_out);
 
     int launches = 1;
-    if (k <= 128)
-        e = topk::i32_launch(plan, s, din, n, k, dout, w->ctrl_cand);
-    else
+    if (k <= 128) {
+        // The streaming kernel may start while the previous one on this stream
+        // finishes, reading its input early: not when that input is the
+        // previous launch's output (a chain of TopKs).
+        bool early;
+        {
+            std::lock_guard<std::mutex> lock(g_ws_mutex);
+            early = !in_host && !overlaps(din, n * sizeof(int32_t), w->stream_out, w->stream_out_bytes);
+            w->stream_out = dout;
+            w->stream_out_bytes = (size_t)k * sizeof(int32_t);
+        }
+        e = topk::i32_launch(plan, s, din, n, k, dout, w->ctrl_cand, early);
+    } else
         e = topk::radix_launch(s, din, n, k, dout, w->ctrl_cand, topk::kRadixCap, &launches);
     g_launches.fetch_add((unsigned long long)launches, std::memory_order_relaxed);
     if (e != cudaSuccess) return cuda_fail(e);

@@ -160,6 +160,15 @@ __device__ __forceinline__ void enqueue(int* q, int& nq, int v, int t, int lane)
     nq += __popc(m);
 }
 
+// Programmatic dependent launch: the kernel is launched so that it may
+// start while the previous kernel on the stream finishes; it must not touch
+// state that kernel uses until grid_dependency_wait() returns (which waits
+// for the previous grid to complete and its writes to be visible), and it
+// lets the next launch start with launch_dependents().  Both are hardware
+// mechanisms, not spins.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- stage 2 --
 //
 // Every block leaves `lists_per_block` sorted lists of K entries (INT_MIN
@@ -387,6 +396,9 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
                 if (lane == 0) atomicMax(&s_thresh, tseed);
             }
         }
+        // The scratch is the previous launch's until it completes (this
+        // kernel may start early, see the host side): wait for it here.
+        grid_dependency_wait();
         int pub_t = INT_MIN, pub_cmax = INT_MIN;
         for (int round = 0; round < kMonitorRounds; ++round) {
             const bool last = *(volatile int*)&s_done == kCons;
@@ -557,6 +569,9 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
         if (lane == 0) atomicAdd(&s_done, 1);
     }
 
+    // Everything below uses the scratch: the previous launch must be done.
+    grid_dependency_wait();
+
     // Block combine (section 2.1's tree, with warps in place of threads):
     // three levels of pairwise bitonic merges of the consumers' register
     // lists through shared memory.
@@ -587,6 +602,9 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
     if (warp == 0) write_list<L>(sc, (int)b, wl.lst, t_now, lane);
     const int block_kth = s_queue[k - 1];
 
+    // This block has read all its input: the next launch on the stream may
+    // start its blocks (they wait for this grid before touching the scratch).
+    launch_dependents();
     // Every threshold this block's warps used went through s_thresh: publish
     // it (and the block's k-th value) before the ticket, whatever the
     // monitor managed to do.
@@ -602,9 +620,23 @@ struct StreamVariant {
     static constexpr int kThreads = kStreamThreads;
     static size_t smem_bytes() { return kRingBytes; }
     static const void* fn() { return reinterpret_cast<const void*>(&topk_i32_stream_kernel<L, GL>); }
-    static void launch(int grid, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
-                       unsigned char* scratch, int cap_limit) {
-        topk_i32_stream_kernel<L, GL><<<grid, kThreads, smem_bytes(), s>>>(in, n, k, out, scratch, cap_limit);
+    // Launched with programmatic stream serialization: when the previous
+    // kernel on the stream is one of these, this one's blocks start once all
+    // of that kernel's blocks have read their input, and overlap its last
+    // block's second stage; every access to the shared scratch waits for it.
+    static cudaError_t launch(int grid, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
+                              unsigned char* scratch, int cap_limit, bool early) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem_bytes();
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = early ? 1 : 0;
+        return cudaLaunchKernelEx(&cfg, topk_i32_stream_kernel<L, GL>, in, n, k, out, scratch, cap_limit);
     }
     static size_t units_per_block() { return kCons; }
 };
@@ -673,16 +705,12 @@ cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan) {
 }
 
 cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
-                       void* scratch) {
+                       void* scratch, bool early) {
     auto* sc = static_cast<unsigned char*>(scratch);
     const int cap = plan.stage2_cap;
-    if (k <= 32)
-        VarK32::launch(plan.grid, s, in, n, k, out, sc, cap);
-    else if (k <= 64)
-        VarK64::launch(plan.grid, s, in, n, k, out, sc, cap);
-    else
-        VarK128::launch(plan.grid, s, in, n, k, out, sc, cap);
-    return cudaGetLastError();
+    if (k <= 32) return VarK32::launch(plan.grid, s, in, n, k, out, sc, cap, early);
+    if (k <= 64) return VarK64::launch(plan.grid, s, in, n, k, out, sc, cap, early);
+    return VarK128::launch(plan.grid, s, in, n, k, out, sc, cap, early);
 }
 
 }  // namespace topk

@@ -102,9 +102,13 @@ cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan);
 
 // Enqueue the single-launch int32 TopK.  scratch holds i32_scratch_bytes(plan.grid)
 // bytes, 256-byte aligned, whose [kI32ResetBegin, kI32ResetEnd) bytes are zero
-// (they are zero again when the launch completes).
+// (they are zero again when the launch completes).  early: launch with
+// programmatic stream serialization, so that when the previous work on the
+// stream is this kernel, this launch starts streaming its input while that
+// one finishes; the input must then not be anything the previous launch
+// writes (its output).
 cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
-                       void* scratch);
+                       void* scratch, bool early);
 
 // Enqueue the row TopK.  status: a device word that bounded waits set to
 // kStatusWaitTimeout when they give up (sticky).

@@ -54,7 +54,7 @@ def assert_rows_equal(tk, x, k, col_offset=0):
     assert np.array_equal(bits(v), bits(ev)), (k, x.shape)
 
 
-SPECIAL = np.array([math.nan, -math.inf, math.inf, -0.0, 0.0, 1.0, -1.0, 3.5e38, -3.5e38, 1e-45, -1e-45],
+SPECIAL = np.array([math.nan, -math.inf, math.inf, -0.0, 0.0, 1.0, -1.0, 3.4e38, -3.4e38, 1e-45, -1e-45],
                    dtype=np.float32)
 
 
@@ -139,3 +139,52 @@ def test_workload_4096x32768(tk, tied):
     assert np.array_equal(bits(v[sample]), bits(ev))
     for lo in range(0, rows, 512):
         check_all_rows(x[lo:lo + 512], k, v[lo:lo + 512], i[lo:lo + 512])
+
+
+def special_rows(rows, cols, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((rows, cols)).astype(np.float32)
+    special = [
+        lambda r: np.full(cols, 1.5, np.float32),                 # one value: every column ties
+        lambda r: np.round(r * 4) / 4,                            # many ties
+        lambda r: SPECIAL[rng.integers(0, SPECIAL.size, cols)],
+        lambda r: -np.abs(r),
+        lambda r: np.concatenate([r[:-5], np.full(5, 9.0, np.float32)]),   # the best values at the end
+        lambda r: np.concatenate([np.full(5, 9.0, np.float32), r[5:]]),    # and at the start
+    ]
+    for i, f in enumerate(special[:rows]):
+        x[i] = f(x[i])
+    if rows > len(special):
+        z = np.full(cols, -0.0, np.float32)
+        z[rng.integers(0, cols, 40)] = 0.0
+        x[len(special)] = z
+    return x
+
+
+def test_long_rows_with_specials(tk):
+    x = special_rows(11, 50_003, 1)
+    for k in (1, 20, 33, 64, 100, 128):
+        assert_rows_equal(tk, x, k)
+    assert_rows_equal(tk, x[:, :49_997], 64, col_offset=3)
+
+
+def test_few_long_rows(tk):
+    x = synth.f32_rows_tied(3, 1_500_001, 11)
+    x[1] = np.float32(0.25)
+    for k in (1, 64, 128):
+        assert_rows_equal(tk, x, k)
+
+
+def test_shapes_back_to_back(tk):
+    # Different shapes one after the other on one stream.
+    shapes = [(7, 100_000, 64), (5000, 800, 10), (64, 32768, 128), (1, 300_000, 1), (4500, 2000, 32)]
+    data = {sh: special_rows(sh[0], sh[1], sum(sh)) for sh in shapes}
+    expect = {sh: oracle.topk_rows_f32(data[sh], sh[2]) for sh in shapes}
+    dev = {sh: torch.from_numpy(data[sh]).cuda() for sh in shapes}
+    for rep in range(2):
+        outs = [(sh, tk.topk_rows_f32(dev[sh], sh[2])) for sh in shapes]
+        torch.cuda.synchronize()
+        for sh, (v, i) in outs:
+            ev, ei = expect[sh]
+            assert np.array_equal(i.cpu().numpy(), ei), (rep, sh)
+            assert np.array_equal(bits(v.cpu().numpy()), bits(ev)), (rep, sh)

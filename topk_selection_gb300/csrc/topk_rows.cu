@@ -288,9 +288,10 @@ topk_rows_smem_kernel(const float* __restrict__ in, int cols, int k, float* __re
 //   * start threshold: the k-th largest of 32*GL group maxima of the row's
 //     first tile (disjoint groups of real elements, so at least k elements
 //     of the row reach it);
-//   * every element is compared once, as a float, against the threshold's
-//     score; those that may pass get their exact 64-bit key, and keys above
-//     the warp's threshold are queued and merged 32 at a time into the
+//   * every 4-float vector is checked once, by its largest element, against
+//     the threshold; flagged vectors are queued as they are, and 32 queued
+//     vectors at a time are expanded into exact 64-bit keys, of which those
+//     above the threshold are queued again and merged 32 at a time into the
 //     warp's sorted register list, whose k-th key raises the threshold;
 //   * the warp writes the row's k best (value, column) pairs.
 constexpr int kRowWarps = 9;                         // 3 blocks x 9 warps = 27 warps per SM
@@ -298,7 +299,8 @@ constexpr int kRowThreads = kRowWarps * 32;
 constexpr int kRowU = 6;                             // 16-byte vectors per lane per tile
 constexpr int kRowTileVec = 32 * kRowU;              // 3 KiB tiles
 constexpr int kRowStages = 2;                        // tiles in flight per warp
-constexpr int kRowQueue = 160;                       // per-warp key queue (>= 31 + 128)
+constexpr int kRowQueue = 160;                       // per-warp key queue (>= 31 + 4 * 32)
+constexpr int kRowVQueue = 48;                       // per-warp vector queue (>= 31 + kRowU)
 constexpr int kRowRingBytes = kRowWarps * kRowStages * kRowTileVec * 16;
 
 struct RowGeom {
@@ -349,6 +351,8 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
     constexpr int GL = kRowU;  // groups of 4 elements per lane for the start threshold: 32*GL >= k
     extern __shared__ __align__(128) float4 rring[];       // per-warp stages
     __shared__ __align__(16) u64 s_q[kRowWarps * kRowQueue];  // key queues
+    __shared__ __align__(16) float4 s_qv[kRowWarps * kRowVQueue];  // vector queues: values
+    __shared__ unsigned s_qc[kRowWarps * kRowVQueue];              // and first columns
     __shared__ __align__(8) uint64_t s_bar[kRowWarps * kRowStages];
 
     const int lane = threadIdx.x & 31;
@@ -362,6 +366,8 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
     float4* my_ring = rring + (size_t)warp * kRowStages * kRowTileVec;
     uint64_t* my_bar = s_bar + warp * kRowStages;
     u64* q = s_q + warp * kRowQueue;
+    float4* qv = s_qv + warp * kRowVQueue;
+    unsigned* qc = s_qc + warp * kRowVQueue;
     const int W = gridDim.x * kRowWarps;
     const int gw = blockIdx.x * kRowWarps + warp;
 
@@ -397,19 +403,18 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
         RegList<L, u64> wl;
         wl.init(0ull);
         u64 T = 0ull;  // only keys above T are kept
-        int nq = 0;
-        // The queue holds raw (value bits << 32 | column) entries that beat
-        // the threshold when they were queued.  A drain turns 32 of them into
-        // exact keys, drops those no longer above T, and merges the rest.
+        int nq = 0;  // keys in q; below 32 between tiles
+        int nv = 0;  // vectors in qv/qc; below 32 between tiles
+        // The key queue holds exact keys that beat T when they were queued.
+        // A drain takes 32 of them, drops those no longer above T, and merges
+        // the rest into the list.
         auto drain = [&](bool all_of_it) {
             while (nq >= 32 || (all_of_it && nq > 0)) {
                 const int c = nq >= 32 ? 32 : nq;
                 __syncwarp();
-                const u64 raw = lane < c ? q[nq - c + lane] : 0ull;
+                u64 key = lane < c ? q[nq - c + lane] : 0ull;
                 __syncwarp();
                 nq -= c;
-                u64 key = 0ull;
-                if (lane < c) key = full_key(__uint_as_float((unsigned)(raw >> 32)), (unsigned)raw);
                 if (key <= T) key = 0ull;
                 const unsigned m = __ballot_sync(kFullMask, key != 0ull);
                 if (m) {
@@ -420,39 +425,57 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
                 }
             }
         };
-        // Queue a lane's elements that may beat T, given T's score as a
-        // float (tf) and T's column (tc): greater than tf (or NaN), or equal
-        // to it with a lower column.
-        auto queue4 = [&](bool has, float4 v, unsigned c0, float tf, unsigned tc) {
-            unsigned bits = 0u;
-            if (has) {
-                if (!(v.x <= tf) || (v.x == tf && c0 + 0 < tc)) bits |= 1u;
-                if (!(v.y <= tf) || (v.y == tf && c0 + 1 < tc)) bits |= 2u;
-                if (!(v.z <= tf) || (v.z == tf && c0 + 2 < tc)) bits |= 4u;
-                if (!(v.w <= tf) || (v.w == tf && c0 + 3 < tc)) bits |= 8u;
-            }
-            const int c = __popc(bits);
-            // Warp-wide exclusive prefix of the counts (0..4): one ballot per bit.
+        // The exact keys of a vector's elements that beat T; 0 for the
+        // others (every real key is above 0).
+        auto keys4 = [&](bool has, float4 v, unsigned c0, u64 (&kk)[4]) {
+            kk[0] = has ? full_key(v.x, c0 + 0) : 0ull;
+            kk[1] = has ? full_key(v.y, c0 + 1) : 0ull;
+            kk[2] = has ? full_key(v.z, c0 + 2) : 0ull;
+            kk[3] = has ? full_key(v.w, c0 + 3) : 0ull;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (kk[j] <= T) kk[j] = 0ull;
+        };
+        // Queue a lane's (up to 4) nonzero keys with one warp-wide prefix of
+        // the counts (0..4, one ballot per bit), then drain full batches.
+        // Needs nq < 32 on entry, so that 31 + 4 * 32 fit.
+        auto push4 = [&](const u64 (&kk)[4]) {
+            const int c = (kk[0] != 0ull) + (kk[1] != 0ull) + (kk[2] != 0ull) + (kk[3] != 0ull);
             const unsigned b0 = __ballot_sync(kFullMask, c & 1), b1 = __ballot_sync(kFullMask, c & 2),
                            b2 = __ballot_sync(kFullMask, c & 4);
-            if (bits) {
+            if (c) {
                 const unsigned lt = lanemask_lt();
                 int o = nq + __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
-                if (bits & 1u) q[o++] = ((u64)__float_as_uint(v.x) << 32) | (c0 + 0);
-                if (bits & 2u) q[o++] = ((u64)__float_as_uint(v.y) << 32) | (c0 + 1);
-                if (bits & 4u) q[o++] = ((u64)__float_as_uint(v.z) << 32) | (c0 + 2);
-                if (bits & 8u) q[o++] = ((u64)__float_as_uint(v.w) << 32) | (c0 + 3);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (kk[j]) q[o++] = kk[j];
             }
             nq += __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
             if (nq >= 32) drain(false);
         };
+        // Expand queued vectors 32 at a time into exact keys and queue those
+        // above T (which may have risen since the vectors were flagged).
+        auto expand = [&](bool all_of_it) {
+            while (nv >= 32 || (all_of_it && nv > 0)) {
+                const int c = nv >= 32 ? 32 : nv;
+                const bool has = lane < c;
+                __syncwarp();
+                const float4 v = has ? qv[nv - c + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+                const unsigned c0 = has ? qc[nv - c + lane] : 0u;
+                __syncwarp();
+                nv -= c;
+                u64 kk[4];
+                keys4(has, v, c0, kk);
+                push4(kk);
+            }
+        };
 
-        // Scalars outside the aligned body (fewer than 8): queued raw.
+        // Scalars outside the aligned body (fewer than 8).
         {
             const int col = lane < g.head ? lane : g.tail0 + (lane - g.head);
-            const bool has = lane < g.ns;
-            const unsigned m = __ballot_sync(kFullMask, has);
-            if (has) q[nq + __popc(m & lanemask_lt())] = ((u64)__float_as_uint(g.rp[col]) << 32) | (unsigned)col;
+            const u64 key = lane < g.ns ? full_key(g.rp[col], (unsigned)col) : 0ull;
+            const unsigned m = __ballot_sync(kFullMask, key != 0ull);
+            if (key) q[nq + __popc(m & lanemask_lt())] = key;
             nq += __popc(m);
         }
 
@@ -495,56 +518,37 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
                     if (!(m <= tf) || (m == tf && c0 < tc)) slots |= 1u << u;
                 }
             }
-            // Slow pass: each lane checks its flagged vectors (read again from
-            // the stage) exactly against T, one warp-wide prefix of the
-            // per-lane counts (0..4*kRowU, one ballot per bit) places every
-            // candidate of the tile in the queue at once.
+            // Slow pass: the flagged vectors go to the vector queue as they
+            // are, placed with one warp-wide prefix of the per-lane counts
+            // (0..kRowU, one ballot per bit); expand() turns them into keys.
             if (__any_sync(kFullMask, slots != 0u)) {
-                const float tf2 = key_float((unsigned)(T >> 32));
-                const unsigned tc2 = 0xFFFFFFFFu - (unsigned)T;
-                unsigned pass[kRowU];
-                int c = 0;
-#pragma unroll
-                for (int u = 0; u < kRowU; ++u) {
-                    pass[u] = 0u;
-                    if ((slots >> u) & 1u) {
-                        const float4 v = st[u * 32 + lane];
-                        const unsigned c0 = (unsigned)(g.head + (base + u * 32 + lane) * 4);
-                        unsigned bits = 0u;
-                        if (!(v.x <= tf2) || (v.x == tf2 && c0 + 0 < tc2)) bits |= 1u;
-                        if (!(v.y <= tf2) || (v.y == tf2 && c0 + 1 < tc2)) bits |= 2u;
-                        if (!(v.z <= tf2) || (v.z == tf2 && c0 + 2 < tc2)) bits |= 4u;
-                        if (!(v.w <= tf2) || (v.w == tf2 && c0 + 3 < tc2)) bits |= 8u;
-                        pass[u] = bits;
-                        c += __popc(bits);
-                    }
-                }
+                static_assert(kRowU < 8, "three ballots count 0..7 vectors");
+                const int c = __popc(slots);
                 const unsigned lt = lanemask_lt();
                 int off = 0, total = 0;
 #pragma unroll
-                for (int bit = 0; bit < 5; ++bit) {
+                for (int bit = 0; bit < 3; ++bit) {
                     const unsigned bb = __ballot_sync(kFullMask, (c >> bit) & 1);
                     off += __popc(bb & lt) << bit;
                     total += __popc(bb) << bit;
                 }
-                if (nq + total <= kRowQueue) {
-                    int o = nq + off;
+                if (nv + total > kRowVQueue) expand(true);
+                if (total <= kRowVQueue) {
+                    int o = nv + off;
 #pragma unroll
                     for (int u = 0; u < kRowU; ++u) {
-                        if (pass[u]) {
-                            const float4 v = st[u * 32 + lane];
-                            const unsigned c0 = (unsigned)(g.head + (base + u * 32 + lane) * 4);
-                            if (pass[u] & 1u) q[o++] = ((u64)__float_as_uint(v.x) << 32) | (c0 + 0);
-                            if (pass[u] & 2u) q[o++] = ((u64)__float_as_uint(v.y) << 32) | (c0 + 1);
-                            if (pass[u] & 4u) q[o++] = ((u64)__float_as_uint(v.z) << 32) | (c0 + 2);
-                            if (pass[u] & 8u) q[o++] = ((u64)__float_as_uint(v.w) << 32) | (c0 + 3);
+                        if ((slots >> u) & 1u) {
+                            qv[o] = st[u * 32 + lane];
+                            qc[o] = (unsigned)(g.head + (base + u * 32 + lane) * 4);
+                            ++o;
                         }
                     }
-                    nq += total;
-                    if (nq >= 32) drain(false);
+                    nv += total;
+                    if (nv >= 32) expand(false);
                 } else {
-                    // Too many for the queue at once (a weak threshold early in
-                    // a row): one flagged vector at a time, draining between.
+                    // More flagged vectors than the queue holds (a weak
+                    // threshold early in a row): one vector position at a
+                    // time, straight to keys.
                     unsigned todo = __reduce_or_sync(kFullMask, slots);
 #pragma unroll 1
                     while (todo) {
@@ -552,9 +556,9 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
                         todo &= todo - 1;
                         const bool has = (slots >> u) & 1u;
                         const float4 v = has ? st[u * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-                        // T may have risen in a drain above: queue against the current one.
-                        queue4(has, v, (unsigned)(g.head + (base + u * 32 + lane) * 4),
-                               key_float((unsigned)(T >> 32)), 0xFFFFFFFFu - (unsigned)T);
+                        u64 kk[4];
+                        keys4(has, v, (unsigned)(g.head + (base + u * 32 + lane) * 4), kk);
+                        push4(kk);
                     }
                 }
             }
@@ -565,6 +569,7 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
                 issue_next();
             }
         }
+        expand(true);
         drain(true);
 
         // The row's k best.  The key gives the value back exactly except for

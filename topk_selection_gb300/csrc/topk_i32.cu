@@ -160,14 +160,6 @@ __device__ __forceinline__ void enqueue(int* q, int& nq, int v, int t, int lane)
     nq += __popc(m);
 }
 
-// Programmatic dependent launch: the kernel is launched so that it may
-// start while the previous kernel on the stream finishes; it must not touch
-// state that kernel uses until grid_dependency_wait() returns (which waits
-// for the previous grid to complete and its writes to be visible), and it
-// lets the next launch start with launch_dependents().  Both are hardware
-// mechanisms, not spins.
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---------------------------------------------------------------- stage 2 --
 //

@@ -300,6 +300,8 @@ radix_filter_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned ch
     __shared__ unsigned stage[kRThreads / 32][64];
     __shared__ unsigned long long s_neq;
     __shared__ int s_last;
+    grid_dependency_wait();  // launched early (launch_pdl): wait for the previous kernel's writes
+    launch_dependents();
     const RadixView rv = radix_view(scratch);
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) s_neq = 0ull;
@@ -350,6 +352,8 @@ radix_exact1_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned ch
     __shared__ unsigned long long s_scan[64];
     __shared__ Bucket s_pick;
     __shared__ int s_last, s_go;
+    grid_dependency_wait();  // launched early (launch_pdl): wait for the previous kernel's writes
+    launch_dependents();
     const RadixView rv = radix_view(scratch);
     if (threadIdx.x == 0) s_go = __ldcg(&rv.ctrl->state) == kStateExact;
     for (int i = threadIdx.x; i < kBins; i += blockDim.x) sh[i] = 0u;
@@ -376,6 +380,8 @@ radix_exact2_kernel(const int32_t* __restrict__ in, size_t n, unsigned char* __r
     __shared__ unsigned stage[kRThreads / 32][64];
     __shared__ unsigned long long s_scan[64];
     __shared__ Bucket s_pick;
+    grid_dependency_wait();  // launched early (launch_pdl): wait for the previous kernel's writes
+    launch_dependents();
     __shared__ int s_last, s_go;
     __shared__ unsigned s_prefix, s_mode, s_need;
     const RadixView rv = radix_view(scratch);
@@ -426,6 +432,8 @@ radix_exact3_kernel(const int32_t* __restrict__ in, size_t n, unsigned char* __r
     __shared__ unsigned stage[kRThreads / 32][64];
     __shared__ unsigned long long s_scan[64];
     __shared__ Bucket s_pick;
+    grid_dependency_wait();  // launched early (launch_pdl): wait for the previous kernel's writes
+    launch_dependents();
     __shared__ unsigned s_cnt[256], s_off[256];
     __shared__ int s_last, s_go;
     __shared__ unsigned s_prefix, s_need;
@@ -634,6 +642,8 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
                      unsigned char* __restrict__ scratch, unsigned cap, int mode) {
     extern __shared__ __align__(16) unsigned char radix_cl_smem[];
     ClSmem& S = *reinterpret_cast<ClSmem*>(radix_cl_smem);
+    grid_dependency_wait();  // launched early (launch_pdl): wait for the previous kernel's writes
+    launch_dependents();
     const RadixView rv = radix_view(scratch);
     const unsigned rank = cluster_rank();
     const unsigned tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -1011,6 +1021,8 @@ __device__ __forceinline__ bool single_value_range(const RadixPlan* plan, unsign
 __global__ void __launch_bounds__(kSortWarps * 32, 1)
 radix_sort_kernel(int32_t* __restrict__ out, const unsigned char* __restrict__ scratch) {
     extern __shared__ __align__(16) unsigned radix_sort_smem[];
+    grid_dependency_wait();  // launched early (launch_pdl): wait for the previous kernel's writes
+    launch_dependents();
     const RadixPlan* plan = reinterpret_cast<const RadixPlan*>(scratch + kRadixCandOffset);
     const unsigned nr = __ldcg(&plan->nranges);
     const unsigned q0 = blockIdx.x * kSortWarps;
@@ -1093,11 +1105,15 @@ cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int
     const unsigned ucap = (unsigned)cap;
     const size_t cl_smem = sizeof(ClSmem), sort_smem = kSortCap * sizeof(unsigned);
     constexpr int sort_grid = kMaxRanges / kSortWarps;
+    // Every kernel of the plan waits for its predecessor's writes before it
+    // reads anything, so each is launched early (launch_pdl), whatever
+    // precedes it on the stream.
     if (n <= cap) {
-        radix_cluster_kernel<<<kClCtas, kClThreads, cl_smem, s>>>(in, n, k, 0u, out, sc, ucap, kClFull);
-        radix_sort_kernel<<<sort_grid, kSortWarps * 32, sort_smem, s>>>(out, sc);
+        e = launch_pdl(radix_cluster_kernel, kClCtas, kClThreads, cl_smem, s, in, n, k, 0u, out, sc, ucap, kClFull);
+        if (e == cudaSuccess)
+            e = launch_pdl(radix_sort_kernel, sort_grid, kSortWarps * 32, sort_smem, s, out, sc);
         *launches = 2;
-        return cudaGetLastError();
+        return e;
     }
     // Sample rank: k's expected share of the sample plus four standard
     // deviations and a floor of 16, so that at least k keys are >= t.
@@ -1110,15 +1126,17 @@ cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int
     size_t grid = (n + per_block - 1) / per_block;
     if (grid > (size_t)f.grid) grid = f.grid;
     if (grid < 1) grid = 1;
-    radix_cluster_kernel<<<kClCtas, kClThreads, cl_smem, s>>>(in, n, k, j, out, sc, ucap, kClSample);
-    radix_filter_kernel<<<(int)grid, kRThreads, 0, s>>>(in, n, k, sc, ucap);
-    radix_exact1_kernel<<<(int)grid, kRThreads, 0, s>>>(in, n, k, sc, ucap);
-    radix_exact2_kernel<<<(int)grid, kRThreads, 0, s>>>(in, n, sc, ucap);
-    radix_exact3_kernel<<<(int)grid, kRThreads, 0, s>>>(in, n, sc, ucap);
-    radix_cluster_kernel<<<kClCtas, kClThreads, cl_smem, s>>>(in, n, k, 0u, out, sc, ucap, kClFinal);
-    radix_sort_kernel<<<sort_grid, kSortWarps * 32, sort_smem, s>>>(out, sc);
+    const unsigned g = (unsigned)grid;
+    e = launch_pdl(radix_cluster_kernel, kClCtas, kClThreads, cl_smem, s, in, n, k, j, out, sc, ucap, kClSample);
+    if (e == cudaSuccess) e = launch_pdl(radix_filter_kernel, g, kRThreads, 0, s, in, n, k, sc, ucap);
+    if (e == cudaSuccess) e = launch_pdl(radix_exact1_kernel, g, kRThreads, 0, s, in, n, k, sc, ucap);
+    if (e == cudaSuccess) e = launch_pdl(radix_exact2_kernel, g, kRThreads, 0, s, in, n, sc, ucap);
+    if (e == cudaSuccess) e = launch_pdl(radix_exact3_kernel, g, kRThreads, 0, s, in, n, sc, ucap);
+    if (e == cudaSuccess)
+        e = launch_pdl(radix_cluster_kernel, kClCtas, kClThreads, cl_smem, s, in, n, k, 0u, out, sc, ucap, kClFinal);
+    if (e == cudaSuccess) e = launch_pdl(radix_sort_kernel, sort_grid, kSortWarps * 32, sort_smem, s, out, sc);
     *launches = 7;
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace topk

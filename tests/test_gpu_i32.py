@@ -211,6 +211,31 @@ def test_chained_calls_read_the_previous_output(tk):
     assert e.cpu().numpy()[0] == exp[0]
 
 
+def test_chains_through_the_large_k_plan(tk):
+    # The large-k kernels release their successors early as well: a
+    # streaming call on a large-k call's output must still see it finished,
+    # and the other way round.
+    x = synth.i32_uniform(4_000_000, 32)
+    d = torch.from_numpy(x).cuda()
+    s = torch.cuda.Stream()
+    exp = oracle.topk_i32(x, 5000)
+    with torch.cuda.stream(s):
+        for _ in range(4):
+            a = tk.topk_i32(d, 5000, stream=s)    # large-k plan
+            b = tk.topk_i32(a, 100, stream=s)     # streaming, input = a
+            c = tk.topk_i32(d, 120, stream=s)     # streaming, independent
+            f = tk.topk_i32(c, 110, stream=s)     # streaming on c
+            g = tk.topk_i32(a, 4000, stream=s)    # large-k on a
+            h = tk.topk_i32(g, 7, stream=s)       # streaming on g
+    s.synchronize()
+    assert np.array_equal(a.cpu().numpy(), exp)
+    assert np.array_equal(b.cpu().numpy(), exp[:100])
+    assert np.array_equal(c.cpu().numpy(), exp[:120])
+    assert np.array_equal(f.cpu().numpy(), exp[:110])
+    assert np.array_equal(g.cpu().numpy(), exp[:4000])
+    assert np.array_equal(h.cpu().numpy(), exp[:7])
+
+
 def test_many_back_to_back_calls(tk):
     # A long run of overlapping launches on one stream, inputs and outputs
     # distinct: every result must match.

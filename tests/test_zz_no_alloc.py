@@ -64,6 +64,34 @@ def test_noalloc_large_k_and_small_input(entry):
             assert torch.equal(got.cpu(), exp.cpu()), (n, k)
 
 
+
+def test_noalloc_and_cached_calls_chained_on_one_stream(entry):
+    # Calls of both entry points feed each other on one stream: every call
+    # must see the previous one's output finished, whichever entry point
+    # launched it.
+    tk, f = entry
+    import oracle
+    x = synth.i32_uniform(3_000_029, 43)
+    d = torch.from_numpy(x).cuda()
+    s = torch.cuda.Stream()
+    exp = oracle.topk_i32(x, 3000)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            a = run_noalloc(f, d, 3000, s)          # large-k plan, fixed scratch
+            b = tk.topk_i32(a, 100, stream=s)       # cached workspace, streaming, reads a
+            c = run_noalloc(f, b, 50, s)            # fixed scratch, streaming, reads b
+            e = tk.topk_i32(c, 20, stream=s)        # reads c
+            g = tk.topk_i32(d, 128, stream=s)       # independent input
+            h = run_noalloc(f, g, 1, s)             # reads g
+    s.synchronize()
+    assert np.array_equal(a.cpu().numpy(), exp)
+    assert np.array_equal(b.cpu().numpy(), exp[:100])
+    assert np.array_equal(c.cpu().numpy(), exp[:50])
+    assert np.array_equal(e.cpu().numpy(), exp[:20])
+    assert np.array_equal(g.cpu().numpy(), exp[:128])
+    assert h.cpu().numpy()[0] == exp[0]
+
+
 def test_noalloc_rejects_what_it_cannot_take(entry):
     tk, f = entry
     x = torch.zeros(5000, dtype=torch.int32, device="cuda")

@@ -36,7 +36,7 @@ struct Workspace {
     size_t stage_out_bytes = 0;
     void* items = nullptr;      // topk_items_f32 scratch
     size_t items_bytes = 0;
-    const void* stream_out = nullptr;  // output of the last streaming-plan launch on this stream
+    const void* stream_out = nullptr;  // output of the last int32 TopK launch on this stream
     size_t stream_out_bytes = 0;
     void* sort = nullptr;       // topk_sort_u32 scratch (its header zero between calls)
     size_t sort_bytes = 0;
@@ -172,9 +172,18 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
             w->stream_out = dout;
             w->stream_out_bytes = (size_t)k * sizeof(int32_t);
         }
-        e = topk::i32_launch(plan, s, din, n, k, dout, w->ctrl_cand, early);
-    } else
-        e = topk::radix_launch(s, din, n, k, dout, w->ctrl_cand, topk::kRadixCap, &launches);
+        e = topk::i32_launch(plan, s, din, n, k, dout, w->ctrl_cand, early, true);
+    } else {
+        // The large-k kernels let their successors start early too (each of
+        // them waits before reading anything): a streaming launch after this
+        // one must know what it writes.
+        {
+            std::lock_guard<std::mutex> lock(g_ws_mutex);
+            w->stream_out = dout;
+            w->stream_out_bytes = (size_t)k * sizeof(int32_t);
+        }
+        e = topk::radix_launch(s, din, n, k, dout, w->ctrl_cand, topk::kRadixCap, &launches, true);
+    }
     g_launches.fetch_add((unsigned long long)launches, std::memory_order_relaxed);
     if (e != cudaSuccess) return cuda_fail(e);
 

@@ -342,7 +342,7 @@ constexpr int kMonitorRounds = 1 << 20;      // bound on the monitor's polling r
 template <int L, int GL>
 __global__ void __launch_bounds__(kStreamThreads, 2)
 topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* __restrict__ out,
-                       unsigned char* __restrict__ scratch, int cap_limit) {
+                       unsigned char* __restrict__ scratch, int cap_limit, int release) {
     constexpr int K = 32 * L;
     extern __shared__ __align__(128) int4 ring[];             // per-warp stages; later the stage-2 list
     __shared__ __align__(16) int s_queue[kCons * kQueue];      // survivor queues, then the merge area
@@ -595,8 +595,9 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
     const int block_kth = s_queue[k - 1];
 
     // This block has read all its input: the next launch on the stream may
-    // start its blocks (they wait for this grid before touching the scratch).
-    launch_dependents();
+    // start its blocks (they wait for this grid before touching the scratch),
+    // when the caller keeps track of what this launch writes.
+    if (release) launch_dependents();
     // Every threshold this block's warps used went through s_thresh: publish
     // it (and the block's k-th value) before the ticket, whatever the
     // monitor managed to do.
@@ -617,7 +618,7 @@ struct StreamVariant {
     // of that kernel's blocks have read their input, and overlap its last
     // block's second stage; every access to the shared scratch waits for it.
     static cudaError_t launch(int grid, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
-                              unsigned char* scratch, int cap_limit, bool early) {
+                              unsigned char* scratch, int cap_limit, bool early, bool release) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid);
         cfg.blockDim = dim3(kThreads);
@@ -628,7 +629,8 @@ struct StreamVariant {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = early ? 1 : 0;
-        return cudaLaunchKernelEx(&cfg, topk_i32_stream_kernel<L, GL>, in, n, k, out, scratch, cap_limit);
+        return cudaLaunchKernelEx(&cfg, topk_i32_stream_kernel<L, GL>, in, n, k, out, scratch, cap_limit,
+                                  release ? 1 : 0);
     }
     static size_t units_per_block() { return kCons; }
 };
@@ -697,12 +699,12 @@ cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan) {
 }
 
 cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
-                       void* scratch, bool early) {
+                       void* scratch, bool early, bool release) {
     auto* sc = static_cast<unsigned char*>(scratch);
     const int cap = plan.stage2_cap;
-    if (k <= 32) return VarK32::launch(plan.grid, s, in, n, k, out, sc, cap, early);
-    if (k <= 64) return VarK64::launch(plan.grid, s, in, n, k, out, sc, cap, early);
-    return VarK128::launch(plan.grid, s, in, n, k, out, sc, cap, early);
+    if (k <= 32) return VarK32::launch(plan.grid, s, in, n, k, out, sc, cap, early, release);
+    if (k <= 64) return VarK64::launch(plan.grid, s, in, n, k, out, sc, cap, early, release);
+    return VarK128::launch(plan.grid, s, in, n, k, out, sc, cap, early, release);
 }
 
 }  // namespace topk

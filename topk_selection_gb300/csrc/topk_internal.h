@@ -72,9 +72,13 @@ constexpr size_t radix_scratch_bytes(size_t cap) { return kRadixBufOffset + cap 
 // cluster, else seven; any k up to kRadixMaxK).  scratch holds radix_scratch_bytes(cap)
 // bytes, 256-byte aligned, whose [kI32ResetBegin, kI32ResetEnd) bytes are
 // zero (they are zero again afterwards); cap is the candidate buffer's
-// capacity in keys, k <= cap <= kRadixClusterCap.
+// capacity in keys, k <= cap <= kRadixClusterCap.  Every kernel of the plan
+// waits for its predecessor's writes before reading anything.  release: the
+// plan's last kernel lets the next launch on the stream start before it
+// completes; only for callers that make sure such a launch does not read
+// `out` before it waits (see i32_launch's `early`).
 cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out, void* scratch,
-                         size_t cap, int* launches);
+                         size_t cap, int* launches, bool release);
 
 // Test options of the radix plan (TOPK_OPT_RADIX_CAP, TOPK_OPT_RADIX_SAMPLE_RANK; 0 = default).
 int radix_cap_option();
@@ -103,12 +107,14 @@ cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan);
 // Enqueue the single-launch int32 TopK.  scratch holds i32_scratch_bytes(plan.grid)
 // bytes, 256-byte aligned, whose [kI32ResetBegin, kI32ResetEnd) bytes are zero
 // (they are zero again when the launch completes).  early: launch with
-// programmatic stream serialization, so that when the previous work on the
-// stream is this kernel, this launch starts streaming its input while that
-// one finishes; the input must then not be anything the previous launch
-// writes (its output).
+// programmatic stream serialization, so that when the previous kernel on the
+// stream released its successors early (see `release`), this launch starts
+// streaming its input while that one finishes; the input must then not be
+// anything the previous launch writes (its output).  release: once its
+// blocks have read their input, let the next launch start early; only for
+// callers that record this launch's output for that check.
 cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
-                       void* scratch, bool early);
+                       void* scratch, bool early, bool release);
 
 // Enqueue the row TopK.  status: a device word that bounded waits set to
 // kStatusWaitTimeout when they give up (sticky).

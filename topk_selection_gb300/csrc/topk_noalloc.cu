@@ -102,7 +102,7 @@ extern "C" int topk_i32_noalloc(const int32_t* in, size_t n, int k, int32_t* out
         int launches = 0;
         e = cudaMemsetAsync(static_cast<char*>(scratch) + topk::kI32ResetBegin, 0,
                             topk::kI32ResetEnd - topk::kI32ResetBegin, s);
-        if (e == cudaSuccess) e = topk::radix_launch(s, in, n, k, out, scratch, cap, &launches);
+        if (e == cudaSuccess) e = topk::radix_launch(s, in, n, k, out, scratch, cap, &launches, false);
         for (int i = 0; i < launches; ++i) topk::note_launch();
         if (e != cudaSuccess) {
             topk::note_cuda_error((int)e);
@@ -127,7 +127,7 @@ extern "C" int topk_i32_noalloc(const int32_t* in, size_t n, int k, int32_t* out
     // before the launch (the sticky status word is left alone).
     e = cudaMemsetAsync(static_cast<char*>(scratch) + topk::kI32ResetBegin, 0,
                         topk::kI32ResetEnd - topk::kI32ResetBegin, s);
-    if (e == cudaSuccess) e = topk::i32_launch(plan, s, in, n, k, out, scratch, false);
+    if (e == cudaSuccess) e = topk::i32_launch(plan, s, in, n, k, out, scratch, false, false);
     if (e != cudaSuccess) {
         topk::note_cuda_error((int)e);
         return TOPK_ERR_CUDA;

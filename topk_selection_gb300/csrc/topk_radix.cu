@@ -1019,10 +1019,12 @@ __device__ __forceinline__ bool single_value_range(const RadixPlan* plan, unsign
 }
 
 __global__ void __launch_bounds__(kSortWarps * 32, 1)
-radix_sort_kernel(int32_t* __restrict__ out, const unsigned char* __restrict__ scratch) {
+radix_sort_kernel(int32_t* __restrict__ out, const unsigned char* __restrict__ scratch, int release) {
     extern __shared__ __align__(16) unsigned radix_sort_smem[];
     grid_dependency_wait();  // launched early (launch_pdl): wait for the previous kernel's writes
-    launch_dependents();
+    // The plan's last kernel lets the next launch start early only when the
+    // caller keeps track of what this one writes.
+    if (release) launch_dependents();
     const RadixPlan* plan = reinterpret_cast<const RadixPlan*>(scratch + kRadixCandOffset);
     const unsigned nr = __ldcg(&plan->nranges);
     const unsigned q0 = blockIdx.x * kSortWarps;
@@ -1089,7 +1091,7 @@ cudaError_t radix_fit(int device, RadixFit* out) {
 }  // namespace
 
 cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out, void* scratch,
-                         size_t cap, int* launches) {
+                         size_t cap, int* launches, bool release) {
     *launches = 0;
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
@@ -1111,7 +1113,7 @@ cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int
     if (n <= cap) {
         e = launch_pdl(radix_cluster_kernel, kClCtas, kClThreads, cl_smem, s, in, n, k, 0u, out, sc, ucap, kClFull);
         if (e == cudaSuccess)
-            e = launch_pdl(radix_sort_kernel, sort_grid, kSortWarps * 32, sort_smem, s, out, sc);
+            e = launch_pdl(radix_sort_kernel, sort_grid, kSortWarps * 32, sort_smem, s, out, sc, release ? 1 : 0);
         *launches = 2;
         return e;
     }
@@ -1134,7 +1136,7 @@ cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int
     if (e == cudaSuccess) e = launch_pdl(radix_exact3_kernel, g, kRThreads, 0, s, in, n, sc, ucap);
     if (e == cudaSuccess)
         e = launch_pdl(radix_cluster_kernel, kClCtas, kClThreads, cl_smem, s, in, n, k, 0u, out, sc, ucap, kClFinal);
-    if (e == cudaSuccess) e = launch_pdl(radix_sort_kernel, sort_grid, kSortWarps * 32, sort_smem, s, out, sc);
+    if (e == cudaSuccess) e = launch_pdl(radix_sort_kernel, sort_grid, kSortWarps * 32, sort_smem, s, out, sc, release ? 1 : 0);
     *launches = 7;
     return e;
 }

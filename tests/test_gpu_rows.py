@@ -188,3 +188,29 @@ def test_shapes_back_to_back(tk):
             ev, ei = expect[sh]
             assert np.array_equal(i.cpu().numpy(), ei), (rep, sh)
             assert np.array_equal(bits(v.cpu().numpy()), bits(ev)), (rep, sh)
+
+
+def test_chained_and_overlapping_calls(tk):
+    # Row calls (k <= 128) may start while the previous launch on the stream
+    # finishes, except when their input is that launch's output; int32 calls
+    # share the rule.
+    x = special_rows(300, 20_000, 9)
+    y = synth.f32_rows_tied(200, 9000, 10)
+    dx, dy = torch.from_numpy(x).cuda(), torch.from_numpy(y).cuda()
+    ev1, ei1 = oracle.topk_rows_f32(x, 64)
+    ev2, ei2 = oracle.topk_rows_f32(ev1, 8)
+    evy, eiy = oracle.topk_rows_f32(y, 32)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(4):
+            v1, i1 = tk.topk_rows_f32(dx, 64, stream=s)
+            v2, i2 = tk.topk_rows_f32(v1, 8, stream=s)       # input = previous vals
+            vy, iy = tk.topk_rows_f32(dy, 32, stream=s)      # independent
+            t = tk.topk_i32(iy.view(-1), 5, stream=s)        # int32 on the previous idx
+            v3, i3 = tk.topk_rows_f32(dy, 32, stream=s)      # after an int32 call
+    s.synchronize()
+    assert np.array_equal(i1.cpu().numpy(), ei1) and np.array_equal(bits(v1.cpu().numpy()), bits(ev1))
+    assert np.array_equal(i2.cpu().numpy(), ei2) and np.array_equal(bits(v2.cpu().numpy()), bits(ev2))
+    assert np.array_equal(iy.cpu().numpy(), eiy) and np.array_equal(bits(vy.cpu().numpy()), bits(evy))
+    assert np.array_equal(t.cpu().numpy(), oracle.topk_i32(eiy.reshape(-1).astype(np.int32), 5))
+    assert np.array_equal(i3.cpu().numpy(), eiy) and np.array_equal(bits(v3.cpu().numpy()), bits(evy))

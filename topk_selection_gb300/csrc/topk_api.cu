@@ -36,8 +36,11 @@ struct Workspace {
     size_t stage_out_bytes = 0;
     void* items = nullptr;      // topk_items_f32 scratch
     size_t items_bytes = 0;
-    const void* stream_out = nullptr;  // output of the last int32 TopK launch on this stream
-    size_t stream_out_bytes = 0;
+    // What the last launch on this stream that lets its successor start
+    // early writes (up to two ranges): a successor that starts early must
+    // not read it.
+    const void* stream_out[2] = {nullptr, nullptr};
+    size_t stream_out_bytes[2] = {0, 0};
     void* sort = nullptr;       // topk_sort_u32 scratch (its header zero between calls)
     size_t sort_bytes = 0;
     unsigned sort_epoch = 0;    // tags the sort's look-back words, one per call
@@ -110,6 +113,23 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
+// Whether a launch reading `in` may start early (see i32_launch): when `in`
+// does not overlap what the stream's last releasing launch writes.  Records
+// what this launch writes (ranges a and b; b may be empty) for the next one.
+// Only launches that release their successors early may call it; host
+// inputs are staged by a copy, which never overlaps a kernel.
+bool early_start(Workspace* w, const void* in, size_t in_bytes, const void* a, size_t a_bytes, const void* b,
+                 size_t b_bytes) {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    bool ok = true;
+    for (int i = 0; i < 2; ++i) ok = ok && !overlaps(in, in_bytes, w->stream_out[i], w->stream_out_bytes[i]);
+    w->stream_out[0] = a;
+    w->stream_out_bytes[0] = a_bytes;
+    w->stream_out[1] = b;
+    w->stream_out_bytes[1] = b_bytes;
+    return ok;
+}
+
 }  // namespace
 
 namespace topk {
@@ -165,23 +185,14 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
         // The streaming kernel may start while the previous one on this stream
         // finishes, reading its input early: not when that input is the
         // previous launch's output (a chain of TopKs).
-        bool early;
-        {
-            std::lock_guard<std::mutex> lock(g_ws_mutex);
-            early = !in_host && !overlaps(din, n * sizeof(int32_t), w->stream_out, w->stream_out_bytes);
-            w->stream_out = dout;
-            w->stream_out_bytes = (size_t)k * sizeof(int32_t);
-        }
+        const bool early = early_start(w, din, n * sizeof(int32_t), dout, (size_t)k * sizeof(int32_t), nullptr, 0) &&
+                           !in_host;
         e = topk::i32_launch(plan, s, din, n, k, dout, w->ctrl_cand, early, true);
     } else {
         // The large-k kernels let their successors start early too (each of
         // them waits before reading anything): a streaming launch after this
         // one must know what it writes.
-        {
-            std::lock_guard<std::mutex> lock(g_ws_mutex);
-            w->stream_out = dout;
-            w->stream_out_bytes = (size_t)k * sizeof(int32_t);
-        }
+        early_start(w, din, 0, dout, (size_t)k * sizeof(int32_t), nullptr, 0);
         e = topk::radix_launch(s, din, n, k, dout, w->ctrl_cand, topk::kRadixCap, &launches, true);
     }
     g_launches.fetch_add((unsigned long long)launches, std::memory_order_relaxed);
@@ -379,7 +390,11 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
     if (vals_host) dvals = static_cast<float*>(w->stage_out);
     if (idx_host) didx = reinterpret_cast<int32_t*>(static_cast<char*>(w->stage_out) + nout);
 
-    e = topk::rows_launch(s, din, rows, cols, k, dvals, didx, status);
+    // The streamed row kernel (k <= 128) starts early and releases its
+    // successors like the int32 streaming kernel.
+    bool early = false;
+    if (k <= 128) early = early_start(w, din, nin, dvals, nout, didx, nout) && !in_host;
+    e = topk::rows_launch(s, din, rows, cols, k, dvals, didx, status, early, k <= 128);
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
 

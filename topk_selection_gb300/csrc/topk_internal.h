@@ -117,9 +117,12 @@ cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, s
                        void* scratch, bool early, bool release);
 
 // Enqueue the row TopK.  status: a device word that bounded waits set to
-// kStatusWaitTimeout when they give up (sticky).
+// kStatusWaitTimeout when they give up (sticky).  early and release as for
+// i32_launch (k <= 128 only): with early, the launch reads its input while
+// the previous kernel on the stream finishes, so the input must not overlap
+// what that launch writes; with release, the next launch may start early.
 cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
-                        unsigned* status);
+                        unsigned* status, bool early, bool release);
 
 // Enqueue a one-launch reduction (op 0 sum, 1 max, 2 min) of n int32 or
 // float32 values.  out: one int64 (int32 input) or one double (float32

@@ -453,7 +453,7 @@ cudaError_t items_launch(cudaStream_t s, const float* score, const int64_t* item
         size_t C = level_cols(real, ke, first);
         if (C > len) C = len;  // fewer candidates than one row of 8 ke: a single row of all of them
         const size_t R = len / C, tail = len - R * C;  // later levels: len is a multiple of C, tail 0
-        e = rows_launch(s, cur, (int)R, (int)C, ke, wv, wx, status);
+        e = rows_launch(s, cur, (int)R, (int)C, ke, wv, wx, status, false, false);
         if (e != cudaSuccess) return e;
         *launches += 1;
         const size_t next_real = R * ke + tail;

@@ -347,7 +347,7 @@ __device__ __forceinline__ void group_max_keys(const float4 (&r)[kRowU], int nva
 template <int L>
 __global__ void __launch_bounds__(kRowThreads, 3)
 topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k, float* __restrict__ vals,
-                        int32_t* __restrict__ idx, unsigned* __restrict__ status) {
+                        int32_t* __restrict__ idx, unsigned* __restrict__ status, int release) {
     constexpr int GL = kRowU;  // groups of 4 elements per lane for the start threshold: 32*GL >= k
     extern __shared__ __align__(128) float4 rring[];       // per-warp stages
     __shared__ __align__(16) u64 s_q[kRowWarps * kRowQueue];  // key queues
@@ -362,6 +362,11 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
         mbar_init_fence();
     }
     __syncthreads();
+    // Launched early (see the host side), this kernel reads only its input
+    // until it waits, before its first output write, for the previous
+    // kernel on the stream.  It lets the next launch start now when the
+    // caller keeps track of what this launch writes.
+    if (release) launch_dependents();
 
     float4* my_ring = rring + (size_t)warp * kRowStages * kRowTileVec;
     uint64_t* my_bar = s_bar + warp * kRowStages;
@@ -574,6 +579,7 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
 
         // The row's k best.  The key gives the value back exactly except for
         // -0.0 (keyed as +0.0) and NaN payloads: those are read from the row.
+        grid_dependency_wait();  // the previous kernel's writes come first
 #pragma unroll
         for (int j = 0; j < L; ++j) {
             const int p = j * 32 + lane;
@@ -603,7 +609,7 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
 
 template <int L>
 cudaError_t launch_stream(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
-                          unsigned* status) {
+                          unsigned* status, bool early, bool release) {
     constexpr int kMaxDev = 64;
     static std::mutex mu;
     static int grid_cache[kMaxDev] = {};
@@ -629,18 +635,28 @@ cudaError_t launch_stream(cudaStream_t s, const float* in, int rows, int cols, i
     }
     const int want = (rows + kRowWarps - 1) / kRowWarps;
     const int grid = want < full ? want : full;
-    topk_rows_stream_kernel<L><<<grid, kRowThreads, kRowRingBytes, s>>>(in, rows, cols, k, vals, idx, status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kRowThreads);
+    cfg.dynamicSmemBytes = kRowRingBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, topk_rows_stream_kernel<L>, in, rows, cols, k, vals, idx, status,
+                              release ? 1 : 0);
 }
 
 cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
-                        unsigned* status) {
+                        unsigned* status, bool early, bool release) {
     // k <= 128 streams (one warp per row); k > 128 uses one block per row
     // with shared-memory buffers.
     const bool stream = k <= 128;
-    if (stream && k <= 32) return launch_stream<1>(s, in, rows, cols, k, vals, idx, status);
-    if (stream && k <= 64) return launch_stream<2>(s, in, rows, cols, k, vals, idx, status);
-    if (stream) return launch_stream<4>(s, in, rows, cols, k, vals, idx, status);
+    if (stream && k <= 32) return launch_stream<1>(s, in, rows, cols, k, vals, idx, status, early, release);
+    if (stream && k <= 64) return launch_stream<2>(s, in, rows, cols, k, vals, idx, status, early, release);
+    if (stream) return launch_stream<4>(s, in, rows, cols, k, vals, idx, status, early, release);
     const size_t smem = (size_t)kWarps * 2048 * sizeof(u64);
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&topk_rows_smem_kernel<2048>),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -132,11 +132,15 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
  *
  * The selection runs the row TopK level by level (two-stage reduction):
  * rows of at least 8k scores give their k best, whose winners, in order,
- * are the next level's rows, until one row is left.  With keep, an ordered
- * compaction of the kept scores runs first, and the call waits for the
- * kept count (a 4-byte copy to the host) before it enqueues the levels;
- * without keep it only enqueues.  Scratch: about 8n bytes with keep, plus
- * 24 * 4097 * k bytes, in the library's per-stream workspace.
+ * are the next level's rows, until one row is left.  With keep, when
+ * n >= 2^20, k <= 128 and keep's address is congruent to score's / 4
+ * (mod 4) (e.g. score 16-byte aligned, keep 4-byte aligned), the first
+ * level skips filtered positions itself and the call only enqueues.
+ * Otherwise an ordered compaction of the kept scores runs first, and the
+ * call waits for the kept count (a 4-byte copy to the host) before it
+ * enqueues the levels; that form needs about 8n bytes more scratch.  Without
+ * keep the call only enqueues.  Scratch: about 24 * 4097 * k bytes besides,
+ * in the library's per-stream workspace.
  * Host pointers are rejected with TOPK_ERR_INVALID_ARG.
  */
 int topk_items_f32(const float* score, const int64_t* item, const uint8_t* keep, size_t n, int k, float* out_score,

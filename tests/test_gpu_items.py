@@ -136,6 +136,71 @@ def test_large_filtered(tk):
     check(tk, x, 128)
 
 
+
+def run_views(tk, score, k, keep, item=None, score_off=0, keep_off=0):
+    """topk_items_f32 on device views placed at element offsets."""
+    n = score.size
+    d = torch.empty(n + score_off, dtype=torch.float32, device="cuda")
+    d[score_off:].copy_(torch.from_numpy(score))
+    kk = torch.empty(n + keep_off, dtype=torch.uint8, device="cuda")
+    kk[keep_off:].copy_(torch.from_numpy(keep))
+    di = None if item is None else torch.from_numpy(item).cuda()
+    s_, i_, c_ = tk.topk_items_f32(d[score_off:], k, item=di, keep=kk[keep_off:])
+    torch.cuda.synchronize()
+    return s_.cpu().numpy(), i_.cpu().numpy(), int(c_.item())
+
+
+def check_views(tk, score, k, keep, item=None, score_off=0, keep_off=0):
+    gs, gi, gc = run_views(tk, score, k, keep, item, score_off, keep_off)
+    es, ei, ec = oracle.topk_items_f32(score, k, item=item, keep=keep)
+    assert gc == ec, (score.size, k, score_off, keep_off, gc, ec)
+    assert np.array_equal(gi, ei), (score.size, k, score_off, keep_off, gi[:5], ei[:5])
+    assert np.array_equal(bits(gs), bits(es)), (score.size, k, score_off, keep_off)
+
+
+@pytest.mark.parametrize("frac", [0.5, 0.01, 1.0, 0.0])
+def test_filter_folded_into_first_level(tk, frac):
+    # Large inputs with k <= 128 skip filtered positions inside the first
+    # level: rows with fewer kept elements than k, kept -inf and NaN next to
+    # larger filtered-out scores, and every offset pairing that keeps the
+    # keep words aligned (and some that do not, which take the compaction).
+    rng = np.random.default_rng(int(frac * 1000) + 77)
+    n = (1 << 20) + 12_345
+    x = make("specials", n, 7) if frac == 0.5 else make("ties", n, 8)
+    keep = (rng.random(n) < frac).astype(np.uint8)
+    keep[keep != 0] = rng.integers(1, 256, size=int(keep.sum()), dtype=np.uint8)  # any nonzero byte keeps
+    items = rng.integers(-2**50, 2**50, size=n, dtype=np.int64)
+    for k in (1, 20, 64, 100, 128):
+        check(tk, x, k, item=items, keep=keep)
+    for so, ko in ((1, 1), (2, 2), (3, 3), (4, 0), (1, 0), (0, 3)):
+        check_views(tk, x, 64, keep, item=items, score_off=so, keep_off=ko)
+
+
+def test_filter_folded_sparse_and_tail(tk):
+    rng = np.random.default_rng(91)
+    n = 3_000_017
+    x = make("normal", n, 9)
+    # So sparse that most first-level rows keep nothing.
+    keep = (rng.random(n) < 1e-4).astype(np.uint8)
+    for k in (1, 64, 128):
+        check(tk, x, k, keep=keep)
+    # Kept elements only at the very end (the part after the last full row).
+    keep = np.zeros(n, dtype=np.uint8)
+    keep[-37:] = 1
+    check(tk, x, 64, keep=keep)
+    check(tk, x, 20, keep=keep)
+    # Only -inf kept, while larger scores are filtered out.
+    y = x.copy()
+    y[::1000] = -np.inf
+    keep = np.zeros(n, dtype=np.uint8)
+    keep[::1000] = 1
+    check(tk, y, 100, keep=keep)
+    # One kept NaN among kept -inf.
+    y[5000] = np.nan
+    keep[5000] = 1
+    check(tk, y, 10, keep=keep)
+
+
 def test_host_pointers_rejected(tk):
     x = torch.from_numpy(make("normal", 100, 1))
     out_s = torch.empty(5, dtype=torch.float32)

@@ -335,7 +335,8 @@ int topk_items_f32(const float* score, const int64_t* item, const uint8_t* keep,
     Workspace* w = nullptr;
     int rc = workspace(s, device, topk::kI32CandOffset, 0, 0, &w);
     if (rc != TOPK_OK) return rc;
-    const size_t need = topk::items_scratch_bytes(n, k, keep != nullptr);
+    const size_t need = topk::items_scratch_bytes(
+        n, k, keep != nullptr && !topk::items_fused_filter(score, keep, n, k));
     {
         std::lock_guard<std::mutex> lock(g_ws_mutex);
         rc = grow(&w->items, &w->items_bytes, need);

@@ -124,6 +124,14 @@ cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, s
 cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
                         unsigned* status, bool early, bool release);
 
+// The row TopK over kept elements only (k <= 128): element (r, c) takes part
+// when keep[r * cols + c] != 0.  Each row's outputs hold its valid winners
+// first, then (-inf, -1); row_count[r] is how many are valid.  Needs
+// rows_mask_aligned(in, keep) (cudaErrorInvalidValue otherwise).
+bool rows_mask_aligned(const float* in, const uint8_t* keep);
+cudaError_t rows_launch_masked(cudaStream_t s, const float* in, const uint8_t* keep, int rows, int cols, int k,
+                               float* vals, int32_t* idx, int32_t* row_count, unsigned* status);
+
 // Enqueue a one-launch reduction (op 0 sum, 1 max, 2 min) of n int32 or
 // float32 values.  out: one int64 (int32 input) or one double (float32
 // input), in device memory.  scratch: the int32 workspace (its ticket word in
@@ -133,10 +141,17 @@ cudaError_t reduce_launch(cudaStream_t s, const void* in, size_t n, bool is_floa
 constexpr size_t kReduceScratchBytes = kI32CandOffset + (size_t)kI32MaxGrid * 32;
 
 // Score-keyed TopK with item ids and an optional keep filter (topk_items.cu).
-// scratch: items_scratch_bytes(n, k, keep != null) bytes of device memory
-// (no contents needed).  With a filter the call waits for the kept count (one
-// 4-byte copy to the host) before enqueueing the selection.
-size_t items_scratch_bytes(size_t n, int k, bool filtered);
+// scratch: items_scratch_bytes(n, k, compact) bytes of device memory, compact
+// = keep != null && !items_fused_filter(score, keep, n, k)
+// (no contents needed).  With a filter that does not fold into the first
+// level, the call waits for the kept count (one 4-byte copy to the host)
+// before enqueueing the selection.
+// compact: the filter runs as a separate compaction (a keep array that
+// items_fused_filter turns down); its arrays need n * 8 more bytes.
+size_t items_scratch_bytes(size_t n, int k, bool compact);
+// Whether a filtered call folds the filter into its first level (no
+// compaction, no wait for the kept count).
+bool items_fused_filter(const float* score, const uint8_t* keep, size_t n, int k);
 cudaError_t items_launch(cudaStream_t s, const float* score, const int64_t* item, const uint8_t* keep, size_t n,
                          int k, float* out_score, int64_t* out_item, int64_t* out_count, void* scratch,
                          size_t scratch_bytes, unsigned* status, int* launches);

@@ -11,9 +11,13 @@
 //
 // Plan: the page's two-stage reduction, applied level by level with the row
 // kernel (topk_rows.cu) as the block-level TopK:
-//   filter   (keep given) an ordered compaction of the kept scores and their
-//            positions: per-block counts over contiguous ranges, then every
-//            block writes its kept elements at its offset, in order.
+//   filter   (keep given, large n, k <= 128) folded into level 1: the row
+//            kernel skips filtered elements and says how many winners each
+//            row has; a gather packs the rows' winners and the kept tail in
+//            position order, padding at the end.  Otherwise an ordered
+//            compaction of the kept scores and their positions (per-block
+//            counts over contiguous ranges, then every block writes its kept
+//            elements at its offset, in order) comes first.
 //   level 1  the m candidates, as rows of C >= 8k scores plus one shorter
 //            tail row: the row kernel leaves each row's k best.
 //   level j  the previous level's winners, in row order, are the next
@@ -29,6 +33,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "../../include/topk.h"
 #include "topk_device.cuh"
 #include "topk_internal.h"
 
@@ -280,6 +285,111 @@ __global__ void items_gather_kernel(const float* __restrict__ wv, const int32_t*
     }
 }
 
+// Next level's candidates after a filtered level 1: the valid winners of
+// the R rows (wc[r] of them in row r, first in its k outputs; row r's
+// columns count from r * C), then the kept elements of the tail [R * C, n),
+// all in position order, then (-inf, -1) pads up to `len`.  Block b packs
+// rows [b * rb, (b + 1) * rb); the last block also packs the tail.
+constexpr int kGatherThreads = 512;
+__global__ void __launch_bounds__(kGatherThreads)
+items_gather_masked_kernel(const float* __restrict__ wv, const int32_t* __restrict__ wx,
+                           const int32_t* __restrict__ wc, int R, int C, int k, const float* __restrict__ score,
+                           const uint8_t* __restrict__ keep, size_t n, size_t len, float* __restrict__ ns,
+                           int32_t* __restrict__ npos) {
+    __shared__ unsigned s_red[kGatherThreads / 32][2];
+    __shared__ unsigned s_rowbase[kGatherThreads];
+    __shared__ unsigned s_warp[kGatherThreads / 32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int rb = (R + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int r0 = (int)blockIdx.x * rb < R ? (int)blockIdx.x * rb : R;
+    const int r1 = r0 + rb < R ? r0 + rb : R;
+    // Winners of the rows before this block's, and of all rows.
+    unsigned before = 0, all = 0;
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+        const unsigned c = (unsigned)wc[r];
+        before += r < r0 ? c : 0u;
+        all += c;
+    }
+    before = __reduce_add_sync(kFullMask, before);
+    all = __reduce_add_sync(kFullMask, all);
+    if (lane == 0) {
+        s_red[w][0] = before;
+        s_red[w][1] = all;
+    }
+    __syncthreads();
+    before = all = 0;
+    for (int j = 0; j < kGatherThreads / 32; ++j) {
+        before += s_red[j][0];
+        all += s_red[j][1];
+    }
+    // This block's rows, rb <= blockDim at a time: an exclusive scan of
+    // their counts, then one warp per row copies its winners.
+    for (int c0 = r0; c0 < r1; c0 += blockDim.x) {
+        const int r = c0 + (int)threadIdx.x;
+        const unsigned c = r < r1 ? (unsigned)wc[r] : 0u;
+        unsigned x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(kFullMask, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_warp[w] = x;
+        __syncthreads();
+        unsigned wb = 0, tot = 0;
+        for (int j = 0; j < kGatherThreads / 32; ++j) {
+            wb += j < w ? s_warp[j] : 0u;
+            tot += s_warp[j];
+        }
+        s_rowbase[threadIdx.x] = before + wb + x - c;
+        __syncthreads();
+        const int nr = r1 - c0 < (int)blockDim.x ? r1 - c0 : (int)blockDim.x;
+        for (int i = w; i < nr; i += kGatherThreads / 32) {
+            const int rr = c0 + i;
+            const int cnt = wc[rr];
+            const size_t dst = s_rowbase[i];
+            for (int j = lane; j < cnt; j += 32) {
+                ns[dst + j] = wv[(size_t)rr * k + j];
+                npos[dst + j] = (int32_t)((size_t)rr * C + (size_t)wx[(size_t)rr * k + j]);
+            }
+        }
+        before += tot;
+        __syncthreads();
+    }
+    // Pads after the tail's room, by every block; the tail itself and the
+    // pads in the rest of its room, by the last block.
+    const size_t tail0 = (size_t)R * (size_t)C, tail_len = n - tail0;
+    for (size_t j = all + tail_len + (size_t)blockIdx.x * blockDim.x + threadIdx.x; j < len;
+         j += (size_t)gridDim.x * blockDim.x) {
+        ns[j] = __int_as_float(0xFF800000);
+        npos[j] = -1;
+    }
+    if (blockIdx.x != gridDim.x - 1) return;
+    unsigned base = all;
+    for (size_t c0 = tail0; c0 < n; c0 += blockDim.x) {
+        const size_t i = c0 + threadIdx.x;
+        const bool p = i < n && keep[i] != 0;
+        const unsigned b = __ballot_sync(kFullMask, p);
+        if (lane == 0) s_warp[w] = __popc(b);
+        __syncthreads();
+        unsigned wb = 0, tot = 0;
+        for (int j = 0; j < kGatherThreads / 32; ++j) {
+            wb += j < w ? s_warp[j] : 0u;
+            tot += s_warp[j];
+        }
+        if (p) {
+            const unsigned slot = base + wb + __popc(b & lanemask_lt());
+            ns[slot] = score[i];
+            npos[slot] = (int32_t)i;
+        }
+        base += tot;
+        __syncthreads();
+    }
+    for (size_t j = base + threadIdx.x; j < all + tail_len && j < len; j += blockDim.x) {
+        ns[j] = __int_as_float(0xFF800000);
+        npos[j] = -1;
+    }
+}
+
 // Order key of a score: value descending with NaN on top and -0 equal to +0
 // (the row order), then the lower array index first.
 __device__ __forceinline__ unsigned long long items_key(float v, unsigned j) {
@@ -307,18 +417,24 @@ items_final_sort_kernel(const float* __restrict__ cv, const int32_t* __restrict_
     const int L = next_pow2(count < 2 ? 2 : count);
     for (int j = threadIdx.x; j < L; j += blockDim.x) keys[j] = j < count ? items_key(cv[j], (unsigned)j) : 0ull;
     block_sort_smem_desc(keys, L);
+    // Pads (position -1) sort after every real candidate, so the valid
+    // outputs come first; their number is the count.
+    int valid = 0;
     for (int j = threadIdx.x; j < k; j += blockDim.x) {
         const unsigned idx = 0xFFFFFFFFu - (unsigned)(keys[j] & 0xFFFFFFFFull);
-        const int32_t p = j < ke ? (cp ? cp[idx] : (int32_t)idx) : -1;
-        if (p >= 0) {  // a pad (p = -1) never ranks among the best ke; guarded all the same
+        const int32_t p = (j < ke && j < count) ? (cp ? cp[idx] : (int32_t)idx) : -1;
+        if (p >= 0) {
             out_score[j] = cv[idx];
             out_item[j] = item ? item[p] : (int64_t)p;
+            ++valid;
         } else {
             out_score[j] = __int_as_float(0xFF800000);
             out_item[j] = -1;
         }
     }
-    if (threadIdx.x == 0 && out_count) *out_count = ke;
+    static_assert(TOPK_MAX_K_ROWS <= kFinalThreads, "one output per thread: the count is a thread count");
+    valid = __syncthreads_count(valid);
+    if (threadIdx.x == 0 && out_count) *out_count = valid;
 }
 
 // Pads the outputs when nothing is kept.
@@ -348,13 +464,22 @@ inline size_t next_cap(size_t n, int k) {
     return (kTargetRows + 1) * (size_t)k + 4 * (n / kTargetRows + 32 * (size_t)k + 2);
 }
 
+// The filter folds into level 1 for large inputs, k <= 128 and a keep array
+// whose 4-byte words line up with the score array's 16-byte vectors.
+constexpr size_t kFusedMinN = size_t(1) << 20;
+
 }  // namespace
 
-size_t items_scratch_bytes(size_t n, int k, bool filtered) {
+bool items_fused_filter(const float* score, const uint8_t* keep, size_t n, int k) {
+    return keep && n >= kFusedMinN && k <= 128 && rows_mask_aligned(score, keep);
+}
+
+size_t items_scratch_bytes(size_t n, int k, bool compact) {
     size_t b = 0;
-    if (filtered) b += kFiltMaxGrid * 4 + 256 + n * 8 + 512;  // counts, total, compacted scores and positions
+    if (compact) b += kFiltMaxGrid * 4 + 256 + n * 8 + 512;  // counts, total, compacted scores and positions
     const size_t winners = (kTargetRows + 1) * (size_t)k;
     b += winners * 8 + 2 * next_cap(n, k) * 8 + 6 * 256;      // winners, two candidate arrays
+    b += (kTargetRows + 1) * 4 + 256;                          // winners per row (filtered level 1)
     return b;
 }
 
@@ -367,7 +492,8 @@ cudaError_t items_launch(cudaStream_t s, const float* score, const int64_t* item
                          int k, float* out_score, int64_t* out_item, int64_t* out_count, void* scratch,
                          size_t scratch_bytes, unsigned* status, int* launches) {
     *launches = 0;
-    if (scratch_bytes < items_scratch_bytes(n, k, keep != nullptr)) return cudaErrorInvalidValue;
+    const bool fused = items_fused_filter(score, keep, n, k);
+    if (scratch_bytes < items_scratch_bytes(n, k, keep != nullptr && !fused)) return cudaErrorInvalidValue;
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
@@ -392,7 +518,7 @@ cudaError_t items_launch(cudaStream_t s, const float* score, const int64_t* item
     const float* cur = score;
     const int32_t* cur_pos = nullptr;
     size_t m = n;
-    if (keep) {
+    if (keep && !fused) {
         const size_t per0 = (n + kFiltMaxGrid - 1) / kFiltMaxGrid;
         const size_t per = per0 < (size_t)kFiltThreads ? (size_t)kFiltThreads : (per0 + 511) / 512 * 512;
         const int grid = (int)((n + per - 1) / per);
@@ -429,7 +555,7 @@ cudaError_t items_launch(cudaStream_t s, const float* score, const int64_t* item
             return cudaGetLastError();
         }
     }
-    const int ke = m < (size_t)k ? (int)m : k;
+    const int ke = m < (size_t)k ? (int)m : k;  // with a fused filter m is not known here: ke = k
     const size_t winners = (kTargetRows + 1) * (size_t)k;
     auto* wv = static_cast<float*>(take(winners * 4));
     auto* wx = static_cast<int32_t*>(take(winners * 4));
@@ -442,6 +568,36 @@ cudaError_t items_launch(cudaStream_t s, const float* score, const int64_t* item
     size_t len = m;      // entries of cur, pads included
     size_t real = m;     // entries of cur that are not pads (an upper bound after level 1)
     bool first = true;
+    if (fused) {
+        // Level 1 over the kept elements of the whole input, then the packed
+        // winners and kept tail (pads at the end) are the next candidates.
+        auto* wc = static_cast<int32_t*>(take((kTargetRows + 1) * 4));
+        // The last block of the gather packs the tail alone: keep it short.
+        // Rows of n / kTargetRows leave fewer than kTargetRows elements over
+        // whenever that is a row's worth of at least 8k; otherwise the
+        // rounded-up rows are short themselves (fewer than kTargetRows).
+        size_t C = n / kTargetRows;
+        if (C < (size_t)8 * ke || C <= n % kTargetRows) C = level_cols(n, ke, true);
+        const size_t R = n / C;
+        e = rows_launch_masked(s, score, keep, (int)R, (int)C, ke, wv, wx, wc, status);
+        if (e != cudaSuccess) return e;
+        *launches += 1;
+        const size_t next_real = R * ke + (n - R * C);
+        const size_t Cn = level_cols(next_real, ke, false);
+        const size_t next_len = next_real <= (size_t)kFinalCap ? next_real : (next_real + Cn - 1) / Cn * Cn;
+        const int gb = R < 128 ? (R < 1 ? 1 : (int)R) : 128;
+        items_gather_masked_kernel<<<gb, kGatherThreads, 0, s>>>(wv, wx, wc, (int)R, (int)C, ke, score, keep, n,
+                                                                 next_len, nb_s[0], nb_p[0]);
+        *launches += 1;
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        cur = nb_s[0];
+        cur_pos = nb_p[0];
+        flip = 1;
+        len = next_len;
+        real = next_real;
+        first = false;
+    }
     for (;;) {
         if (real <= (size_t)kFinalCap) {
             // cur holds real entries only here (a single-row level adds no pads)

@@ -344,10 +344,43 @@ __device__ __forceinline__ void group_max_keys(const float4 (&r)[kRowU], int nva
     }
 }
 
-template <int L>
+// The same over kept elements only: mk[u] holds the keep bytes of vector u
+// (byte b for element b; 0 = filtered out).  A group with no kept element
+// gives 0.
+template <int GL>
+__device__ __forceinline__ void group_max_keys_kept(const float4 (&r)[kRowU], const unsigned (&mk)[kRowU],
+                                                    int nvalid, unsigned (&gk)[GL]) {
+#pragma unroll
+    for (int j = 0; j < GL; ++j) {
+        float fm = -INFINITY;
+        bool nan = false, any = false;
+#pragma unroll
+        for (int u = j * (kRowU / GL); u < (j + 1) * (kRowU / GL); ++u) {
+            if (u < nvalid) {
+                const float e[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    if ((mk[u] >> (8 * b)) & 0xFFu) {
+                        fm = fmaxf(fm, e[b]);
+                        nan |= e[b] != e[b];
+                        any = true;
+                    }
+                }
+            }
+        }
+        gk[j] = !any ? 0u : (nan ? 0xFFFFFFFFu : score_key(__float_as_uint(fm)));
+    }
+}
+
+// kMask: only elements whose keep byte (same layout as `in`) is nonzero take
+// part; each row's outputs hold its valid winners first, then (-inf, -1), and
+// row_count[row] says how many are valid.  The keep word of a 16-byte vector
+// is read with one 4-byte load (the host checks the alignment that needs).
+template <int L, bool kMask>
 __global__ void __launch_bounds__(kRowThreads, 3)
 topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k, float* __restrict__ vals,
-                        int32_t* __restrict__ idx, unsigned* __restrict__ status, int release) {
+                        int32_t* __restrict__ idx, unsigned* __restrict__ status, int release,
+                        const uint8_t* __restrict__ keep, int32_t* __restrict__ row_count) {
     constexpr int GL = kRowU;  // groups of 4 elements per lane for the start threshold: 32*GL >= k
     extern __shared__ __align__(128) float4 rring[];       // per-warp stages
     __shared__ __align__(16) u64 s_q[kRowWarps * kRowQueue];  // key queues
@@ -437,6 +470,13 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
             kk[1] = has ? full_key(v.y, c0 + 1) : 0ull;
             kk[2] = has ? full_key(v.z, c0 + 2) : 0ull;
             kk[3] = has ? full_key(v.w, c0 + 3) : 0ull;
+            if constexpr (kMask) {
+                const unsigned mw =
+                    has ? __ldg(reinterpret_cast<const unsigned*>(keep + (size_t)row * (size_t)cols + c0)) : 0u;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (((mw >> (8 * j)) & 0xFFu) == 0u) kk[j] = 0ull;
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 if (kk[j] <= T) kk[j] = 0ull;
@@ -478,7 +518,9 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
         // Scalars outside the aligned body (fewer than 8).
         {
             const int col = lane < g.head ? lane : g.tail0 + (lane - g.head);
-            const u64 key = lane < g.ns ? full_key(g.rp[col], (unsigned)col) : 0ull;
+            bool has = lane < g.ns;
+            if constexpr (kMask) has = has && keep[(size_t)row * (size_t)cols + col] != 0;
+            const u64 key = has ? full_key(g.rp[col], (unsigned)col) : 0ull;
             const unsigned m = __ballot_sync(kFullMask, key != 0ull);
             if (key) q[nq + __popc(m & lanemask_lt())] = key;
             nq += __popc(m);
@@ -502,7 +544,16 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
                 for (int u = 0; u < kRowU; ++u)
                     r[u] = u < nvalid ? st[u * 32 + lane] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
                 unsigned gk[GL];
-                group_max_keys<GL>(r, nvalid, gk);
+                if constexpr (kMask) {
+                    unsigned mk[kRowU];
+                    const uint8_t* krow = keep + (size_t)row * (size_t)cols + g.head;
+#pragma unroll
+                    for (int u = 0; u < kRowU; ++u)
+                        mk[u] = u < nvalid ? __ldg(reinterpret_cast<const unsigned*>(krow + 4 * (u * 32 + lane))) : 0u;
+                    group_max_keys_kept<GL>(r, mk, nvalid, gk);
+                } else {
+                    group_max_keys<GL>(r, nvalid, gk);
+                }
                 warp_sort_desc<GL>(gk, lane);
                 const unsigned seed = warp_sorted_at<GL>(gk, k - 1);
                 T = kmax(T, (u64)seed << 32);  // keeps every key with score >= seed
@@ -580,14 +631,22 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
         // The row's k best.  The key gives the value back exactly except for
         // -0.0 (keyed as +0.0) and NaN payloads: those are read from the row.
         grid_dependency_wait();  // the previous kernel's writes come first
+        int valid = 0;
 #pragma unroll
         for (int j = 0; j < L; ++j) {
             const int p = j * 32 + lane;
+            if constexpr (kMask) valid += __popc(__ballot_sync(kFullMask, p < k && wl.lst[j] != 0ull));
             if (p < k) {
                 const u64 key = wl.lst[j];
                 const unsigned col = 0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull);
                 const unsigned u = (unsigned)(key >> 32);
                 float v;
+                if (kMask && key == 0ull) {
+                    v = __int_as_float(0xFF800000);  // fewer than k kept elements: (-inf, -1)
+                    vals[(size_t)row * k + p] = v;
+                    idx[(size_t)row * k + p] = -1;
+                    continue;
+                }
                 if (col >= (unsigned)cols)
                     v = __int_as_float(0x7fc00000);  // unreachable: every list entry is a real element
                 else if (u == 0x80000000u || u == 0xFFFFFFFFu)
@@ -598,6 +657,8 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
                 idx[(size_t)row * k + p] = (int32_t)col;
             }
         }
+        if constexpr (kMask)
+            if (lane == 0) row_count[row] = valid;
     }
     // After a wait gave up, let the copies still in flight land before exit.
     if (lane == 0)
@@ -607,9 +668,9 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
 
 }  // namespace
 
-template <int L>
+template <int L, bool kMask>
 cudaError_t launch_stream(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
-                          unsigned* status, bool early, bool release) {
+                          unsigned* status, bool early, bool release, const uint8_t* keep, int32_t* row_count) {
     constexpr int kMaxDev = 64;
     static std::mutex mu;
     static int grid_cache[kMaxDev] = {};
@@ -617,7 +678,7 @@ cudaError_t launch_stream(cudaStream_t s, const float* in, int rows, int cols, i
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
     if (device < 0 || device >= kMaxDev) return cudaErrorInvalidDevice;
-    const void* fn = reinterpret_cast<const void*>(&topk_rows_stream_kernel<L>);
+    const void* fn = reinterpret_cast<const void*>(&topk_rows_stream_kernel<L, kMask>);
     int full;
     {
         std::lock_guard<std::mutex> lock(mu);
@@ -645,8 +706,8 @@ cudaError_t launch_stream(cudaStream_t s, const float* in, int rows, int cols, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = early ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, topk_rows_stream_kernel<L>, in, rows, cols, k, vals, idx, status,
-                              release ? 1 : 0);
+    return cudaLaunchKernelEx(&cfg, topk_rows_stream_kernel<L, kMask>, in, rows, cols, k, vals, idx, status,
+                              release ? 1 : 0, keep, row_count);
 }
 
 cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
@@ -654,9 +715,11 @@ cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int
     // k <= 128 streams (one warp per row); k > 128 uses one block per row
     // with shared-memory buffers.
     const bool stream = k <= 128;
-    if (stream && k <= 32) return launch_stream<1>(s, in, rows, cols, k, vals, idx, status, early, release);
-    if (stream && k <= 64) return launch_stream<2>(s, in, rows, cols, k, vals, idx, status, early, release);
-    if (stream) return launch_stream<4>(s, in, rows, cols, k, vals, idx, status, early, release);
+    const uint8_t* nk = nullptr;
+    int32_t* nc = nullptr;
+    if (stream && k <= 32) return launch_stream<1, false>(s, in, rows, cols, k, vals, idx, status, early, release, nk, nc);
+    if (stream && k <= 64) return launch_stream<2, false>(s, in, rows, cols, k, vals, idx, status, early, release, nk, nc);
+    if (stream) return launch_stream<4, false>(s, in, rows, cols, k, vals, idx, status, early, release, nk, nc);
     const size_t smem = (size_t)kWarps * 2048 * sizeof(u64);
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&topk_rows_smem_kernel<2048>),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -668,6 +731,22 @@ cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int
         topk_rows_smem_kernel<2048><<<rows, kWarps * 32, smem, s>>>(in, cols, k, vals, idx);
     }
     return cudaGetLastError();
+}
+
+bool rows_mask_aligned(const float* in, const uint8_t* keep) {
+    // A row's 16-byte vectors start at element offsets congruent to -in/4
+    // (mod 4); their keep words are 4-byte aligned when keep is congruent to
+    // in/4 (mod 4).
+    const uintptr_t a = reinterpret_cast<uintptr_t>(in), b = reinterpret_cast<uintptr_t>(keep);
+    return (a & 3u) == 0 && ((b - (a >> 2)) & 3u) == 0;
+}
+
+cudaError_t rows_launch_masked(cudaStream_t s, const float* in, const uint8_t* keep, int rows, int cols, int k,
+                               float* vals, int32_t* idx, int32_t* row_count, unsigned* status) {
+    if (k < 1 || k > 128 || !rows_mask_aligned(in, keep)) return cudaErrorInvalidValue;
+    if (k <= 32) return launch_stream<1, true>(s, in, rows, cols, k, vals, idx, status, false, false, keep, row_count);
+    if (k <= 64) return launch_stream<2, true>(s, in, rows, cols, k, vals, idx, status, false, false, keep, row_count);
+    return launch_stream<4, true>(s, in, rows, cols, k, vals, idx, status, false, false, keep, row_count);
 }
 
 }  // namespace topk

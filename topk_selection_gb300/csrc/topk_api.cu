@@ -395,7 +395,7 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
     // successors like the int32 streaming kernel.
     bool early = false;
     if (k <= 128) early = early_start(w, din, nin, dvals, nout, didx, nout) && !in_host;
-    e = topk::rows_launch(s, din, rows, cols, k, dvals, didx, status, early, k <= 128);
+    e = topk::rows_launch(s, din, rows, cols, k, dvals, didx, status, early, k <= 128 ? topk::kRowsRelease : 0);
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
 

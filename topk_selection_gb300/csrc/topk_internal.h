@@ -117,12 +117,17 @@ cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, s
                        void* scratch, bool early, bool release);
 
 // Enqueue the row TopK.  status: a device word that bounded waits set to
-// kStatusWaitTimeout when they give up (sticky).  early and release as for
-// i32_launch (k <= 128 only): with early, the launch reads its input while
-// the previous kernel on the stream finishes, so the input must not overlap
-// what that launch writes; with release, the next launch may start early.
+// kStatusWaitTimeout when they give up (sticky).  For k <= 128: early
+// launches with programmatic stream serialization, so the kernel may start
+// while the previous kernel on the stream finishes; flags:
+//   kRowsRelease    let the next launch start early (as i32_launch's release);
+//   kRowsWaitFirst  wait for the previous kernel before reading the input
+//                   (its input is that kernel's output); without it an early
+//                   launch reads its input first, so the input must not
+//                   overlap what the previous launch writes.
+constexpr int kRowsRelease = 1, kRowsWaitFirst = 2;
 cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
-                        unsigned* status, bool early, bool release);
+                        unsigned* status, bool early, int flags);
 
 // The row TopK over kept elements only (k <= 128): element (r, c) takes part
 // when keep[r * cols + c] != 0.  Each row's outputs hold its valid winners
@@ -130,7 +135,8 @@ cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int
 // rows_mask_aligned(in, keep) (cudaErrorInvalidValue otherwise).
 bool rows_mask_aligned(const float* in, const uint8_t* keep);
 cudaError_t rows_launch_masked(cudaStream_t s, const float* in, const uint8_t* keep, int rows, int cols, int k,
-                               float* vals, int32_t* idx, int32_t* row_count, unsigned* status);
+                               float* vals, int32_t* idx, int32_t* row_count, unsigned* status, bool early,
+                               int flags);
 
 // Enqueue a one-launch reduction (op 0 sum, 1 max, 2 min) of n int32 or
 // float32 values.  out: one int64 (int32 input) or one double (float32

@@ -264,6 +264,8 @@ __global__ void items_gather_kernel(const float* __restrict__ wv, const int32_t*
                                     int ke, const float* __restrict__ cur, const int32_t* __restrict__ pos,
                                     size_t tail_begin, size_t tail_len, size_t len, float* __restrict__ ns,
                                     int32_t* __restrict__ npos) {
+    grid_dependency_wait();  // launched early (launch_pdl): the previous kernel's writes first
+    launch_dependents();
     const size_t nw = (size_t)R * ke;
     for (size_t j = (size_t)blockIdx.x * blockDim.x + threadIdx.x; j < len; j += (size_t)gridDim.x * blockDim.x) {
         float v;
@@ -299,6 +301,8 @@ items_gather_masked_kernel(const float* __restrict__ wv, const int32_t* __restri
     __shared__ unsigned s_red[kGatherThreads / 32][2];
     __shared__ unsigned s_rowbase[kGatherThreads];
     __shared__ unsigned s_warp[kGatherThreads / 32];
+    grid_dependency_wait();  // launched early (launch_pdl): the previous kernel's writes first
+    launch_dependents();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int rb = (R + (int)gridDim.x - 1) / (int)gridDim.x;
     const int r0 = (int)blockIdx.x * rb < R ? (int)blockIdx.x * rb : R;
@@ -414,6 +418,8 @@ items_final_sort_kernel(const float* __restrict__ cv, const int32_t* __restrict_
                         const int64_t* __restrict__ item, float* __restrict__ out_score,
                         int64_t* __restrict__ out_item, int64_t* __restrict__ out_count) {
     __shared__ unsigned long long keys[kFinalCap];
+    grid_dependency_wait();  // launched early (launch_pdl): the previous kernel's writes first
+    // The call's last kernel: its successor must not start before it ends.
     const int L = next_pow2(count < 2 ? 2 : count);
     for (int j = threadIdx.x; j < L; j += blockDim.x) keys[j] = j < count ? items_key(cv[j], (unsigned)j) : 0ull;
     block_sort_smem_desc(keys, L);
@@ -435,6 +441,57 @@ items_final_sort_kernel(const float* __restrict__ cv, const int32_t* __restrict_
     static_assert(TOPK_MAX_K_ROWS <= kFinalThreads, "one output per thread: the count is a thread count");
     valid = __syncthreads_count(valid);
     if (threadIdx.x == 0 && out_count) *out_count = valid;
+}
+
+// The last level for k <= 128: each of 32 warps sorts its 128 of the at
+// most kFinalCap candidates in registers, and the warps' lists are merged
+// pairwise (five levels) into warp 0, whose best k are the outputs.  Same
+// keys and outputs as items_final_sort_kernel.
+constexpr int kSelWarps = 32, kSelN = kFinalCap / (32 * kSelWarps);  // 4 keys per lane
+__global__ void __launch_bounds__(kSelWarps * 32)
+items_final_select_kernel(const float* __restrict__ cv, const int32_t* __restrict__ cp, int count, int ke, int k,
+                          const int64_t* __restrict__ item, float* __restrict__ out_score,
+                          int64_t* __restrict__ out_item, int64_t* __restrict__ out_count) {
+    __shared__ unsigned long long s_l[kSelWarps][32 * kSelN];
+    grid_dependency_wait();  // launched early (launch_pdl): the previous kernel's writes first
+    // The call's last kernel: its successor must not start before it ends.
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    RegList<kSelN, unsigned long long> wl;
+#pragma unroll
+    for (int j = 0; j < kSelN; ++j) {
+        const int p = w * 32 * kSelN + j * 32 + lane;
+        wl.lst[j] = p < count ? items_key(cv[p], (unsigned)p) : 0ull;  // every real key is above 0
+    }
+    warp_sort_desc<kSelN>(wl.lst, lane);
+#pragma unroll 1
+    for (int s = 1; s < kSelWarps; s <<= 1) {
+        if ((w & (2 * s - 1)) == s)
+#pragma unroll
+            for (int j = 0; j < kSelN; ++j) s_l[w][j * 32 + lane] = wl.lst[j];
+        __syncthreads();
+        if ((w & (2 * s - 1)) == 0) wl.merge_list(s_l[w + s], lane);
+        __syncthreads();
+    }
+    if (w != 0) return;
+    int valid = 0;
+#pragma unroll
+    for (int j = 0; j < kSelN; ++j) {
+        const int o = j * 32 + lane;
+        const unsigned long long key = wl.lst[j];
+        const unsigned idx = 0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull);
+        const int32_t p = (o < ke && key != 0ull) ? (cp ? cp[idx] : (int32_t)idx) : -1;
+        if (o < k) {
+            if (p >= 0) {
+                out_score[o] = cv[idx];
+                out_item[o] = item ? item[p] : (int64_t)p;
+            } else {
+                out_score[o] = __int_as_float(0xFF800000);
+                out_item[o] = -1;
+            }
+        }
+        valid += __popc(__ballot_sync(kFullMask, o < k && p >= 0));
+    }
+    if (lane == 0 && out_count) *out_count = valid;
 }
 
 // Pads the outputs when nothing is kept.
@@ -579,17 +636,20 @@ cudaError_t items_launch(cudaStream_t s, const float* score, const int64_t* item
         size_t C = n / kTargetRows;
         if (C < (size_t)8 * ke || C <= n % kTargetRows) C = level_cols(n, ke, true);
         const size_t R = n / C;
-        e = rows_launch_masked(s, score, keep, (int)R, (int)C, ke, wv, wx, wc, status);
+        // Every kernel from here on waits for its predecessor before it
+        // reads anything, so each is launched early (programmatic stream
+        // serialization) and only the launch gaps go.
+        e = rows_launch_masked(s, score, keep, (int)R, (int)C, ke, wv, wx, wc, status, true,
+                               kRowsRelease | kRowsWaitFirst);
         if (e != cudaSuccess) return e;
         *launches += 1;
         const size_t next_real = R * ke + (n - R * C);
         const size_t Cn = level_cols(next_real, ke, false);
         const size_t next_len = next_real <= (size_t)kFinalCap ? next_real : (next_real + Cn - 1) / Cn * Cn;
         const int gb = R < 128 ? (R < 1 ? 1 : (int)R) : 128;
-        items_gather_masked_kernel<<<gb, kGatherThreads, 0, s>>>(wv, wx, wc, (int)R, (int)C, ke, score, keep, n,
-                                                                 next_len, nb_s[0], nb_p[0]);
+        e = launch_pdl(items_gather_masked_kernel, gb, kGatherThreads, 0, s, wv, wx, wc, (int)R, (int)C, ke, score,
+                       keep, n, next_len, nb_s[0], nb_p[0]);
         *launches += 1;
-        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         cur = nb_s[0];
         cur_pos = nb_p[0];
@@ -601,25 +661,26 @@ cudaError_t items_launch(cudaStream_t s, const float* score, const int64_t* item
     for (;;) {
         if (real <= (size_t)kFinalCap) {
             // cur holds real entries only here (a single-row level adds no pads)
-            items_final_sort_kernel<<<1, kFinalThreads, 0, s>>>(cur, cur_pos, (int)real, ke, k, item, out_score,
-                                                                out_item, out_count);
             *launches += 1;
-            return cudaGetLastError();
+            if (k <= 32 * kSelN)
+                return launch_pdl(items_final_select_kernel, 1, kSelWarps * 32, 0, s, cur, cur_pos, (int)real, ke, k,
+                                  item, out_score, out_item, out_count);
+            return launch_pdl(items_final_sort_kernel, 1, kFinalThreads, 0, s, cur, cur_pos, (int)real, ke, k, item,
+                              out_score, out_item, out_count);
         }
         size_t C = level_cols(real, ke, first);
         if (C > len) C = len;  // fewer candidates than one row of 8 ke: a single row of all of them
         const size_t R = len / C, tail = len - R * C;  // later levels: len is a multiple of C, tail 0
-        e = rows_launch(s, cur, (int)R, (int)C, ke, wv, wx, status, false, false);
+        e = rows_launch(s, cur, (int)R, (int)C, ke, wv, wx, status, true, kRowsRelease | kRowsWaitFirst);
         if (e != cudaSuccess) return e;
         *launches += 1;
         const size_t next_real = R * ke + tail;
         const size_t Cn = level_cols(next_real, ke, false);
         const size_t next_len = next_real <= (size_t)kFinalCap ? next_real : (next_real + Cn - 1) / Cn * Cn;
         const int gb = (int)((next_len + 255) / 256 < 1024 ? (next_len + 255) / 256 : 1024);
-        items_gather_kernel<<<gb, 256, 0, s>>>(wv, wx, (int)R, (int)C, ke, cur, cur_pos, R * C, tail, next_len,
-                                               nb_s[flip], nb_p[flip]);
+        e = launch_pdl(items_gather_kernel, gb, 256, 0, s, wv, wx, (int)R, (int)C, ke, cur, cur_pos, R * C, tail,
+                       next_len, nb_s[flip], nb_p[flip]);
         *launches += 1;
-        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         cur = nb_s[flip];
         cur_pos = nb_p[flip];

@@ -379,7 +379,7 @@ __device__ __forceinline__ void group_max_keys_kept(const float4 (&r)[kRowU], co
 template <int L, bool kMask>
 __global__ void __launch_bounds__(kRowThreads, 3)
 topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k, float* __restrict__ vals,
-                        int32_t* __restrict__ idx, unsigned* __restrict__ status, int release,
+                        int32_t* __restrict__ idx, unsigned* __restrict__ status, int flags,
                         const uint8_t* __restrict__ keep, int32_t* __restrict__ row_count) {
     constexpr int GL = kRowU;  // groups of 4 elements per lane for the start threshold: 32*GL >= k
     extern __shared__ __align__(128) float4 rring[];       // per-warp stages
@@ -397,9 +397,11 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
     __syncthreads();
     // Launched early (see the host side), this kernel reads only its input
     // until it waits, before its first output write, for the previous
-    // kernel on the stream.  It lets the next launch start now when the
-    // caller keeps track of what this launch writes.
-    if (release) launch_dependents();
+    // kernel on the stream -- or first thing, when that kernel writes its
+    // input (kRowsWaitFirst).  It lets the next launch start now when the
+    // caller keeps track of what this launch writes (kRowsRelease).
+    if (flags & kRowsWaitFirst) grid_dependency_wait();
+    if (flags & kRowsRelease) launch_dependents();
 
     float4* my_ring = rring + (size_t)warp * kRowStages * kRowTileVec;
     uint64_t* my_bar = s_bar + warp * kRowStages;
@@ -670,7 +672,7 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
 
 template <int L, bool kMask>
 cudaError_t launch_stream(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
-                          unsigned* status, bool early, bool release, const uint8_t* keep, int32_t* row_count) {
+                          unsigned* status, bool early, int flags, const uint8_t* keep, int32_t* row_count) {
     constexpr int kMaxDev = 64;
     static std::mutex mu;
     static int grid_cache[kMaxDev] = {};
@@ -706,20 +708,20 @@ cudaError_t launch_stream(cudaStream_t s, const float* in, int rows, int cols, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = early ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, topk_rows_stream_kernel<L, kMask>, in, rows, cols, k, vals, idx, status,
-                              release ? 1 : 0, keep, row_count);
+    return cudaLaunchKernelEx(&cfg, topk_rows_stream_kernel<L, kMask>, in, rows, cols, k, vals, idx, status, flags,
+                              keep, row_count);
 }
 
 cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
-                        unsigned* status, bool early, bool release) {
+                        unsigned* status, bool early, int flags) {
     // k <= 128 streams (one warp per row); k > 128 uses one block per row
     // with shared-memory buffers.
     const bool stream = k <= 128;
     const uint8_t* nk = nullptr;
     int32_t* nc = nullptr;
-    if (stream && k <= 32) return launch_stream<1, false>(s, in, rows, cols, k, vals, idx, status, early, release, nk, nc);
-    if (stream && k <= 64) return launch_stream<2, false>(s, in, rows, cols, k, vals, idx, status, early, release, nk, nc);
-    if (stream) return launch_stream<4, false>(s, in, rows, cols, k, vals, idx, status, early, release, nk, nc);
+    if (stream && k <= 32) return launch_stream<1, false>(s, in, rows, cols, k, vals, idx, status, early, flags, nk, nc);
+    if (stream && k <= 64) return launch_stream<2, false>(s, in, rows, cols, k, vals, idx, status, early, flags, nk, nc);
+    if (stream) return launch_stream<4, false>(s, in, rows, cols, k, vals, idx, status, early, flags, nk, nc);
     const size_t smem = (size_t)kWarps * 2048 * sizeof(u64);
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&topk_rows_smem_kernel<2048>),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -742,11 +744,12 @@ bool rows_mask_aligned(const float* in, const uint8_t* keep) {
 }
 
 cudaError_t rows_launch_masked(cudaStream_t s, const float* in, const uint8_t* keep, int rows, int cols, int k,
-                               float* vals, int32_t* idx, int32_t* row_count, unsigned* status) {
+                               float* vals, int32_t* idx, int32_t* row_count, unsigned* status, bool early,
+                               int flags) {
     if (k < 1 || k > 128 || !rows_mask_aligned(in, keep)) return cudaErrorInvalidValue;
-    if (k <= 32) return launch_stream<1, true>(s, in, rows, cols, k, vals, idx, status, false, false, keep, row_count);
-    if (k <= 64) return launch_stream<2, true>(s, in, rows, cols, k, vals, idx, status, false, false, keep, row_count);
-    return launch_stream<4, true>(s, in, rows, cols, k, vals, idx, status, false, false, keep, row_count);
+    if (k <= 32) return launch_stream<1, true>(s, in, rows, cols, k, vals, idx, status, early, flags, keep, row_count);
+    if (k <= 64) return launch_stream<2, true>(s, in, rows, cols, k, vals, idx, status, early, flags, keep, row_count);
+    return launch_stream<4, true>(s, in, rows, cols, k, vals, idx, status, early, flags, keep, row_count);
 }
 
 }  // namespace topk

@@ -159,7 +159,7 @@ int topk_items_f32(const float* score, const int64_t* item, const uint8_t* keep,
  *   vals_out   uint32[n], written; null exactly when vals is null.
  *
  * Five launches: one histogram pass for all four digits, then one pass per
- * digit in which every 4096-key tile ranks its keys, finds where its keys of
+ * digit in which every 8192-key tile ranks its keys, finds where its keys of
  * each digit go from the tiles before it (decoupled look-back, bounded
  * waits) and writes them in digit order.  Scratch (in the library's
  * per-stream workspace): about 4n bytes (8n with values) plus 0.5 byte per

@@ -55,7 +55,7 @@ def make(kind, n, seed):
     raise KeyError(kind)
 
 
-SIZES = [1, 2, 3, 31, 32, 33, 4095, 4096, 4097, 8193, 65537, 1_000_003]
+SIZES = [1, 2, 3, 31, 32, 33, 4095, 4096, 4097, 8191, 8192, 8193, 16385, 65537, 1_000_003]  # around one and two tiles
 
 
 @pytest.mark.parametrize("kind", ["uniform", "few", "equal", "descending", "sorted", "extremes", "high_byte"])

@@ -3,7 +3,7 @@
 // shared-memory histograms; its extensions section adds key-value pairs).
 //
 // GB300 form: one histogram pass for all four digits, then one launch per
-// digit in which every tile of 4096 keys
+// digit in which every tile of 8192 keys
 //   1. takes the next tile id from a counter (so a tile only ever waits for
 //      tiles whose blocks are already running),
 //   2. ranks its keys stably: per warp, keys go slot by slot (32
@@ -38,7 +38,7 @@ namespace {
 
 constexpr int kST = 512;            // threads per tile
 constexpr int kSW = kST / 32;       // warps per tile
-constexpr int kSI = 8;              // keys per thread
+constexpr int kSI = 16;             // keys per thread (8192-key tiles: measured best of 256..1024 x 8..24)
 constexpr int kTile = kST * kSI;    // keys per tile
 constexpr int kRadix = 256;
 constexpr int kSpins = 1 << 22;     // polls of one look-back word before giving up

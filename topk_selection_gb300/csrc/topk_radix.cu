@@ -555,23 +555,6 @@ struct ClSmem {
 };
 static_assert(kMaxRanges == 256, "a level's histogram fits a row of part");
 
-// Sort a[0..m) descending in place, m <= 32 N, by one warp in registers.
-template <int N>
-__device__ __forceinline__ void warp_sort_smem_list(unsigned* a, unsigned m, unsigned lane) {
-    unsigned v[N];
-#pragma unroll
-    for (int jj = 0; jj < N; ++jj) {
-        const unsigned p = jj * 32 + lane;
-        v[jj] = p < m ? a[p] : 0u;
-    }
-    warp_sort_desc(v, (int)lane);
-#pragma unroll
-    for (int jj = 0; jj < N; ++jj) {
-        const unsigned p = jj * 32 + lane;
-        if (p < m) a[p] = v[jj];
-    }
-}
-
 // After the cluster barrier that completes every CTA's histogram H: sum the
 // 8 histograms (warp r reads CTA r's with 16-byte remote loads) and find the
 // bucket holding the need-th largest key.  Every CTA finds the same one.
@@ -823,11 +806,13 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
             }
             S.mysamp[i] = S.keys[a * share + (g - S.woff[a])];
         }
-        __syncthreads();
-        // This CTA's samples, sorted descending by one warp (zeros pad past
-        // my_s; every sample is above T, so nonzero).
-        if (w == 0 && my_s > 128) warp_sort_smem_list<kPlanSamples / 32>(S.mysamp, my_s, lane);
-        if (w == 0 && my_s <= 128) warp_sort_smem_list<4>(S.mysamp, my_s, lane);
+        // This CTA's samples, sorted descending by the whole CTA (zeros pad
+        // past my_s; every sample is above T, so nonzero).  A rolled loop:
+        // this runs once per launch, and an unrolled sort's straight-line
+        // code would mostly wait on instruction fetch.
+        const int P = next_pow2(my_s < 2 ? 2 : (int)my_s);
+        for (unsigned i = my_s + tid; i < (unsigned)P; i += kClThreads) S.mysamp[i] = 0u;
+        block_sort_smem_desc(S.mysamp, P);
     }
     cluster_barrier();  // sorted samples out
 
@@ -895,18 +880,23 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
                     }
                 }
                 if (lane == 31) bnd[7] = T + 1;  // position 255: no splitter lands there (R <= 128)
-                warp_sort_desc(bnd, (int)lane);
+                // Sorted below by the whole CTA, in rank 0's own sample
+                // array (merged into samp above, read by no other CTA).
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) S.mysamp[jj * 32 + lane] = bnd[jj];
+            }
+            block_sort_smem_desc(S.mysamp, 256);  // rolled, like the sample sort
+            __syncthreads();
+            if (w == 0) {
                 // The distinct nonzero bounds, in descending order.
                 unsigned nr = 0;
-#pragma unroll
+#pragma unroll 1
                 for (int jj = 0; jj < 8; ++jj) {
-                    const unsigned prev_in_warp = __shfl_up_sync(kFullMask, bnd[jj], 1);
-                    const unsigned prev_last = __shfl_sync(kFullMask, jj ? bnd[jj - 1] : 0u, 31);
-                    const bool first = jj == 0 && lane == 0;
-                    const unsigned prev = lane ? prev_in_warp : prev_last;
-                    const bool keep = bnd[jj] != 0u && (first || bnd[jj] != prev);
+                    const unsigned p = jj * 32 + lane;
+                    const unsigned v = S.mysamp[p];
+                    const bool keep = v != 0u && (p == 0 || v != S.mysamp[p - 1]);
                     const unsigned b = __ballot_sync(kFullMask, keep);
-                    if (keep) S.lb[nr + __popc(b & lanemask_lt())] = bnd[jj];
+                    if (keep) S.lb[nr + __popc(b & lanemask_lt())] = v;
                     nr += __popc(b);
                 }
                 if (lane == 0) S.nranges = nr;

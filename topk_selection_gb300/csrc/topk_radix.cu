@@ -521,6 +521,7 @@ constexpr int kMaxRanges = 256;          // output ranges (one sorting warp each
 constexpr unsigned kMaxPlanned = 128;    // ranges cut from the sample; repeated values add up to as many
 constexpr unsigned kRangeKeys = 256;     // keys a range aims at
 constexpr unsigned kPlanSamples = 512;   // splitter sample, at most
+constexpr unsigned kSmallCap = 4096;     // at most this many keys above T: rank 0 sorts them all itself
 static_assert(2 * kMaxPlanned <= (unsigned)kMaxRanges, "range table");
 static_assert(kClCtas * kMaxRanges == 2 * kClThreads, "two (CTA, range) counts per thread");
 constexpr int kSortWarps = 4;            // warps per CTA of the sort kernel
@@ -541,6 +542,7 @@ struct ClSmem {
     unsigned part[kClCtas][kMaxRanges];   // the cluster's histograms of a level; later the range counts
     unsigned samp[kPlanSamples];          // rank 0: the gathered sample
     unsigned mysamp[kPlanSamples];        // this CTA's part of it (read by rank 0)
+    unsigned mysmall[kSmallCap];          // few keys above T: this CTA's, packed (read by rank 0)
     unsigned lb[kMaxRanges];              // range bounds (rank 0 builds them; the others copy)
     unsigned rcnt[kMaxRanges];            // this CTA's keys per range (read by the others)
     unsigned rstart[kMaxRanges + 1];      // output offset of each range
@@ -782,189 +784,212 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
     __syncthreads();
     cluster_barrier();  // every CTA's count is out
 
-    // Splitter sample: a CTA's share of kPlanSamples follows its share of the
-    // keys above T.
     if (tid < (unsigned)kClCtas) S.ccount[tid] = ld_cluster(&S.mine_count, tid);
     __syncthreads();
     unsigned total = 0;
 #pragma unroll
     for (int r = 0; r < kClCtas; ++r) total += S.ccount[r];
-    auto samples_of = [&](unsigned c) -> unsigned {
-        return total ? (unsigned)(((unsigned long long)c * kPlanSamples) / total) : 0u;
-    };
-    {
-        const unsigned my_c = S.mine_count, my_s = samples_of(my_c);
-        for (unsigned i = tid; i < my_s; i += kClThreads) {
-            const unsigned g = (unsigned)((unsigned long long)i * my_c / my_s);
-            unsigned a = 0, b = kClWarps - 1;  // the last warp whose run starts at or before g
-            while (a < b) {
-                const unsigned mid = (a + b + 1) >> 1;
-                if (S.woff[mid] <= g)
-                    a = mid;
-                else
-                    b = mid - 1;
-            }
-            S.mysamp[i] = S.keys[a * share + (g - S.woff[a])];
-        }
-        // This CTA's samples, sorted descending by the whole CTA (zeros pad
-        // past my_s; every sample is above T, so nonzero).  A rolled loop:
-        // this runs once per launch, and an unrolled sort's straight-line
-        // code would mostly wait on instruction fetch.
-        const int P = next_pow2(my_s < 2 ? 2 : (int)my_s);
-        for (unsigned i = my_s + tid; i < (unsigned)P; i += kClThreads) S.mysamp[i] = 0u;
-        block_sort_smem_desc(S.mysamp, P);
-    }
-    cluster_barrier();  // sorted samples out
-
-    if (rank == 0) {
-        if (total) {
-            unsigned soff[kClCtas + 1], ns = 0;
-#pragma unroll
+    unsigned nr = 0;  // ranges for the sort kernel
+    if (total <= kSmallCap) {
+        // Few keys above T: rank 0 gathers them all, sorts them with the
+        // whole CTA and writes them; the sort kernel has no ranges to do.
+        // Each CTA first packs its warps' runs, in order, into mysmall.
+        for (unsigned m = lane; m < cw; m += 32) S.mysmall[S.woff[w] + m] = S.keys[w0 + m];
+        cluster_barrier();  // every CTA's packed keys are out
+        if (rank == 0) {
+            // rank 0's own keys have been packed: its key area is free.
+            unsigned* all = S.keys;
+            unsigned off = 0;
             for (int r = 0; r < kClCtas; ++r) {
-                soff[r] = ns;
-                ns += samples_of(S.ccount[r]);
+                const unsigned c = S.ccount[r];
+                for (unsigned i = tid; i < c; i += kClThreads) all[off + i] = ld_cluster(&S.mysmall[i], (unsigned)r);
+                off += c;
             }
-            soff[kClCtas] = ns;
-            // Gather the 8 sorted lists, then merge them by rank: an element's
-            // place is its index in its own list plus, in every other list,
-            // the count of greater keys (equal keys count from lower ranks).
-            unsigned* lists = &S.part[0][0];
-            for (unsigned i = tid; i < ns; i += kClThreads) {
-                unsigned r = 0;
-                while (r + 1 < (unsigned)kClCtas && soff[r + 1] <= i) ++r;
-                lists[i] = ld_cluster(&S.mysamp[i - soff[r]], r);
-            }
-            __syncthreads();
-            for (unsigned i = tid; i < ns; i += kClThreads) {
-                unsigned r = 0;
-                while (r + 1 < (unsigned)kClCtas && soff[r + 1] <= i) ++r;
-                const unsigned v = lists[i];
-                unsigned place = i - soff[r];
-                for (unsigned o = 0; o < (unsigned)kClCtas; ++o) {
-                    if (o == r) continue;
-                    // first index in list o whose key is below v (o < r) or not above v (o > r)
-                    unsigned a = soff[o], b = soff[o + 1];
-                    while (a < b) {
-                        const unsigned mid = (a + b) >> 1;
-                        const unsigned x = lists[mid];
-                        if (o < r ? x >= v : x > v)
-                            a = mid + 1;
-                        else
-                            b = mid;
-                    }
-                    place += a - soff[o];
-                }
-                S.samp[place] = v;
-            }
-            __syncthreads();
-            if (w == 0) {
-                // R - 1 splitters at even positions of the sorted sample,
-                // about kRangeKeys keys apart.  A splitter value that repeats
-                // at a neighbouring position (a value holding a range's worth
-                // of keys) also bounds a range holding only that value, which
-                // needs no sorting.  The last range ends at T + 1.
-                // At least 4 samples per range keep the ranges' sizes close
-                // to their mean.
-                const unsigned R =
-                    min(min(kMaxPlanned, max(1u, ns / 4)), max(1u, (total + kRangeKeys - 1) / kRangeKeys));
-                unsigned bnd[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // candidates at positions jj * 32 + lane
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const unsigned q = lane + 1 + 32 * h;  // splitter q of 1 .. R-1
-                    if (q < R) {
-                        const unsigned c = S.samp[q * ns / R];
-                        const bool dup = (q >= 2 && S.samp[(q - 1) * ns / R] == c) ||
-                                         (q + 1 < R && S.samp[(q + 1) * ns / R] == c);
-                        bnd[2 * h] = c;
-                        bnd[2 * h + 1] = (dup && c != 0xFFFFFFFFu) ? c + 1 : 0u;
-                    }
-                }
-                if (lane == 31) bnd[7] = T + 1;  // position 255: no splitter lands there (R <= 128)
-                // Sorted below by the whole CTA, in rank 0's own sample
-                // array (merged into samp above, read by no other CTA).
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) S.mysamp[jj * 32 + lane] = bnd[jj];
-            }
-            block_sort_smem_desc(S.mysamp, 256);  // rolled, like the sample sort
-            __syncthreads();
-            if (w == 0) {
-                // The distinct nonzero bounds, in descending order.
-                unsigned nr = 0;
-#pragma unroll 1
-                for (int jj = 0; jj < 8; ++jj) {
-                    const unsigned p = jj * 32 + lane;
-                    const unsigned v = S.mysamp[p];
-                    const bool keep = v != 0u && (p == 0 || v != S.mysamp[p - 1]);
-                    const unsigned b = __ballot_sync(kFullMask, keep);
-                    if (keep) S.lb[nr + __popc(b & lanemask_lt())] = v;
-                    nr += __popc(b);
-                }
-                if (lane == 0) S.nranges = nr;
-            }
-        } else if (tid == 0) {
-            S.nranges = 0u;
+            const int P = next_pow2(total < 2 ? 2 : (int)total);
+            for (unsigned i = total + tid; i < (unsigned)P; i += kClThreads) all[i] = 0u;  // below every key > T
+            block_sort_smem_desc(all, P);
+            for (unsigned i = tid; i < total; i += kClThreads) out[i] = value_of(all[i]);
         }
-    }
-    cluster_barrier();  // rank 0's range table is out
+    } else {
+        // Splitter sample: a CTA's share of kPlanSamples follows its share
+        // of the keys above T.
+        auto samples_of = [&](unsigned c) -> unsigned {
+            return total ? (unsigned)(((unsigned long long)c * kPlanSamples) / total) : 0u;
+        };
+        {
+            const unsigned my_c = S.mine_count, my_s = samples_of(my_c);
+            for (unsigned i = tid; i < my_s; i += kClThreads) {
+                const unsigned g = (unsigned)((unsigned long long)i * my_c / my_s);
+                unsigned a = 0, b = kClWarps - 1;  // the last warp whose run starts at or before g
+                while (a < b) {
+                    const unsigned mid = (a + b + 1) >> 1;
+                    if (S.woff[mid] <= g)
+                        a = mid;
+                    else
+                        b = mid - 1;
+                }
+                S.mysamp[i] = S.keys[a * share + (g - S.woff[a])];
+            }
+            // This CTA's samples, sorted descending by the whole CTA (zeros pad
+            // past my_s; every sample is above T, so nonzero).  A rolled loop:
+            // this runs once per launch, and an unrolled sort's straight-line
+            // code would mostly wait on instruction fetch.
+            const int P = next_pow2(my_s < 2 ? 2 : (int)my_s);
+            for (unsigned i = my_s + tid; i < (unsigned)P; i += kClThreads) S.mysamp[i] = 0u;
+            block_sort_smem_desc(S.mysamp, P);
+        }
+        cluster_barrier();  // sorted samples out
 
-    if (rank != 0 && tid <= (unsigned)kMaxRanges) {
-        if (tid < (unsigned)kMaxRanges)
-            S.lb[tid] = ld_cluster(&S.lb[tid], 0);
-        else
-            S.nranges = ld_cluster(&S.nranges, 0);
-    }
-    if (tid < (unsigned)kMaxRanges) S.rcnt[tid] = 0u;
-    __syncthreads();
-    const unsigned nr = S.nranges;
-    if (nr) {
-        for (unsigned m = lane; m < cw; m += 32) atomicAdd(&S.rcnt[range_of(S.lb, nr, S.keys[w0 + m])], 1u);
-    }
-    __syncthreads();
-    cluster_barrier();  // every CTA's range counts are out
+        if (rank == 0) {
+            if (total) {
+                unsigned soff[kClCtas + 1], ns = 0;
+    #pragma unroll
+                for (int r = 0; r < kClCtas; ++r) {
+                    soff[r] = ns;
+                    ns += samples_of(S.ccount[r]);
+                }
+                soff[kClCtas] = ns;
+                // Gather the 8 sorted lists, then merge them by rank: an element's
+                // place is its index in its own list plus, in every other list,
+                // the count of greater keys (equal keys count from lower ranks).
+                unsigned* lists = &S.part[0][0];
+                for (unsigned i = tid; i < ns; i += kClThreads) {
+                    unsigned r = 0;
+                    while (r + 1 < (unsigned)kClCtas && soff[r + 1] <= i) ++r;
+                    lists[i] = ld_cluster(&S.mysamp[i - soff[r]], r);
+                }
+                __syncthreads();
+                for (unsigned i = tid; i < ns; i += kClThreads) {
+                    unsigned r = 0;
+                    while (r + 1 < (unsigned)kClCtas && soff[r + 1] <= i) ++r;
+                    const unsigned v = lists[i];
+                    unsigned place = i - soff[r];
+                    for (unsigned o = 0; o < (unsigned)kClCtas; ++o) {
+                        if (o == r) continue;
+                        // first index in list o whose key is below v (o < r) or not above v (o > r)
+                        unsigned a = soff[o], b = soff[o + 1];
+                        while (a < b) {
+                            const unsigned mid = (a + b) >> 1;
+                            const unsigned x = lists[mid];
+                            if (o < r ? x >= v : x > v)
+                                a = mid + 1;
+                            else
+                                b = mid;
+                        }
+                        place += a - soff[o];
+                    }
+                    S.samp[place] = v;
+                }
+                __syncthreads();
+                if (w == 0) {
+                    // R - 1 splitters at even positions of the sorted sample,
+                    // about kRangeKeys keys apart.  A splitter value that repeats
+                    // at a neighbouring position (a value holding a range's worth
+                    // of keys) also bounds a range holding only that value, which
+                    // needs no sorting.  The last range ends at T + 1.
+                    // At least 4 samples per range keep the ranges' sizes close
+                    // to their mean.
+                    const unsigned R =
+                        min(min(kMaxPlanned, max(1u, ns / 4)), max(1u, (total + kRangeKeys - 1) / kRangeKeys));
+                    unsigned bnd[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // candidates at positions jj * 32 + lane
+    #pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const unsigned q = lane + 1 + 32 * h;  // splitter q of 1 .. R-1
+                        if (q < R) {
+                            const unsigned c = S.samp[q * ns / R];
+                            const bool dup = (q >= 2 && S.samp[(q - 1) * ns / R] == c) ||
+                                             (q + 1 < R && S.samp[(q + 1) * ns / R] == c);
+                            bnd[2 * h] = c;
+                            bnd[2 * h + 1] = (dup && c != 0xFFFFFFFFu) ? c + 1 : 0u;
+                        }
+                    }
+                    if (lane == 31) bnd[7] = T + 1;  // position 255: no splitter lands there (R <= 128)
+                    // Sorted below by the whole CTA, in rank 0's own sample
+                    // array (merged into samp above, read by no other CTA).
+    #pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) S.mysamp[jj * 32 + lane] = bnd[jj];
+                }
+                block_sort_smem_desc(S.mysamp, 256);  // rolled, like the sample sort
+                __syncthreads();
+                if (w == 0) {
+                    // The distinct nonzero bounds, in descending order.
+                    unsigned nr = 0;
+    #pragma unroll 1
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const unsigned p = jj * 32 + lane;
+                        const unsigned v = S.mysamp[p];
+                        const bool keep = v != 0u && (p == 0 || v != S.mysamp[p - 1]);
+                        const unsigned b = __ballot_sync(kFullMask, keep);
+                        if (keep) S.lb[nr + __popc(b & lanemask_lt())] = v;
+                        nr += __popc(b);
+                    }
+                    if (lane == 0) S.nranges = nr;
+                }
+            } else if (tid == 0) {
+                S.nranges = 0u;
+            }
+        }
+        cluster_barrier();  // rank 0's range table is out
 
-    // part[r][q]: CTA r's keys in range q.  Range q starts at the keys of
-    // all lower ranges; this CTA's keys in it follow those of lower ranks.
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const unsigned e = tid + h * kClThreads, r = e / kMaxRanges, q = e % kMaxRanges;
-        S.part[r][q] = q < nr ? ld_cluster(&S.rcnt[q], r) : 0u;
-    }
-    __syncthreads();
-    if (w == 0) {
-        unsigned c[8], tot = 0;
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-            const unsigned q = lane * 8 + h;
-            c[h] = 0;
-#pragma unroll
-            for (int r = 0; r < kClCtas; ++r) c[h] += S.part[r][q];
-            tot += c[h];
+        if (rank != 0 && tid <= (unsigned)kMaxRanges) {
+            if (tid < (unsigned)kMaxRanges)
+                S.lb[tid] = ld_cluster(&S.lb[tid], 0);
+            else
+                S.nranges = ld_cluster(&S.nranges, 0);
         }
-        unsigned x = tot;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned y = __shfl_up_sync(kFullMask, x, o);
-            if ((int)lane >= o) x += y;
+        if (tid < (unsigned)kMaxRanges) S.rcnt[tid] = 0u;
+        __syncthreads();
+        nr = S.nranges;
+        if (nr) {
+            for (unsigned m = lane; m < cw; m += 32) atomicAdd(&S.rcnt[range_of(S.lb, nr, S.keys[w0 + m])], 1u);
         }
-        unsigned acc = x - tot;
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-            S.rstart[lane * 8 + h] = acc;
-            acc += c[h];
+        __syncthreads();
+        cluster_barrier();  // every CTA's range counts are out
+
+        // part[r][q]: CTA r's keys in range q.  Range q starts at the keys of
+        // all lower ranges; this CTA's keys in it follow those of lower ranks.
+    #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const unsigned e = tid + h * kClThreads, r = e / kMaxRanges, q = e % kMaxRanges;
+            S.part[r][q] = q < nr ? ld_cluster(&S.rcnt[q], r) : 0u;
         }
-        if (lane == 31) S.rstart[kMaxRanges] = acc;
-    }
-    __syncthreads();
-    if (tid < (unsigned)kMaxRanges) {
-        unsigned below = 0;
-        for (unsigned r = 0; r < rank; ++r) below += S.part[r][tid];
-        S.rpos[tid] = S.rstart[tid] + below;
-    }
-    __syncthreads();
-    if (nr) {
-        for (unsigned m = lane; m < cw; m += 32) {
-            const unsigned u = S.keys[w0 + m];
-            out[atomicAdd(&S.rpos[range_of(S.lb, nr, u)], 1u)] = value_of(u);
+        __syncthreads();
+        if (w == 0) {
+            unsigned c[8], tot = 0;
+    #pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const unsigned q = lane * 8 + h;
+                c[h] = 0;
+    #pragma unroll
+                for (int r = 0; r < kClCtas; ++r) c[h] += S.part[r][q];
+                tot += c[h];
+            }
+            unsigned x = tot;
+    #pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned y = __shfl_up_sync(kFullMask, x, o);
+                if ((int)lane >= o) x += y;
+            }
+            unsigned acc = x - tot;
+    #pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                S.rstart[lane * 8 + h] = acc;
+                acc += c[h];
+            }
+            if (lane == 31) S.rstart[kMaxRanges] = acc;
+        }
+        __syncthreads();
+        if (tid < (unsigned)kMaxRanges) {
+            unsigned below = 0;
+            for (unsigned r = 0; r < rank; ++r) below += S.part[r][tid];
+            S.rpos[tid] = S.rstart[tid] + below;
+        }
+        __syncthreads();
+        if (nr) {
+            for (unsigned m = lane; m < cw; m += 32) {
+                const unsigned u = S.keys[w0 + m];
+                out[atomicAdd(&S.rpos[range_of(S.lb, nr, u)], 1u)] = value_of(u);
+            }
         }
     }
     // Copies of the k-th key after the keys above it.
@@ -975,7 +1000,7 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
         RadixPlan* plan = reinterpret_cast<RadixPlan*>(scratch + kRadixCandOffset);
         for (unsigned i = tid; i <= (unsigned)kMaxRanges; i += kClThreads) {
             if (i < nr) plan->lb[i] = S.lb[i];
-            if (i <= nr) plan->rstart[i] = S.rstart[i];
+            if (nr && i <= nr) plan->rstart[i] = S.rstart[i];
         }
         if (tid == 0) plan->nranges = nr;
     }

@@ -75,7 +75,7 @@ enum topk_status {
  * finish merges the candidates (section 2.2's second pass, fused into the
  * same launch).  k > 128: a radix select on order-preserving keys ("GPU
  * radix sort", histogram section).  When n exceeds 2^18, a threshold is
- * taken from a 2^18-key sample, one pass over the input keeps the keys above
+ * taken from a 2^16-key sample, one pass over the input keeps the keys above
  * it, and one 8-CTA cluster selects the k-th key among them and sorts the
  * answer (six launches, one input pass; two more input passes run only when
  * the sample misled the filter).  When n <= 2^18 the cluster does it all in
@@ -261,7 +261,7 @@ enum topk_option {
      * whose candidates overflow it take the exact radix passes.  Lower it
      * only to exercise those passes; results are the same either way. */
     TOPK_OPT_RADIX_CAP = 2,
-    /* Rank, within the large-k plan's 2^18-key sample, of the key used as
+    /* Rank, within the large-k plan's 2^16-key sample, of the key used as
      * the filter threshold (0 restores the automatic choice).  A rank that
      * is too small makes the filter keep fewer than k keys, and the plan
      * takes the exact radix passes.  For tests of that path only. */

@@ -10,7 +10,7 @@
 // that holds the k-th key, not a reordering.
 //
 // Plan when n exceeds what one cluster holds (kRadixClusterCap keys):
-//   sample   one cluster of 8 CTAs gathers 2^18 keys from 16384 evenly
+//   sample   one cluster of 8 CTAs gathers 2^16 keys from 4096 evenly
 //            spaced 16-element segments and selects the j-th largest, j a few
 //            standard deviations above k's expected share of the sample.
 //            That key is the filter threshold t.
@@ -66,7 +66,13 @@ constexpr int kClThreads = 1024;
 constexpr int kClWarps = kClThreads / 32;
 constexpr int kClSlice = 32768;  // keys per CTA
 constexpr unsigned kSegLen = 16;
-constexpr unsigned kSegments = (unsigned)(kRadixClusterCap / kSegLen);
+// The threshold sample: 2^16 keys (a quarter of what a cluster holds)
+// still put the filter's expected candidates far below the buffer (about
+// j * n / 2^16 for the sample rank j below), at a quarter of the loads.
+constexpr unsigned kSampleKeys = 1u << 16;
+constexpr unsigned kSegments = kSampleKeys / kSegLen;
+constexpr int kSampleVec = (int)(kSampleKeys / (4u * kClCtas * kClThreads));  // 16-byte loads per thread
+static_assert(kSampleVec >= 1 && kSampleVec * 4 * kClCtas * kClThreads == (int)kSampleKeys, "sample split");
 static_assert((size_t)kClCtas * kClSlice == kRadixClusterCap, "cluster capacity");
 static_assert(kClSlice == kClWarps * 1024, "a warp owns a 1024-key sub-slice");
 
@@ -618,7 +624,7 @@ __device__ __forceinline__ unsigned range_of(const unsigned* lb, unsigned nr, un
 }
 
 // mode kClFull:   the TopK of the n input values (n <= cap).
-// mode kClSample: select the j-th largest of 2^18 sampled keys; write it to
+// mode kClSample: select the j-th largest of kSampleKeys sampled keys; write it to
 //                 the control words as the filter threshold.
 // mode kClFinal:  the TopK from the buffered keys, as the control words say;
 //                 zero the control words.
@@ -641,7 +647,7 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
         C = (unsigned)n;
         j = (unsigned)k;
     } else if (mode == kClSample) {
-        C = (unsigned)kRadixClusterCap;
+        C = kSampleKeys;
         j = j_sample;
     } else {
         // The earlier launches leave Select (nbuf >= k keys, at most cap) or
@@ -668,19 +674,20 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
     __syncthreads();
     if (mode == kClSample) {
         // Segment g of the sample: 16 keys from the 16-byte-aligned body,
-        // four vector loads; this CTA's 2048 segments, 8 vectors per thread.
+        // four vector loads; this CTA's kSegments / 8 segments, kSampleVec
+        // vectors per thread.
         const unsigned head = (unsigned)(((16u - (unsigned)(reinterpret_cast<uintptr_t>(in) & 15u)) & 15u) >> 2);
         const int4* body = reinterpret_cast<const int4*>(in + head);
         const size_t nvec = (n - head) >> 2;
-        int4 v[8];
+        int4 v[kSampleVec];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
+        for (int m = 0; m < kSampleVec; ++m) {
             const unsigned x = lo / 4 + m * kClThreads + tid;
             const size_t vi = (size_t)(x >> 2) * (nvec - 4) / (kSegments - 1) + (x & 3);
             v[m] = __ldg(body + vi);
         }
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
+        for (int m = 0; m < kSampleVec; ++m) {
             const uint4 u = make_uint4(key_of(v[m].x), key_of(v[m].y), key_of(v[m].z), key_of(v[m].w));
             *reinterpret_cast<uint4*>(&S.keys[(m * kClThreads + tid) * 4]) = u;
             hist_add(S.hist[0], u.x >> 24, true);
@@ -1134,11 +1141,11 @@ cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int
     }
     // Sample rank: k's expected share of the sample plus four standard
     // deviations and a floor of 16, so that at least k keys are >= t.
-    const double lam = (double)k * (double)kRadixClusterCap / (double)n;
+    const double lam = (double)k * (double)kSampleKeys / (double)n;
     const double jd = std::ceil(lam + 4.0 * std::sqrt(lam) + 16.0);
-    unsigned j = jd >= (double)kRadixClusterCap ? (unsigned)kRadixClusterCap : (unsigned)jd;
+    unsigned j = jd >= (double)kSampleKeys ? kSampleKeys : (unsigned)jd;
     const int opt_j = radix_sample_rank_option();
-    if (opt_j > 0) j = (size_t)opt_j < kRadixClusterCap ? (unsigned)opt_j : (unsigned)kRadixClusterCap;
+    if (opt_j > 0) j = (unsigned)opt_j < kSampleKeys ? (unsigned)opt_j : kSampleKeys;
     const size_t per_block = (size_t)kRThreads * kRU * 4;
     size_t grid = (n + per_block - 1) / per_block;
     if (grid > (size_t)f.grid) grid = f.grid;

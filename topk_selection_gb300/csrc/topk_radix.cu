@@ -527,7 +527,10 @@ constexpr int kMaxRanges = 256;          // output ranges (one sorting warp each
 constexpr unsigned kMaxPlanned = 128;    // ranges cut from the sample; repeated values add up to as many
 constexpr unsigned kRangeKeys = 256;     // keys a range aims at
 constexpr unsigned kPlanSamples = 512;   // splitter sample, at most
-constexpr unsigned kSmallCap = 4096;     // at most this many keys above T: rank 0 sorts them all itself
+// At most this many keys above T: rank 0 gathers and sorts them all itself
+// (measured faster than the range plan up to ~2000 keys, slower at 4096).
+constexpr unsigned kSmallCap = 2048;
+static_assert(kSmallCap >= 1024, "the radix range plan sums its 1024 buckets in mysmall");
 static_assert(2 * kMaxPlanned <= (unsigned)kMaxRanges, "range table");
 static_assert(kClCtas * kMaxRanges == 2 * kClThreads, "two (CTA, range) counts per thread");
 constexpr int kSortWarps = 4;            // warps per CTA of the sort kernel
@@ -560,6 +563,10 @@ struct ClSmem {
     unsigned nranges;                     // (rank 0's is read by the others)
     unsigned pick_digit;
     unsigned pick_above;
+    unsigned wmax[kClWarps];              // radix range plan: per-warp maxima of the keys above T
+    unsigned cmax;                        // the CTA's maximum (read by the others)
+    unsigned hi_key;                      // the cluster's maximum
+    unsigned plan_ok;                     // the radix plan fits (else the splitter-sample plan)
 };
 static_assert(kMaxRanges == 256, "a level's histogram fits a row of part");
 
@@ -818,131 +825,234 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
             for (unsigned i = tid; i < total; i += kClThreads) out[i] = value_of(all[i]);
         }
     } else {
-        // Splitter sample: a CTA's share of kPlanSamples follows its share
-        // of the keys above T.
-        auto samples_of = [&](unsigned c) -> unsigned {
-            return total ? (unsigned)(((unsigned long long)c * kPlanSamples) / total) : 0u;
-        };
+        // Radix range plan.  The keys above T lie in [lo, hi] (lo = T + 1, hi
+        // their maximum) and share every bit above the highest bit where lo
+        // and hi differ; the 10 bits below it cut them into at most 1024
+        // buckets in key order.  Every CTA sums the cluster's bucket
+        // histogram over DSMEM and builds the same range table: a range ends
+        // where the exclusive count (from the top) crosses a multiple of
+        // kRangeKeys, so a range holds at most kRangeKeys - 1 + its last
+        // bucket's keys.  A bucket of more than kRangeKeys + 1 keys (a dense
+        // value range) would overflow a warp's register sort: then the
+        // splitter-sample plan runs instead.
         {
-            const unsigned my_c = S.mine_count, my_s = samples_of(my_c);
-            for (unsigned i = tid; i < my_s; i += kClThreads) {
-                const unsigned g = (unsigned)((unsigned long long)i * my_c / my_s);
-                unsigned a = 0, b = kClWarps - 1;  // the last warp whose run starts at or before g
-                while (a < b) {
-                    const unsigned mid = (a + b + 1) >> 1;
-                    if (S.woff[mid] <= g)
-                        a = mid;
-                    else
-                        b = mid - 1;
-                }
-                S.mysamp[i] = S.keys[a * share + (g - S.woff[a])];
+            unsigned mx = 0;
+            for (unsigned m = lane; m < cw; m += 32) mx = max(mx, S.keys[w0 + m]);
+            mx = __reduce_max_sync(kFullMask, mx);
+            if (lane == 0) S.wmax[w] = mx;
+            unsigned* hist = &S.part[0][0];  // 1024 buckets (the level histograms are done)
+            hist[tid] = 0u;
+            __syncthreads();
+            if (w == 0) {
+                const unsigned v = __reduce_max_sync(kFullMask, S.wmax[lane]);
+                if (lane == 0) S.cmax = v;
             }
-            // This CTA's samples, sorted descending by the whole CTA (zeros pad
-            // past my_s; every sample is above T, so nonzero).  A rolled loop:
-            // this runs once per launch, and an unrolled sort's straight-line
-            // code would mostly wait on instruction fetch.
-            const int P = next_pow2(my_s < 2 ? 2 : (int)my_s);
-            for (unsigned i = my_s + tid; i < (unsigned)P; i += kClThreads) S.mysamp[i] = 0u;
-            block_sort_smem_desc(S.mysamp, P);
-        }
-        cluster_barrier();  // sorted samples out
-
-        if (rank == 0) {
-            if (total) {
-                unsigned soff[kClCtas + 1], ns = 0;
-    #pragma unroll
-                for (int r = 0; r < kClCtas; ++r) {
-                    soff[r] = ns;
-                    ns += samples_of(S.ccount[r]);
-                }
-                soff[kClCtas] = ns;
-                // Gather the 8 sorted lists, then merge them by rank: an element's
-                // place is its index in its own list plus, in every other list,
-                // the count of greater keys (equal keys count from lower ranks).
-                unsigned* lists = &S.part[0][0];
-                for (unsigned i = tid; i < ns; i += kClThreads) {
-                    unsigned r = 0;
-                    while (r + 1 < (unsigned)kClCtas && soff[r + 1] <= i) ++r;
-                    lists[i] = ld_cluster(&S.mysamp[i - soff[r]], r);
-                }
-                __syncthreads();
-                for (unsigned i = tid; i < ns; i += kClThreads) {
-                    unsigned r = 0;
-                    while (r + 1 < (unsigned)kClCtas && soff[r + 1] <= i) ++r;
-                    const unsigned v = lists[i];
-                    unsigned place = i - soff[r];
-                    for (unsigned o = 0; o < (unsigned)kClCtas; ++o) {
-                        if (o == r) continue;
-                        // first index in list o whose key is below v (o < r) or not above v (o > r)
-                        unsigned a = soff[o], b = soff[o + 1];
-                        while (a < b) {
-                            const unsigned mid = (a + b) >> 1;
-                            const unsigned x = lists[mid];
-                            if (o < r ? x >= v : x > v)
-                                a = mid + 1;
-                            else
-                                b = mid;
-                        }
-                        place += a - soff[o];
-                    }
-                    S.samp[place] = v;
-                }
-                __syncthreads();
-                if (w == 0) {
-                    // R - 1 splitters at even positions of the sorted sample,
-                    // about kRangeKeys keys apart.  A splitter value that repeats
-                    // at a neighbouring position (a value holding a range's worth
-                    // of keys) also bounds a range holding only that value, which
-                    // needs no sorting.  The last range ends at T + 1.
-                    // At least 4 samples per range keep the ranges' sizes close
-                    // to their mean.
-                    const unsigned R =
-                        min(min(kMaxPlanned, max(1u, ns / 4)), max(1u, (total + kRangeKeys - 1) / kRangeKeys));
-                    unsigned bnd[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // candidates at positions jj * 32 + lane
-    #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const unsigned q = lane + 1 + 32 * h;  // splitter q of 1 .. R-1
-                        if (q < R) {
-                            const unsigned c = S.samp[q * ns / R];
-                            const bool dup = (q >= 2 && S.samp[(q - 1) * ns / R] == c) ||
-                                             (q + 1 < R && S.samp[(q + 1) * ns / R] == c);
-                            bnd[2 * h] = c;
-                            bnd[2 * h + 1] = (dup && c != 0xFFFFFFFFu) ? c + 1 : 0u;
-                        }
-                    }
-                    if (lane == 31) bnd[7] = T + 1;  // position 255: no splitter lands there (R <= 128)
-                    // Sorted below by the whole CTA, in rank 0's own sample
-                    // array (merged into samp above, read by no other CTA).
-    #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) S.mysamp[jj * 32 + lane] = bnd[jj];
-                }
-                block_sort_smem_desc(S.mysamp, 256);  // rolled, like the sample sort
-                __syncthreads();
-                if (w == 0) {
-                    // The distinct nonzero bounds, in descending order.
-                    unsigned nr = 0;
-    #pragma unroll 1
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const unsigned p = jj * 32 + lane;
-                        const unsigned v = S.mysamp[p];
-                        const bool keep = v != 0u && (p == 0 || v != S.mysamp[p - 1]);
-                        const unsigned b = __ballot_sync(kFullMask, keep);
-                        if (keep) S.lb[nr + __popc(b & lanemask_lt())] = v;
-                        nr += __popc(b);
-                    }
-                    if (lane == 0) S.nranges = nr;
-                }
-            } else if (tid == 0) {
-                S.nranges = 0u;
+            __syncthreads();
+            cluster_barrier();  // every CTA's maximum is out
+            if (w == 0) {
+                const unsigned v = lane < (unsigned)kClCtas ? ld_cluster(&S.cmax, lane) : 0u;
+                const unsigned h = __reduce_max_sync(kFullMask, v);
+                if (lane == 0) S.hi_key = h;
             }
+            __syncthreads();
+            const unsigned lo = T + 1, hi = S.hi_key;  // total > 0 keys above T: lo <= hi
+            const int span = 32 - __clz((int)(lo ^ hi));  // bits below the common prefix
+            const int shift = span > 10 ? span - 10 : 0;
+            const unsigned base = lo >> shift, nb = (hi >> shift) - base + 1;  // nb <= 1024
+            for (unsigned m = lane; m < cw; m += 32) atomicAdd(&hist[(S.keys[w0 + m] >> shift) - base], 1u);
+            __syncthreads();
+            cluster_barrier();  // every CTA's histogram is out
+            unsigned* sum = S.mysmall;  // 1024 summed buckets
+            {
+                unsigned c = 0;
+                if (tid < nb)
+#pragma unroll 1
+                    for (int r = 0; r < kClCtas; ++r) c += ld_cluster(&hist[tid], (unsigned)r);
+                sum[tid] = c;
+            }
+            __syncthreads();
+            if (w == 0) {
+                // Lane l takes buckets i = 32 l .. 32 l + 31 counted from the
+                // top (bucket b = nb - 1 - i).
+                unsigned tot = 0, heavy = 0;
+#pragma unroll 1
+                for (unsigned j = 0; j < 32; ++j) {
+                    const unsigned i = lane * 32 + j;
+                    const unsigned c = i < nb ? sum[nb - 1 - i] : 0u;
+                    tot += c;
+                    heavy |= c > kRangeKeys + 1 ? 1u : 0u;
+                }
+                unsigned x = tot;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned y = __shfl_up_sync(kFullMask, x, o);
+                    if ((int)lane >= o) x += y;
+                }
+                unsigned excl = x - tot;
+                unsigned nrr = 0;
+#pragma unroll 1
+                for (unsigned j = 0; j < 32; ++j) {
+                    // Round j: lane l looks at bucket i = 32 l + j; the bounds
+                    // come out in key order within each round only, so each
+                    // lane first keeps its own (lanes own contiguous buckets).
+                    const unsigned i = lane * 32 + j;
+                    const unsigned c = i < nb ? sum[nb - 1 - i] : 0u;
+                    const bool last = i < nb && (i == nb - 1 || ((excl + c) / kRangeKeys) != (excl / kRangeKeys));
+                    if (last) {
+                        const unsigned b = nb - 1 - i;
+                        const unsigned bl = (base + b) << shift;
+                        S.samp[lane * 16 + (nrr & 15)] = bl > lo ? bl : lo;  // at most 16 cuts in 32 buckets of a lane? checked below
+                        ++nrr;
+                    }
+                    excl += c;
+                }
+                // A lane's 32 buckets hold at most 32 cuts; 16 slots per lane
+                // suffice only when its cuts are few: otherwise the sample plan.
+                const unsigned over = __reduce_or_sync(kFullMask, nrr > 16 ? 1u : 0u);
+                unsigned pre = nrr;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned y = __shfl_up_sync(kFullMask, pre, o);
+                    if ((int)lane >= o) pre += y;
+                }
+                const unsigned all_nr = __shfl_sync(kFullMask, pre, 31);
+                const bool ok = !__reduce_or_sync(kFullMask, heavy) && !over && all_nr <= (unsigned)kMaxRanges;
+                if (ok)
+                    for (unsigned q = 0; q < nrr; ++q) S.lb[pre - nrr + q] = S.samp[lane * 16 + q];
+                if (lane == 0) {
+                    S.plan_ok = ok ? 1u : 0u;
+                    S.nranges = ok ? all_nr : 0u;
+                }
+            }
+            __syncthreads();
         }
-        cluster_barrier();  // rank 0's range table is out
+        if (!S.plan_ok) {
+            // Splitter sample: a CTA's share of kPlanSamples follows its share
+            // of the keys above T.
+            auto samples_of = [&](unsigned c) -> unsigned {
+                return total ? (unsigned)(((unsigned long long)c * kPlanSamples) / total) : 0u;
+            };
+            {
+                const unsigned my_c = S.mine_count, my_s = samples_of(my_c);
+                for (unsigned i = tid; i < my_s; i += kClThreads) {
+                    const unsigned g = (unsigned)((unsigned long long)i * my_c / my_s);
+                    unsigned a = 0, b = kClWarps - 1;  // the last warp whose run starts at or before g
+                    while (a < b) {
+                        const unsigned mid = (a + b + 1) >> 1;
+                        if (S.woff[mid] <= g)
+                            a = mid;
+                        else
+                            b = mid - 1;
+                    }
+                    S.mysamp[i] = S.keys[a * share + (g - S.woff[a])];
+                }
+                // This CTA's samples, sorted descending by the whole CTA (zeros pad
+                // past my_s; every sample is above T, so nonzero).  A rolled loop:
+                // this runs once per launch, and an unrolled sort's straight-line
+                // code would mostly wait on instruction fetch.
+                const int P = next_pow2(my_s < 2 ? 2 : (int)my_s);
+                for (unsigned i = my_s + tid; i < (unsigned)P; i += kClThreads) S.mysamp[i] = 0u;
+                block_sort_smem_desc(S.mysamp, P);
+            }
+            cluster_barrier();  // sorted samples out
 
-        if (rank != 0 && tid <= (unsigned)kMaxRanges) {
-            if (tid < (unsigned)kMaxRanges)
-                S.lb[tid] = ld_cluster(&S.lb[tid], 0);
-            else
-                S.nranges = ld_cluster(&S.nranges, 0);
+            if (rank == 0) {
+                if (total) {
+                    unsigned soff[kClCtas + 1], ns = 0;
+        #pragma unroll
+                    for (int r = 0; r < kClCtas; ++r) {
+                        soff[r] = ns;
+                        ns += samples_of(S.ccount[r]);
+                    }
+                    soff[kClCtas] = ns;
+                    // Gather the 8 sorted lists, then merge them by rank: an element's
+                    // place is its index in its own list plus, in every other list,
+                    // the count of greater keys (equal keys count from lower ranks).
+                    unsigned* lists = &S.part[0][0];
+                    for (unsigned i = tid; i < ns; i += kClThreads) {
+                        unsigned r = 0;
+                        while (r + 1 < (unsigned)kClCtas && soff[r + 1] <= i) ++r;
+                        lists[i] = ld_cluster(&S.mysamp[i - soff[r]], r);
+                    }
+                    __syncthreads();
+                    for (unsigned i = tid; i < ns; i += kClThreads) {
+                        unsigned r = 0;
+                        while (r + 1 < (unsigned)kClCtas && soff[r + 1] <= i) ++r;
+                        const unsigned v = lists[i];
+                        unsigned place = i - soff[r];
+                        for (unsigned o = 0; o < (unsigned)kClCtas; ++o) {
+                            if (o == r) continue;
+                            // first index in list o whose key is below v (o < r) or not above v (o > r)
+                            unsigned a = soff[o], b = soff[o + 1];
+                            while (a < b) {
+                                const unsigned mid = (a + b) >> 1;
+                                const unsigned x = lists[mid];
+                                if (o < r ? x >= v : x > v)
+                                    a = mid + 1;
+                                else
+                                    b = mid;
+                            }
+                            place += a - soff[o];
+                        }
+                        S.samp[place] = v;
+                    }
+                    __syncthreads();
+                    if (w == 0) {
+                        // R - 1 splitters at even positions of the sorted sample,
+                        // about kRangeKeys keys apart.  A splitter value that repeats
+                        // at a neighbouring position (a value holding a range's worth
+                        // of keys) also bounds a range holding only that value, which
+                        // needs no sorting.  The last range ends at T + 1.
+                        // At least 4 samples per range keep the ranges' sizes close
+                        // to their mean.
+                        const unsigned R =
+                            min(min(kMaxPlanned, max(1u, ns / 4)), max(1u, (total + kRangeKeys - 1) / kRangeKeys));
+                        unsigned bnd[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // candidates at positions jj * 32 + lane
+        #pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const unsigned q = lane + 1 + 32 * h;  // splitter q of 1 .. R-1
+                            if (q < R) {
+                                const unsigned c = S.samp[q * ns / R];
+                                const bool dup = (q >= 2 && S.samp[(q - 1) * ns / R] == c) ||
+                                                 (q + 1 < R && S.samp[(q + 1) * ns / R] == c);
+                                bnd[2 * h] = c;
+                                bnd[2 * h + 1] = (dup && c != 0xFFFFFFFFu) ? c + 1 : 0u;
+                            }
+                        }
+                        if (lane == 31) bnd[7] = T + 1;  // position 255: no splitter lands there (R <= 128)
+                        // Sorted below by the whole CTA, in rank 0's own sample
+                        // array (merged into samp above, read by no other CTA).
+        #pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) S.mysamp[jj * 32 + lane] = bnd[jj];
+                    }
+                    block_sort_smem_desc(S.mysamp, 256);  // rolled, like the sample sort
+                    __syncthreads();
+                    if (w == 0) {
+                        // The distinct nonzero bounds, in descending order.
+                        unsigned nr = 0;
+        #pragma unroll 1
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const unsigned p = jj * 32 + lane;
+                            const unsigned v = S.mysamp[p];
+                            const bool keep = v != 0u && (p == 0 || v != S.mysamp[p - 1]);
+                            const unsigned b = __ballot_sync(kFullMask, keep);
+                            if (keep) S.lb[nr + __popc(b & lanemask_lt())] = v;
+                            nr += __popc(b);
+                        }
+                        if (lane == 0) S.nranges = nr;
+                    }
+                } else if (tid == 0) {
+                    S.nranges = 0u;
+                }
+            }
+            cluster_barrier();  // rank 0's range table is out
+
+            if (rank != 0 && tid <= (unsigned)kMaxRanges) {
+                if (tid < (unsigned)kMaxRanges)
+                    S.lb[tid] = ld_cluster(&S.lb[tid], 0);
+                else
+                    S.nranges = ld_cluster(&S.nranges, 0);
+            }
         }
         if (tid < (unsigned)kMaxRanges) S.rcnt[tid] = 0u;
         __syncthreads();

@@ -255,6 +255,36 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return false;
 }
 
+// An L2 cache policy that marks lines as first to evict: for inputs read
+// once, so that streaming them does not push out what the kernels that
+// follow need (their code and small working arrays).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// A read-only 16-byte load with the L2 policy `policy` (see above).
+__device__ __forceinline__ int4 ld_nc_hint(const int4* p, uint64_t policy) {
+    int4 v;
+    asm("ld.global.nc.L2::cache_hint.v4.s32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p), "l"(policy));
+    return v;
+}
+
+// Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// to this block's shared memory with the L2 policy `policy` (see above);
+// completion is signalled on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                   uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 // Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
 // to this block's shared memory; completion is signalled on `bar`.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

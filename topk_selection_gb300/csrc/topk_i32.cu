@@ -487,6 +487,8 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
             const size_t cnt = sp.nvec - base < (size_t)kTileVec ? sp.nvec - base : (size_t)kTileVec;
             const int st = (int)(i % kWarpStages);
             mbar_arrive_expect_tx(&my_bar[st], (uint32_t)(cnt * 16));
+            // Default L2 policy: an evict-first hint measured ~1.5% slower
+            // here (one launch per call, nothing after it to protect).
             bulk_copy_g2s(my_ring + (size_t)st * kTileVec, sp.body + base, (uint32_t)(cnt * 16), &my_bar[st]);
         };
         if (lane == 0)

@@ -494,6 +494,69 @@ items_final_select_kernel(const float* __restrict__ cv, const int32_t* __restric
     if (lane == 0 && out_count) *out_count = valid;
 }
 
+// Later levels for k <= 128: block b takes candidates [b * kChunk,
+// (b + 1) * kChunk) -- 32 warps of 256 -- ranks them like the final select
+// (register sort per warp, five pairwise merges) and writes its best ke, in
+// order, at b * ke of the next arrays (pads, -inf and -1, when the chunk has
+// fewer).  Chunks are in array order, so equal scores stay in position
+// order; pads only ever sit at the end of the array, hence in the last
+// chunks, and stay at the end.
+constexpr int kChunkN = 8;                                 // keys per lane
+constexpr int kChunk = kSelWarps * 32 * kChunkN;           // 8192 candidates per block
+__global__ void __launch_bounds__(kSelWarps * 32)
+items_select_chunks_kernel(const float* __restrict__ cv, const int32_t* __restrict__ cp, size_t count, int ke,
+                           float* __restrict__ nv, int32_t* __restrict__ np) {
+    __shared__ unsigned long long s_l[kSelWarps][32 * kSelN];
+    grid_dependency_wait();  // launched early (launch_pdl): the previous kernel's writes first
+    launch_dependents();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const size_t base = (size_t)blockIdx.x * kChunk + (size_t)w * 32 * kChunkN;
+    // The warp's 256 candidates as two sorted halves of 128 (the same
+    // register sort as the final select), merged through its own slot.
+    RegList<kSelN, unsigned long long> wl;  // the warp's best 32 * kSelN >= ke
+#pragma unroll 1
+    for (int h = 0; h < kChunkN / kSelN; ++h) {
+        unsigned long long v[kSelN];
+#pragma unroll
+        for (int j = 0; j < kSelN; ++j) {
+            const size_t p = base + (size_t)(h * kSelN + j) * 32 + lane;
+            v[j] = p < count ? items_key(cv[p], (unsigned)p) : 0ull;  // every real key is above 0
+        }
+        warp_sort_desc<kSelN>(v, lane);
+        if (h == 0) {
+#pragma unroll
+            for (int j = 0; j < kSelN; ++j) wl.lst[j] = v[j];
+        } else {
+#pragma unroll
+            for (int j = 0; j < kSelN; ++j) s_l[w][j * 32 + lane] = v[j];
+            __syncwarp();
+            wl.merge_list(s_l[w], lane);
+            __syncwarp();
+        }
+    }
+#pragma unroll 1
+    for (int s = 1; s < kSelWarps; s <<= 1) {
+        if ((w & (2 * s - 1)) == s)
+#pragma unroll
+            for (int j = 0; j < kSelN; ++j) s_l[w][j * 32 + lane] = wl.lst[j];
+        __syncthreads();
+        if ((w & (2 * s - 1)) == 0) wl.merge_list(s_l[w + s], lane);
+        __syncthreads();
+    }
+    if (w != 0) return;
+#pragma unroll
+    for (int j = 0; j < kSelN; ++j) {
+        const int o = j * 32 + lane;
+        if (o < ke) {
+            const unsigned long long key = wl.lst[j];
+            const unsigned idx = 0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull);
+            const size_t dst = (size_t)blockIdx.x * ke + o;
+            nv[dst] = key ? cv[idx] : __int_as_float(0xFF800000);
+            np[dst] = key ? (cp ? cp[idx] : (int32_t)idx) : -1;
+        }
+    }
+}
+
 // Pads the outputs when nothing is kept.
 __global__ void items_empty_kernel(int k, float* __restrict__ out_score, int64_t* __restrict__ out_item,
                                    int64_t* __restrict__ out_count) {
@@ -667,6 +730,19 @@ cudaError_t items_launch(cudaStream_t s, const float* score, const int64_t* item
                                   item, out_score, out_item, out_count);
             return launch_pdl(items_final_sort_kernel, 1, kFinalThreads, 0, s, cur, cur_pos, (int)real, ke, k, item,
                               out_score, out_item, out_count);
+        }
+        if (!first && k <= 32 * kSelN) {
+            // A chunk round: ceil(len / kChunk) blocks each keep their ke best.
+            const size_t nb = (len + kChunk - 1) / kChunk;
+            e = launch_pdl(items_select_chunks_kernel, (unsigned)nb, kSelWarps * 32, 0, s, cur, cur_pos, len, ke,
+                           nb_s[flip], nb_p[flip]);
+            *launches += 1;
+            if (e != cudaSuccess) return e;
+            cur = nb_s[flip];
+            cur_pos = nb_p[flip];
+            flip ^= 1;
+            len = real = nb * (size_t)ke;
+            continue;
         }
         size_t C = level_cols(real, ke, first);
         if (C > len) C = len;  // fewer candidates than one row of 8 ke: a single row of all of them

@@ -212,12 +212,13 @@ __device__ __forceinline__ void for_each_vec(const int32_t* __restrict__ in, siz
     const size_t nvec = (n - head) >> 2;
     const size_t tail0 = head + nvec * 4;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
+    const uint64_t policy = l2_evict_first_policy();  // the input is read once per pass
     for (size_t base = (size_t)blockIdx.x * blockDim.x * kRU; base < nvec; base += stride * kRU) {
         int4 r[kRU];
 #pragma unroll
         for (int u = 0; u < kRU; ++u) {
             const size_t i = base + (size_t)u * blockDim.x + threadIdx.x;
-            r[u] = i < nvec ? __ldg(body + i) : make_int4(0, 0, 0, 0);
+            r[u] = i < nvec ? ld_nc_hint(body + i, policy) : make_int4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kRU; ++u) f_vec(r[u], base + (size_t)u * blockDim.x + threadIdx.x < nvec);

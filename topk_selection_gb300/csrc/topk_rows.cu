@@ -416,6 +416,7 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
     int it_row = gw, it_t = 0;
     RowGeom it_g = row_geom(in, it_row < rows ? it_row : 0, cols);
     size_t issued = 0;
+    const uint64_t l2_policy = l2_evict_first_policy();  // the rows are read once
     auto issue_next = [&]() {  // lane 0 only; false when the stream is over
         while (it_row < rows && it_t >= it_g.tiles) {
             it_row += W;
@@ -427,7 +428,8 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
         const int cnt = it_g.nvec - base < kRowTileVec ? it_g.nvec - base : kRowTileVec;
         const int st = (int)(issued % kRowStages);
         mbar_arrive_expect_tx(&my_bar[st], (uint32_t)cnt * 16u);
-        bulk_copy_g2s(my_ring + (size_t)st * kRowTileVec, it_g.body + base, (uint32_t)cnt * 16u, &my_bar[st]);
+        bulk_copy_g2s_hint(my_ring + (size_t)st * kRowTileVec, it_g.body + base, (uint32_t)cnt * 16u, &my_bar[st],
+                           l2_policy);
         ++issued;
         ++it_t;
         return true;

@@ -56,7 +56,6 @@ namespace {
 constexpr int kU = 8;              // 16-byte loads in flight per lane
 constexpr int kTileVec = 32 * kU;  // int4 vectors per warp-tile (4 KiB)
 constexpr int kTailVec = 64;       // int4 vectors in the tail sample (256 elements)
-constexpr int kWarps = 16;         // warps per block
 constexpr int kQueue = 256;        // per-warp survivor queue (>= 31 + 128)
 
 __device__ __forceinline__ unsigned bias(int v) { return (unsigned)v ^ 0x80000000u; }
@@ -101,24 +100,6 @@ __device__ __forceinline__ Split split_input(const int32_t* in, size_t n) {
     s.tail0 = s.head + s.nvec * 4;
     s.ntiles = (s.nvec + kTileVec - 1) / kTileVec;
     return s;
-}
-
-// One warp-tile: kU int4 per lane, lane-interleaved so that every load
-// instruction covers 512 contiguous bytes.  Vectors past nvec read as INT_MIN,
-// which is never admitted (the filter is strict and thresholds are >= INT_MIN).
-__device__ __forceinline__ void load_tile(int4 (&r)[kU], const int4* __restrict__ body, size_t nvec,
-                                          size_t tile, int lane) {
-    const size_t base = tile * kTileVec + lane;
-    if (base + (kU - 1) * 32 < nvec) {
-#pragma unroll
-        for (int u = 0; u < kU; ++u) r[u] = __ldg(body + base + u * 32);
-    } else {
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const size_t i = base + u * 32;
-            r[u] = i < nvec ? __ldg(body + i) : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
-        }
-    }
 }
 
 // k-th largest of the warp's 32*GL group maxima (each group a disjoint set of

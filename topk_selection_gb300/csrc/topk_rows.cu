@@ -100,47 +100,23 @@ template <int B>
 __device__ bool rows_flush(RowBufT& w, int k, int lane) {
     __syncwarp();
     bool raised = false;
-    if constexpr (B == 256) {
-        u64 v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int p = j * 32 + lane;
-            v[j] = p < w.cnt ? w.buf[p] : 0ull;
+    for (int p = w.cnt + lane; p < B; p += 32) w.buf[p] = 0ull;
+    __syncwarp();
+    warp_sort_smem_desc(w.buf, B, lane);
+    if (w.cnt >= k) {
+        const u64 kth = w.buf[k - 1];
+        if (kth > w.T) {
+            w.T = kth;
+            raised = true;
         }
-        warp_sort_desc<8>(v, lane);
-        const int keep = w.cnt < k ? w.cnt : k;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int p = j * 32 + lane;
-            if (p < keep) w.buf[p] = v[j];
-        }
-        if (w.cnt >= k) {
-            const u64 kth = warp_sorted_at<8>(v, k - 1);
-            if (kth > w.T) {
-                w.T = kth;
-                raised = true;
-            }
-        }
-        w.cnt = keep;
-    } else {
-        for (int p = w.cnt + lane; p < B; p += 32) w.buf[p] = 0ull;
-        __syncwarp();
-        warp_sort_smem_desc(w.buf, B, lane);
-        if (w.cnt >= k) {
-            const u64 kth = w.buf[k - 1];
-            if (kth > w.T) {
-                w.T = kth;
-                raised = true;
-            }
-        }
-        w.cnt = w.cnt < k ? w.cnt : k;
     }
+    w.cnt = w.cnt < k ? w.cnt : k;
     __syncwarp();
     return raised;
 }
 
 template <int B>
-__global__ void __launch_bounds__(kWarps * 32, (B <= 256 ? 4 : 1))
+__global__ void __launch_bounds__(kWarps * 32, 1)
 topk_rows_smem_kernel(const float* __restrict__ in, int cols, int k, float* __restrict__ vals,
                       int32_t* __restrict__ idx) {
     extern __shared__ __align__(16) u64 smem64[];

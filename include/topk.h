@@ -130,9 +130,11 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
  *   k          1 <= k <= min(n, TOPK_MAX_K_ROWS).
  *   out_score  float32[k]; out_item int64[k]; out_count one int64 or null.
  *
- * The selection runs the row TopK level by level (two-stage reduction):
- * rows of at least 8k scores give their k best, whose winners, in order,
- * are the next level's rows, until one row is left.  With keep, when
+ * The selection is a two-stage reduction applied level by level: rows of at
+ * least 8k scores give their k best (the row TopK), and their winners, in
+ * order, are the next level's candidates (blocks of 8192 keeping their k
+ * best for k <= 128, rows again otherwise) until one block ranks the last
+ * at most 4096.  With keep, when
  * n >= 2^20, k <= 128 and keep's address is congruent to score's / 4
  * (mod 4) (e.g. score 16-byte aligned, keep 4-byte aligned), the first
  * level skips filtered positions itself and the call only enqueues.

@@ -23,9 +23,12 @@
 //   level j  the previous level's winners, in row order, are the next
 //            level's candidates.  Equal scores stay in position order: rows
 //            are in position order, and a row's winners with equal scores
-//            come in column order.  Repeat until one row is left.
-//   final    the last row's winners map back to input positions, items and
-//            score bits.
+//            come in column order.  For k <= 128 a level is a chunk round
+//            (each block keeps the k best of 8192 candidates, in order);
+//            larger k take row-kernel levels.  Repeat until at most
+//            kFinalCap candidates are left.
+//   final    one block ranks those; the best k map back to input positions,
+//            items and score bits.
 // Merging several TopK results is this call on their concatenation.
 #include <cuda_runtime.h>
 

@@ -31,10 +31,13 @@
 //                       fixes the k-th key T, and the keys between T and the
 //                       prefix's top are written from the histogram
 //   final    one cluster loads the buffer into its 8 CTAs' shared memory and
-//            selects the k-th key with four cluster-wide 8-bit digit
-//            histograms (summed through distributed shared memory).  Rank 0
-//            cuts the value range of the keys above it into ranges of about
-//            256 keys, from a sample weighted by each CTA's share (a value
+//            selects the k-th key T with four cluster-wide 8-bit digit
+//            histograms (summed through distributed shared memory).  At most
+//            kSmallCap keys above T: rank 0 gathers and sorts them all.
+//            Otherwise their value range is cut into ranges of about 256
+//            keys -- from a cluster-wide histogram of the 10 bits below the
+//            common prefix of [T + 1, max], or, when one bucket is too dense,
+//            from a splitter sample weighted by each CTA's share (a value
 //            that dominates the sample gets a range of its own).  Every CTA
 //            counts its keys per range, writes them straight to their range
 //            of the output, and each range is then sorted in place by one

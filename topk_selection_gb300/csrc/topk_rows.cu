@@ -692,7 +692,7 @@ cudaError_t launch_stream(cudaStream_t s, const float* in, int rows, int cols, i
 
 cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
                         unsigned* status, bool early, int flags) {
-    // k <= 128 streams (one warp per row); k > 128 uses one block per row
+    // k <= 128 streams rows (one warp per row); k > 128 uses one block per row
     // with shared-memory buffers.
     const bool stream = k <= 128;
     const uint8_t* nk = nullptr;

@@ -43,6 +43,7 @@ constexpr int kTile = kST * kSI;    // keys per tile
 constexpr int kRadix = 256;
 constexpr int kSpins = 1 << 22;     // polls of one look-back word before giving up
 constexpr int kHT = 512, kHU = 8;   // histogram pass: threads, 16-byte loads in flight
+constexpr int kHR = 8;              // histogram pass: copies of each digit histogram
 
 constexpr unsigned long long kAgg = 1ull << 62;   // word holds this tile's count
 constexpr unsigned long long kIncl = 2ull << 62;  // word holds the count up to and including this tile
@@ -68,15 +69,19 @@ __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned l
 
 __global__ void __launch_bounds__(kHT, 2)
 sort_hist_kernel(const uint32_t* __restrict__ keys, size_t n, SortHeader* __restrict__ h) {
-    __shared__ unsigned sh[4][kRadix];
+    // kHR copies of each digit histogram, bin b of copy r at word b * kHR + r
+    // with r = lane % kHR: lanes of different copies never share a bank, so a
+    // warp's 32 random bins meet fewer bank conflicts than in one copy.
+    __shared__ unsigned sh[4][kRadix * kHR];
     __shared__ int s_last;
-    for (int i = threadIdx.x; i < 4 * kRadix; i += blockDim.x) (&sh[0][0])[i] = 0u;
+    for (int i = threadIdx.x; i < 4 * kRadix * kHR; i += blockDim.x) (&sh[0][0])[i] = 0u;
     __syncthreads();
+    const unsigned r = threadIdx.x % kHR;
     auto add = [&](uint32_t k) {
-        atomicAdd(&sh[0][k & 0xFFu], 1u);
-        atomicAdd(&sh[1][(k >> 8) & 0xFFu], 1u);
-        atomicAdd(&sh[2][(k >> 16) & 0xFFu], 1u);
-        atomicAdd(&sh[3][k >> 24], 1u);
+        atomicAdd(&sh[0][(k & 0xFFu) * kHR + r], 1u);
+        atomicAdd(&sh[1][((k >> 8) & 0xFFu) * kHR + r], 1u);
+        atomicAdd(&sh[2][((k >> 16) & 0xFFu) * kHR + r], 1u);
+        atomicAdd(&sh[3][(k >> 24) * kHR + r], 1u);
     };
     const uintptr_t addr = reinterpret_cast<uintptr_t>(keys);
     size_t head = ((16u - (unsigned)(addr & 15u)) & 15u) >> 2;
@@ -106,7 +111,10 @@ sort_hist_kernel(const uint32_t* __restrict__ keys, size_t n, SortHeader* __rest
     }
     __syncthreads();
     for (int i = threadIdx.x; i < 4 * kRadix; i += blockDim.x) {
-        const unsigned v = (&sh[0][0])[i];
+        const unsigned* c = &sh[i / kRadix][(i % kRadix) * kHR];
+        unsigned v = 0;
+#pragma unroll
+        for (int q = 0; q < kHR; ++q) v += c[q];
         if (v) atomicAdd(&(&h->hist[0][0])[i], v);
     }
     __threadfence();

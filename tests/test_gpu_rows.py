@@ -163,9 +163,27 @@ def special_rows(rows, cols, seed):
 
 def test_long_rows_with_specials(tk):
     x = special_rows(11, 50_003, 1)
-    for k in (1, 20, 33, 64, 100, 128):
+    for k in (1, 20, 33, 64, 100, 128, 129, 300, 1024):
         assert_rows_equal(tk, x, k)
     assert_rows_equal(tk, x[:, :49_997], 64, col_offset=3)
+    assert_rows_equal(tk, x[:, :49_997], 777, col_offset=1)
+
+
+@pytest.mark.parametrize("k", [256, 1024])
+@pytest.mark.parametrize("tied", [True, False])
+def test_workload_shape_large_k(tk, k, tied):
+    # k > 128: one block per row with a shared candidate buffer.
+    w = synth.ROWS_WORKLOAD
+    rows, cols = w["rows"], w["cols"]
+    x = synth.f32_rows_tied(rows, cols, w["seed"], w["tie_frac"]) if tied else \
+        synth.f32_rows_normal(rows, cols, w["seed"])
+    v, i = gpu_rows(tk, x, k)
+    sample = np.unique(np.linspace(0, rows - 1, 64).astype(np.int64))
+    ev, ei = oracle.topk_rows_f32(x[sample], k)
+    assert np.array_equal(i[sample], ei)
+    assert np.array_equal(bits(v[sample]), bits(ev))
+    for lo in range(0, rows, 512):
+        check_all_rows(x[lo:lo + 512], k, v[lo:lo + 512], i[lo:lo + 512])
 
 
 def test_few_long_rows(tk):

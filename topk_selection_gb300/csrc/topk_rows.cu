@@ -14,19 +14,11 @@
 // and its order is "score descending, lower column first", so the selection
 // is exact and needs no tie handling beyond comparing keys.
 //
-// One block per row, 8 warps:
-//   1. Every warp loads its first 4 KiB tile; each lane's maximum score key
-//      is a group maximum.  The k-th largest of the 256 group maxima (at
-//      least k elements reach it) becomes the row's start threshold.
-//   2. Warps stream their tiles (128-bit loads, 8 in flight per lane) and
-//      compare each float once against the threshold score; elements at or
-//      above it get their exact 64-bit key, and keys above the warp's
-//      threshold are compacted into a per-warp shared buffer.  A full
-//      buffer is sorted and cut back to k, raising the warp's threshold,
-//      which is shared with the other warps through shared memory.
-//   3. The warps' sorted lists are merged pairwise (bitonic), and the k best
-//      keys give the columns; values are re-read from the row so their bits
-//      are the input's.
+// k <= 128: one warp streams each row, keeping its list in registers (see
+// the streamed kernel below).  128 < k <= 1024: one block per row with a
+// shared-memory candidate buffer.  Output values are decoded from the keys,
+// except -0.0 and NaN payloads, which are read again from the row so their
+// bits are the input's.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -40,9 +32,6 @@ namespace topk {
 
 namespace {
 
-constexpr int kU = 8;              // 16-byte loads in flight per lane
-constexpr int kTileVec = 32 * kU;  // float4 vectors per warp-tile
-constexpr int kWarps = 8;
 
 typedef unsigned long long u64;
 
@@ -69,189 +58,6 @@ __device__ __forceinline__ float max_nan(float a, float b) {
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
     return d;
 }
-
-// Elements that may beat threshold score tf: v >= tf, or v is NaN.
-__device__ __forceinline__ bool maybe(float v, float tf) { return !(v < tf); }
-
-__device__ __forceinline__ float4 ld4(const float4* p) { return __ldg(p); }
-
-struct RowBufT {
-    u64* buf;
-    int cnt;
-    u64 T;  // only keys > T are admitted
-};
-
-template <int B>
-__device__ __forceinline__ void rows_admit(RowBufT& w, float v, unsigned col, float tf, int lane) {
-    bool p = false;
-    u64 key = 0;
-    if (maybe(v, tf)) {
-        key = full_key(v, col);
-        p = key > w.T;
-    }
-    const unsigned m = __ballot_sync(kFullMask, p);
-    if (p) w.buf[w.cnt + __popc(m & lanemask_lt())] = key;
-    w.cnt += __popc(m);
-}
-
-// Sort the buffer, keep the k best keys, raise T to the k-th.  Returns true
-// when T was raised.
-template <int B>
-__device__ bool rows_flush(RowBufT& w, int k, int lane) {
-    __syncwarp();
-    bool raised = false;
-    for (int p = w.cnt + lane; p < B; p += 32) w.buf[p] = 0ull;
-    __syncwarp();
-    warp_sort_smem_desc(w.buf, B, lane);
-    if (w.cnt >= k) {
-        const u64 kth = w.buf[k - 1];
-        if (kth > w.T) {
-            w.T = kth;
-            raised = true;
-        }
-    }
-    w.cnt = w.cnt < k ? w.cnt : k;
-    __syncwarp();
-    return raised;
-}
-
-template <int B>
-__global__ void __launch_bounds__(kWarps * 32, 1)
-topk_rows_smem_kernel(const float* __restrict__ in, int cols, int k, float* __restrict__ vals,
-                      int32_t* __restrict__ idx) {
-    extern __shared__ __align__(16) u64 smem64[];
-    __shared__ u64 s_T;
-    __shared__ unsigned s_gmax[kWarps * 32];
-
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const size_t row = blockIdx.x;
-    const float* rp = in + row * (size_t)cols;
-
-    // Row split: unaligned head (< 4), 16-byte aligned float4 body, tail.
-    const uintptr_t addr = reinterpret_cast<uintptr_t>(rp);
-    int head = (int)(((16u - (unsigned)(addr & 15u)) & 15u) >> 2);
-    if (head > cols) head = cols;
-    const float4* body = reinterpret_cast<const float4*>(rp + head);
-    const int nvec = (cols - head) >> 2;
-    const int tail0 = head + nvec * 4;
-    const int ntiles = (nvec + kTileVec - 1) / kTileVec;
-
-    RowBufT w{smem64 + warp * B, 0, 0ull};
-
-    // 1. First tile of each warp: group maxima -> start threshold.
-    float4 r[kU];
-    const int t0 = warp;
-    auto load = [&](int tile) {
-        const int base = tile * kTileVec + lane;
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int i = base + u * 32;
-            r[u] = (tile < ntiles && i < nvec) ? ld4(body + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
-    load(t0);
-    {
-        unsigned gm = 0u;  // key 0 is below every real key
-        if (t0 < ntiles) {
-            const int base = t0 * kTileVec + lane;
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                if (base + u * 32 < nvec) {
-                    gm = max(gm, score_key(__float_as_uint(r[u].x)));
-                    gm = max(gm, score_key(__float_as_uint(r[u].y)));
-                    gm = max(gm, score_key(__float_as_uint(r[u].z)));
-                    gm = max(gm, score_key(__float_as_uint(r[u].w)));
-                }
-            }
-        }
-        s_gmax[threadIdx.x] = gm;
-    }
-    if (threadIdx.x == 0) s_T = 0ull;
-    __syncthreads();
-    if (warp == 0 && k <= kWarps * 32) {
-        unsigned g[kWarps];
-#pragma unroll
-        for (int j = 0; j < kWarps; ++j) g[j] = s_gmax[j * 32 + lane];
-        warp_sort_desc<kWarps>(g, lane);
-        const unsigned seed = warp_sorted_at<kWarps>(g, k - 1);
-        if (lane == 0) s_T = (u64)seed << 32;  // admits every key with score >= seed
-    }
-    __syncthreads();
-    w.T = s_T;
-
-    // Scalars outside the aligned body: taken by warp 0.
-    if (warp == 0) {
-        const int ns = head + (cols - tail0);
-        const int col = lane < head ? lane : tail0 + (lane - head);
-        const float v = lane < ns ? rp[col] : 0.f;
-        const float tf = key_float((unsigned)(w.T >> 32));
-        bool p = false;
-        u64 key = 0;
-        if (lane < ns && maybe(v, tf)) {
-            key = full_key(v, (unsigned)col);
-            p = key > w.T;
-        }
-        const unsigned m = __ballot_sync(kFullMask, p);
-        if (p) w.buf[w.cnt + __popc(m & lanemask_lt())] = key;
-        w.cnt += __popc(m);
-    }
-
-    // 2. Stream the row.
-    for (int tile = t0; tile < ntiles; tile += kWarps) {
-        if (tile != t0) load(tile);
-        w.T = kmax(w.T, *(volatile u64*)&s_T);
-        const float tf = key_float((unsigned)(w.T >> 32));
-        bool any = false;
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-            any |= maybe(r[u].x, tf) | maybe(r[u].y, tf) | maybe(r[u].z, tf) | maybe(r[u].w, tf);
-        if (__any_sync(kFullMask, any)) {
-            const int base = tile * kTileVec + lane;
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                if (w.cnt > B - 128) {
-                    if (rows_flush<B>(w, k, lane) && lane == 0) atomicMax(&s_T, w.T);
-                }
-                const float tfu = key_float((unsigned)(w.T >> 32));
-                const int vi = base + u * 32;
-                const bool valid = vi < nvec;
-                const unsigned c0 = (unsigned)(head + vi * 4);
-                rows_admit<B>(w, r[u].x, c0 + 0, valid ? tfu : __int_as_float(0x7f800000), lane);
-                rows_admit<B>(w, r[u].y, c0 + 1, valid ? tfu : __int_as_float(0x7f800000), lane);
-                rows_admit<B>(w, r[u].z, c0 + 2, valid ? tfu : __int_as_float(0x7f800000), lane);
-                rows_admit<B>(w, r[u].w, c0 + 3, valid ? tfu : __int_as_float(0x7f800000), lane);
-            }
-        }
-    }
-
-    // 3. Per-warp sorted lists, block merge, output.
-    if (rows_flush<B>(w, k, lane) && lane == 0) atomicMax(&s_T, w.T);
-    const int K = next_pow2(k < 32 ? 32 : k);
-    for (int p = w.cnt + lane; p < K; p += 32) w.buf[p] = 0ull;
-#pragma unroll 1
-    for (int s = 1; s < kWarps; s <<= 1) {
-        __syncthreads();
-        if ((warp & (2 * s - 1)) == 0) {
-            u64* a = smem64 + warp * B;
-            const u64* b = smem64 + (warp + s) * B;
-            for (int i = lane; i < K; i += 32) a[i] = kmax(a[i], b[K - 1 - i]);
-            __syncwarp();
-            warp_merge_smem_desc(a, K, lane);
-        }
-    }
-    __syncthreads();
-    for (int j = threadIdx.x; j < k; j += blockDim.x) {
-        const u64 key = smem64[j];
-        const unsigned col = 0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull);
-        // Every key in the merged list is a real element (at least k elements
-        // reach the start threshold), so col < cols; the guard only keeps a
-        // broken invariant from turning into an out-of-row read.
-        vals[row * (size_t)k + j] = col < (unsigned)cols ? __ldg(rp + col) : __int_as_float(0x7fc00000);
-        idx[row * (size_t)k + j] = (int32_t)col;
-    }
-}
-
 
 // ------------------------------------------ k <= 128: streamed rows --
 //
@@ -646,6 +452,354 @@ topk_rows_stream_kernel(const float* __restrict__ in, int rows, int cols, int k,
             if (!mbar_wait(&my_bar[c % kRowStages], (uint32_t)((c / kRowStages) & 1))) break;
 }
 
+// ------------------------------------- 128 < k <= 1024: one block per row --
+//
+// Each block streams its rows (rows b, b + G, ... for block b of G) through
+// a ring of kBigStages shared-memory stages of 8 KiB, filled by bulk copies
+// that thread 0 keeps in flight across row boundaries.  A round consumes one
+// stage: every thread checks one 16-byte vector, by its largest element,
+// against the block's threshold T (a lower bound of the row's k-th key);
+// flagged vectors go to the warp's queue, and once 32 are queued the warp
+// expands them into exact 64-bit keys, of which those above T go to a shared
+// candidate buffer (one atomic per warp).  So most rounds cost a warp a
+// compare and a ballot, however many of its warps' vectors pass.  T only
+// rises and stays below the row's k-th key, so every key of the row's k best
+// reaches the buffer and stays there.
+//
+// Cutting the buffer is a radix select, not a sort.  Its keys share a
+// common prefix (found with one OR-reduction of key ^ buf[0]); histograms of
+// the next 11 bits narrow down the bucket that holds the k-th largest key
+// until the keys at or above that bucket's lower edge L number at most
+// `limit`.  Those keys stay, and T becomes L - 1.  At the row's end a cut
+// with limit k leaves exactly the k best keys, which a bitonic sort orders.
+constexpr int kBigThreads = 512;
+constexpr int kBigStageVec = kBigThreads;    // 16-byte vectors per stage (one per thread)
+constexpr int kBigStages = 6;                // stages in flight per block (48 KiB)
+constexpr int kBigCap = 4096;                // candidate buffer (32 KiB)
+constexpr int kBigRound = kBigStageVec * 4;  // keys one round can add
+constexpr int kBigKeep = kBigCap - kBigRound;  // most keys a cut may keep
+constexpr int kBigDigit = 11;
+constexpr int kBigBins = 1 << kBigDigit;
+constexpr int kBigPer = kBigCap / kBigThreads;  // buffer keys per thread
+constexpr int kBigSlack = 256;                 // keys above k that a cut inside the row may keep
+constexpr int kBigQueue = 64;                  // per-warp vector queue (>= 31 + 32)
+constexpr int kBigRingBytes = kBigStages * kBigStageVec * 16;
+static_assert(1024 + kBigSlack <= kBigKeep, "k <= 1024 best keys plus the slack fit");
+static_assert(kBigBins == 4 * kBigThreads, "the bin scan gives each thread four bins");
+static_assert(kBigRound >= (kBigThreads / 32) * 32 * 4, "a round's queue drains add at most kBigRound keys");
+
+// Append a thread's keys (those that are nonzero) to buf at *cnt: a
+// warp-wide prefix of the per-thread counts (one ballot per bit of the
+// count) and one shared atomic per warp.  Returns the warp's end position in
+// the buffer (the largest such end is the buffer's count).  Keys past
+// kBigCap are dropped (the callers' cuts keep the buffer below it; this only
+// bounds the writes).
+template <int N>
+__device__ __forceinline__ unsigned big_append(const u64 (&kk)[N], u64* buf, unsigned* cnt, int lane) {
+    constexpr int kBits = N < 2 ? 1 : (N < 4 ? 2 : (N < 8 ? 3 : 4));
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < N; ++j) c += kk[j] != 0ull;
+    const unsigned lt = lanemask_lt();
+    int tot = 0, before = 0;
+#pragma unroll
+    for (int b = 0; b < kBits; ++b) {
+        const unsigned m = __ballot_sync(kFullMask, (c >> b) & 1);
+        tot += __popc(m) << b;
+        before += __popc(m & lt) << b;
+    }
+    unsigned base = 0;
+    if (lane == 0 && tot) base = atomicAdd(cnt, (unsigned)tot);
+    base = __shfl_sync(kFullMask, base, 0);
+    int o = (int)base + before;
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+        if (kk[j]) {
+            if (o < kBigCap) buf[o] = kk[j];
+            ++o;
+        }
+    return tot ? base + (unsigned)tot : 0u;
+}
+
+__global__ void __launch_bounds__(kBigThreads, 2)
+topk_rows_big_kernel(const float* __restrict__ in, int rows, int cols, int k, float* __restrict__ vals,
+                     int32_t* __restrict__ idx, unsigned* __restrict__ status) {
+    extern __shared__ __align__(128) float4 bring[];  // kBigStages stages
+    __shared__ __align__(16) u64 buf[kBigCap];
+    __shared__ __align__(16) unsigned hist[kBigBins];
+    __shared__ __align__(16) float4 s_qv[(kBigThreads / 32) * kBigQueue];  // queued vectors
+    __shared__ unsigned s_qi[(kBigThreads / 32) * kBigQueue];               // and their vector index
+    __shared__ __align__(8) uint64_t s_bar[kBigStages];
+    __shared__ unsigned s_wsum[kBigThreads / 32];
+    __shared__ unsigned s_or[2];
+    __shared__ unsigned s_cnt, s_bin, s_above, s_inbin, s_fail;
+    __shared__ u64 s_T;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        for (int i = 0; i < kBigStages; ++i) mbar_init(&s_bar[i], 1);
+        mbar_init_fence();
+        s_or[0] = s_or[1] = 0u;
+        s_fail = 0u;
+    }
+    __syncthreads();
+
+    // Issue side (thread 0): the next (row, tile) of this block's stream,
+    // with that row's geometry.  refill(released) keeps tiles up to
+    // released + kBigStages - 1 in flight, where the first `released`
+    // consumed tiles are those whose reads a block barrier has followed.
+    // The issue state lives in shared memory: only thread 0 uses it.
+    __shared__ const float4* s_it_body;
+    __shared__ int s_it_row, s_it_base, s_it_nvec;
+    __shared__ unsigned s_issued;
+    unsigned consumed = 0;
+    const uint64_t l2_policy = l2_evict_first_policy();  // the rows are read once
+    auto refill = [&](unsigned released) {  // thread 0
+        int it_row = s_it_row, it_base = s_it_base, it_nvec = s_it_nvec;
+        const float4* it_body = s_it_body;
+        unsigned issued = s_issued;
+        while (issued < released + kBigStages) {
+            while (it_row < rows && it_base >= it_nvec) {
+                it_row += gridDim.x;
+                it_base = 0;
+                if (it_row < rows) {
+                    const RowGeom ig = row_geom(in, it_row, cols);
+                    it_body = ig.body;
+                    it_nvec = ig.nvec;
+                }
+            }
+            if (it_row >= rows) break;
+            const int n = it_nvec - it_base < kBigStageVec ? it_nvec - it_base : kBigStageVec;
+            const int st = (int)(issued % kBigStages);
+            mbar_arrive_expect_tx(&s_bar[st], (uint32_t)n * 16u);
+            bulk_copy_g2s_hint(bring + (size_t)st * kBigStageVec, it_body + it_base, (uint32_t)n * 16u, &s_bar[st],
+                               l2_policy);
+            ++issued;
+            it_base += kBigStageVec;
+        }
+        s_it_row = it_row;
+        s_it_base = it_base;
+        s_it_nvec = it_nvec;
+        s_it_body = it_body;
+        s_issued = issued;
+    };
+    if (tid == 0) {
+        const RowGeom g0 = row_geom(in, blockIdx.x < rows ? blockIdx.x : 0, cols);
+        s_it_row = blockIdx.x;
+        s_it_base = 0;
+        s_it_nvec = (int)blockIdx.x < rows ? g0.nvec : 0;
+        s_it_body = g0.body;
+        s_issued = 0u;
+        refill(0u);
+    }
+
+    // Cut the buffer (every thread, after a barrier; s_cnt >= k): keep the
+    // keys at or above the lower edge L of the smallest bucket that holds
+    // the k-th largest key and has at most `limit` keys at or above it;
+    // T = L - 1.
+    auto cut = [&](unsigned limit) {
+        const unsigned cnt = kmin(s_cnt, (unsigned)kBigCap);
+        const int nj = (int)((cnt + kBigThreads - 1) / kBigThreads);  // key slots in use (block-uniform)
+        u64 kv[kBigPer];
+#pragma unroll
+        for (int j = 0; j < kBigPer; ++j) {
+            const unsigned i = (unsigned)(tid + j * kBigThreads);
+            kv[j] = j < nj && i < cnt ? buf[i] : 0ull;  // real keys are nonzero
+        }
+        const u64 x0 = buf[0];
+        u64 d = 0ull;
+#pragma unroll
+        for (int j = 0; j < kBigPer; ++j)
+            if (kv[j]) d |= kv[j] ^ x0;
+        const unsigned dh = __reduce_or_sync(kFullMask, (unsigned)(d >> 32));
+        const unsigned dl = __reduce_or_sync(kFullMask, (unsigned)d);
+        if (lane == 0) {
+            if (dh) atomicOr(&s_or[0], dh);
+            if (dl) atomicOr(&s_or[1], dl);
+        }
+        __syncthreads();
+        const u64 dall = ((u64)s_or[0] << 32) | (u64)s_or[1];
+        if (tid == 0) s_cnt = 0u;  // every thread has read it
+        int pb = dall ? __clzll((long long)dall) : 64;  // bits every key shares
+        u64 P = pb == 0 ? 0ull : (pb == 64 ? x0 : x0 >> (64 - pb));
+        unsigned above = 0u;  // keys above the current bucket
+        u64 L = x0;
+        while (pb < 64) {
+            const int D = 64 - pb < kBigDigit ? 64 - pb : kBigDigit;
+            const int shift = 64 - pb - D;
+            reinterpret_cast<uint4*>(hist)[tid] = make_uint4(0u, 0u, 0u, 0u);
+            const u64 hmask = pb == 0 ? 0ull : ~0ull << (64 - pb);  // the bucket's known bits
+            const u64 hval = pb == 0 ? 0ull : P << (64 - pb);
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < kBigPer; ++j)
+                if (j < nj && kv[j] && (kv[j] & hmask) == hval)
+                    atomicAdd(&hist[(unsigned)(kv[j] >> shift) & (kBigBins - 1)], 1u);
+            __syncthreads();
+            // Thread t takes bins 4t'..4t'+3 with t' = kBigThreads-1-t, so the
+            // threads run from the top bin down.
+            const uint4 h4 = reinterpret_cast<const uint4*>(hist)[kBigThreads - 1 - tid];
+            const unsigned hq[4] = {h4.w, h4.z, h4.y, h4.x};
+            const unsigned s = hq[0] + hq[1] + hq[2] + hq[3];
+            unsigned incl = s;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned y = __shfl_up_sync(kFullMask, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) s_wsum[warp] = incl;
+            __syncthreads();
+            unsigned c = above + incl - s;
+            for (int w = 0; w < warp; ++w) c += s_wsum[w];
+            if (c < (unsigned)k && c + s >= (unsigned)k) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (c < (unsigned)k && c + hq[q] >= (unsigned)k) {
+                        s_bin = (unsigned)(4 * (kBigThreads - 1 - tid) + 3 - q);
+                        s_above = c;
+                        s_inbin = hq[q];
+                    }
+                    c += hq[q];
+                }
+            }
+            __syncthreads();
+            const unsigned b = s_bin;
+            above = s_above;
+            const unsigned inb = s_inbin;
+            P = (P << D) | (u64)b;
+            pb += D;
+            L = shift ? P << shift : P;
+            if (above + inb <= limit) break;
+            __syncthreads();  // s_wsum, s_bin, hist are rewritten by the next pass
+        }
+#pragma unroll
+        for (int j = 0; j < kBigPer; ++j)
+            if (!(j < nj && kv[j] >= L)) kv[j] = 0ull;
+        big_append<kBigPer>(kv, buf, &s_cnt, lane);
+        if (tid == 0) {
+            s_T = L ? L - 1 : 0ull;
+            s_or[0] = s_or[1] = 0u;
+        }
+        __syncthreads();
+    };
+
+    float4* qv = s_qv + warp * kBigQueue;
+    unsigned* qi = s_qi + warp * kBigQueue;
+    for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+        const RowGeom g = row_geom(in, row, cols);
+        int nq = 0;  // vectors in this warp's queue (warp-uniform); below 32 between rounds
+        // The end of this warp's last append since the last barrier.  A
+        // barrier that ORs (hi > kBigKeep) tells every thread, alike, whether
+        // the buffer holds more than kBigKeep keys -- reading the count
+        // instead would race with warps that have already moved on and
+        // append.
+        unsigned hi = 0u;
+        // Expand the warp's last c <= 32 queued vectors into keys above T and
+        // append them to the buffer.
+        auto drain = [&](int c, u64 T) {
+            __syncwarp();
+            u64 kk[4] = {0ull, 0ull, 0ull, 0ull};
+            if (lane < c) {
+                const float4 v = qv[nq - c + lane];
+                const unsigned c0 = (unsigned)g.head + 4u * qi[nq - c + lane];
+                const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const u64 key = full_key(e[j], c0 + j);
+                    kk[j] = key > T ? key : 0ull;
+                }
+            }
+            __syncwarp();  // read before the slots are queued to again
+            nq -= c;
+            hi = kmax(hi, big_append<4>(kk, buf, &s_cnt, lane));
+        };
+        if (tid == 0) {
+            s_cnt = 0u;
+            s_T = 0ull;
+        }
+        __syncthreads();
+        // Scalars outside the aligned body (fewer than 8): warp 0.
+        if (tid < 32) {
+            const int col = lane < g.head ? lane : g.tail0 + (lane - g.head);
+            const u64 kk[1] = {lane < g.ns ? full_key(g.rp[col], (unsigned)col) : 0ull};
+            hi = big_append<1>(kk, buf, &s_cnt, lane);
+        }
+        const int tiles = (g.nvec + kBigStageVec - 1) / kBigStageVec;
+        for (int t = 0; t < tiles; ++t) {
+            // Thread 0 alone waits for this round's stage; the barrier hands
+            // the landed data to the block (and the other threads sleep
+            // there instead of polling).
+            const int st = (int)(consumed % kBigStages);
+            if (tid == 0 && !mbar_wait(&s_bar[st], (uint32_t)((consumed / kBigStages) & 1))) {
+                atomicOr(status, kStatusWaitTimeout);
+                s_fail = 1u;
+            }
+            // The last round's keys are in, its stage is read, this one has landed.
+            const bool full = __syncthreads_or(hi > (unsigned)kBigKeep);
+            hi = 0u;
+            if (s_fail) break;
+            const unsigned released = consumed;
+            ++consumed;
+            if (full) cut((unsigned)k + kBigSlack);
+            const u64 T = s_T;
+            const float tf = key_float((unsigned)(T >> 32));
+            const int i = t * kBigStageVec + tid;
+            // A vector whose largest element (NaN if it holds one) is not
+            // below T's score may hold a key above T: queue it.
+            bool flag = false;
+            float4 v;
+            if (i < g.nvec) {
+                v = bring[(size_t)st * kBigStageVec + tid];
+                flag = !(max_nan(max_nan(v.x, v.y), max_nan(v.z, v.w)) < tf);
+            }
+            const unsigned bal = __ballot_sync(kFullMask, flag);
+            if (bal) {
+                if (flag) {
+                    const int pos = nq + __popc(bal & lanemask_lt());
+                    qv[pos] = v;
+                    qi[pos] = (unsigned)i;
+                }
+                nq += __popc(bal);
+                if (nq >= 32) drain(32, T);
+            }
+            if (tid == 0) refill(released);
+        }
+        const bool full = __syncthreads_or(hi > (unsigned)kBigKeep);
+        if (s_fail) break;
+        if (tid == 0) refill(consumed);
+        // Empty the queues (at most 31 vectors each, after a cut if the
+        // buffer could not take them), then a cut with limit k leaves the k
+        // best keys.  (No warp appends between a barrier and the next cut's
+        // first barrier, so the cut and the test below read a settled count.)
+        if (full) cut((unsigned)k + kBigSlack);
+        if (nq) drain(nq, s_T);
+        __syncthreads();
+        if (s_cnt >= (unsigned)k) cut((unsigned)k);
+        const int n = (int)kmin(s_cnt, (unsigned)kBigCap);  // k (fewer only if the row were shorter than k)
+        const int L2 = next_pow2(n < 2 ? 2 : n);
+        for (int j = n + tid; j < L2; j += kBigThreads) buf[j] = 0ull;  // below every real key
+        block_sort_smem_desc(buf, L2);
+        for (int j = tid; j < k; j += kBigThreads) {
+            const u64 key = j < n ? buf[j] : 0ull;
+            const unsigned col = 0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull);
+            const unsigned u = (unsigned)(key >> 32);
+            float v;
+            if (col >= (unsigned)cols)
+                v = __int_as_float(0x7fc00000);  // unreachable: the row has at least k elements
+            else if (u == 0x80000000u || u == 0xFFFFFFFFu)
+                v = g.rp[col];  // -0.0 and NaN payloads: the input's bits
+            else
+                v = key_float(u);
+            vals[(size_t)row * k + j] = v;
+            idx[(size_t)row * k + j] = (int32_t)col;
+        }
+        __syncthreads();  // the buffer is reused by the next row
+    }
+    // After a wait gave up, let the copies still in flight land before exit.
+    if (tid == 0)
+        for (unsigned c = consumed; c < s_issued; ++c)
+            if (!mbar_wait(&s_bar[c % kBigStages], (uint32_t)((c / kBigStages) & 1))) break;
+}
+
 }  // namespace
 
 template <int L, bool kMask>
@@ -692,24 +846,39 @@ cudaError_t launch_stream(cudaStream_t s, const float* in, int rows, int cols, i
 
 cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
                         unsigned* status, bool early, int flags) {
-    // k <= 128 streams rows (one warp per row); k > 128 uses one block per row
-    // with shared-memory buffers.
+    // k <= 128 streams rows (one warp per row); k > 128 takes one block per
+    // row with a shared-memory candidate buffer.
     const bool stream = k <= 128;
     const uint8_t* nk = nullptr;
     int32_t* nc = nullptr;
     if (stream && k <= 32) return launch_stream<1, false>(s, in, rows, cols, k, vals, idx, status, early, flags, nk, nc);
     if (stream && k <= 64) return launch_stream<2, false>(s, in, rows, cols, k, vals, idx, status, early, flags, nk, nc);
     if (stream) return launch_stream<4, false>(s, in, rows, cols, k, vals, idx, status, early, flags, nk, nc);
-    const size_t smem = (size_t)kWarps * 2048 * sizeof(u64);
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&topk_rows_smem_kernel<2048>),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    constexpr int kMaxDev = 64;
+    static std::mutex mu;
+    static int grid_cache[kMaxDev] = {};
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
-    if (k <= 128) {
-        const size_t smem256 = (size_t)kWarps * 256 * sizeof(u64);
-        topk_rows_smem_kernel<256><<<rows, kWarps * 32, smem256, s>>>(in, cols, k, vals, idx);
-    } else {
-        topk_rows_smem_kernel<2048><<<rows, kWarps * 32, smem, s>>>(in, cols, k, vals, idx);
+    if (device < 0 || device >= kMaxDev) return cudaErrorInvalidDevice;
+    int full;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (grid_cache[device] == 0) {
+            int sms = 0, per_sm = 0;
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+            if (e != cudaSuccess) return e;
+            const void* fn = reinterpret_cast<const void*>(&topk_rows_big_kernel);
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kBigRingBytes);
+            if (e != cudaSuccess) return e;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kBigThreads, kBigRingBytes);
+            if (e != cudaSuccess) return e;
+            grid_cache[device] = sms * (per_sm < 1 ? 1 : per_sm);
+        }
+        full = grid_cache[device];
     }
+    const int grid = rows < full ? rows : full;
+    topk_rows_big_kernel<<<grid, kBigThreads, kBigRingBytes, s>>>(in, rows, cols, k, vals, idx, status);
     return cudaGetLastError();
 }
 

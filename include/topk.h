@@ -132,7 +132,7 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
  *
  * The selection is a two-stage reduction applied level by level: rows of at
  * least 8k scores give their k best (the row TopK), and their winners, in
- * order, are the next level's candidates (blocks of 8192 keeping their k
+ * order, are the next level's candidates (blocks of 1024 keeping their k
  * best for k <= 128, rows again otherwise) until one block ranks the last
  * at most 4096.  With keep, when
  * n >= 2^20, k <= 128 and keep's address is congruent to score's / 4

@@ -24,7 +24,7 @@
 //            level's candidates.  Equal scores stay in position order: rows
 //            are in position order, and a row's winners with equal scores
 //            come in column order.  For k <= 128 a level is a chunk round
-//            (each block keeps the k best of 8192 candidates, in order);
+//            (each block keeps the k best of 1024 candidates, in order);
 //            larger k take row-kernel levels.  Repeat until at most
 //            kFinalCap candidates are left.
 //   final    one block ranks those; the best k map back to input positions,
@@ -459,20 +459,23 @@ items_final_select_kernel(const float* __restrict__ cv, const int32_t* __restric
     grid_dependency_wait();  // launched early (launch_pdl): the previous kernel's writes first
     // The call's last kernel: its successor must not start before it ends.
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    // Warps whose slots start at or past `count` hold no candidate; they
+    // skip the sort, and no merge takes their (empty) lists.
+    auto live = [&](int warp) { return warp * 32 * kSelN < count; };
     RegList<kSelN, unsigned long long> wl;
 #pragma unroll
     for (int j = 0; j < kSelN; ++j) {
         const int p = w * 32 * kSelN + j * 32 + lane;
         wl.lst[j] = p < count ? items_key(cv[p], (unsigned)p) : 0ull;  // every real key is above 0
     }
-    warp_sort_desc<kSelN>(wl.lst, lane);
+    if (live(w)) warp_sort_desc<kSelN>(wl.lst, lane);
 #pragma unroll 1
     for (int s = 1; s < kSelWarps; s <<= 1) {
-        if ((w & (2 * s - 1)) == s)
+        if ((w & (2 * s - 1)) == s && live(w))
 #pragma unroll
             for (int j = 0; j < kSelN; ++j) s_l[w][j * 32 + lane] = wl.lst[j];
         __syncthreads();
-        if ((w & (2 * s - 1)) == 0) wl.merge_list(s_l[w + s], lane);
+        if ((w & (2 * s - 1)) == 0 && live(w + s)) wl.merge_list(s_l[w + s], lane);
         __syncthreads();
     }
     if (w != 0) return;
@@ -498,18 +501,23 @@ items_final_select_kernel(const float* __restrict__ cv, const int32_t* __restric
 }
 
 // Later levels for k <= 128: block b takes candidates [b * kChunk,
-// (b + 1) * kChunk) -- 32 warps of 256 -- ranks them like the final select
-// (register sort per warp, five pairwise merges) and writes its best ke, in
-// order, at b * ke of the next arrays (pads, -inf and -1, when the chunk has
-// fewer).  Chunks are in array order, so equal scores stay in position
-// order; pads only ever sit at the end of the array, hence in the last
-// chunks, and stay at the end.
+// (b + 1) * kChunk) -- kChunkWarps warps of 256 -- ranks them like the
+// final select (register sort per warp, pairwise merges) and writes its best
+// ke, in order, at b * ke of the next arrays (pads, -inf and -1, when the
+// chunk has fewer).  Chunks are in array order, so equal scores stay in
+// position order; pads only ever sit at the end of the array, hence in the
+// last chunks, and stay at the end.  Small blocks spread a round over every
+// SM (the work is about 10 instructions per candidate, in register sorts).
+// Measured per call on 1e8 scores, k = 64: 129 us with 4 warps per block,
+// 131 with 8, 134 with 2, and 140 with 32 (8192 candidates per block, so
+// the first round had 32 blocks).
 constexpr int kChunkN = 8;                                 // keys per lane
-constexpr int kChunk = kSelWarps * 32 * kChunkN;           // 8192 candidates per block
-__global__ void __launch_bounds__(kSelWarps * 32)
+constexpr int kChunkWarps = 4;
+constexpr int kChunk = kChunkWarps * 32 * kChunkN;         // 1024 candidates per block
+__global__ void __launch_bounds__(kChunkWarps * 32)
 items_select_chunks_kernel(const float* __restrict__ cv, const int32_t* __restrict__ cp, size_t count, int ke,
                            float* __restrict__ nv, int32_t* __restrict__ np) {
-    __shared__ unsigned long long s_l[kSelWarps][32 * kSelN];
+    __shared__ unsigned long long s_l[kChunkWarps][32 * kSelN];
     grid_dependency_wait();  // launched early (launch_pdl): the previous kernel's writes first
     launch_dependents();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -538,7 +546,7 @@ items_select_chunks_kernel(const float* __restrict__ cv, const int32_t* __restri
         }
     }
 #pragma unroll 1
-    for (int s = 1; s < kSelWarps; s <<= 1) {
+    for (int s = 1; s < kChunkWarps; s <<= 1) {
         if ((w & (2 * s - 1)) == s)
 #pragma unroll
             for (int j = 0; j < kSelN; ++j) s_l[w][j * 32 + lane] = wl.lst[j];
@@ -737,7 +745,7 @@ cudaError_t items_launch(cudaStream_t s, const float* score, const int64_t* item
         if (!first && k <= 32 * kSelN) {
             // A chunk round: ceil(len / kChunk) blocks each keep their ke best.
             const size_t nb = (len + kChunk - 1) / kChunk;
-            e = launch_pdl(items_select_chunks_kernel, (unsigned)nb, kSelWarps * 32, 0, s, cur, cur_pos, len, ke,
+            e = launch_pdl(items_select_chunks_kernel, (unsigned)nb, kChunkWarps * 32, 0, s, cur, cur_pos, len, ke,
                            nb_s[flip], nb_p[flip]);
             *launches += 1;
             if (e != cudaSuccess) return e;

@@ -187,9 +187,11 @@ def test_workload_shape_large_k(tk, k, tied):
 
 
 def test_few_long_rows(tk):
+    # 1.5M columns: hundreds of rounds and many cuts per row for k > 128;
+    # row 1 is all equal (the cuts separate keys by column alone).
     x = synth.f32_rows_tied(3, 1_500_001, 11)
     x[1] = np.float32(0.25)
-    for k in (1, 64, 128):
+    for k in (1, 64, 128, 129, 1024):
         assert_rows_equal(tk, x, k)
 
 

@@ -88,8 +88,8 @@ def load_peaks():
 
 KERNEL_SOURCES = {
     "topk_i32_stream_kernel": ("topk_i32.cu", "topk_device.cuh", "topk_internal.h"),
-    "topk_rows_stream_kernel": ("topk_rows.cu", "topk_device.cuh", "topk_internal.h"),
-    "radix_filter_kernel": ("topk_radix.cu", "topk_device.cuh", "topk_internal.h"),
+    "topk_rows_stream_kernel": ("topk_rows.cu", "topk_device.cuh", "topk_internal.h", "topk_sortnet.cuh"),
+    "radix_filter_kernel": ("topk_radix.cu", "topk_device.cuh", "topk_internal.h", "topk_sortnet.cuh"),
 }
 
 

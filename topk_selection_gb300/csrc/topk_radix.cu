@@ -55,6 +55,7 @@
 
 #include "topk_device.cuh"
 #include "topk_internal.h"
+#include "topk_sortnet.cuh"
 
 namespace topk {
 
@@ -823,9 +824,10 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
                 for (unsigned i = tid; i < c; i += kClThreads) all[off + i] = ld_cluster(&S.mysmall[i], (unsigned)r);
                 off += c;
             }
-            const int P = next_pow2(total < 2 ? 2 : (int)total);
+            const int P = next_pow2(total < 64 ? 64 : (int)total);
             for (unsigned i = total + tid; i < (unsigned)P; i += kClThreads) all[i] = 0u;  // below every key > T
-            block_sort_smem_desc(all, P);
+            static_assert(kSmallCap <= 2 * kClThreads, "the register-stage sort takes two keys per thread");
+            block_sort_reg_desc<unsigned, kClThreads>(all, P);
             for (unsigned i = tid; i < total; i += kClThreads) out[i] = value_of(all[i]);
         }
     } else {

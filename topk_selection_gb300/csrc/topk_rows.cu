@@ -27,6 +27,7 @@
 
 #include "topk_device.cuh"
 #include "topk_internal.h"
+#include "topk_sortnet.cuh"
 
 namespace topk {
 
@@ -521,65 +522,6 @@ __device__ __forceinline__ unsigned big_append(const u64 (&kk)[N], u64* buf, uns
     return tot ? base + (unsigned)tot : 0u;
 }
 
-// Bitonic sort, descending, of a[0, L) in shared memory by a block of
-// kBigThreads threads, for L a power of two in [64, 2 * kBigThreads].  Warp
-// w holds elements 64w + lane and 64w + 32 + lane in registers: strides
-// below 32 are lane exchanges (shuffles) and 32 a register exchange, so only
-// strides of 64 and more go through shared memory, each with two barriers
-// (10 such stages for L = 1024, against 55 barriered stages of the plain
-// shared-memory network).  Every thread of the block must call it.
-__device__ void big_sort_desc(u64* a, int L) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const bool act = 64 * w < L;
-    const int e0 = 64 * w + lane, e1 = e0 + 32;
-    u64 x0 = 0ull, x1 = 0ull;
-    __syncthreads();
-    if (act) {
-        x0 = a[e0];
-        x1 = a[e1];
-    }
-    // Strides `from` down to 1 of the merge for sequences of `size`.
-    auto reg_stages = [&](int size, int from) {
-        for (int st = from; st > 0; st >>= 1) {
-            const bool d0 = (e0 & size) == 0, d1 = (e1 & size) == 0;  // descending here
-            if (st == 32) {
-                const u64 hi = kmax(x0, x1), lo = kmin(x0, x1);
-                x0 = d0 ? hi : lo;
-                x1 = d0 ? lo : hi;
-            } else {
-                const u64 y0 = __shfl_xor_sync(kFullMask, x0, st), y1 = __shfl_xor_sync(kFullMask, x1, st);
-                const bool low = (lane & st) == 0;
-                x0 = low == d0 ? kmax(x0, y0) : kmin(x0, y0);
-                x1 = low == d1 ? kmax(x1, y1) : kmin(x1, y1);
-            }
-        }
-    };
-    if (act)
-        for (int size = 2; size <= 64; size <<= 1) reg_stages(size, size >> 1);
-    for (int size = 128; size <= L; size <<= 1) {
-        for (int st = size >> 1; st >= 64; st >>= 1) {
-            if (act) {
-                a[e0] = x0;
-                a[e1] = x1;
-            }
-            __syncthreads();
-            if (act) {
-                const u64 y0 = a[e0 ^ st], y1 = a[e1 ^ st];
-                const bool d0 = (e0 & size) == 0, d1 = (e1 & size) == 0;
-                x0 = ((e0 & st) == 0) == d0 ? kmax(x0, y0) : kmin(x0, y0);
-                x1 = ((e1 & st) == 0) == d1 ? kmax(x1, y1) : kmin(x1, y1);
-            }
-            __syncthreads();
-        }
-        if (act) reg_stages(size, 32);
-    }
-    if (act) {
-        a[e0] = x0;
-        a[e1] = x1;
-    }
-    __syncthreads();
-}
-
 __global__ void __launch_bounds__(kBigThreads, 2)
 topk_rows_big_kernel(const float* __restrict__ in, int rows, int cols, int k, float* __restrict__ vals,
                      int32_t* __restrict__ idx, unsigned* __restrict__ status) {
@@ -837,7 +779,7 @@ topk_rows_big_kernel(const float* __restrict__ in, int rows, int cols, int k, fl
         const int L2 = next_pow2(n < 64 ? 64 : n);
         for (int j = n + tid; j < L2; j += kBigThreads) buf[j] = 0ull;  // below every real key
         if (L2 <= 2 * kBigThreads)
-            big_sort_desc(buf, L2);
+            block_sort_reg_desc<u64, kBigThreads>(buf, L2);
         else
             block_sort_smem_desc(buf, L2);
         for (int j = tid; j < k; j += kBigThreads) {

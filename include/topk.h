@@ -225,7 +225,7 @@ int topk_reduce_f32(const float* in, size_t n, int op, double* out, struct CUstr
  *     block's candidate lists fit (1 MiB holds 239 blocks' worth), so on
  *     GPUs with more SMs this entry point runs fewer blocks than topk_i32;
  *     for larger k the radix select's candidate buffer is what the array
- *     has left (253,824 keys instead of 262,144), so slightly fewer inputs
+ *     has left (252,800 keys instead of 262,144), so slightly fewer inputs
  *     avoid the exact passes.
  *   - Every call uses the same array.  Each call clears the control words
  *     on `stream` before its launch, but calls whose work overlaps on the
@@ -247,6 +247,11 @@ int topk_i32_noalloc(const int32_t* in, size_t n, int k, int32_t* out, struct CU
  * and lets the launch finish, leaving invalid results.  This call reads and
  * clears that word.  Returns TOPK_OK, TOPK_ERR_DEVICE_TIMEOUT or
  * TOPK_ERR_CUDA.
+ *
+ * topk_i32_noalloc has one status word per device, shared by every stream:
+ * a timeout of a no-alloc call on another stream is reported to whichever
+ * caller checks first, and one set while this call runs may be missed.
+ * Synchronise the device first when that matters.
  */
 int topk_check_stream(struct CUstream_st* stream);
 
@@ -283,8 +288,24 @@ int topk_last_cuda_error(void);
 
 /* Free every cached workspace of the calling process (all devices, all
  * streams).  The caller must make sure no TopK work is still running.
- * Returns TOPK_OK or TOPK_ERR_CUDA. */
+ * Workspaces are kept per (device, stream handle) and are not dropped when a
+ * stream is destroyed, so a program that creates and destroys streams in a
+ * loop should call this now and then.  Returns TOPK_OK or TOPK_ERR_CUDA. */
 int topk_release_workspace(void);
+
+/* Whether the last TopK launch this thread enqueued may start while the
+ * previous kernel on its stream finishes (1) or waits for it (0); a
+ * diagnostic for tests of the early-start rule below.
+ *
+ * Early start: the streaming kernels of topk_i32 (k <= 128) and
+ * topk_rows_f32 (k <= 128) are launched with programmatic stream
+ * serialization.  When the previous kernel on the stream is one of those
+ * launches (or the last kernel of topk_i32's large-k plan), the new call
+ * begins reading its input while that launch finishes, provided the input
+ * does not overlap what that launch writes; everything else the call
+ * touches waits for it.  Every other entry point, and a call whose buffers
+ * are host memory, resets this, so the call after it starts normally. */
+int topk_last_launch_early(void);
 
 /* Number of CUDA kernels this library has launched in this process; a
  * diagnostic for benchmarks that count launches. */

@@ -73,6 +73,8 @@ def _load():
     lib.topk_items_f32.restype = ci
     lib.topk_sort_u32.argtypes = [vp, vp, sz, vp, vp, vp]
     lib.topk_sort_u32.restype = ci
+    lib.topk_last_launch_early.argtypes = []
+    lib.topk_last_launch_early.restype = ci
     return lib
 
 
@@ -95,6 +97,12 @@ def release_workspace() -> None:
 
 def launch_count() -> int:
     return int(_lib.topk_launch_count())
+
+
+def last_launch_early() -> bool:
+    """Whether this thread's last TopK launch may start while the previous
+    kernel on its stream finishes (topk_last_launch_early)."""
+    return bool(_lib.topk_last_launch_early())
 
 
 OPT_STAGE2_CAP = 1

@@ -20,6 +20,7 @@ std::atomic<int> g_stage2_cap{0};
 std::atomic<int> g_radix_cap{0};
 std::atomic<int> g_radix_sample_rank{0};
 thread_local int t_last_cuda_error = 0;
+thread_local int t_last_early = 0;  // whether this thread's last TopK launch started early
 
 int cuda_fail(cudaError_t e) {
     t_last_cuda_error = (int)e;
@@ -36,11 +37,13 @@ struct Workspace {
     size_t stage_out_bytes = 0;
     void* items = nullptr;      // topk_items_f32 scratch
     size_t items_bytes = 0;
-    // What the last launch on this stream that lets its successor start
-    // early writes (up to two ranges): a successor that starts early must
-    // not read it.
+    // What the last launch on this stream writes, when that launch lets its
+    // successor start early (up to two ranges): a successor that starts early
+    // must not read it.  After any other launch of this library on the
+    // stream, and before the first one, the record covers all memory, so
+    // that the next launch does not start early.
     const void* stream_out[2] = {nullptr, nullptr};
-    size_t stream_out_bytes[2] = {0, 0};
+    size_t stream_out_bytes[2] = {SIZE_MAX, 0};
     void* sort = nullptr;       // topk_sort_u32 scratch (its header zero between calls)
     size_t sort_bytes = 0;
     unsigned sort_epoch = 0;    // tags the sort's look-back words, one per call
@@ -120,6 +123,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 // inputs are staged by a copy, which never overlaps a kernel.
 bool early_start(Workspace* w, const void* in, size_t in_bytes, const void* a, size_t a_bytes, const void* b,
                  size_t b_bytes) {
+    t_last_early = 0;
     std::lock_guard<std::mutex> lock(g_ws_mutex);
     bool ok = true;
     for (int i = 0; i < 2; ++i) ok = ok && !overlaps(in, in_bytes, w->stream_out[i], w->stream_out_bytes[i]);
@@ -127,7 +131,19 @@ bool early_start(Workspace* w, const void* in, size_t in_bytes, const void* a, s
     w->stream_out_bytes[0] = a_bytes;
     w->stream_out[1] = b;
     w->stream_out_bytes[1] = b_bytes;
+    t_last_early = ok ? 1 : 0;
     return ok;
+}
+
+// Record that the last launch on w's stream does not release its successor
+// early: the next launch there must not start early, whatever it reads.
+void mark_not_released(Workspace* w) {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    w->stream_out[0] = nullptr;
+    w->stream_out_bytes[0] = SIZE_MAX;
+    w->stream_out[1] = nullptr;
+    w->stream_out_bytes[1] = 0;
+    t_last_early = 0;
 }
 
 }  // namespace
@@ -138,6 +154,20 @@ int radix_cap_option() { return g_radix_cap.load(std::memory_order_relaxed); }
 int radix_sample_rank_option() { return g_radix_sample_rank.load(std::memory_order_relaxed); }
 void note_cuda_error(int err) { t_last_cuda_error = err; }
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+void note_unreleased_launch(int device, cudaStream_t s) {
+    Workspace* w = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_ws_mutex);
+        auto it = g_ws.find({device, reinterpret_cast<uintptr_t>(s)});
+        if (it == g_ws.end()) {
+            // A workspace made later starts with a record that covers all memory.
+            t_last_early = 0;
+            return;
+        }
+        w = &it->second;
+    }
+    mark_not_released(w);
+}
 }  // namespace topk
 
 extern "C" {
@@ -193,6 +223,7 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
         // them waits before reading anything): a streaming launch after this
         // one must know what it writes.
         early_start(w, din, 0, dout, (size_t)k * sizeof(int32_t), nullptr, 0);
+        t_last_early = 0;  // every kernel of the plan waits before it reads its input
         e = topk::radix_launch(s, din, n, k, dout, w->ctrl_cand, topk::kRadixCap, &launches, true);
     }
     g_launches.fetch_add((unsigned long long)launches, std::memory_order_relaxed);
@@ -237,6 +268,7 @@ int reduce_common(const void* in, size_t n, int op, void* out, bool is_float, st
         din = w->stage_in;
     }
     if (out_host) dout = w->stage_out;
+    mark_not_released(w);
     e = topk::reduce_launch(s, din, n, is_float, op, dout, w->ctrl_cand);
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -300,6 +332,7 @@ int topk_sort_u32(const uint32_t* keys, const uint32_t* vals, size_t n, uint32_t
     }
     auto* status = reinterpret_cast<unsigned*>(static_cast<char*>(w->ctrl_cand) + topk::kI32StatusOffset);
     int launches = 0;
+    mark_not_released(w);
     e = topk::sort_launch(s, keys, vals, n, keys_out, vals_out, w->sort, epoch, status, &launches);
     g_launches.fetch_add((unsigned long long)launches, std::memory_order_relaxed);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -344,6 +377,7 @@ int topk_items_f32(const float* score, const int64_t* item, const uint8_t* keep,
     if (rc != TOPK_OK) return rc;
     auto* status = reinterpret_cast<unsigned*>(static_cast<char*>(w->ctrl_cand) + topk::kI32StatusOffset);
     int launches = 0;
+    mark_not_released(w);
     e = topk::items_launch(s, score, item, keep, n, k, out_score, out_item, out_count, w->items, w->items_bytes,
                            status, &launches);
     g_launches.fetch_add((unsigned long long)launches, std::memory_order_relaxed);
@@ -394,7 +428,10 @@ int topk_rows_f32(const float* in, int rows, int cols, int k, float* vals, int32
     // The streamed row kernel (k <= 128) starts early and releases its
     // successors like the int32 streaming kernel.
     bool early = false;
-    if (k <= 128) early = early_start(w, din, nin, dvals, nout, didx, nout) && !in_host;
+    if (k <= 128)
+        early = early_start(w, din, nin, dvals, nout, didx, nout) && !in_host;
+    else
+        mark_not_released(w);
     e = topk::rows_launch(s, din, rows, cols, k, dvals, didx, status, early, k <= 128 ? topk::kRowsRelease : 0);
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -476,6 +513,8 @@ const char* topk_status_string(int status) {
 }
 
 int topk_last_cuda_error(void) { return t_last_cuda_error; }
+
+int topk_last_launch_early(void) { return t_last_early; }
 
 int topk_release_workspace(void) {
     std::lock_guard<std::mutex> lock(g_ws_mutex);

@@ -181,4 +181,9 @@ void note_launch();
 // entry point has not run there yet.
 void* noalloc_scratch_if_ready(int device);
 
+// Record, for entry points without a cached workspace, that the last launch
+// on stream s of `device` does not let its successor start early (so the
+// next launch there does not start early either).
+void note_unreleased_launch(int device, cudaStream_t s);
+
 }  // namespace topk

@@ -28,6 +28,9 @@ static_assert(kNoallocScratchBytes >= topk::i32_scratch_bytes(1),
               "the scratch must hold the control words, block maxima, counts and one block's candidates");
 static_assert(kNoallocScratchBytes >= topk::radix_scratch_bytes(TOPK_MAX_K),
               "the radix plan's candidate buffer must hold at least the largest k keys");
+// The candidate buffer of the radix plan here, in keys (the header quotes it).
+constexpr size_t kNoallocRadixCap = (kNoallocScratchBytes - topk::radix_scratch_bytes(0)) / sizeof(unsigned);
+static_assert(kNoallocRadixCap == 252800, "topk.h states this capacity");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -98,10 +101,11 @@ extern "C" int topk_i32_noalloc(const int32_t* in, size_t n, int k, int32_t* out
     if (k > 128) {
         // Large k: radix select, its candidate buffer sized to what the
         // array leaves after the control words and the histogram.
-        const size_t cap = (kNoallocScratchBytes - topk::radix_scratch_bytes(0)) / sizeof(unsigned);
+        const size_t cap = kNoallocRadixCap;
         int launches = 0;
         e = cudaMemsetAsync(static_cast<char*>(scratch) + topk::kI32ResetBegin, 0,
                             topk::kI32ResetEnd - topk::kI32ResetBegin, s);
+        topk::note_unreleased_launch(device, s);
         if (e == cudaSuccess) e = topk::radix_launch(s, in, n, k, out, scratch, cap, &launches, false);
         for (int i = 0; i < launches; ++i) topk::note_launch();
         if (e != cudaSuccess) {
@@ -127,6 +131,9 @@ extern "C" int topk_i32_noalloc(const int32_t* in, size_t n, int k, int32_t* out
     // before the launch (the sticky status word is left alone).
     e = cudaMemsetAsync(static_cast<char*>(scratch) + topk::kI32ResetBegin, 0,
                         topk::kI32ResetEnd - topk::kI32ResetBegin, s);
+    // A launch of this library that follows on the stream must not start
+    // early: it may read this call's output.
+    topk::note_unreleased_launch(device, s);
     if (e == cudaSuccess) e = topk::i32_launch(plan, s, in, n, k, out, scratch, false, false);
     if (e != cudaSuccess) {
         topk::note_cuda_error((int)e);

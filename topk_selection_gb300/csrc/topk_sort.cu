@@ -7,9 +7,10 @@
 //   1. takes the next tile id from a counter (so a tile only ever waits for
 //      tiles whose blocks are already running),
 //   2. ranks its keys stably: per warp, keys go slot by slot (32
-//      consecutive keys per slot) and __match_any_sync groups the lanes
-//      with equal digits, so a key's rank among equal digits follows input
-//      order; warps then add the counts of the warps before them,
+//      consecutive keys per slot); eight ballots, one per digit bit, give
+//      every lane the mask of lanes with its digit (a warp multisplit), so a
+//      key's rank among equal digits follows input order; warps then add the
+//      counts of the warps before them,
 //   3. publishes its per-digit counts and looks back over earlier tiles for
 //      the keys of each digit before it (decoupled look-back: a tile's word
 //      says "my count" or "count of every tile up to me"),

@@ -54,6 +54,50 @@ def build(plant: str | None = None, force: bool = False) -> str:
     return path
 
 
+_FAST_SRC = os.path.join(_HERE, "cpu_fast.cc")
+_FAST_PATH = os.path.join(_LIB_DIR, "libcpu_fast.so")
+_fast_lib = None
+
+
+def build_fast(force: bool = False) -> str:
+    """Compile cpu_fast.cc, the multi-threaded CPU baseline (not an oracle)."""
+    if not force and os.path.exists(_FAST_PATH) and os.path.getmtime(_FAST_PATH) >= os.path.getmtime(_FAST_SRC):
+        return _FAST_PATH
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    tmp = _FAST_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", "-o", tmp, _FAST_SRC], check=True)
+    os.replace(tmp, _FAST_PATH)
+    return _FAST_PATH
+
+
+def fast_topk_i32(x, k: int, threads: int = 0):
+    """The fast CPU baseline (cpu_fast.cc): per-thread std::nth_element over
+    contiguous chunks, then a merge.  Returns (top-k descending, threads
+    used).  Timed by bench.py beside the oracle; never used as a check."""
+    global _fast_lib
+    with _lock:
+        if _fast_lib is None:
+            lib = ctypes.CDLL(build_fast())
+            lib.cpu_fast_topk_i32.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_int]
+            lib.cpu_fast_topk_i32.restype = ctypes.c_int
+            lib.cpu_fast_hardware_threads.argtypes = []
+            lib.cpu_fast_hardware_threads.restype = ctypes.c_int
+            _fast_lib = lib
+    a = np.ascontiguousarray(x, dtype=np.int32).reshape(-1)
+    out = np.empty(max(k, 0), dtype=np.int32)
+    used = _fast_lib.cpu_fast_topk_i32(a.ctypes.data, a.size, int(k), out.ctypes.data, int(threads))
+    if used < 0:
+        raise OracleError(f"cpu_fast_topk_i32 rejected n={a.size} k={k}")
+    return out, int(used)
+
+
+def hardware_threads() -> int:
+    """std::thread::hardware_concurrency() of this host."""
+    fast_topk_i32(np.zeros(1, np.int32), 1)  # loads the library
+    return int(_fast_lib.cpu_fast_hardware_threads())
+
+
 def load(plant: str | None = None):
     with _lock:
         lib = _libs.get(plant)

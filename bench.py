@@ -177,8 +177,10 @@ class Timer:
     """CUDA-event timing of library calls on one stream.
 
     single(fn): one call alone -- the previous work on the stream has
-    finished and L2 holds none of the input (a 512 MiB buffer is written
-    first, outside the timed region); the median over `reps` calls.
+    finished and L2 holds none of the input (a 512 MiB buffer is read
+    first, outside the timed region: reading leaves clean lines in L2, so no
+    write-back of the flush lands in the timed call); the median over `reps`
+    calls.
     pipelined(fn): `reps` calls back to back between two events; the mean per
     call.  Consecutive calls may overlap (a call starts streaming its input
     while the previous one's last block finishes), which is what a stream of
@@ -191,7 +193,7 @@ class Timer:
 
     def flush(self):
         self.flips += 1
-        self.flush_buf.fill_(self.flips & 0xFF)
+        self.sink = torch.sum(self.flush_buf, dtype=torch.int32)
 
     def single(self, fn, reps):
         ts = []

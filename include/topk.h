@@ -272,7 +272,13 @@ enum topk_option {
      * the filter threshold (0 restores the automatic choice).  A rank that
      * is too small makes the filter keep fewer than k keys, and the plan
      * takes the exact radix passes.  For tests of that path only. */
-    TOPK_OPT_RADIX_SAMPLE_RANK = 3
+    TOPK_OPT_RADIX_SAMPLE_RANK = 3,
+    /* Share of the input tiles that topk_i32's streaming plan (k <= 128)
+     * assigns to warps up front, as percent + 1 (1 = none, 101 = all; 0
+     * restores the default).  The other tiles are claimed one at a time
+     * from counters as warps finish, so that fast SMs take the slow ones'
+     * share.  For tests of both schedules; results are the same either way. */
+    TOPK_OPT_STREAM_STATIC = 4
 };
 
 /* Set a process-wide option; takes effect for calls made afterwards.

@@ -311,3 +311,57 @@ def test_workload_1e9(tk, name):
         assert got.tolist() == list(range(10**9 - 1, 10**9 - 21, -1))
     if name == "i32_dup1000_1e9":
         assert got.tolist() == [999] * 20
+
+
+@pytest.mark.parametrize("static", [1, 51, 101])
+def test_tile_schedules(tk, static):
+    # The streaming plan shares out part of the tiles up front and lets warps
+    # claim the rest from 64 counters; all-claimed (1), half (51) and
+    # all-static (101) schedules must give the same exact result, including
+    # sizes with fewer dynamic tiles than counters and a ragged last tile.
+    tk.set_option(tk.OPT_STREAM_STATIC, static)
+    try:
+        for kind, n in (("uniform", 4_194_305), ("ascending", 3_000_001), ("dups", 1_000_003),
+                        ("uniform", 65_537), ("few", 300_007), ("uniform", 25_000_003)):
+            x = make(kind, n, seed=n + static)
+            for k in (1, 20, 64, 128):
+                assert np.array_equal(gpu_topk(tk, x, k), oracle.topk_i32(x, k)), (kind, n, k, static)
+        # Back-to-back calls on one stream reuse the claim counters.
+        x = make("uniform", 9_000_011, seed=5)
+        d = torch.from_numpy(x).cuda()
+        outs = [tk.topk_i32(d, 20) for _ in range(6)]
+        exp = oracle.topk_i32(x, 20)
+        for o in outs:
+            assert np.array_equal(o.cpu().numpy(), exp)
+    finally:
+        tk.set_option(tk.OPT_STREAM_STATIC, 0)
+
+
+def test_few_blocks_many_k(tk):
+    # Inputs small enough that the grid has fewer blocks than k: the second
+    # stage bounds the answer by the k-th largest tile maximum.
+    for kind in KINDS:
+        for n in (40_000, 100_003, 300_007, 900_001):
+            x = make(kind, n, seed=n + 3)
+            for k in (65, 100, 128):
+                assert np.array_equal(gpu_topk(tk, x, k), oracle.topk_i32(x, k)), (kind, n, k)
+
+
+def test_early_start_record(tk):
+    # A streaming call may start early only after a releasing launch whose
+    # output it does not read (topk_last_launch_early reports the decision).
+    s = torch.cuda.Stream()
+    x = torch.from_numpy(synth.i32_uniform(2_000_003, 9)).cuda()
+    with torch.cuda.stream(s):
+        a = tk.topk_i32(x, 64, stream=s)          # first call on this stream
+        assert not tk.last_launch_early()
+        tk.topk_i32(x, 20, stream=s)              # after a releasing launch, independent input
+        assert tk.last_launch_early()
+        b = tk.topk_i32(a, 10, stream=s)          # reads an older call's output, finished before the last one released
+        assert tk.last_launch_early()
+        tk.topk_i32(b, 5, stream=s)               # reads the previous call's output
+        assert not tk.last_launch_early()
+        tk.reduce(x, "sum", stream=s)             # does not release
+        tk.topk_i32(x, 20, stream=s)
+        assert not tk.last_launch_early()
+    s.synchronize()

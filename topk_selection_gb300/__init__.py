@@ -108,6 +108,7 @@ def last_launch_early() -> bool:
 OPT_STAGE2_CAP = 1
 OPT_RADIX_CAP = 2
 OPT_RADIX_SAMPLE_RANK = 3
+OPT_STREAM_STATIC = 4
 
 
 def set_option(option: int, value: int) -> None:

@@ -19,6 +19,7 @@ std::atomic<unsigned long long> g_launches{0};
 std::atomic<int> g_stage2_cap{0};
 std::atomic<int> g_radix_cap{0};
 std::atomic<int> g_radix_sample_rank{0};
+std::atomic<int> g_stream_static{0};
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_early = 0;  // whether this thread's last TopK launch started early
 
@@ -152,6 +153,7 @@ namespace topk {
 int stage2_cap_option() { return g_stage2_cap.load(std::memory_order_relaxed); }
 int radix_cap_option() { return g_radix_cap.load(std::memory_order_relaxed); }
 int radix_sample_rank_option() { return g_radix_sample_rank.load(std::memory_order_relaxed); }
+int stream_static_option() { return g_stream_static.load(std::memory_order_relaxed); }
 void note_cuda_error(int err) { t_last_cuda_error = err; }
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 void note_unreleased_launch(int device, cudaStream_t s) {
@@ -494,6 +496,10 @@ int topk_set_option(int option, int value) {
         case TOPK_OPT_RADIX_SAMPLE_RANK:
             if (value < 0) return TOPK_ERR_INVALID_ARG;
             g_radix_sample_rank.store(value, std::memory_order_relaxed);
+            return TOPK_OK;
+        case TOPK_OPT_STREAM_STATIC:
+            if (value < 0 || value > 101) return TOPK_ERR_INVALID_ARG;
+            g_stream_static.store(value, std::memory_order_relaxed);
             return TOPK_OK;
         default:
             return TOPK_ERR_INVALID_ARG;

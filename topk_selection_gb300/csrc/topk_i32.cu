@@ -73,14 +73,22 @@ struct Scratch {
     unsigned* status;  // sticky error bits (kStatusWaitTimeout)
     I32Ctrl* ctrl;
     unsigned* bmax;    // per-block running maxima, biased
+    unsigned char* dyn;  // tile-claim counters, one per kI32DynStride bytes
     int32_t* counts;   // per list: entries above the grid threshold at the block's end
+    int32_t* tmax;     // per tile: its maximum (grids with fewer blocks than k)
     int32_t* cand;     // per block: its sorted candidate lists
 };
 
 __device__ __forceinline__ Scratch scratch_view(unsigned char* base) {
     return Scratch{reinterpret_cast<unsigned*>(base + kI32StatusOffset), reinterpret_cast<I32Ctrl*>(base + kI32CtrlOffset),
-                   reinterpret_cast<unsigned*>(base + kI32BmaxOffset), reinterpret_cast<int32_t*>(base + kI32CountOffset),
+                   reinterpret_cast<unsigned*>(base + kI32BmaxOffset), base + kI32DynOffset,
+                   reinterpret_cast<int32_t*>(base + kI32CountOffset),
+                   reinterpret_cast<int32_t*>(base + kI32TileMaxOffset),
                    reinterpret_cast<int32_t*>(base + kI32CandOffset)};
+}
+
+__device__ __forceinline__ unsigned* dyn_counter(const Scratch& sc, int c) {
+    return reinterpret_cast<unsigned*>(sc.dyn + (size_t)c * kI32DynStride);
 }
 
 // Input split: an unaligned head (< 4 elements), a 16-byte aligned body of
@@ -153,10 +161,39 @@ __device__ __forceinline__ void enqueue(int* q, int& nq, int v, int t, int lane)
 // Run by the last block to finish.  `room` ints of shared memory at `list`;
 // cap_limit > 0 lowers the list capacity (to exercise the radix-select path).
 __device__ void second_stage(const Scratch& sc, int k, int lists_per_block, int K, int32_t* __restrict__ out,
-                             int* list, int room, int cap_limit, int* s_count) {
+                             int* list, int room, int cap_limit, int* s_count, int ntmax) {
     const int lane = threadIdx.x & 31;
     __threadfence();
-    const int tg = unbias(ld_relaxed_gpu(&sc.ctrl->thresh));
+    int tg = unbias(ld_relaxed_gpu(&sc.ctrl->thresh));
+    if (ntmax >= k) {
+        // The k-th largest tile maximum: k distinct tiles each hold an
+        // element at least that large, so it is a valid threshold too, and
+        // with few blocks per k it is far tighter than the blocks' own.
+        // Bit by bit from the top: the largest u with at least k tile maxima
+        // (biased) >= u.
+        __shared__ int s_cnt;
+        unsigned tm[kI32MaxTileMax / 256];
+#pragma unroll
+        for (int q = 0; q < kI32MaxTileMax / 256; ++q) {
+            const int t = q * (int)blockDim.x + (int)threadIdx.x;
+            tm[q] = t < ntmax ? bias(__ldcg(sc.tmax + t)) : 0u;
+        }
+        unsigned ans = 0;
+        for (int bit = 31; bit >= 0; --bit) {
+            const unsigned cand = ans | (1u << bit);
+            int c = 0;
+#pragma unroll
+            for (int q = 0; q < kI32MaxTileMax / 256; ++q) c += tm[q] >= cand ? 1 : 0;
+            if (threadIdx.x == 0) s_cnt = 0;
+            __syncthreads();
+            c = __reduce_add_sync(kFullMask, c);
+            if (lane == 0 && c) atomicAdd(&s_cnt, c);
+            __syncthreads();
+            if (s_cnt >= k) ans = cand;
+            __syncthreads();
+        }
+        tg = kmax(tg, unbias(ans));
+    }
     // The list is bitonic-sorted in place at a power-of-two length, so its
     // capacity is the largest power of two that fits.
     int cap = 1;
@@ -267,6 +304,7 @@ __device__ void second_stage(const Scratch& sc, int k, int lists_per_block, int 
     }
     // Leave the scratch as the next launch expects it.
     for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) sc.bmax[i] = 0u;
+    for (int c = threadIdx.x; c < kI32DynRanges; c += blockDim.x) *dyn_counter(sc, c) = 0u;
     if (threadIdx.x == 0) {
         sc.ctrl->thresh = 0u;
         sc.ctrl->ticket = 0u;
@@ -319,17 +357,20 @@ constexpr int kStreamThreads = (kCons + 1) * 32;
 constexpr int kWarpStages = 3;               // tiles in flight per consumer warp
 constexpr int kRingBytes = kCons * kWarpStages * kTileVec * 16;
 constexpr int kMonitorRounds = 1 << 20;      // bound on the monitor's polling rounds
+constexpr int kStaticPct = 70;               // share of the tiles assigned up front (percent)
+static_assert(kStreamThreads >= kI32MaxTileMax / 4, "second stage: four tile maxima per thread at most");
 
 template <int L, int GL>
 __global__ void __launch_bounds__(kStreamThreads, 2)
 topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* __restrict__ out,
-                       unsigned char* __restrict__ scratch, int cap_limit, int release) {
+                       unsigned char* __restrict__ scratch, int cap_limit, int release, int static_pct) {
     constexpr int K = 32 * L;
     extern __shared__ __align__(128) int4 ring[];             // per-warp stages; later the stage-2 list
     __shared__ __align__(16) int s_queue[kCons * kQueue];      // survivor queues, then the merge area
     __shared__ int s_sel[256];                                 // monitor: block maxima above t
     __shared__ __align__(8) uint64_t full_bar[kCons * kWarpStages];
     __shared__ int s_thresh, s_cmax, s_done, s_last, s_count;
+    __shared__ int s_tile[kCons * kWarpStages];                // tile id of each stage's copy
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -346,7 +387,24 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
     const Split sp = split_input(in, n);
     const size_t G = gridDim.x;
     const size_t b = blockIdx.x;
-    const size_t J = b < sp.ntiles ? (sp.ntiles - b + G - 1) / G : 0;  // tiles of this block: b + j*G
+    // Tile schedule.  Rounds [0, R): consumer warp w of block b takes tile
+    // b + G*(w + kCons*i) in round i, so the first S = R*G*kCons tiles are
+    // shared out up front, with no atomics and before the previous launch on
+    // the stream has finished.  Tiles [S, ntiles) are cut into nr contiguous
+    // ranges, each with a claim counter; a warp that has used up its static
+    // tiles claims one tile at a time, from its own range first and then
+    // from any range that has tiles left.  Fast warps (and SMs) so take more
+    // tiles than slow ones, and all warps finish at about the same time.
+    // Tile ids fit 32 bits: n <= 2^40 elements is at most 2^30 tiles.
+    const unsigned ntiles = (unsigned)sp.ntiles;
+    const unsigned per_round = (unsigned)G * kCons;
+    const unsigned R = (unsigned)(((unsigned long long)ntiles * (unsigned)static_pct / 100) / per_round);
+    const unsigned S = R * per_round;
+    const unsigned D = ntiles - S;
+    const int nr = D < (unsigned)kI32DynRanges ? (int)D : kI32DynRanges;
+    // With fewer blocks than k, the k-th largest tile maximum bounds the
+    // answer instead of the blocks' maxima (second stage).
+    const bool use_tmax = (int)G < k && ntiles <= (unsigned)kI32MaxTileMax;
     // The block-maxima threshold needs at least k blocks.
     const bool use_bmax = (int)G >= k;
 
@@ -458,32 +516,110 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
             enqueue(q, nq, (size_t)lane < ns ? in[pos] : INT_MIN, INT_MIN, lane);
         }
 
-        // This warp's tiles are j = warp + i*kCons (i = 0, 1, ...), tile
-        // b + j*G; tile i goes through stage i % kWarpStages.
+        // The warp's i-th tile goes through stage i % kWarpStages; s_tile
+        // holds the tile id of each stage's copy.
         int4* my_ring = ring + (size_t)warp * kWarpStages * kTileVec;
         uint64_t* my_bar = full_bar + warp * kWarpStages;
-        const size_t my_tiles = (size_t)warp < J ? (J - warp + kCons - 1) / kCons : 0;
-        auto issue = [&](size_t i) {  // lane 0 only
-            const size_t base = (b + (warp + i * kCons) * G) * kTileVec;
-            const size_t cnt = sp.nvec - base < (size_t)kTileVec ? sp.nvec - base : (size_t)kTileVec;
-            const int st = (int)(i % kWarpStages);
-            mbar_arrive_expect_tx(&my_bar[st], (uint32_t)(cnt * 16));
-            // Default L2 policy: an evict-first hint measured ~1.5% slower
-            // here (one launch per call, nothing after it to protect).
-            bulk_copy_g2s(my_ring + (size_t)st * kTileVec, sp.body + base, (uint32_t)(cnt * 16), &my_bar[st]);
+        int* my_tile = s_tile + warp * kWarpStages;
+        unsigned static_i = 0;   // static rounds used
+        int cur = nr > 0 ? (int)(((unsigned)b * kCons + (unsigned)warp) % (unsigned)nr) : 0;  // range claimed from
+        bool done = false;       // no tile left anywhere
+        bool waited = false;     // grid dependency waited for (the counters are the previous launch's until then)
+        auto range_lo = [&](int c) -> unsigned {
+            return S + (unsigned)((unsigned long long)D * (unsigned)c / (unsigned)nr);
         };
-        if (lane == 0)
-            for (size_t i = 0; i < my_tiles && i < (size_t)kWarpStages; ++i) issue(i);
+        // A claim in two steps, so that the atomic's round trip overlaps other
+        // work: start_claim returns a static tile, or -1, or (kCounter) says
+        // that lane 0 holds a counter value in `got`; finish_claim turns that
+        // into a tile id, or -1 when every range is used up.
+        constexpr int kCounter = -2;
+        unsigned got = 0;
+        auto start_claim = [&]() -> int {
+            if (static_i < R) {
+                const unsigned t = (unsigned)b + (unsigned)G * ((unsigned)warp + kCons * static_i);
+                ++static_i;
+                return (int)t;
+            }
+            if (done || nr == 0) return -1;
+            if (!waited) {
+                grid_dependency_wait();
+                waited = true;
+            }
+            if (lane == 0) got = atomicAdd(dyn_counter(sc, cur), 1u);
+            return kCounter;
+        };
+        auto finish_claim = [&](int raw) -> int {
+            if (raw != kCounter) return raw;
+            for (int tries = 0; tries <= 2 * kI32DynRanges + 2; ++tries) {
+                got = __shfl_sync(kFullMask, got, 0);
+                const unsigned lo = range_lo(cur), len = range_lo(cur + 1) - lo;
+                if (got < len) return (int)(lo + got);
+                // Range `cur` is used up (for good: its counter only grows).
+                // Read every counter once and move to the first range after
+                // it, cyclically, that still has tiles.
+                unsigned word[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = h * 32 + lane;
+                    bool left = false;
+                    if (c < nr) left = ld_relaxed_gpu(dyn_counter(sc, c)) < range_lo(c + 1) - range_lo(c);
+                    word[h] = __ballot_sync(kFullMask, left);
+                }
+                const unsigned long long has = ((unsigned long long)word[1] << 32) | word[0];
+                const unsigned long long after = cur < 63 ? has & (~0ull << (cur + 1)) : 0ull;
+                const unsigned long long pickm = after ? after : has;
+                if (pickm == 0ull) {
+                    done = true;
+                    return -1;
+                }
+                cur = __ffsll((long long)pickm) - 1;
+                if (lane == 0) got = atomicAdd(dyn_counter(sc, cur), 1u);
+            }
+            // Not reachable: each failed try finds one more range used up.
+            if (lane == 0) atomicOr(sc.status, kStatusWaitTimeout);
+            done = true;
+            return -1;
+        };
+        auto issue = [&](unsigned i, int tile) {  // whole warp; lane 0 copies
+            const int st = (int)(i % kWarpStages);
+            if (lane == 0) {
+                my_tile[st] = tile;
+                const size_t base = (size_t)tile * kTileVec;
+                const size_t cnt = sp.nvec - base < (size_t)kTileVec ? sp.nvec - base : (size_t)kTileVec;
+                mbar_arrive_expect_tx(&my_bar[st], (uint32_t)(cnt * 16));
+                // Default L2 policy: an evict-first hint measured ~1.5% slower
+                // here (one launch per call, nothing after it to protect).
+                bulk_copy_g2s(my_ring + (size_t)st * kTileVec, sp.body + base, (uint32_t)(cnt * 16), &my_bar[st]);
+            }
+            __syncwarp();
+        };
+        if (use_tmax && !waited) {  // tile maxima go to the scratch
+            grid_dependency_wait();
+            waited = true;
+        }
+
+        unsigned issued = 0;
+        while (issued < (unsigned)kWarpStages) {
+            const int t = finish_claim(start_claim());
+            if (t < 0) break;
+            issue(issued++, t);
+        }
+        int pending = issued == (unsigned)kWarpStages ? start_claim() : -1;
 
         bool first = true;
-        size_t i = 0;
-        for (; i < my_tiles; ++i) {
+        unsigned i = 0;
+        for (; i < issued; ++i) {
             const int stg = (int)(i % kWarpStages);
             if (!mbar_wait(&my_bar[stg], (uint32_t)((i / kWarpStages) & 1))) {
                 if (lane == 0) atomicOr(sc.status, kStatusWaitTimeout);
+                // A claim in progress must not be lost: finish it and give
+                // its tile to nobody (the status word marks the result bad).
+                finish_claim(pending);
+                pending = -1;
                 break;
             }
-            const size_t base = (b + (warp + i * kCons) * G) * kTileVec;
+            const unsigned tile = (unsigned)my_tile[stg];
+            const size_t base = (size_t)tile * kTileVec;
             const size_t cnt = sp.nvec - base < (size_t)kTileVec ? sp.nvec - base : (size_t)kTileVec;
             const int4* st = my_ring + (size_t)stg * kTileVec;
             int4 r[kU];
@@ -497,10 +633,16 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
                                                          : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
             }
             __syncwarp();
-            // The tile is in registers: re-arm its stage with tile i + kWarpStages.
-            if (lane == 0 && i + kWarpStages < my_tiles) {
-                fence_proxy_async_smem();
-                issue(i + kWarpStages);
+            // The tile is in registers: re-arm its stage with the next tile
+            // (claimed one tile earlier), and start the claim after that.
+            {
+                const int t = finish_claim(pending);
+                pending = -1;
+                if (t >= 0) {
+                    if (lane == 0) fence_proxy_async_smem();
+                    issue(issued++, t);
+                    pending = start_claim();
+                }
             }
 
             if (first) {
@@ -518,6 +660,7 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
 #pragma unroll
             for (int u = 0; u < kU; ++u) m = kmax(m, max4(r[u]));
             const int wm = __reduce_max_sync(kFullMask, m);
+            if (use_tmax && lane == 0) sc.tmax[tile] = wm;
             if (wm > pushed_max) {
                 if (lane == 0) atomicMax(&s_cmax, wm);
                 pushed_max = wm;
@@ -538,7 +681,7 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
 
         // After an early exit, let the copies this warp issued land before
         // the block moves on.
-        for (size_t w2 = i + 1; w2 < my_tiles && w2 < i + kWarpStages; ++w2)
+        for (unsigned w2 = i + 1; w2 < issued; ++w2)
             if (!mbar_wait(&my_bar[w2 % kWarpStages], (uint32_t)((w2 / kWarpStages) & 1))) break;
         drain(true);
         if (lane == 0) atomicAdd(&s_done, 1);
@@ -586,7 +729,7 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
     // monitor managed to do.
     if (block_done(sc, kmax(s_thresh, block_kth), &s_last))
         second_stage(sc, k, 1, K, out, reinterpret_cast<int*>(ring), kRingBytes / (int)sizeof(int), cap_limit,
-                     &s_count);
+                     &s_count, use_tmax ? (int)sp.ntiles : 0);
 }
 
 // ------------------------------------------------------------ host side --
@@ -601,7 +744,7 @@ struct StreamVariant {
     // of that kernel's blocks have read their input, and overlap its last
     // block's second stage; every access to the shared scratch waits for it.
     static cudaError_t launch(int grid, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
-                              unsigned char* scratch, int cap_limit, bool early, bool release) {
+                              unsigned char* scratch, int cap_limit, bool early, bool release, int static_pct) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid);
         cfg.blockDim = dim3(kThreads);
@@ -613,7 +756,7 @@ struct StreamVariant {
         cfg.attrs = attr;
         cfg.numAttrs = early ? 1 : 0;
         return cudaLaunchKernelEx(&cfg, topk_i32_stream_kernel<L, GL>, in, n, k, out, scratch, cap_limit,
-                                  release ? 1 : 0);
+                                  release ? 1 : 0, static_pct);
     }
     static size_t units_per_block() { return kCons; }
 };
@@ -670,6 +813,8 @@ cudaError_t plan_for(int device, size_t n, I32Plan* plan) {
     plan->grid = (int)grid;
     plan->max_grid = (int)full;
     plan->stage2_cap = stage2_cap_option();
+    const int opt = stream_static_option();
+    plan->static_pct = opt > 0 ? opt - 1 : kStaticPct;
     return cudaSuccess;
 }
 
@@ -684,10 +829,10 @@ cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan) {
 cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
                        void* scratch, bool early, bool release) {
     auto* sc = static_cast<unsigned char*>(scratch);
-    const int cap = plan.stage2_cap;
-    if (k <= 32) return VarK32::launch(plan.grid, s, in, n, k, out, sc, cap, early, release);
-    if (k <= 64) return VarK64::launch(plan.grid, s, in, n, k, out, sc, cap, early, release);
-    return VarK128::launch(plan.grid, s, in, n, k, out, sc, cap, early, release);
+    const int cap = plan.stage2_cap, sp = plan.static_pct;
+    if (k <= 32) return VarK32::launch(plan.grid, s, in, n, k, out, sc, cap, early, release, sp);
+    if (k <= 64) return VarK64::launch(plan.grid, s, in, n, k, out, sc, cap, early, release, sp);
+    return VarK128::launch(plan.grid, s, in, n, k, out, sc, cap, early, release, sp);
 }
 
 }  // namespace topk

@@ -27,13 +27,15 @@ struct I32Ctrl {
 //   [256, 512)                   control words: I32Ctrl (streaming) or the
 //                                radix control words
 //   [512, 512 + 8*4096)          streaming: per-block running maxima (first
-//                                4 KiB); radix: the global 12-bit digit
+//                                4 KiB), then the tile-claim counters (64 x
+//                                128 bytes); radix: the global 12-bit digit
 //                                histogram (64-bit counts)
 //   -- everything above is zero between launches: [kI32ResetBegin, kI32ResetEnd) --
 //   [kRadixCandOffset, +4096)    radix: the range table the cluster kernel
 //                                leaves for the sort kernel
 //   [kRadixBufOffset, ...)       radix: the candidate buffer (cap keys)
-//   [kI32CountOffset, +4*8192)   streaming: per-list survivor counts
+//   [kI32CountOffset, +4*8192)   streaming: per-list survivor counts (the
+//                                first 1024), then tile maxima (1024)
 //   [kI32CandOffset, ...)        streaming: per block, its candidate lists
 //                                (up to kI32CandPerBlock ints)
 // The last two areas overlap the radix buffer; none of them needs any value
@@ -56,6 +58,20 @@ constexpr size_t kI32CandOffset =
     kI32CountOffset + (size_t)kI32MaxGrid * kI32MaxListsPerBlock * sizeof(int32_t);
 constexpr int kRadixMaxK = 32768;
 static_assert(kI32BmaxOffset + kI32MaxGrid * sizeof(unsigned) <= kI32ResetEnd, "block maxima are reset");
+// Streaming plan: the tile-claim counters of the dynamic part of the
+// schedule, one per 128-byte line (zero between launches), ...
+constexpr int kI32DynRanges = 64;  // two warp-wide words of ballots
+constexpr size_t kI32DynStride = 128;
+constexpr size_t kI32DynOffset = kI32BmaxOffset + kI32MaxGrid * sizeof(unsigned);
+static_assert(kI32DynOffset + kI32DynRanges * kI32DynStride <= kI32ResetEnd, "claim counters are reset");
+// ... and, when the grid has fewer blocks than k, every tile's maximum
+// (written before it is read; at most kI32MaxTileMax tiles), after the
+// per-list counts of kI32MaxGrid lists.
+constexpr int kI32MaxTileMax = 1024;
+constexpr size_t kI32TileMaxOffset = kI32ResetEnd + (size_t)kI32MaxGrid * sizeof(int32_t);
+static_assert(kI32TileMaxOffset + kI32MaxTileMax * sizeof(int32_t) <=
+                  kI32ResetEnd + (size_t)kI32MaxGrid * kI32MaxListsPerBlock * sizeof(int32_t),
+              "tile maxima sit in the unused part of the per-list counts");
 static_assert(kRadixCandOffset % 256 == 0 && kRadixBufOffset % 256 == 0 && kI32CountOffset % 256 == 0 &&
                   kI32CandOffset % 256 == 0,
               "area alignment");
@@ -95,10 +111,13 @@ struct I32Plan {
     int grid;        // blocks launched (<= kI32MaxGrid)
     int max_grid;    // persistent grid size for this device (blocks per SM x SMs), <= kI32MaxGrid
     int stage2_cap;  // 0, or a lower capacity for the second stage's shared list (TOPK_OPT_STAGE2_CAP)
+    int static_pct;  // share of the tiles, in percent, assigned statically; the rest are claimed
 };
 
 // Current value of TOPK_OPT_STAGE2_CAP (0 = default).
 int stage2_cap_option();
+// Current value of TOPK_OPT_STREAM_STATIC (0 = default, else percent + 1).
+int stream_static_option();
 
 // Grid for an n-element, k-wide selection on `device` (k <= 128: the
 // streaming plan; larger k use radix_launch).

@@ -30,7 +30,8 @@ _libs: dict = {}
 # reject them.  The plain build defines none of these.
 PLANTED = ("ORACLE_PLANT_ASCENDING", "ORACLE_PLANT_DEDUP", "ORACLE_PLANT_UNSTABLE",
            "ORACLE_PLANT_NAN_LOW", "ORACLE_PLANT_SIGNED_ZERO", "ORACLE_PLANT_SUM_WRAP", "ORACLE_PLANT_ZERO_ORDER",
-           "ORACLE_PLANT_KEEP_IGNORED", "ORACLE_PLANT_SORT_UNSTABLE")
+           "ORACLE_PLANT_KEEP_IGNORED", "ORACLE_PLANT_SORT_UNSTABLE", "ORACLE_PLANT_U32_SIGNED",
+           "ORACLE_PLANT_F32_SIGNED_BITS", "ORACLE_PLANT_NAN_PAYLOAD")
 
 
 def _lib_path(plant):
@@ -118,6 +119,10 @@ def load(plant: str | None = None):
             lib.oracle_topk_items_f32.restype = ci
             lib.oracle_sort_u32.argtypes = [vp, vp, sz, vp, vp]
             lib.oracle_sort_u32.restype = ci
+            lib.oracle_topk_u32.argtypes = [vp, sz, ci, vp]
+            lib.oracle_topk_u32.restype = ci
+            lib.oracle_topk_f32.argtypes = [vp, sz, ci, vp]
+            lib.oracle_topk_f32.restype = ci
             _libs[plant] = lib
     return lib
 
@@ -133,6 +138,27 @@ def topk_i32(x, k: int, plant: str | None = None) -> np.ndarray:
     rc = load(plant).oracle_topk_i32(a.ctypes.data, a.size, int(k), out.ctypes.data)
     if rc != 0:
         raise OracleError(f"oracle_topk_i32 rejected n={a.size} k={k}")
+    return out
+
+
+def topk_u32(x, k: int, plant: str | None = None) -> np.ndarray:
+    """The k largest values of uint32 array ``x``, sorted descending."""
+    a = np.ascontiguousarray(x, dtype=np.uint32).reshape(-1)
+    out = np.empty(max(k, 0), dtype=np.uint32)
+    rc = load(plant).oracle_topk_u32(a.ctypes.data, a.size, int(k), out.ctypes.data)
+    if rc != 0:
+        raise OracleError(f"oracle_topk_u32 rejected n={a.size} k={k}")
+    return out
+
+
+def topk_f32(x, k: int, plant: str | None = None) -> np.ndarray:
+    """The k largest values of float32 array ``x`` under IEEE 754 totalOrder,
+    sorted descending (bits copied; -0 below +0, NaNs by sign and payload)."""
+    a = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    out = np.empty(max(k, 0), dtype=np.float32)
+    rc = load(plant).oracle_topk_f32(a.ctypes.data, a.size, int(k), out.ctypes.data)
+    if rc != 0:
+        raise OracleError(f"oracle_topk_f32 rejected n={a.size} k={k}")
     return out
 
 

@@ -72,9 +72,81 @@ bool ranks_above(float a, float b) {
 }
 #endif
 
+// IEEE 754 totalOrder, strictly: x comes before y in ascending order.  It
+// orders every float bit pattern: -NaN (by payload, larger payloads lower)
+// < -inf < ... < -0 < +0 < ... < +inf < +NaN (larger payloads higher).
+// It is the order the "GPU radix sort" page's float bit transform gives
+// (extensions section: flip every bit of a negative float, only the sign
+// bit of a positive one, then compare as unsigned integers); written here
+// from the standard's definition, not through that transform.
+bool total_less(float x, float y) {
+    const bool nx = std::isnan(x), ny = std::isnan(y);
+    const bool sx = std::signbit(x), sy = std::signbit(y);
+    if (!nx && !ny) {
+        if (x < y) return true;
+        if (x > y) return false;
+        return sx && !sy;  // numerically equal: only -0 < +0 differ
+    }
+    if (nx && ny) {
+        if (sx != sy) return sx;  // -NaN < +NaN
+        uint32_t px, py;
+        std::memcpy(&px, &x, 4);
+        std::memcpy(&py, &y, 4);
+        px &= 0x7FFFFFu;
+        py &= 0x7FFFFFu;
+#if defined(ORACLE_PLANT_NAN_PAYLOAD)
+        return px < py;  // planted mistake: negative NaNs ordered like positive ones
+#else
+        return sx ? px > py : px < py;
+#endif
+    }
+    if (nx) return sx;  // -NaN below every number, +NaN above
+    return !sy;         // y is a NaN
+}
+
 }  // namespace
 
 extern "C" {
+
+// The k largest of the uint32 values in[0..n) (unsigned order), sorted
+// descending, written to out[0..k): the TopK of topk_i32 with unsigned keys.
+// Returns 0, or -1 for invalid arguments.
+int oracle_topk_u32(const uint32_t* in, size_t n, int k, uint32_t* out) {
+    if (!in || !out || n == 0 || k < 1 || (size_t)k > n) return -1;
+#if defined(ORACLE_PLANT_U32_SIGNED)
+    std::vector<int32_t> v(n);  // planted mistake: compared as signed
+    std::memcpy(v.data(), in, n * 4);
+    std::sort(v.begin(), v.end(), std::greater<int32_t>());
+    std::memcpy(out, v.data(), (size_t)k * 4);
+#else
+    std::vector<uint32_t> v(in, in + n);
+    std::sort(v.begin(), v.end(), std::greater<uint32_t>());
+    std::copy(v.begin(), v.begin() + k, out);
+#endif
+    return 0;
+}
+
+// The k largest float32 values of in[0..n) under IEEE 754 totalOrder (see
+// total_less), sorted descending, their bits copied to out[0..k).  Every bit
+// pattern is its own key, so the output multiset is unique.
+// Returns 0, or -1 for invalid arguments.
+int oracle_topk_f32(const float* in, size_t n, int k, float* out) {
+    if (!in || !out || n == 0 || k < 1 || (size_t)k > n) return -1;
+    std::vector<float> v(in, in + n);
+#if defined(ORACLE_PLANT_F32_SIGNED_BITS)
+    // planted mistake: raw bits compared as signed integers (negatives reversed)
+    std::sort(v.begin(), v.end(), [](float a, float b) {
+        int32_t x, y;
+        std::memcpy(&x, &a, 4);
+        std::memcpy(&y, &b, 4);
+        return x > y;
+    });
+#else
+    std::sort(v.begin(), v.end(), [](float a, float b) { return total_less(b, a); });
+#endif
+    std::memcpy(out, v.data(), (size_t)k * 4);
+    return 0;
+}
 
 // The k largest values of in[0..n), sorted descending, written to out[0..k).
 // Returns 0, or -1 for invalid arguments (nothing written).

@@ -51,3 +51,16 @@ def bits(a):
 
 def f32_from_bits(u):
     return struct.unpack("<f", struct.pack("<I", u & 0xFFFFFFFF))[0]
+
+
+def u32_cases():
+    for inp, k, exp in _lines("topk_u32_hand.txt"):
+        yield (np.array([int(v) for v in inp.split()], dtype=np.uint32), int(k),
+               np.array([int(v) for v in exp.split()], dtype=np.uint32))
+
+
+def f32_cases():
+    """(input patterns, k, expected patterns), all uint32 bit patterns."""
+    for inp, k, exp in _lines("topk_f32_hand.txt"):
+        yield (np.array([int(v, 16) for v in inp.split()], dtype=np.uint32), int(k),
+               np.array([int(v, 16) for v in exp.split()], dtype=np.uint32))

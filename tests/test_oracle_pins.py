@@ -24,7 +24,7 @@ import numpy as np
 import pytest
 
 import oracle
-from _golden import bits, i32_cases, items_cases, reduce_cases, rows_cases
+from _golden import bits, f32_cases, i32_cases, items_cases, reduce_cases, rows_cases, u32_cases
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
@@ -283,7 +283,68 @@ def pin_sort_numpy(plant=None):
         assert np.array_equal(ko2, keys[order]) and vo2 is None
 
 
-ALL_PINS = [pin_golden_i32, pin_golden_rows, pin_exhaustive_i32, pin_exhaustive_rows,
+U32_ALPHABET = [0, 1, 2**31 - 1, 2**31, 2**32 - 1]
+# Bit patterns: -qNaN payload 1, -qNaN, -inf, -1, -denormal, -0, +0, +denormal, 1, +inf, +qNaN, +qNaN payload 1
+F32_PATTERNS = [0xFFC00001, 0xFFC00000, 0xFF800000, 0xBF800000, 0x80000001, 0x80000000, 0x00000000,
+                0x00000001, 0x3F800000, 0x7F800000, 0x7FC00000, 0x7FC00001]
+
+
+def total_order_key(b):
+    """IEEE 754 totalOrder as a sort key on a float32 bit pattern, written
+    from the standard's description: every non-negative-signed datum above
+    every negative-signed one; within a sign, order by magnitude (the
+    exponent and significand read as one unsigned number, NaN payloads
+    beyond infinity), reversed for the negative sign."""
+    mag = b & 0x7FFFFFFF
+    return (1, mag) if b >> 31 == 0 else (0, -mag)
+
+
+def pin_golden_u32(plant=None):
+    for x, k, exp in u32_cases():
+        assert oracle.topk_u32(x, k, plant=plant).tolist() == exp.tolist(), (x.tolist(), k)
+
+
+def pin_golden_f32(plant=None):
+    for xb, k, expb in f32_cases():
+        got = oracle.topk_f32(xb.view(np.float32), k, plant=plant)
+        assert bits(got).tolist() == expb.tolist(), ([hex(v) for v in xb], k)
+
+
+def pin_exhaustive_u32(plant=None, max_n=5):
+    for n in range(1, max_n + 1):
+        for combo in itertools.product(U32_ALPHABET, repeat=n):
+            x = np.array(combo, dtype=np.uint32)
+            for k in range(1, n + 1):
+                assert oracle.topk_u32(x, k, plant=plant).tolist() == brute_topk_i32(combo, k), (combo, k)
+
+
+def pin_exhaustive_f32(plant=None, max_n=3):
+    for n in range(1, max_n + 1):
+        for combo in itertools.product(F32_PATTERNS, repeat=n):
+            xb = np.array(combo, dtype=np.uint32)
+            exp = sorted(combo, key=total_order_key, reverse=True)
+            for k in range(1, n + 1):
+                got = bits(oracle.topk_f32(xb.view(np.float32), k, plant=plant)).tolist()
+                assert got == exp[:k], ([hex(v) for v in combo], k)
+
+
+def pin_numpy_u32_f32(plant=None):
+    rng = np.random.default_rng(11)
+    u = rng.integers(0, 2**32, size=60_000, dtype=np.uint64).astype(np.uint32)
+    for k in (1, 7, 1000, u.size):
+        assert np.array_equal(oracle.topk_u32(u, k, plant=plant), np.sort(u)[::-1][:k])
+    # Numbers only, no zeros and no NaN: totalOrder is numeric order there,
+    # so numpy's sort decides.  Magnitudes from denormal to large.
+    f = (rng.standard_normal(60_000) * np.exp(rng.uniform(-100, 80, 60_000))).astype(np.float32)
+    f = f[f != 0]
+    for k in (1, 13, 2000, f.size):
+        assert np.array_equal(bits(oracle.topk_f32(f, k, plant=plant)), bits(np.sort(f)[::-1][:k]))
+    same = np.full(500, -2.5, dtype=np.float32)
+    assert bits(oracle.topk_f32(same, 499, plant=plant)).tolist() == [bits(same)[0]] * 499
+
+
+ALL_PINS = [pin_golden_u32, pin_golden_f32, pin_exhaustive_u32, pin_exhaustive_f32, pin_numpy_u32_f32,
+            pin_golden_i32, pin_golden_rows, pin_exhaustive_i32, pin_exhaustive_rows,
             pin_closed_forms_i32, pin_rows_numpy, pin_golden_reduce, pin_exhaustive_reduce,
             pin_closed_forms_reduce, pin_golden_items, pin_exhaustive_items, pin_items_numpy,
             pin_golden_sort, pin_exhaustive_sort, pin_sort_numpy]
@@ -293,6 +354,29 @@ ALL_PINS = [pin_golden_i32, pin_golden_rows, pin_exhaustive_i32, pin_exhaustive_
 
 def test_golden_i32():
     pin_golden_i32()
+
+
+def test_golden_u32_f32():
+    pin_golden_u32()
+    pin_golden_f32()
+
+
+def test_exhaustive_u32_f32():
+    pin_exhaustive_u32()
+    pin_exhaustive_f32()
+
+
+def test_u32_f32_numpy():
+    pin_numpy_u32_f32()
+
+
+def test_total_order_key_is_numeric_on_numbers():
+    # The brute force's key agrees with float comparison on ordered numbers.
+    nums = [b for b in F32_PATTERNS if (b & 0x7F800000) != 0x7F800000 or (b & 0x7FFFFF) == 0]
+    for a, b in itertools.product(nums, repeat=2):
+        fa, fb = struct.unpack("<ff", struct.pack("<II", a, b))
+        if fa != fb:
+            assert (total_order_key(a) > total_order_key(b)) == (fa > fb), (hex(a), hex(b))
 
 
 def test_golden_rows():
@@ -464,6 +548,10 @@ def test_pins_reject_planted_mistake(plant):
                 pin(plant=plant, max_n=3)
             elif pin is pin_exhaustive_sort:
                 pin(plant=plant, max_n=4)
+            elif pin is pin_exhaustive_u32:
+                pin(plant=plant, max_n=4)
+            elif pin is pin_exhaustive_f32:
+                pin(plant=plant, max_n=2)
             else:
                 pin(plant=plant)
         except AssertionError:

@@ -176,7 +176,7 @@ class ClockSampler:
 class Timer:
     """CUDA-event timing of library calls on one stream.
 
-    single(fn): one call alone -- the previous work on the stream has
+    single(fn): one call alone, device time -- the previous work on the stream has
     finished and L2 holds none of the input (a 512 MiB buffer is read
     first, outside the timed region: reading leaves clean lines in L2, so no
     write-back of the flush lands in the timed call); the median over `reps`
@@ -199,6 +199,10 @@ class Timer:
         ts = []
         for _ in range(reps):
             self.flush()
+            # Keep the stream busy until the call below is enqueued, so the
+            # first event marks the GPU reaching the call, not the host
+            # entering it (host-side API time is in `e2e`).
+            torch.cuda._sleep(100_000)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(self.stream)
             fn()
@@ -275,6 +279,7 @@ def run_ours(args, world, rank, local):
         extra["rows_f32"] = run_rows(tk, dev, stream, args, timer, peak, configs)
         extra["large_k"] = run_large_k(tk, x, stream, args, timer)
         extra["noalloc"] = run_noalloc(tk, x, stream, timer, peak)
+        extra["keys"] = run_keys(tk, x, stream, timer, peak)
         extra["reduce"] = run_reduce(tk, x, stream, args)
         extra["items"] = run_items(tk, dev, stream, args)
         extra["sort"] = run_sort(tk, x, stream, args)
@@ -517,6 +522,32 @@ def run_large_k(tk, x, stream, args, timer):
                                      "traffic_dominant_kernel": recorded_traffic("radix_filter_kernel",
                                                                                  "i32_uniform_1e8_k1000")}}
     res["workload"] = "int32 TopK, N=1e8 uniform full range (seed 2), k in (1000, 32768), sorted descending"
+    return res
+
+
+def run_keys(tk, x, stream, timer, peak):
+    """topk_u32 and topk_f32 on the 1e8 input's bits (uniform uint32 keys;
+    float32 bit patterns, half negative, ~0.4% NaN), and topk_i32 at
+    k = 131072 (the large-k plan with the LSD sort ordering the answer)."""
+    n = x.numel()
+    h = stream.cuda_stream
+    xf = x.view(torch.float32)
+    res = {}
+    for name, fn, src, k in (("u32_k20", tk.topk_u32_ptr, x, 20), ("f32_k20", tk.topk_f32_ptr, xf, 20),
+                             ("f32_k1000", tk.topk_f32_ptr, xf, 1000), ("i32_k131072", tk.topk_i32_ptr, x, 131072)):
+        out = torch.empty(k, dtype=torch.int32, device=x.device)
+
+        def step():
+            rc = fn(src.data_ptr(), n, k, out.data_ptr(), h)
+            if rc != 0:
+                raise tk.TopKError(rc, name)
+
+        step()
+        su = timer.single(step, 20)
+        pu = timer.pipelined(step, 20)
+        res[name] = {"single_us": round(su, 2), "pipe_us": round(pu, 2), "frac_single": _frac(4 * n, su, peak),
+                     "frac_pipe": _frac(4 * n, pu, peak)}
+    res["workload"] = "N=1e8 words of the uniform int32 input (seed 2) read as uint32 / float32 bits"
     return res
 
 

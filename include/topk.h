@@ -54,8 +54,11 @@ enum topk_status {
     TOPK_ERR_DEVICE_TIMEOUT = 5 /* a kernel's bounded wait gave up; its results are not valid */
 };
 
-/* Largest k accepted by topk_i32 (and topk_i32_noalloc). */
-#define TOPK_MAX_K 32768
+/* Largest k accepted by topk_i32, topk_u32 and topk_f32. */
+#define TOPK_MAX_K 131072
+
+/* Largest k accepted by topk_i32_noalloc. */
+#define TOPK_NOALLOC_MAX_K 32768
 
 /* Largest k accepted by topk_rows_f32. */
 #define TOPK_MAX_K_ROWS 1024
@@ -79,11 +82,32 @@ enum topk_status {
  * it, and one 8-CTA cluster selects the k-th key among them and sorts the
  * answer (six launches, one input pass; two more input passes run only when
  * the sample misled the filter).  When n <= 2^18 the cluster does it all in
- * one launch.
+ * one launch.  k > 32768: the cluster leaves the answer unordered and the
+ * library's LSD radix sort (topk_sort_u32's kernels) orders it, plus one
+ * launch that writes it out; that form needs about 4k more bytes of
+ * workspace and sort scratch for k keys.
  *
  * Returns TOPK_OK or an error code; on error nothing is written to out.
  */
 int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_st* stream);
+
+/*
+ * topk_u32 -- topk_i32 for uint32 keys: the k largest of in[0..n) in
+ * unsigned order, descending ("GPU radix sort" sorts uint32 keys; the TopK
+ * of sections 2.1-2.2 on them).  Arguments, limits, plans and errors are
+ * those of topk_i32.
+ *
+ * topk_f32 -- topk_i32 for float32 keys: the k largest of in[0..n) under
+ * IEEE 754 totalOrder, descending, each output the bits of an input
+ * element.  totalOrder is the order the "GPU radix sort" page gives floats
+ * with its bit transform (extensions section): -NaN < -inf < ... < -0.0 <
+ * +0.0 < ... < +inf < +NaN, NaNs of one sign ordered by payload (larger
+ * payloads further from zero).  So every bit pattern is its own key: -0.0
+ * ranks below +0.0, and a NaN with the sign bit set ranks below -inf.
+ * Arguments, limits, plans and errors are those of topk_i32.
+ */
+int topk_u32(const uint32_t* in, size_t n, int k, uint32_t* out, struct CUstream_st* stream);
+int topk_f32(const float* in, size_t n, int k, float* out, struct CUstream_st* stream);
 
 /*
  * topk_rows_f32 -- for each row r of the row-major rows x cols matrix `in`,
@@ -220,7 +244,7 @@ int topk_reduce_f32(const float* in, size_t n, int op, double* out, struct CUstr
  *   - The scratch is one file-scope device array of
  *     TOPK_NOALLOC_SCRATCH_BYTES (1 MiB): control words, per-block maxima
  *     and per-block candidates.  Every GPU that loads the library holds it
- *     until the process exits.  k above TOPK_MAX_K is rejected with
+ *     until the process exits.  k above TOPK_NOALLOC_MAX_K is rejected with
  *     TOPK_ERR_UNSUPPORTED.  For k <= 128 the grid is cut so that every
  *     block's candidate lists fit (1 MiB holds 239 blocks' worth), so on
  *     GPUs with more SMs this entry point runs fewer blocks than topk_i32;
@@ -278,7 +302,25 @@ enum topk_option {
      * restores the default).  The other tiles are claimed one at a time
      * from counters as warps finish, so that fast SMs take the slow ones'
      * share.  For tests of both schedules; results are the same either way. */
-    TOPK_OPT_STREAM_STATIC = 4
+    TOPK_OPT_STREAM_STATIC = 4,
+    /* 1: no call starts early (see topk_last_launch_early); every launch
+     * waits for the previous work on its stream.  0 (the default): early
+     * start as described there.  Set it when work that is not this
+     * library's writes a TopK input on the same stream between two calls
+     * and must be finished, memory flushed, before the next call reads. */
+    TOPK_OPT_NO_EARLY_START = 5,
+    /* 1: every later workspace or staging allocation fails with
+     * TOPK_ERR_NO_MEMORY, as if the device were full; 0: normal.  The
+     * environment variable TOPK_FAULT_ALLOC=1, read at the first
+     * allocation, sets it too.  For tests of callers' error paths (the
+     * failure is made on the host; no device fault). */
+    TOPK_OPT_FAULT_ALLOC = 6,
+    /* Polls of one look-back word before a tile of topk_sort_u32 gives up
+     * (0 restores the default, 2^22).  A tile that gives up writes its keys
+     * to wrong places inside the output (never outside it), and
+     * topk_check_stream then reports TOPK_ERR_DEVICE_TIMEOUT.  Lower it
+     * only to exercise that report. */
+    TOPK_OPT_SORT_SPINS = 7
 };
 
 /* Set a process-wide option; takes effect for calls made afterwards.

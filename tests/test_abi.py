@@ -68,7 +68,7 @@ A, B, C = 0x10000000, 0x20000000, 0x30000000
     ((A + 2, 100, 5, B), 1),      # misaligned input
     ((A, 100, 5, B + 1), 1),      # misaligned output
     ((A, 100, 5, A + 40), 1),     # output overlaps input
-    ((A, 40000, 32769, B), 2),    # k above the maximum
+    ((A, 200000, 131073, B), 2),  # k above the maximum
     ((B, (1 << 40) + 4, 5, A), 2),  # n above the maximum
 ])
 def test_topk_i32_argument_errors(lib, args, status):
@@ -175,3 +175,31 @@ def test_header_limits_match_binding(lib):
     text = open(os.path.join(ROOT, "include", "topk.h")).read()
     assert re.search(r"#define TOPK_MAX_K\s+%d\b" % tk.MAX_K, text)
     assert re.search(r"#define TOPK_MAX_K_ROWS\s+%d\b" % tk.MAX_K_ROWS, text)
+
+
+def test_options_accept_and_reject(lib):
+    import topk_selection_gb300 as tk
+
+    for opt, good, bad in ((tk.OPT_NO_EARLY_START, (1, 0), (2, -1)), (tk.OPT_FAULT_ALLOC, (1, 0), (2, -1)),
+                           (tk.OPT_SORT_SPINS, (1, 0), (-1,)), (tk.OPT_STREAM_STATIC, (1, 101, 0), (102, -1)),
+                           (tk.OPT_STAGE2_CAP, (64, 0), (3, 1))):
+        for v in good:
+            tk.set_option(opt, v)
+        for v in bad:
+            with pytest.raises(tk.TopKError):
+                tk.set_option(opt, v)
+    with pytest.raises(tk.TopKError):
+        tk.set_option(99, 0)
+
+
+@pytest.mark.parametrize("fn", ["topk_u32_ptr", "topk_f32_ptr"])
+def test_u32_f32_argument_errors(lib, fn):
+    import topk_selection_gb300 as tk
+
+    f = getattr(tk, fn)
+    assert f(0, 100, 5, B) == 1
+    assert f(A, 0, 1, B) == 1
+    assert f(A, 100, 101, B) == 1
+    assert f(A + 2, 100, 5, B) == 1
+    assert f(A, 100, 5, A + 40) == 1
+    assert f(A, 200000, 131073, B) == 2

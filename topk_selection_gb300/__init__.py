@@ -27,7 +27,8 @@ __all__ = ["topk_i32", "topk_rows_f32", "topk_i32_ptr", "topk_rows_f32_ptr", "To
            "reduce", "reduce_ptr", "REDUCE_OPS", "topk_items_f32", "topk_items_f32_ptr", "sort_u32",
            "sort_u32_ptr"]
 
-MAX_K = 32768       # topk_i32
+MAX_K = 131072      # topk_i32, topk_u32, topk_f32
+NOALLOC_MAX_K = 32768  # topk_i32_noalloc
 MAX_K_ROWS = 1024   # topk_rows_f32
 (TOPK_OK, TOPK_ERR_INVALID_ARG, TOPK_ERR_UNSUPPORTED, TOPK_ERR_NO_MEMORY, TOPK_ERR_CUDA,
  TOPK_ERR_DEVICE_TIMEOUT) = range(6)
@@ -73,6 +74,10 @@ def _load():
     lib.topk_items_f32.restype = ci
     lib.topk_sort_u32.argtypes = [vp, vp, sz, vp, vp, vp]
     lib.topk_sort_u32.restype = ci
+    lib.topk_u32.argtypes = [vp, sz, ci, vp, vp]
+    lib.topk_u32.restype = ci
+    lib.topk_f32.argtypes = [vp, sz, ci, vp, vp]
+    lib.topk_f32.restype = ci
     lib.topk_last_launch_early.argtypes = []
     lib.topk_last_launch_early.restype = ci
     return lib
@@ -109,6 +114,9 @@ OPT_STAGE2_CAP = 1
 OPT_RADIX_CAP = 2
 OPT_RADIX_SAMPLE_RANK = 3
 OPT_STREAM_STATIC = 4
+OPT_NO_EARLY_START = 5
+OPT_FAULT_ALLOC = 6
+OPT_SORT_SPINS = 7
 
 
 def set_option(option: int, value: int) -> None:
@@ -171,6 +179,45 @@ def topk_i32(x: torch.Tensor, k: int, out: torch.Tensor | None = None, stream=No
     if rc != TOPK_OK:
         raise TopKError(rc, "topk_i32")
     return out
+
+
+def topk_u32_ptr(in_ptr: int, n: int, k: int, out_ptr: int, stream: int = 0) -> int:
+    """Raw C-ABI call; returns the status code."""
+    return int(_lib.topk_u32(ctypes.c_void_p(in_ptr), n, k, ctypes.c_void_p(out_ptr), ctypes.c_void_p(stream)))
+
+
+def topk_f32_ptr(in_ptr: int, n: int, k: int, out_ptr: int, stream: int = 0) -> int:
+    """Raw C-ABI call; returns the status code."""
+    return int(_lib.topk_f32(ctypes.c_void_p(in_ptr), n, k, ctypes.c_void_p(out_ptr), ctypes.c_void_p(stream)))
+
+
+def _topk_words(fn, name, x, k, out, stream, dtypes):
+    if x.dtype not in dtypes:
+        raise TypeError(f"x must be one of {dtypes}, got {x.dtype}")
+    _check_input(x, x.dtype, "x")
+    if out is None:
+        out = torch.empty(max(int(k), 0), dtype=x.dtype, device=x.device)
+    _check_input(out, x.dtype, "out")
+    if out.numel() != k:
+        raise ValueError("out must have k elements")
+    dev = x.device if x.is_cuda else (out.device if out.is_cuda else None)
+    with torch.cuda.device(dev) if dev is not None else _null():
+        rc = fn(x.data_ptr(), x.numel(), int(k), out.data_ptr(), _stream_handle(stream, dev))
+    if rc != TOPK_OK:
+        raise TopKError(rc, name)
+    return out
+
+
+def topk_u32(x: torch.Tensor, k: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The k largest of the uint32 keys in x (flattened), descending.  x may
+    be torch.uint32, or int32 holding the keys' bits (out has x's dtype)."""
+    return _topk_words(topk_u32_ptr, "topk_u32", x, k, out, stream, (torch.uint32, torch.int32))
+
+
+def topk_f32(x: torch.Tensor, k: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The k largest float32 values of x (flattened) under IEEE 754 totalOrder,
+    descending (see topk_f32 in include/topk.h)."""
+    return _topk_words(topk_f32_ptr, "topk_f32", x, k, out, stream, (torch.float32,))
 
 
 def topk_rows_f32(x: torch.Tensor, k: int, vals: torch.Tensor | None = None, idx: torch.Tensor | None = None,

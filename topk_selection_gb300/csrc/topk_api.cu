@@ -5,6 +5,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -13,6 +14,8 @@
 #include "../../include/topk.h"
 #include "topk_internal.h"
 
+static_assert(TOPK_MAX_K == topk::kBigKMax, "the header states the big-k form's limit");
+
 namespace {
 
 std::atomic<unsigned long long> g_launches{0};
@@ -20,6 +23,24 @@ std::atomic<int> g_stage2_cap{0};
 std::atomic<int> g_radix_cap{0};
 std::atomic<int> g_radix_sample_rank{0};
 std::atomic<int> g_stream_static{0};
+std::atomic<int> g_no_early{0};
+std::atomic<int> g_sort_spins{0};
+std::atomic<int> g_fault_alloc{-1};  // -1: not read yet from TOPK_FAULT_ALLOC
+
+// Fault injection on the host: when set (environment TOPK_FAULT_ALLOC=1 at
+// the first allocation, or TOPK_OPT_FAULT_ALLOC), every workspace or staging
+// allocation fails as if the device were out of memory.
+bool fault_alloc() {
+    int v = g_fault_alloc.load(std::memory_order_relaxed);
+    if (v < 0) {
+        const char* env = std::getenv("TOPK_FAULT_ALLOC");
+        v = (env && env[0] == '1') ? 1 : 0;
+        int expected = -1;
+        g_fault_alloc.compare_exchange_strong(expected, v);
+        v = g_fault_alloc.load(std::memory_order_relaxed);
+    }
+    return v == 1;
+}
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_early = 0;  // whether this thread's last TopK launch started early
 
@@ -45,6 +66,8 @@ struct Workspace {
     // that the next launch does not start early.
     const void* stream_out[2] = {nullptr, nullptr};
     size_t stream_out_bytes[2] = {SIZE_MAX, 0};
+    void* bigk = nullptr;       // large-k TopK beyond the range plan: two k-word buffers
+    size_t bigk_bytes = 0;
     void* sort = nullptr;       // topk_sort_u32 scratch (its header zero between calls)
     size_t sort_bytes = 0;
     unsigned sort_epoch = 0;    // tags the sort's look-back words, one per call
@@ -55,6 +78,10 @@ std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
 
 int grow(void** p, size_t* have, size_t need) {
     if (*have >= need) return TOPK_OK;
+    if (fault_alloc()) {
+        t_last_cuda_error = (int)cudaErrorMemoryAllocation;
+        return TOPK_ERR_NO_MEMORY;
+    }
     if (*p) {
         cudaError_t e = cudaFree(*p);
         *p = nullptr;
@@ -128,6 +155,7 @@ bool early_start(Workspace* w, const void* in, size_t in_bytes, const void* a, s
     std::lock_guard<std::mutex> lock(g_ws_mutex);
     bool ok = true;
     for (int i = 0; i < 2; ++i) ok = ok && !overlaps(in, in_bytes, w->stream_out[i], w->stream_out_bytes[i]);
+    if (g_no_early.load(std::memory_order_relaxed)) ok = false;
     w->stream_out[0] = a;
     w->stream_out_bytes[0] = a_bytes;
     w->stream_out[1] = b;
@@ -154,6 +182,7 @@ int stage2_cap_option() { return g_stage2_cap.load(std::memory_order_relaxed); }
 int radix_cap_option() { return g_radix_cap.load(std::memory_order_relaxed); }
 int radix_sample_rank_option() { return g_radix_sample_rank.load(std::memory_order_relaxed); }
 int stream_static_option() { return g_stream_static.load(std::memory_order_relaxed); }
+int sort_spins_option() { return g_sort_spins.load(std::memory_order_relaxed); }
 void note_cuda_error(int err) { t_last_cuda_error = err; }
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 void note_unreleased_launch(int device, cudaStream_t s) {
@@ -174,7 +203,11 @@ void note_unreleased_launch(int device, cudaStream_t s) {
 
 extern "C" {
 
-int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_st* stream) {
+namespace {
+
+// Body of topk_i32, topk_u32 and topk_f32: n 32-bit words in, k words out,
+// ordered as `kind` says (KeyKind).
+int topk_words(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_st* stream, int kind) {
     if (!in || !out || n == 0 || k < 1 || (size_t)k > n) return TOPK_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 3u) return TOPK_ERR_INVALID_ARG;
     if (overlaps(in, n * sizeof(int32_t), out, (size_t)k * sizeof(int32_t))) return TOPK_ERR_INVALID_ARG;
@@ -192,7 +225,7 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
     if (rc != TOPK_OK) return rc;
 
     topk::I32Plan plan;
-    e = topk::i32_plan(device, n, k <= 128 ? k : 128, &plan);
+    e = topk::i32_plan(device, n, k <= 128 ? k : 128, &plan, kind);
     if (e != cudaSuccess) return cuda_fail(e);
     // One workspace serves both plans (k <= 128 streams; larger k use radix select).
     size_t ctrl_cand = topk::i32_scratch_bytes(plan.max_grid);
@@ -213,7 +246,35 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
     if (out_host) dout = static_cast<int32_t*>(w->stage_out);
 
     int launches = 1;
-    if (k <= 128) {
+    if (k > topk::kRadixMaxK) {
+        // Beyond the range plan's k: the plan leaves the answer's keys
+        // unordered in a buffer, the LSD radix sort orders them, and a last
+        // kernel writes them out.  None of these releases its successor.
+        const size_t need_sort = topk::sort_scratch_bytes((size_t)k, false);
+        unsigned epoch = 0;
+        {
+            std::lock_guard<std::mutex> lock(g_ws_mutex);
+            rc = grow(&w->bigk, &w->bigk_bytes, 2 * (size_t)k * sizeof(uint32_t));
+            if (rc == TOPK_OK && w->sort_bytes < need_sort) {
+                rc = grow(&w->sort, &w->sort_bytes, need_sort);
+                if (rc == TOPK_OK) {
+                    e = cudaMemsetAsync(w->sort, 0, topk::kSortHeaderBytes, s);
+                    if (e != cudaSuccess) return cuda_fail(e);
+                }
+            }
+            epoch = ++w->sort_epoch;
+        }
+        if (rc != TOPK_OK) return rc;
+        mark_not_released(w);
+        auto* a = static_cast<uint32_t*>(w->bigk);
+        uint32_t* b = a + k;
+        auto* status = reinterpret_cast<unsigned*>(static_cast<char*>(w->ctrl_cand) + topk::kI32StatusOffset);
+        e = topk::radix_launch(s, din, n, k, dout, w->ctrl_cand, topk::kRadixCap, &launches, false, kind, a);
+        int sl = 0;
+        if (e == cudaSuccess) e = topk::sort_launch(s, a, nullptr, (size_t)k, b, nullptr, w->sort, epoch, status, &sl);
+        if (e == cudaSuccess) e = topk::radix_bigk_out(s, b, k, dout, kind);
+        launches += sl + 1;
+    } else if (k <= 128) {
         // The streaming kernel may start while the previous one on this stream
         // finishes, reading its input early: not when that input is the
         // previous launch's output (a chain of TopKs).
@@ -226,7 +287,7 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
         // one must know what it writes.
         early_start(w, din, 0, dout, (size_t)k * sizeof(int32_t), nullptr, 0);
         t_last_early = 0;  // every kernel of the plan waits before it reads its input
-        e = topk::radix_launch(s, din, n, k, dout, w->ctrl_cand, topk::kRadixCap, &launches, true);
+        e = topk::radix_launch(s, din, n, k, dout, w->ctrl_cand, topk::kRadixCap, &launches, true, kind);
     }
     g_launches.fetch_add((unsigned long long)launches, std::memory_order_relaxed);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -240,6 +301,22 @@ int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_s
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return TOPK_OK;
+}
+
+}  // namespace
+
+int topk_i32(const int32_t* in, size_t n, int k, int32_t* out, struct CUstream_st* stream) {
+    return topk_words(in, n, k, out, stream, topk::kKeyI32);
+}
+
+int topk_u32(const uint32_t* in, size_t n, int k, uint32_t* out, struct CUstream_st* stream) {
+    return topk_words(reinterpret_cast<const int32_t*>(in), n, k, reinterpret_cast<int32_t*>(out), stream,
+                      topk::kKeyU32);
+}
+
+int topk_f32(const float* in, size_t n, int k, float* out, struct CUstream_st* stream) {
+    return topk_words(reinterpret_cast<const int32_t*>(in), n, k, reinterpret_cast<int32_t*>(out), stream,
+                      topk::kKeyF32);
 }
 
 namespace {
@@ -497,6 +574,18 @@ int topk_set_option(int option, int value) {
             if (value < 0) return TOPK_ERR_INVALID_ARG;
             g_radix_sample_rank.store(value, std::memory_order_relaxed);
             return TOPK_OK;
+        case TOPK_OPT_NO_EARLY_START:
+            if (value != 0 && value != 1) return TOPK_ERR_INVALID_ARG;
+            g_no_early.store(value, std::memory_order_relaxed);
+            return TOPK_OK;
+        case TOPK_OPT_SORT_SPINS:
+            if (value < 0) return TOPK_ERR_INVALID_ARG;
+            g_sort_spins.store(value, std::memory_order_relaxed);
+            return TOPK_OK;
+        case TOPK_OPT_FAULT_ALLOC:
+            if (value != 0 && value != 1) return TOPK_ERR_INVALID_ARG;
+            g_fault_alloc.store(value, std::memory_order_relaxed);
+            return TOPK_OK;
         case TOPK_OPT_STREAM_STATIC:
             if (value < 0 || value > 101) return TOPK_ERR_INVALID_ARG;
             g_stream_static.store(value, std::memory_order_relaxed);
@@ -530,7 +619,7 @@ int topk_release_workspace(void) {
     for (auto& kv : g_ws) {
         Workspace& w = kv.second;
         cudaSetDevice(kv.first.first);
-        for (void* p : {w.ctrl_cand, w.stage_in, w.stage_out, w.items, w.sort})
+        for (void* p : {w.ctrl_cand, w.stage_in, w.stage_out, w.items, w.sort, w.bigk})
             if (p && cudaFree(p) != cudaSuccess) rc = TOPK_ERR_CUDA;
     }
     g_ws.clear();

@@ -12,6 +12,8 @@
 #include <climits>
 #include <cstdint>
 
+#include "topk_internal.h"
+
 namespace topk {
 
 constexpr unsigned kFullMask = 0xffffffffu;
@@ -196,6 +198,28 @@ struct RegList {
         bitonic_merge(lane);
     }
 };
+
+// Every kernel works on int32 words whose signed order is the key kind's
+// order (KeyKind, topk_internal.h); ordered<KIND> maps an input word there
+// and back (it is its own inverse):
+//   kKeyI32  int32 values: unchanged;
+//   kKeyU32  uint32 values: the top bit flipped (unsigned order -> signed);
+//   kKeyF32  float32 bit patterns: the low 31 bits flipped when the sign is
+//            set, so that signed order is IEEE 754 totalOrder (-NaN < -inf
+//            < ... < -0 < +0 < ... < +inf < +NaN) -- the order of the "GPU
+//            radix sort" page's float bit transform (its extensions
+//            section), which maps that same order to unsigned integers.
+template <int KIND>
+__device__ __forceinline__ int ordered(int x) {
+    if constexpr (KIND == kKeyU32) return x ^ INT_MIN;
+    else if constexpr (KIND == kKeyF32) return x ^ ((x >> 31) & 0x7FFFFFFF);
+    else return x;
+}
+
+template <int KIND>
+__device__ __forceinline__ int4 ordered4(int4 v) {
+    return make_int4(ordered<KIND>(v.x), ordered<KIND>(v.y), ordered<KIND>(v.z), ordered<KIND>(v.w));
+}
 
 __host__ __device__ __forceinline__ int next_pow2(int x) {
     int p = 1;

@@ -128,19 +128,6 @@ __device__ __forceinline__ int seed_from_groups(const int4 (&r)[NV], int k, int 
     return warp_sorted_at<GL>(g, k - 1);
 }
 
-// Start threshold of a warp from its first tile and the array's tail.
-template <int GL>
-__device__ __forceinline__ int start_threshold(const int4 (&r)[kU], const Split& sp, int k, int lane) {
-    int4 s[2];
-    const long long tv = (long long)sp.nvec - kTailVec + 2 * lane;
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
-        s[q] = tv + q >= 0 ? __ldg(sp.body + tv + q) : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
-    int seed = seed_from_groups<GL>(r, k, lane);
-    if constexpr (GL <= 2) seed = kmax(seed, seed_from_groups<GL>(s, k, lane));
-    return seed;
-}
-
 // Append the lanes' values that exceed t to q[*nq...] (warp-uniform count).
 __device__ __forceinline__ void enqueue(int* q, int& nq, int v, int t, int lane) {
     const bool p = v > t;
@@ -149,6 +136,74 @@ __device__ __forceinline__ void enqueue(int* q, int& nq, int v, int t, int lane)
     nq += __popc(m);
 }
 
+
+// The k-th largest (1 <= k) of the unsigned values that the block's threads
+// hold, N per thread (pad with 0): an 8-bit-digit radix select ("GPU radix
+// sort", histogram section), most significant digit first, four rounds of
+// a shared 256-bin histogram.  Every thread must call it; every thread
+// gets the result.  With fewer than k values in all, the result is 0.
+template <int N>
+__device__ unsigned block_kth_largest(const unsigned (&v)[N], unsigned k, unsigned* hist, unsigned* pick) {
+    const int lane = threadIdx.x & 31;
+    unsigned prefix = 0, need = k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        const unsigned mask = shift == 24 ? 0u : 0xFFFFFFFFu << (shift + 8);
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
+        if (threadIdx.x == 0) pick[0] = 0u, pick[1] = need;
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < N; ++q)
+            if ((v[q] & mask) == prefix) atomicAdd(&hist[(v[q] >> shift) & 255u], 1u);
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            unsigned cnt[8], tot = 0;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) tot += (cnt[b] = hist[lane * 8 + b]);
+            unsigned x = tot;  // sum over this lane and the lanes above (higher bins)
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned y = __shfl_down_sync(kFullMask, x, o);
+                if (lane + o < 32) x += y;
+            }
+            unsigned acc = x - tot;  // values in higher bins
+            if (acc < need && need <= acc + tot) {
+#pragma unroll
+                for (int b = 7; b >= 0; --b) {
+                    if (acc + cnt[b] >= need) {
+                        pick[0] = (unsigned)(lane * 8 + b);
+                        pick[1] = need - acc;
+                        break;
+                    }
+                    acc += cnt[b];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= pick[0] << shift;
+        need = pick[1];
+        __syncthreads();
+    }
+    return prefix;
+}
+
+// One warp: sort list[0, nlist) (nlist <= 32*N) descending in registers and
+// write out[0, k): the sorted entries, then copies of T; in the kind's words.
+template <int N, int KIND>
+__device__ __forceinline__ void warp_sort_out(const int* list, int nlist, int k, int T, int32_t* out, int lane) {
+    int v[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        const int p = j * 32 + lane;
+        v[j] = p < nlist ? list[p] : INT_MIN;
+    }
+    warp_sort_desc<N>(v, lane);
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        const int p = j * 32 + lane;
+        if (p < k) out[p] = ordered<KIND>(p < nlist ? v[j] : T);
+    }
+    for (int p = 32 * N + lane; p < k; p += 32) out[p] = ordered<KIND>(T);
+}
 
 // ---------------------------------------------------------------- stage 2 --
 //
@@ -160,39 +215,29 @@ __device__ __forceinline__ void enqueue(int* q, int& nq, int v, int t, int lane)
 
 // Run by the last block to finish.  `room` ints of shared memory at `list`;
 // cap_limit > 0 lowers the list capacity (to exercise the radix-select path).
+template <int KIND>
 __device__ void second_stage(const Scratch& sc, int k, int lists_per_block, int K, int32_t* __restrict__ out,
                              int* list, int room, int cap_limit, int* s_count, int ntmax) {
     const int lane = threadIdx.x & 31;
-    __threadfence();
+    __shared__ unsigned s_hist[256];
+    __shared__ unsigned s_pick[2];
+    // Every other block's writes are visible here: thread 0 drew the last
+    // ticket with acquire semantics, and the barrier after it orders this
+    // block's reads after that.
     int tg = unbias(ld_relaxed_gpu(&sc.ctrl->thresh));
-    if (ntmax >= k) {
-        // The k-th largest tile maximum: k distinct tiles each hold an
-        // element at least that large, so it is a valid threshold too, and
-        // with few blocks per k it is far tighter than the blocks' own.
-        // Bit by bit from the top: the largest u with at least k tile maxima
-        // (biased) >= u.
-        __shared__ int s_cnt;
-        unsigned tm[kI32MaxTileMax / 256];
+    const int nlists = (int)gridDim.x * lists_per_block;
+    // Each list's count and its first four entries, loaded together (one
+    // round trip for the usual case of at most four survivors per list).
+    // Lists and tile maxima: at most kBatch per thread.
+    constexpr int kBatch = kI32MaxTileMax / 256;
+    int c[kBatch];
+    int4 h[kBatch];
 #pragma unroll
-        for (int q = 0; q < kI32MaxTileMax / 256; ++q) {
-            const int t = q * (int)blockDim.x + (int)threadIdx.x;
-            tm[q] = t < ntmax ? bias(__ldcg(sc.tmax + t)) : 0u;
-        }
-        unsigned ans = 0;
-        for (int bit = 31; bit >= 0; --bit) {
-            const unsigned cand = ans | (1u << bit);
-            int c = 0;
-#pragma unroll
-            for (int q = 0; q < kI32MaxTileMax / 256; ++q) c += tm[q] >= cand ? 1 : 0;
-            if (threadIdx.x == 0) s_cnt = 0;
-            __syncthreads();
-            c = __reduce_add_sync(kFullMask, c);
-            if (lane == 0 && c) atomicAdd(&s_cnt, c);
-            __syncthreads();
-            if (s_cnt >= k) ans = cand;
-            __syncthreads();
-        }
-        tg = kmax(tg, unbias(ans));
+    for (int q = 0; q < kBatch; ++q) {
+        const int l = q * (int)blockDim.x + (int)threadIdx.x;
+        c[q] = l < nlists ? __ldcg(sc.counts + l) : 0;
+        h[q] = l < nlists ? __ldcg(reinterpret_cast<const int4*>(sc.cand + (size_t)l * K))
+                          : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
     }
     // The list is bitonic-sorted in place at a power-of-two length, so its
     // capacity is the largest power of two that fits.
@@ -200,28 +245,50 @@ __device__ void second_stage(const Scratch& sc, int k, int lists_per_block, int 
     while (2 * cap <= room) cap *= 2;
     if (cap_limit > 0 && cap_limit < cap) cap = cap_limit;
     if (cap < k) cap = k;  // the sorted list must be able to hold the answer
-    const int nlists = (int)gridDim.x * lists_per_block;
 
+    // Before gathering: when the lists' counts (entries above each block's
+    // threshold at its end, so at least as many as will pass) add up to more
+    // than one warp's sort (256), tighten tg with a bound of the gather's
+    // own, so that each list yields few entries: with at least k lists, the
+    // k-th largest list head (each list starts with its block's maximum, and
+    // k distinct blocks hold an element that large); with fewer blocks than
+    // k, the k-th largest tile maximum (k distinct tiles).  Both are valid
+    // thresholds however little the blocks learnt from each other while
+    // streaming (a launch that started early, a short input).
+    {
+        int cs = 0;
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) cs += c[q];
+        cs = __reduce_add_sync(kFullMask, cs);
+        if (threadIdx.x == 0) *s_count = 0;
+        __syncthreads();
+        if (lane == 0 && cs) atomicAdd(s_count, cs);
+        __syncthreads();
+    }
+    if (*s_count > 256 && (nlists >= k || ntmax >= k)) {
+        unsigned v[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            const int l = q * (int)blockDim.x + (int)threadIdx.x;
+            if (nlists >= k)
+                v[q] = bias(h[q].x);
+            else
+                v[q] = l < ntmax ? bias(__ldcg(sc.tmax + l)) : 0u;
+        }
+        tg = kmax(tg, unbias(block_kth_largest<kBatch>(v, (unsigned)k, s_hist, s_pick)));
+    }
+    __syncthreads();
     if (threadIdx.x == 0) *s_count = 0;
     __syncthreads();
-    constexpr int kBatch = 8;
-    for (int base = 0; base < nlists; base += kBatch * (int)blockDim.x) {
-        int c[kBatch];
 #pragma unroll
-        for (int q = 0; q < kBatch; ++q) {
-            const int l = base + q * (int)blockDim.x + (int)threadIdx.x;
-            c[q] = l < nlists ? __ldcg(sc.counts + l) : 0;
-        }
-#pragma unroll
-        for (int q = 0; q < kBatch; ++q) {
-            const int l = base + q * (int)blockDim.x + (int)threadIdx.x;
-            const int32_t* src = sc.cand + (size_t)l * K;
-            for (int p = 0; p < c[q]; ++p) {
-                const int v = __ldcg(src + p);
-                if (v <= tg) break;  // the list is sorted: nothing after this exceeds tg
-                const int pos = atomicAdd(s_count, 1);
-                if (pos < cap) list[pos] = v;
-            }
+    for (int q = 0; q < kBatch; ++q) {
+        const int l = q * (int)blockDim.x + (int)threadIdx.x;
+        const int32_t* src = sc.cand + (size_t)l * K;
+        for (int p = 0; p < c[q]; ++p) {
+            const int v = p == 0 ? h[q].x : p == 1 ? h[q].y : p == 2 ? h[q].z : p == 3 ? h[q].w : __ldcg(src + p);
+            if (v <= tg) break;  // the list is sorted: nothing after this exceeds tg
+            const int pos = atomicAdd(s_count, 1);
+            if (pos < cap) list[pos] = v;
         }
     }
     __syncthreads();
@@ -280,27 +347,22 @@ __device__ void second_stage(const Scratch& sc, int k, int lists_per_block, int 
     }
 
     if (nlist <= 256) {
-        // Small list: one warp sorts it in registers.
+        // Small list: one warp sorts it in registers, as few as it needs.
         if (threadIdx.x < 32) {
-            int v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int p = j * 32 + lane;
-                v[j] = p < nlist ? list[p] : INT_MIN;
-            }
-            warp_sort_desc<8>(v, lane);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int p = j * 32 + lane;
-                if (p < k) out[p] = p < nlist ? v[j] : T;
-            }
-            for (int p = 256 + lane; p < k; p += 32) out[p] = T;
+            if (nlist <= 32)
+                warp_sort_out<1, KIND>(list, nlist, k, T, out, lane);
+            else if (nlist <= 64)
+                warp_sort_out<2, KIND>(list, nlist, k, T, out, lane);
+            else if (nlist <= 128)
+                warp_sort_out<4, KIND>(list, nlist, k, T, out, lane);
+            else
+                warp_sort_out<8, KIND>(list, nlist, k, T, out, lane);
         }
     } else {
         const int L = next_pow2(nlist);
         for (int i = nlist + threadIdx.x; i < L; i += blockDim.x) list[i] = INT_MIN;
         block_sort_smem_desc(list, L);
-        for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < nlist ? list[i] : T;
+        for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = ordered<KIND>(i < nlist ? list[i] : T);
     }
     // Leave the scratch as the next launch expects it.
     for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) sc.bmax[i] = 0u;
@@ -313,13 +375,21 @@ __device__ void second_stage(const Scratch& sc, int k, int lists_per_block, int 
 
 // Publish this block's threshold and take a ticket (after every thread has
 // written its candidates); returns true in the last block to finish.
+// The ticket is an acquire-release atomic: its release makes the block's
+// candidate writes (ordered before it by the barrier) and the threshold
+// published just before it visible to the block that draws the last
+// ticket, whose acquire orders its later reads after them.
+__device__ __forceinline__ unsigned ticket_acq_rel(unsigned* p) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ bool block_done(const Scratch& sc, int block_thresh, int* s_last) {
-    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
         if (block_thresh != INT_MIN) atomicMax(&sc.ctrl->thresh, bias(block_thresh));
-        __threadfence();
-        const unsigned ticket = atomicAdd(&sc.ctrl->ticket, 1u);
+        const unsigned ticket = ticket_acq_rel(&sc.ctrl->ticket);
         *s_last = ticket == gridDim.x - 1;
     }
     __syncthreads();
@@ -357,10 +427,12 @@ constexpr int kStreamThreads = (kCons + 1) * 32;
 constexpr int kWarpStages = 3;               // tiles in flight per consumer warp
 constexpr int kRingBytes = kCons * kWarpStages * kTileVec * 16;
 constexpr int kMonitorRounds = 1 << 20;      // bound on the monitor's polling rounds
-constexpr int kStaticPct = 70;               // share of the tiles assigned up front (percent)
-static_assert(kStreamThreads >= kI32MaxTileMax / 4, "second stage: four tile maxima per thread at most");
+constexpr int kStaticPct = 100;              // share of the input assigned up front (percent)
+static_assert(kStreamThreads * (kI32MaxTileMax / 256) >= kI32MaxTileMax &&
+                  kStreamThreads * (kI32MaxTileMax / 256) >= kI32MaxGrid,
+              "second stage: every list and tile maximum has a thread slot");
 
-template <int L, int GL>
+template <int L, int GL, int KIND>
 __global__ void __launch_bounds__(kStreamThreads, 2)
 topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* __restrict__ out,
                        unsigned char* __restrict__ scratch, int cap_limit, int release, int static_pct) {
@@ -387,24 +459,55 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
     const Split sp = split_input(in, n);
     const size_t G = gridDim.x;
     const size_t b = blockIdx.x;
-    // Tile schedule.  Rounds [0, R): consumer warp w of block b takes tile
-    // b + G*(w + kCons*i) in round i, so the first S = R*G*kCons tiles are
-    // shared out up front, with no atomics and before the previous launch on
-    // the stream has finished.  Tiles [S, ntiles) are cut into nr contiguous
-    // ranges, each with a claim counter; a warp that has used up its static
-    // tiles claims one tile at a time, from its own range first and then
-    // from any range that has tiles left.  Fast warps (and SMs) so take more
-    // tiles than slow ones, and all warps finish at about the same time.
-    // Tile ids fit 32 bits: n <= 2^40 elements is at most 2^30 tiles.
+    // Work schedule, in items of at most one 4 KiB tile (kTileVec vectors).
+    // With P = G*kCons consumer warps, warp p = b + G*w (interleaved, so
+    // that neighbouring warps read neighbouring tiles at the same time):
+    //   full rounds   round i < R: item p + P*i, the tile of that index;
+    //   piece         item R*P + p: the warp's equal share (to one vector)
+    //                 of the vectors left of the static part after the full
+    //                 rounds, so that every warp streams the same bytes;
+    //   claimed       the vectors after the static part (a share of
+    //                 100 - static_pct percent) as tiles in nr contiguous
+    //                 ranges with a claim counter each; a warp that has
+    //                 finished its static items claims one tile at a time,
+    //                 from its own range first, then from any range with
+    //                 tiles left.
+    // Item ids fit 31 bits: n <= 2^40 elements is at most 2^30 tiles.  By
+    // default (static_pct = 100), and always with fewer blocks than k, items
+    // are whole tiles only: rounds up to the last tile, no pieces, nothing
+    // claimed.  (Measured on GB300 at 1e8: equal pieces and claimed tiles
+    // both finished later than whole tiles; the warps' rates differ more
+    // than their shares.)  With fewer blocks than k the k-th largest tile
+    // maximum bounds the answer in the second stage.
     const unsigned ntiles = (unsigned)sp.ntiles;
-    const unsigned per_round = (unsigned)G * kCons;
-    const unsigned R = (unsigned)(((unsigned long long)ntiles * (unsigned)static_pct / 100) / per_round);
-    const unsigned S = R * per_round;
-    const unsigned D = ntiles - S;
-    const int nr = D < (unsigned)kI32DynRanges ? (int)D : kI32DynRanges;
-    // With fewer blocks than k, the k-th largest tile maximum bounds the
-    // answer instead of the blocks' maxima (second stage).
     const bool use_tmax = (int)G < k && ntiles <= (unsigned)kI32MaxTileMax;
+    // All static (the default): whole tiles round-robin, as many rounds as
+    // it takes, no pieces and nothing claimed.
+    const bool whole = use_tmax || static_pct >= 100;
+    const unsigned P = (unsigned)G * kCons;
+    const size_t S_vec = whole ? sp.nvec : sp.nvec * (size_t)static_pct / 100;  // static vectors
+    const unsigned R = whole ? (ntiles + P - 1) / P : (unsigned)(S_vec / ((size_t)P * kTileVec));
+    const size_t full_vec = whole ? sp.nvec : (size_t)R * P * kTileVec;  // vectors of the full rounds
+    const size_t rem = S_vec > full_vec ? S_vec - full_vec : 0;             // vectors of the pieces (< P tiles)
+    const unsigned piece_q = (unsigned)(rem / P), piece_r = (unsigned)(rem % P);
+    const bool pieces = rem > 0;
+    const unsigned D = (unsigned)((sp.nvec - S_vec + kTileVec - 1) / kTileVec);  // claimed tiles
+    const int nr = D < (unsigned)kI32DynRanges ? (int)D : kI32DynRanges;
+    const unsigned dyn_id0 = R * P + (pieces ? P : 0u);  // id of the first claimed tile
+    // Vectors [base, base + cnt) of item `id` (cnt 0: nothing there).
+    auto item_span = [&](unsigned id, size_t& base, unsigned& cnt) {
+        if (id < R * P) {
+            base = (size_t)id * kTileVec;
+        } else if (id < dyn_id0) {
+            const unsigned q = id - R * P;
+            base = full_vec + (size_t)q * piece_q + (q < piece_r ? q : piece_r);
+            cnt = piece_q + (q < piece_r ? 1u : 0u);
+            return;
+        } else {
+            base = S_vec + (size_t)(id - dyn_id0) * kTileVec;
+        }
+        cnt = base >= sp.nvec ? 0u : (sp.nvec - base < (size_t)kTileVec ? (unsigned)(sp.nvec - base) : (unsigned)kTileVec);
+    };
     // The block-maxima threshold needs at least k blocks.
     const bool use_bmax = (int)G >= k;
 
@@ -422,7 +525,7 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
                 const long long tv = (long long)sp.nvec - kTailVec + 2 * lane;
 #pragma unroll
                 for (int q = 0; q < 2; ++q)
-                    s[q] = tv + q >= 0 ? __ldg(sp.body + tv + q) : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
+                    s[q] = tv + q >= 0 ? ordered4<KIND>(__ldg(sp.body + tv + q)) : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
                 const int tseed = seed_from_groups<GL>(s, k, lane);
                 if (lane == 0) atomicMax(&s_thresh, tseed);
             }
@@ -432,7 +535,9 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
         grid_dependency_wait();
         int pub_t = INT_MIN, pub_cmax = INT_MIN;
         for (int round = 0; round < kMonitorRounds; ++round) {
-            const bool last = *(volatile int*)&s_done == kCons;
+            // Once every consumer is done the block publishes its own
+            // threshold with its ticket: nothing is left for the monitor.
+            if (*(volatile int*)&s_done == kCons) break;
             const int st = *(volatile int*)&s_thresh;
             if (st > pub_t) {
                 if (lane == 0) atomicMax(&sc.ctrl->thresh, bias(st));
@@ -443,7 +548,6 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
                 if (lane == 0) atomicMax(&sc.bmax[b], bias(cm));
                 pub_cmax = cm;
             }
-            if (last) break;
             unsigned bv[8];
             if (use_bmax) {
 #pragma unroll
@@ -477,6 +581,7 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
                 __syncwarp();
             }
             if (t > st && lane == 0) atomicMax(&s_thresh, t);
+            if (*(volatile int*)&s_done == kCons) break;
             __nanosleep(256);
         }
     } else {
@@ -513,7 +618,7 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
         if (b == 0 && warp == 0) {
             const size_t ns = sp.head + (n - sp.tail0);
             const size_t pos = (size_t)lane < sp.head ? (size_t)lane : sp.tail0 + (lane - sp.head);
-            enqueue(q, nq, (size_t)lane < ns ? in[pos] : INT_MIN, INT_MIN, lane);
+            enqueue(q, nq, (size_t)lane < ns ? ordered<KIND>(in[pos]) : INT_MIN, INT_MIN, lane);
         }
 
         // The warp's i-th tile goes through stage i % kWarpStages; s_tile
@@ -521,24 +626,29 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
         int4* my_ring = ring + (size_t)warp * kWarpStages * kTileVec;
         uint64_t* my_bar = full_bar + warp * kWarpStages;
         int* my_tile = s_tile + warp * kWarpStages;
-        unsigned static_i = 0;   // static rounds used
+        const unsigned wp = (unsigned)b + (unsigned)G * (unsigned)warp;  // this warp's index p
+        unsigned static_i = 0;   // static items used: R full rounds, then the piece
         int cur = nr > 0 ? (int)(((unsigned)b * kCons + (unsigned)warp) % (unsigned)nr) : 0;  // range claimed from
         bool done = false;       // no tile left anywhere
         bool waited = false;     // grid dependency waited for (the counters are the previous launch's until then)
-        auto range_lo = [&](int c) -> unsigned {
-            return S + (unsigned)((unsigned long long)D * (unsigned)c / (unsigned)nr);
-        };
+        auto range_lo = [&](int c) -> unsigned { return (unsigned)((unsigned long long)D * (unsigned)c / (unsigned)nr); };
         // A claim in two steps, so that the atomic's round trip overlaps other
-        // work: start_claim returns a static tile, or -1, or (kCounter) says
+        // work: start_claim returns a static item, or -1, or (kCounter) says
         // that lane 0 holds a counter value in `got`; finish_claim turns that
-        // into a tile id, or -1 when every range is used up.
+        // into an item id, or -1 when every range is used up.
         constexpr int kCounter = -2;
         unsigned got = 0;
         auto start_claim = [&]() -> int {
-            if (static_i < R) {
-                const unsigned t = (unsigned)b + (unsigned)G * ((unsigned)warp + kCons * static_i);
+            while (static_i < R) {
+                const unsigned id = wp + P * static_i++;
+                size_t bs;
+                unsigned c;
+                item_span(id, bs, c);
+                if (c) return (int)id;
+            }
+            if (static_i == R) {
                 ++static_i;
-                return (int)t;
+                if (pieces && (wp < piece_r || piece_q > 0)) return (int)(R * P + wp);
             }
             if (done || nr == 0) return -1;
             if (!waited) {
@@ -553,7 +663,7 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
             for (int tries = 0; tries <= 2 * kI32DynRanges + 2; ++tries) {
                 got = __shfl_sync(kFullMask, got, 0);
                 const unsigned lo = range_lo(cur), len = range_lo(cur + 1) - lo;
-                if (got < len) return (int)(lo + got);
+                if (got < len) return (int)(dyn_id0 + lo + got);
                 // Range `cur` is used up (for good: its counter only grows).
                 // Read every counter once and move to the first range after
                 // it, cyclically, that still has tiles.
@@ -584,8 +694,9 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
             const int st = (int)(i % kWarpStages);
             if (lane == 0) {
                 my_tile[st] = tile;
-                const size_t base = (size_t)tile * kTileVec;
-                const size_t cnt = sp.nvec - base < (size_t)kTileVec ? sp.nvec - base : (size_t)kTileVec;
+                size_t base;
+                unsigned cnt;
+                item_span((unsigned)tile, base, cnt);
                 mbar_arrive_expect_tx(&my_bar[st], (uint32_t)(cnt * 16));
                 // Default L2 policy: an evict-first hint measured ~1.5% slower
                 // here (one launch per call, nothing after it to protect).
@@ -619,17 +730,18 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
                 break;
             }
             const unsigned tile = (unsigned)my_tile[stg];
-            const size_t base = (size_t)tile * kTileVec;
-            const size_t cnt = sp.nvec - base < (size_t)kTileVec ? sp.nvec - base : (size_t)kTileVec;
+            size_t base;
+            unsigned cnt;
+            item_span(tile, base, cnt);
             const int4* st = my_ring + (size_t)stg * kTileVec;
             int4 r[kU];
-            if (cnt == (size_t)kTileVec) {
+            if (cnt == (unsigned)kTileVec) {
 #pragma unroll
-                for (int u = 0; u < kU; ++u) r[u] = st[u * 32 + lane];
+                for (int u = 0; u < kU; ++u) r[u] = ordered4<KIND>(st[u * 32 + lane]);
             } else {
 #pragma unroll
                 for (int u = 0; u < kU; ++u)
-                    r[u] = (size_t)(u * 32 + lane) < cnt ? st[u * 32 + lane]
+                    r[u] = (unsigned)(u * 32 + lane) < cnt ? ordered4<KIND>(st[u * 32 + lane])
                                                          : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
             }
             __syncwarp();
@@ -728,17 +840,17 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
     // it (and the block's k-th value) before the ticket, whatever the
     // monitor managed to do.
     if (block_done(sc, kmax(s_thresh, block_kth), &s_last))
-        second_stage(sc, k, 1, K, out, reinterpret_cast<int*>(ring), kRingBytes / (int)sizeof(int), cap_limit,
+        second_stage<KIND>(sc, k, 1, K, out, reinterpret_cast<int*>(ring), kRingBytes / (int)sizeof(int), cap_limit,
                      &s_count, use_tmax ? (int)sp.ntiles : 0);
 }
 
 // ------------------------------------------------------------ host side --
 
-template <int L, int GL>
+template <int L, int GL, int KIND>
 struct StreamVariant {
     static constexpr int kThreads = kStreamThreads;
     static size_t smem_bytes() { return kRingBytes; }
-    static const void* fn() { return reinterpret_cast<const void*>(&topk_i32_stream_kernel<L, GL>); }
+    static const void* fn() { return reinterpret_cast<const void*>(&topk_i32_stream_kernel<L, GL, KIND>); }
     // Launched with programmatic stream serialization: when the previous
     // kernel on the stream is one of these, this one's blocks start once all
     // of that kernel's blocks have read their input, and overlap its last
@@ -755,15 +867,18 @@ struct StreamVariant {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = early ? 1 : 0;
-        return cudaLaunchKernelEx(&cfg, topk_i32_stream_kernel<L, GL>, in, n, k, out, scratch, cap_limit,
+        return cudaLaunchKernelEx(&cfg, topk_i32_stream_kernel<L, GL, KIND>, in, n, k, out, scratch, cap_limit,
                                   release ? 1 : 0, static_pct);
     }
     static size_t units_per_block() { return kCons; }
 };
 
-using VarK32 = StreamVariant<1, 1>;
-using VarK64 = StreamVariant<2, 2>;
-using VarK128 = StreamVariant<4, 4>;
+template <int KIND>
+using VarK32 = StreamVariant<1, 1, KIND>;
+template <int KIND>
+using VarK64 = StreamVariant<2, 2, KIND>;
+template <int KIND>
+using VarK128 = StreamVariant<4, 4, KIND>;
 
 // Blocks per SM and SM count of a kernel variant on a device, found once
 // (the shared-memory opt-in is set at the same time) and cached.
@@ -820,19 +935,39 @@ cudaError_t plan_for(int device, size_t n, I32Plan* plan) {
 
 }  // namespace
 
-cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan) {
-    if (k <= 32) return plan_for<VarK32>(device, n, plan);
-    if (k <= 64) return plan_for<VarK64>(device, n, plan);
-    return plan_for<VarK128>(device, n, plan);
+namespace {
+
+template <int KIND>
+cudaError_t plan_kind(int device, size_t n, int k, I32Plan* plan) {
+    if (k <= 32) return plan_for<VarK32<KIND>>(device, n, plan);
+    if (k <= 64) return plan_for<VarK64<KIND>>(device, n, plan);
+    return plan_for<VarK128<KIND>>(device, n, plan);
+}
+
+template <int KIND>
+cudaError_t launch_kind(const I32Plan& plan, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
+                        unsigned char* sc, bool early, bool release) {
+    const int cap = plan.stage2_cap, sp = plan.static_pct;
+    if (k <= 32) return VarK32<KIND>::launch(plan.grid, s, in, n, k, out, sc, cap, early, release, sp);
+    if (k <= 64) return VarK64<KIND>::launch(plan.grid, s, in, n, k, out, sc, cap, early, release, sp);
+    return VarK128<KIND>::launch(plan.grid, s, in, n, k, out, sc, cap, early, release, sp);
+}
+
+}  // namespace
+
+cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan, int kind) {
+    plan->kind = kind;
+    if (kind == kKeyU32) return plan_kind<kKeyU32>(device, n, k, plan);
+    if (kind == kKeyF32) return plan_kind<kKeyF32>(device, n, k, plan);
+    return plan_kind<kKeyI32>(device, n, k, plan);
 }
 
 cudaError_t i32_launch(const I32Plan& plan, cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out,
                        void* scratch, bool early, bool release) {
     auto* sc = static_cast<unsigned char*>(scratch);
-    const int cap = plan.stage2_cap, sp = plan.static_pct;
-    if (k <= 32) return VarK32::launch(plan.grid, s, in, n, k, out, sc, cap, early, release, sp);
-    if (k <= 64) return VarK64::launch(plan.grid, s, in, n, k, out, sc, cap, early, release, sp);
-    return VarK128::launch(plan.grid, s, in, n, k, out, sc, cap, early, release, sp);
+    if (plan.kind == kKeyU32) return launch_kind<kKeyU32>(plan, s, in, n, k, out, sc, early, release);
+    if (plan.kind == kKeyF32) return launch_kind<kKeyF32>(plan, s, in, n, k, out, sc, early, release);
+    return launch_kind<kKeyI32>(plan, s, in, n, k, out, sc, early, release);
 }
 
 }  // namespace topk

@@ -8,6 +8,10 @@
 
 namespace topk {
 
+// Key kinds of the 32-bit TopK entry points: int32 (topk_i32), uint32
+// (topk_u32) and float32 bit patterns under IEEE 754 totalOrder (topk_f32).
+enum KeyKind : int { kKeyI32 = 0, kKeyU32 = 1, kKeyF32 = 2 };
+
 // Control words of one int32 TopK launch.  Both are zero between launches:
 // the last block of a launch resets them after use.
 //   thresh  the largest published threshold, stored as (value ^ 0x80000000)
@@ -93,8 +97,18 @@ constexpr size_t radix_scratch_bytes(size_t cap) { return kRadixBufOffset + cap 
 // plan's last kernel lets the next launch on the stream start before it
 // completes; only for callers that make sure such a launch does not read
 // `out` before it waits (see i32_launch's `early`).
+// kind: the key kind (0 int32, 1 uint32, 2 float32 under totalOrder).
+// bigk: null, or (for k above kRadixMaxK) k words where the plan leaves the
+// complements of the TopK's keys, unordered, instead of sorting them into
+// `out`: the caller sorts them ascending (sort_launch) and writes `out` with
+// radix_bigk_out.
 cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out, void* scratch,
-                         size_t cap, int* launches, bool release);
+                         size_t cap, int* launches, bool release, int kind = 0, uint32_t* bigk = nullptr);
+cudaError_t radix_bigk_out(cudaStream_t s, const uint32_t* sorted, int k, int32_t* out, int kind);
+// Largest k of the big-k form (a share of the candidate buffer, so that the
+// sampled threshold usually keeps few enough candidates).
+constexpr int kBigKMax = 131072;
+static_assert(kBigKMax * 2 <= (int)kRadixCap, "the big-k form keeps half the candidate buffer free");
 
 // Test options of the radix plan (TOPK_OPT_RADIX_CAP, TOPK_OPT_RADIX_SAMPLE_RANK; 0 = default).
 int radix_cap_option();
@@ -112,16 +126,20 @@ struct I32Plan {
     int max_grid;    // persistent grid size for this device (blocks per SM x SMs), <= kI32MaxGrid
     int stage2_cap;  // 0, or a lower capacity for the second stage's shared list (TOPK_OPT_STAGE2_CAP)
     int static_pct;  // share of the tiles, in percent, assigned statically; the rest are claimed
+    int kind;        // key kind (KeyKind of topk_device.cuh): int32, uint32 or float32 words
 };
 
 // Current value of TOPK_OPT_STAGE2_CAP (0 = default).
 int stage2_cap_option();
 // Current value of TOPK_OPT_STREAM_STATIC (0 = default, else percent + 1).
 int stream_static_option();
+// Current value of TOPK_OPT_SORT_SPINS (0 = default).
+int sort_spins_option();
 
 // Grid for an n-element, k-wide selection on `device` (k <= 128: the
 // streaming plan; larger k use radix_launch).
-cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan);
+// kind: the key kind (0 int32, 1 uint32, 2 float32 under totalOrder).
+cudaError_t i32_plan(int device, size_t n, int k, I32Plan* plan, int kind = 0);
 
 // Enqueue the single-launch int32 TopK.  scratch holds i32_scratch_bytes(plan.grid)
 // bytes, 256-byte aligned, whose [kI32ResetBegin, kI32ResetEnd) bytes are zero

@@ -26,7 +26,7 @@ namespace {
 constexpr size_t kNoallocScratchBytes = TOPK_NOALLOC_SCRATCH_BYTES;
 static_assert(kNoallocScratchBytes >= topk::i32_scratch_bytes(1),
               "the scratch must hold the control words, block maxima, counts and one block's candidates");
-static_assert(kNoallocScratchBytes >= topk::radix_scratch_bytes(TOPK_MAX_K),
+static_assert(kNoallocScratchBytes >= topk::radix_scratch_bytes(TOPK_NOALLOC_MAX_K),
               "the radix plan's candidate buffer must hold at least the largest k keys");
 // The candidate buffer of the radix plan here, in keys (the header quotes it).
 constexpr size_t kNoallocRadixCap = (kNoallocScratchBytes - topk::radix_scratch_bytes(0)) / sizeof(unsigned);
@@ -82,7 +82,7 @@ extern "C" int topk_i32_noalloc(const int32_t* in, size_t n, int k, int32_t* out
     if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 3u) return TOPK_ERR_INVALID_ARG;
     const uintptr_t a = reinterpret_cast<uintptr_t>(in), b = reinterpret_cast<uintptr_t>(out);
     if (a < b + (size_t)k * sizeof(int32_t) && b < a + n * sizeof(int32_t)) return TOPK_ERR_INVALID_ARG;
-    if (k > TOPK_MAX_K || n > (size_t(1) << 40)) return TOPK_ERR_UNSUPPORTED;
+    if (k > TOPK_NOALLOC_MAX_K || n > (size_t(1) << 40)) return TOPK_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     int device = 0;

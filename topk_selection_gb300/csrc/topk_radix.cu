@@ -207,7 +207,7 @@ struct WarpAppender {
 // of the 16-byte-aligned body in batches of kRU (coalesced); f_vec(v, ok) is
 // called per vector with warp-uniform control.  The < 8 scalars outside the
 // body go to warp 0 of block 0 through f_tail(value, ok), one per lane.
-template <class FV, class FT>
+template <int KIND, class FV, class FT>
 __device__ __forceinline__ void for_each_vec(const int32_t* __restrict__ in, size_t n, FV f_vec, FT f_tail) {
     const uintptr_t addr = reinterpret_cast<uintptr_t>(in);
     size_t head = ((16u - (unsigned)(addr & 15u)) & 15u) >> 2;
@@ -222,7 +222,7 @@ __device__ __forceinline__ void for_each_vec(const int32_t* __restrict__ in, siz
 #pragma unroll
         for (int u = 0; u < kRU; ++u) {
             const size_t i = base + (size_t)u * blockDim.x + threadIdx.x;
-            r[u] = i < nvec ? ld_nc_hint(body + i, policy) : make_int4(0, 0, 0, 0);
+            r[u] = i < nvec ? ordered4<KIND>(ld_nc_hint(body + i, policy)) : make_int4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kRU; ++u) f_vec(r[u], base + (size_t)u * blockDim.x + threadIdx.x < nvec);
@@ -231,13 +231,13 @@ __device__ __forceinline__ void for_each_vec(const int32_t* __restrict__ in, siz
         const size_t ns = head + (n - tail0);
         const size_t lane = threadIdx.x;
         const size_t pos = lane < head ? lane : tail0 + (lane - head);
-        f_tail(lane < ns ? in[pos] : 0, lane < ns);
+        f_tail(lane < ns ? ordered<KIND>(in[pos]) : 0, lane < ns);
     }
 }
 
-template <class F>
+template <int KIND, class F>
 __device__ __forceinline__ void for_each_key(const int32_t* __restrict__ in, size_t n, F f) {
-    for_each_vec(
+    for_each_vec<KIND>(
         in, n,
         [&](const int4& v, bool ok) {
             f(key_of(v.x), ok);
@@ -305,6 +305,7 @@ __device__ void pick_bucket(const RadixView& rv, int nbins, unsigned need, unsig
 }
 
 // The filter: keys above t to the buffer, keys equal to t counted.
+template <int KIND>
 __global__ void __launch_bounds__(kRThreads, 2)
 radix_filter_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned char* __restrict__ scratch,
                     unsigned cap) {
@@ -323,7 +324,7 @@ radix_filter_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned ch
         neq += (ok && v == tv) ? 1u : 0u;
         ap.push(rv, cap, key_of(v), ok && v > tv);
     };
-    for_each_vec(
+    for_each_vec<KIND>(
         in, n,
         [&](const int4& v, bool ok) {
             const int mx = max(max(v.x, v.y), max(v.z, v.w));
@@ -356,6 +357,7 @@ radix_filter_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned ch
 
 // Exact pass 1: 12-bit histogram of the top bits; the last block picks b1
 // and decides whether pass 2 can collect every key at or above it.
+template <int KIND>
 __global__ void __launch_bounds__(kRThreads, 2)
 radix_exact1_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned char* __restrict__ scratch,
                     unsigned cap) {
@@ -370,7 +372,7 @@ radix_exact1_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned ch
     for (int i = threadIdx.x; i < kBins; i += blockDim.x) sh[i] = 0u;
     __syncthreads();
     if (!s_go) return;
-    for_each_key(in, n, [&](unsigned u, bool ok) { hist_add(sh, u >> 20, ok); });
+    for_each_key<KIND>(in, n, [&](unsigned u, bool ok) { hist_add(sh, u >> 20, ok); });
     if (pass_done(rv, sh, &s_last)) {
         pick_bucket(rv, kBins, (unsigned)k, s_scan, &s_pick);
         if (threadIdx.x == 0) {
@@ -385,6 +387,7 @@ radix_exact1_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned ch
 
 // Exact pass 2: collect every key at or above b1, or histogram the next 12
 // bits of the keys in b1.
+template <int KIND>
 __global__ void __launch_bounds__(kRThreads, 2)
 radix_exact2_kernel(const int32_t* __restrict__ in, size_t n, unsigned char* __restrict__ scratch, unsigned cap) {
     __shared__ unsigned sh[kBins];
@@ -409,10 +412,10 @@ radix_exact2_kernel(const int32_t* __restrict__ in, size_t n, unsigned char* __r
     const bool collect = s_mode == kExactCollectAll;
     if (collect) {
         WarpAppender ap{stage[threadIdx.x >> 5], 0u, false};
-        for_each_key(in, n, [&](unsigned u, bool ok) { ap.push(rv, cap, u, ok && (u & 0xFFF00000u) >= prefix); });
+        for_each_key<KIND>(in, n, [&](unsigned u, bool ok) { ap.push(rv, cap, u, ok && (u & 0xFFF00000u) >= prefix); });
         ap.flush(rv, cap);
     } else {
-        for_each_key(in, n, [&](unsigned u, bool ok) {
+        for_each_key<KIND>(in, n, [&](unsigned u, bool ok) {
             hist_add(sh, (u >> 8) & 0xFFFu, ok && (u & 0xFFF00000u) == prefix);
         });
     }
@@ -437,6 +440,7 @@ radix_exact2_kernel(const int32_t* __restrict__ in, size_t n, unsigned char* __r
 // fixes the k-th key T and appends the keys in (T, prefix | 0xFF], which the
 // histogram gives value by value.  Fewer than k keys are above T, so the
 // buffer (cap >= k) holds them all.
+template <int KIND>
 __global__ void __launch_bounds__(kRThreads, 2)
 radix_exact3_kernel(const int32_t* __restrict__ in, size_t n, unsigned char* __restrict__ scratch, unsigned cap) {
     __shared__ unsigned sh[kBins];
@@ -459,7 +463,7 @@ radix_exact3_kernel(const int32_t* __restrict__ in, size_t n, unsigned char* __r
     if (!s_go) return;
     const unsigned prefix = s_prefix;
     WarpAppender ap{stage[threadIdx.x >> 5], 0u, false};
-    for_each_key(in, n, [&](unsigned u, bool ok) {
+    for_each_key<KIND>(in, n, [&](unsigned u, bool ok) {
         ap.push(rv, cap, u, ok && u > (prefix | 0xFFu));
         hist_add(sh, u & 0xFFu, ok && (u & 0xFFFFFF00u) == prefix);
     });
@@ -640,9 +644,10 @@ __device__ __forceinline__ unsigned range_of(const unsigned* lb, unsigned nr, un
 //                 the control words as the filter threshold.
 // mode kClFinal:  the TopK from the buffered keys, as the control words say;
 //                 zero the control words.
+template <int KIND>
 __global__ void __cluster_dims__(kClCtas, 1, 1) __launch_bounds__(kClThreads, 1)
 radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j_sample, int32_t* __restrict__ out,
-                     unsigned char* __restrict__ scratch, unsigned cap, int mode) {
+                     unsigned char* __restrict__ scratch, unsigned cap, int mode, uint32_t* __restrict__ bigk) {
     extern __shared__ __align__(16) unsigned char radix_cl_smem[];
     ClSmem& S = *reinterpret_cast<ClSmem*>(radix_cl_smem);
     grid_dependency_wait();  // launched early (launch_pdl): wait for the previous kernel's writes
@@ -696,7 +701,7 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
         for (int m = 0; m < kSampleVec; ++m) {
             const unsigned x = lo / 4 + m * kClThreads + tid;
             const size_t vi = (size_t)(x >> 2) * (nvec - 4) / (kSegments - 1) + (x & 3);
-            v[m] = __ldg(body + vi);
+            v[m] = ordered4<KIND>(__ldg(body + vi));
         }
 #pragma unroll
         for (int m = 0; m < kSampleVec; ++m) {
@@ -719,7 +724,7 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
             } else {
 #pragma unroll
                 for (int u = 0; u < kLd; ++u)
-                    v[u] = key_of(__ldg(in + lo + min(base + u * kClThreads + tid, mine - 1)));
+                    v[u] = key_of(ordered<KIND>(__ldg(in + lo + min(base + u * kClThreads + tid, mine - 1))));
             }
 #pragma unroll
             for (int u = 0; u < kLd; ++u) {
@@ -809,6 +814,23 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
 #pragma unroll
     for (int r = 0; r < kClCtas; ++r) total += S.ccount[r];
     unsigned nr = 0;  // ranges for the sort kernel
+    if (bigk) {
+        // k beyond what the range plan sorts: every CTA writes its keys
+        // above T, complemented (so that an ascending sort puts the largest
+        // first), to bigk[0, total) at its offset, and ~T fills [total, k);
+        // the library's LSD radix sort then orders the k words.
+        unsigned off = 0;
+        for (unsigned r = 0; r < rank; ++r) off += S.ccount[r];
+        off += S.woff[w];
+        for (unsigned m = lane; m < cw; m += 32) bigk[off + m] = ~S.keys[w0 + m];
+        for (unsigned i = total + rank * kClThreads + tid; i < (unsigned)k; i += kClCtas * kClThreads)
+            bigk[i] = ~T;
+        if (rank == 0 && tid == 0) reinterpret_cast<RadixPlan*>(scratch + kRadixCandOffset)->nranges = 0u;
+        cluster_barrier();  // no CTA exits while another may read its shared memory
+        if (mode == kClFinal && rank == 0 && tid < (unsigned)kCtrlWords)
+            reinterpret_cast<unsigned*>(rv.ctrl)[tid] = 0u;
+        return;
+    }
     if (total <= kSmallCap) {
         // Few keys above T: rank 0 gathers them all, sorts them with the
         // whole CTA and writes them; the sort kernel has no ranges to do.
@@ -828,7 +850,7 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
             for (unsigned i = total + tid; i < (unsigned)P; i += kClThreads) all[i] = 0u;  // below every key > T
             static_assert(kSmallCap <= 2 * kClThreads, "the register-stage sort takes two keys per thread");
             block_sort_reg_desc<unsigned, kClThreads>(all, P);
-            for (unsigned i = tid; i < total; i += kClThreads) out[i] = value_of(all[i]);
+            for (unsigned i = tid; i < total; i += kClThreads) out[i] = ordered<KIND>(value_of(all[i]));
         }
     } else {
         // Radix range plan.  The keys above T lie in [lo, hi] (lo = T + 1, hi
@@ -1111,13 +1133,13 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
         if (nr) {
             for (unsigned m = lane; m < cw; m += 32) {
                 const unsigned u = S.keys[w0 + m];
-                out[atomicAdd(&S.rpos[range_of(S.lb, nr, u)], 1u)] = value_of(u);
+                out[atomicAdd(&S.rpos[range_of(S.lb, nr, u)], 1u)] = ordered<KIND>(value_of(u));
             }
         }
     }
     // Copies of the k-th key after the keys above it.
     for (unsigned i = total + rank * kClThreads + tid; i < (unsigned)k; i += kClCtas * kClThreads)
-        out[i] = value_of(T);
+        out[i] = ordered<KIND>(value_of(T));
     // The range table for the sort kernel.
     if (rank == 0) {
         RadixPlan* plan = reinterpret_cast<RadixPlan*>(scratch + kRadixCandOffset);
@@ -1135,19 +1157,19 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
 // plan in place, in registers (up to kSortRegCap keys); a range of one value
 // is already in order.  A larger range (the sample missed a dense value
 // range) is sorted by its CTA in shared memory.
-template <int N>
+template <int N, int KIND>
 __device__ __forceinline__ void warp_sort_range(int32_t* __restrict__ a, unsigned sz, int lane) {
     unsigned v[N];
 #pragma unroll
     for (int jj = 0; jj < N; ++jj) {
         const unsigned p = jj * 32 + lane;
-        v[jj] = p < sz ? key_of(__ldcg(a + p)) : 0u;
+        v[jj] = p < sz ? key_of(ordered<KIND>(__ldcg(a + p))) : 0u;
     }
     warp_sort_desc(v, lane);
 #pragma unroll
     for (int jj = 0; jj < N; ++jj) {
         const unsigned p = jj * 32 + lane;
-        if (p < sz) a[p] = value_of(v[jj]);
+        if (p < sz) a[p] = ordered<KIND>(value_of(v[jj]));
     }
 }
 
@@ -1156,6 +1178,7 @@ __device__ __forceinline__ bool single_value_range(const RadixPlan* plan, unsign
     return q ? __ldcg(&plan->lb[q - 1]) == lbq + 1 : lbq == 0xFFFFFFFFu;
 }
 
+template <int KIND>
 __global__ void __launch_bounds__(kSortWarps * 32, 1)
 radix_sort_kernel(int32_t* __restrict__ out, const unsigned char* __restrict__ scratch, int release) {
     extern __shared__ __align__(16) unsigned radix_sort_smem[];
@@ -1172,9 +1195,9 @@ radix_sort_kernel(int32_t* __restrict__ out, const unsigned char* __restrict__ s
     if (q < nr && !single_value_range(plan, q)) {
         const unsigned s0 = __ldcg(&plan->rstart[q]), sz = __ldcg(&plan->rstart[q + 1]) - s0;
         if (sz >= 2 && sz <= 256)
-            warp_sort_range<8>(out + s0, sz, lane);
+            warp_sort_range<8, KIND>(out + s0, sz, lane);
         else if (sz > 256 && sz <= (unsigned)kSortRegCap)
-            warp_sort_range<16>(out + s0, sz, lane);
+            warp_sort_range<16, KIND>(out + s0, sz, lane);
 
     }
     for (unsigned qq = q0; qq < q0 + kSortWarps && qq < nr; ++qq) {
@@ -1183,9 +1206,9 @@ radix_sort_kernel(int32_t* __restrict__ out, const unsigned char* __restrict__ s
         __syncthreads();
         const int L = next_pow2((int)sz);
         for (int i = threadIdx.x; i < L; i += blockDim.x)
-            radix_sort_smem[i] = (unsigned)i < sz ? key_of(__ldcg(out + s0 + i)) : 0u;
+            radix_sort_smem[i] = (unsigned)i < sz ? key_of(ordered<KIND>(__ldcg(out + s0 + i))) : 0u;
         block_sort_smem_desc(radix_sort_smem, L);
-        for (unsigned i = threadIdx.x; i < sz; i += blockDim.x) out[s0 + i] = value_of(radix_sort_smem[i]);
+        for (unsigned i = threadIdx.x; i < sz; i += blockDim.x) out[s0 + i] = ordered<KIND>(value_of(radix_sort_smem[i]));
     }
 }
 
@@ -1203,10 +1226,10 @@ cudaError_t radix_fit(int device, RadixFit* out) {
         int sms = 0;
         cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
         if (e != cudaSuccess) return e;
-        const void* passes[] = {reinterpret_cast<const void*>(&radix_filter_kernel),
-                                reinterpret_cast<const void*>(&radix_exact1_kernel),
-                                reinterpret_cast<const void*>(&radix_exact2_kernel),
-                                reinterpret_cast<const void*>(&radix_exact3_kernel)};
+        const void* passes[] = {reinterpret_cast<const void*>(&radix_filter_kernel<kKeyI32>),
+                                reinterpret_cast<const void*>(&radix_exact1_kernel<kKeyI32>),
+                                reinterpret_cast<const void*>(&radix_exact2_kernel<kKeyI32>),
+                                reinterpret_cast<const void*>(&radix_exact3_kernel<kKeyI32>)};
         int per_sm = 1 << 30;
         for (const void* f : passes) {
             int b = 0;
@@ -1214,22 +1237,36 @@ cudaError_t radix_fit(int device, RadixFit* out) {
             if (e != cudaSuccess) return e;
             if (b < per_sm) per_sm = b;
         }
-        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&radix_cluster_kernel),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(ClSmem));
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&radix_sort_kernel),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kSortCap * sizeof(unsigned)));
-        if (e != cudaSuccess) return e;
+        const void* cl[] = {reinterpret_cast<const void*>(&radix_cluster_kernel<kKeyI32>),
+                            reinterpret_cast<const void*>(&radix_cluster_kernel<kKeyU32>),
+                            reinterpret_cast<const void*>(&radix_cluster_kernel<kKeyF32>)};
+        const void* so[] = {reinterpret_cast<const void*>(&radix_sort_kernel<kKeyI32>),
+                            reinterpret_cast<const void*>(&radix_sort_kernel<kKeyU32>),
+                            reinterpret_cast<const void*>(&radix_sort_kernel<kKeyF32>)};
+        for (int i = 0; i < 3; ++i) {
+            e = cudaFuncSetAttribute(cl[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(ClSmem));
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(so[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(kSortCap * sizeof(unsigned)));
+            if (e != cudaSuccess) return e;
+        }
         cache[device].grid = sms * (per_sm < 1 ? 1 : per_sm);
     }
     *out = cache[device];
     return cudaSuccess;
 }
 
-}  // namespace
+// Big k: the sorted complemented keys back to the kind's words, in order.
+template <int KIND>
+__global__ void __launch_bounds__(256) radix_bigk_out_kernel(const uint32_t* __restrict__ sorted, int k,
+                                                             int32_t* __restrict__ out) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < k; i += gridDim.x * blockDim.x)
+        out[i] = ordered<KIND>(value_of(~__ldg(sorted + i)));
+}
 
-cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out, void* scratch,
-                         size_t cap, int* launches, bool release) {
+template <int KIND>
+cudaError_t radix_launch_kind(cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out, void* scratch,
+                              size_t cap, int* launches, bool release, uint32_t* bigk) {
     *launches = 0;
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
@@ -1249,10 +1286,13 @@ cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int
     // reads anything, so each is launched early (launch_pdl), whatever
     // precedes it on the stream.
     if (n <= cap) {
-        e = launch_pdl(radix_cluster_kernel, kClCtas, kClThreads, cl_smem, s, in, n, k, 0u, out, sc, ucap, kClFull);
-        if (e == cudaSuccess)
-            e = launch_pdl(radix_sort_kernel, sort_grid, kSortWarps * 32, sort_smem, s, out, sc, release ? 1 : 0);
-        *launches = 2;
+        e = launch_pdl(radix_cluster_kernel<KIND>, kClCtas, kClThreads, cl_smem, s, in, n, k, 0u, out, sc, ucap, kClFull,
+                       bigk);
+        *launches = 1;
+        if (e == cudaSuccess && !bigk) {
+            e = launch_pdl(radix_sort_kernel<KIND>, sort_grid, kSortWarps * 32, sort_smem, s, out, sc, release ? 1 : 0);
+            *launches = 2;
+        }
         return e;
     }
     // Sample rank: k's expected share of the sample plus four standard
@@ -1267,16 +1307,38 @@ cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int
     if (grid > (size_t)f.grid) grid = f.grid;
     if (grid < 1) grid = 1;
     const unsigned g = (unsigned)grid;
-    e = launch_pdl(radix_cluster_kernel, kClCtas, kClThreads, cl_smem, s, in, n, k, j, out, sc, ucap, kClSample);
-    if (e == cudaSuccess) e = launch_pdl(radix_filter_kernel, g, kRThreads, 0, s, in, n, k, sc, ucap);
-    if (e == cudaSuccess) e = launch_pdl(radix_exact1_kernel, g, kRThreads, 0, s, in, n, k, sc, ucap);
-    if (e == cudaSuccess) e = launch_pdl(radix_exact2_kernel, g, kRThreads, 0, s, in, n, sc, ucap);
-    if (e == cudaSuccess) e = launch_pdl(radix_exact3_kernel, g, kRThreads, 0, s, in, n, sc, ucap);
+    e = launch_pdl(radix_cluster_kernel<KIND>, kClCtas, kClThreads, cl_smem, s, in, n, k, j, out, sc, ucap, kClSample,
+                   (uint32_t*)nullptr);
+    if (e == cudaSuccess) e = launch_pdl(radix_filter_kernel<KIND>, g, kRThreads, 0, s, in, n, k, sc, ucap);
+    if (e == cudaSuccess) e = launch_pdl(radix_exact1_kernel<KIND>, g, kRThreads, 0, s, in, n, k, sc, ucap);
+    if (e == cudaSuccess) e = launch_pdl(radix_exact2_kernel<KIND>, g, kRThreads, 0, s, in, n, sc, ucap);
+    if (e == cudaSuccess) e = launch_pdl(radix_exact3_kernel<KIND>, g, kRThreads, 0, s, in, n, sc, ucap);
     if (e == cudaSuccess)
-        e = launch_pdl(radix_cluster_kernel, kClCtas, kClThreads, cl_smem, s, in, n, k, 0u, out, sc, ucap, kClFinal);
-    if (e == cudaSuccess) e = launch_pdl(radix_sort_kernel, sort_grid, kSortWarps * 32, sort_smem, s, out, sc, release ? 1 : 0);
-    *launches = 7;
+        e = launch_pdl(radix_cluster_kernel<KIND>, kClCtas, kClThreads, cl_smem, s, in, n, k, 0u, out, sc, ucap, kClFinal,
+                       bigk);
+    *launches = 6;
+    if (e == cudaSuccess && !bigk) {
+        e = launch_pdl(radix_sort_kernel<KIND>, sort_grid, kSortWarps * 32, sort_smem, s, out, sc, release ? 1 : 0);
+        *launches = 7;
+    }
     return e;
+}
+
+}  // namespace
+
+cudaError_t radix_launch(cudaStream_t s, const int32_t* in, size_t n, int k, int32_t* out, void* scratch,
+                         size_t cap, int* launches, bool release, int kind, uint32_t* bigk) {
+    if (kind == kKeyU32) return radix_launch_kind<kKeyU32>(s, in, n, k, out, scratch, cap, launches, release, bigk);
+    if (kind == kKeyF32) return radix_launch_kind<kKeyF32>(s, in, n, k, out, scratch, cap, launches, release, bigk);
+    return radix_launch_kind<kKeyI32>(s, in, n, k, out, scratch, cap, launches, release, bigk);
+}
+
+cudaError_t radix_bigk_out(cudaStream_t s, const uint32_t* sorted, int k, int32_t* out, int kind) {
+    const int grid = (k + 255) / 256 < 1024 ? (k + 255) / 256 : 1024;
+    if (kind == kKeyU32) radix_bigk_out_kernel<kKeyU32><<<grid, 256, 0, s>>>(sorted, k, out);
+    else if (kind == kKeyF32) radix_bigk_out_kernel<kKeyF32><<<grid, 256, 0, s>>>(sorted, k, out);
+    else radix_bigk_out_kernel<kKeyI32><<<grid, 256, 0, s>>>(sorted, k, out);
+    return cudaGetLastError();
 }
 
 }  // namespace topk

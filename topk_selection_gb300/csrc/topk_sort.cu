@@ -156,7 +156,8 @@ template <bool kVals>
 __global__ void __launch_bounds__(kST, 2)
 sort_pass_kernel(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ vin, uint32_t* __restrict__ kout,
                  uint32_t* __restrict__ vout, size_t n, int shift, SortHeader* __restrict__ h, int pass,
-                 unsigned long long* __restrict__ look, unsigned epoch, unsigned ntiles, unsigned* __restrict__ status) {
+                 unsigned long long* __restrict__ look, unsigned epoch, unsigned ntiles, unsigned* __restrict__ status,
+                 int max_spins) {
     extern __shared__ __align__(16) uint32_t sort_smem[];
     uint32_t* s_keys = sort_smem;                       // kTile
     uint32_t* s_vals = sort_smem + kTile;               // kTile (with values)
@@ -253,7 +254,7 @@ sort_pass_kernel(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ 
                 for (int q = 0; q < 4; ++q) {
                     if (done || j < 0) break;
                     if ((v[q] & 0x3FFFFFFF00000000ull) != tag || (v[q] >> 62) == 0) {
-                        if (++spins >= kSpins) {  // give up: go on with what has been summed
+                        if (++spins >= max_spins) {  // give up: go on with what has been summed
                             atomicOr(status, kStatusWaitTimeout);
                             done = true;
                         }
@@ -374,14 +375,21 @@ cudaError_t sort_launch(cudaStream_t s, const uint32_t* keys, const uint32_t* va
     const uint32_t* vi[4] = {vals, tv, vals_out, tv};
     uint32_t* vo[4] = {tv, vals_out, tv, vals_out};
     const size_t smem = (size_t)(vals ? 2 : 1) * kTile * 4;
+    // Polls of one look-back word before a tile gives up (TOPK_OPT_SORT_SPINS
+    // lowers it for tests).  A tile that gives up has summed only some of the
+    // tiles before it, so its digit offsets are too small but never below the
+    // digit's base: every write stays inside [0, n), the order is wrong, and
+    // the status word reports it.
+    const int opt_spins = sort_spins_option();
+    const int spins = opt_spins > 0 ? opt_spins : kSpins;
     for (int p = 0; p < 4; ++p) {
         const unsigned ep = (epoch * 4u + (unsigned)p) & 0x3FFFFFFFu;
         if (vals)
             sort_pass_kernel<true><<<(unsigned)tiles, kST, smem, s>>>(ki[p], vi[p], ko[p], vo[p], n, 8 * p, h, p,
-                                                                     look, ep, (unsigned)tiles, status);
+                                                                     look, ep, (unsigned)tiles, status, spins);
         else
             sort_pass_kernel<false><<<(unsigned)tiles, kST, smem, s>>>(ki[p], nullptr, ko[p], nullptr, n, 8 * p, h,
-                                                                      p, look, ep, (unsigned)tiles, status);
+                                                                      p, look, ep, (unsigned)tiles, status, spins);
         *launches += 1;
     }
     return cudaGetLastError();

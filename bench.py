@@ -188,7 +188,7 @@ class Timer:
 
     def __init__(self, dev, stream):
         self.stream = stream
-        self.flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.flush_buf = torch.empty(128 << 20, dtype=torch.int32, device=dev)  # 512 MiB
         self.flips = 0
 
     def flush(self):
@@ -782,6 +782,43 @@ def run_reference(args, world, rank):
     }
 
 
+PROFILE_TARGETS = ("i32_1e8_k20", "i32_1e8_k100", "rows_tied", "large_k1000_i32", "large_k1000_f32", "sort_keys")
+
+
+def run_profile_target(args):
+    """A few calls of one workload and nothing else: the command that ncu
+    captures take (`--profile NAME`); prints one short line."""
+    import topk_selection_gb300 as tk
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    h = torch.cuda.current_stream(dev).cuda_stream
+    name = args.profile
+    if name.startswith("rows"):
+        w = synth.ROWS_WORKLOAD
+        x = torch.from_numpy(synth.f32_rows_tied(w["rows"], w["cols"], w["seed"], w["tie_frac"])).to(dev)
+        vals = torch.empty(w["rows"], w["k"], dtype=torch.float32, device=dev)
+        idx = torch.empty(w["rows"], w["k"], dtype=torch.int32, device=dev)
+        call = lambda: tk.topk_rows_f32_ptr(x.data_ptr(), w["rows"], w["cols"], w["k"], vals.data_ptr(),
+                                            idx.data_ptr(), h)
+    elif name == "sort_keys":
+        x = torch.from_numpy(synth.i32_workload(WORKLOAD)).to(dev)
+        ko = torch.empty_like(x)
+        call = lambda: tk.sort_u32_ptr(x.data_ptr(), 0, x.numel(), ko.data_ptr(), 0, h)
+    else:
+        x = torch.from_numpy(synth.i32_workload(WORKLOAD)).to(dev)
+        k = {"i32_1e8_k20": 20, "i32_1e8_k100": 100}.get(name, 1000)
+        fn = tk.topk_f32_ptr if name.endswith("f32") else tk.topk_i32_ptr
+        out = torch.empty(k, dtype=torch.int32, device=dev)
+        call = lambda: fn(x.data_ptr(), x.numel(), k, out.data_ptr(), h)
+    for _ in range(args.warmup + args.steps):
+        rc = call()
+        if rc != 0:
+            raise tk.TopKError(rc, name)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": name, "calls": args.warmup + args.steps, "launches": tk.launch_count()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -792,9 +829,14 @@ def main():
     ap.add_argument("--skip-rows", action="store_true", help="leave out the row-TopK, large-k, reduction, item and sort measurements")
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="--impl reference: seconds of oracle work for the whole run (sets the sample size)")
+    ap.add_argument("--profile", choices=PROFILE_TARGETS, default=None,
+                    help="run a few calls of one workload only (for ncu captures) and print a short line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.profile:
+        run_profile_target(args)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         line = run_reference(args, world, rank)

@@ -20,7 +20,7 @@
 //     word before the block finishes.  Sources of t:
 //       - the warp's own k-th largest once its list holds k values;
 //       - a start value: the k-th largest of 32*G group maxima of the warp's
-//         first tile, and of the array's last 256 elements (so that sorted
+//         first tile, and of the array's last 256 (k > 64: 512) elements (so that sorted
 //         ascending input stays cheap);
 //       - each block keeps its running maximum in a global slot; the k-th
 //         largest of all blocks' maxima is a valid t (k distinct blocks each
@@ -55,7 +55,6 @@ namespace {
 
 constexpr int kU = 8;              // 16-byte loads in flight per lane
 constexpr int kTileVec = 32 * kU;  // int4 vectors per warp-tile (4 KiB)
-constexpr int kTailVec = 64;       // int4 vectors in the tail sample (256 elements)
 constexpr int kQueue = 256;        // per-warp survivor queue (>= 31 + 128)
 
 __device__ __forceinline__ unsigned bias(int v) { return (unsigned)v ^ 0x80000000u; }
@@ -186,6 +185,8 @@ __device__ unsigned block_kth_largest(const unsigned (&v)[N], unsigned k, unsign
     return prefix;
 }
 
+constexpr int kLongLists = 64;  // second stage: lists whose survivors the block reads together
+
 // One warp: sort list[0, nlist) (nlist <= 32*N) descending in registers and
 // write out[0, k): the sorted entries, then copies of T; in the kind's words.
 template <int N, int KIND>
@@ -270,28 +271,100 @@ __device__ void second_stage(const Scratch& sc, int k, int lists_per_block, int 
 #pragma unroll
         for (int q = 0; q < kBatch; ++q) {
             const int l = q * (int)blockDim.x + (int)threadIdx.x;
-            if (nlists >= k)
-                v[q] = bias(h[q].x);
-            else
+            if (ntmax >= k)  // tiles, when recorded, outnumber blocks eightfold
                 v[q] = l < ntmax ? bias(__ldcg(sc.tmax + l)) : 0u;
+            else
+                v[q] = bias(h[q].x);
         }
         tg = kmax(tg, unbias(block_kth_largest<kBatch>(v, (unsigned)k, s_hist, s_pick)));
     }
     __syncthreads();
-    if (threadIdx.x == 0) *s_count = 0;
+    // Each thread takes its lists' first four entries; a list whose fourth
+    // entry still exceeds tg is queued, and the block reads the rest of the
+    // queued lists together (a single list can hold up to K survivors, e.g.
+    // the last block of an ascending input).
+    __shared__ int2 s_long[kLongLists];
+    __shared__ int s_nlong;
+    if (threadIdx.x == 0) *s_count = 0, s_nlong = 0;
     __syncthreads();
 #pragma unroll
     for (int q = 0; q < kBatch; ++q) {
         const int l = q * (int)blockDim.x + (int)threadIdx.x;
-        const int32_t* src = sc.cand + (size_t)l * K;
-        for (int p = 0; p < c[q]; ++p) {
-            const int v = p == 0 ? h[q].x : p == 1 ? h[q].y : p == 2 ? h[q].z : p == 3 ? h[q].w : __ldcg(src + p);
-            if (v <= tg) break;  // the list is sorted: nothing after this exceeds tg
+        const int head[4] = {h[q].x, h[q].y, h[q].z, h[q].w};
+        int p = 0;
+#pragma unroll
+        for (; p < 4; ++p) {
+            if (p >= c[q] || head[p] <= tg) break;  // the list is sorted: nothing after this exceeds tg
             const int pos = atomicAdd(s_count, 1);
-            if (pos < cap) list[pos] = v;
+            if (pos < cap) list[pos] = head[p];
+        }
+        if (p == 4 && c[q] > 4) {
+            const int slot = atomicAdd(&s_nlong, 1);
+            if (slot < kLongLists) {
+                s_long[slot] = make_int2(l, c[q]);
+            } else {  // too many long lists to queue: this thread reads the rest
+                const int32_t* src = sc.cand + (size_t)l * K;
+                for (int pp = 4; pp < c[q]; ++pp) {
+                    const int v = __ldcg(src + pp);
+                    if (v <= tg) break;
+                    const int pos = atomicAdd(s_count, 1);
+                    if (pos < cap) list[pos] = v;
+                }
+            }
         }
     }
     __syncthreads();
+    // The queued lists' entries after the fourth, as one flat range read by
+    // the whole block: s_lstart[j] is where list j starts in that range.
+    // Skipped, code and all, when no list was queued (the usual case).
+    __shared__ int s_lstart[kLongLists + 1];
+    const int nlong = s_nlong < kLongLists ? s_nlong : kLongLists;
+    if (nlong > 0) {
+    if (threadIdx.x < 32) {
+        int run = 0;
+        for (int j0 = 0; j0 < nlong; j0 += 32) {
+            const int j = j0 + lane;
+            const int len = j < nlong ? s_long[j].y - 4 : 0;
+            int x = len;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFullMask, x, o);
+                if (lane >= o) x += y;
+            }
+            if (j < nlong) s_lstart[j] = run + x - len;
+            run += __shfl_sync(kFullMask, x, 31);
+        }
+        if (lane == 0) s_lstart[nlong] = run;
+    }
+    __syncthreads();
+    const int flat = s_lstart[nlong];
+    constexpr int kFlatU = 4;  // loads in flight per thread
+    for (int e0 = (int)threadIdx.x; e0 < flat; e0 += kFlatU * (int)blockDim.x) {
+        int v[kFlatU];
+#pragma unroll
+        for (int u = 0; u < kFlatU; ++u) {
+            const int e = e0 + u * (int)blockDim.x;
+            v[u] = INT_MIN;
+            if (e < flat) {
+                int lo = 0, hi = nlong - 1;  // the list holding e: last j with s_lstart[j] <= e
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_lstart[mid] <= e) lo = mid; else hi = mid - 1;
+                }
+                v[u] = __ldcg(sc.cand + (size_t)s_long[lo].x * K + 4 + (e - s_lstart[lo]));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kFlatU; ++u) {
+            const int e = e0 + u * (int)blockDim.x;
+            if (e < flat && v[u] > tg) {
+                const int pos = atomicAdd(s_count, 1);
+                if (pos < cap) list[pos] = v[u];
+            }
+        }
+    }
+    __syncthreads();
+    }
     const int above = *s_count;
 
     int T = tg;         // value that fills the places after the sorted list
@@ -346,19 +419,28 @@ __device__ void second_stage(const Scratch& sc, int k, int lists_per_block, int 
         nlist = *s_count;
     }
 
-    if (nlist <= 256) {
-        // Small list: one warp sorts it in registers, as few as it needs.
-        if (threadIdx.x < 32) {
-            if (nlist <= 32)
-                warp_sort_out<1, KIND>(list, nlist, k, T, out, lane);
-            else if (nlist <= 64)
-                warp_sort_out<2, KIND>(list, nlist, k, T, out, lane);
-            else if (nlist <= 128)
-                warp_sort_out<4, KIND>(list, nlist, k, T, out, lane);
-            else
-                warp_sort_out<8, KIND>(list, nlist, k, T, out, lane);
+    if (nlist <= 32) {
+        // At most 32: one warp sorts them in registers.
+        if (threadIdx.x < 32) warp_sort_out<1, KIND>(list, nlist, k, T, out, lane);
+    } else if (nlist <= 512) {
+        // Up to 512: every entry's place is the number of entries above it
+        // (equal entries ordered by their slot), one pass over the list in
+        // shared memory and no barrier.  This code runs once, after the
+        // input stream has pushed it out of L2: a small loop beats an
+        // unrolled sorting network here (measured at 1e8, k = 100, 146
+        // entries: warp network 6.9 us, block network 4.1 us).
+        for (int i = threadIdx.x; i < nlist; i += blockDim.x) {
+            const int v = list[i];
+            int r = 0;
+            for (int j = 0; j < nlist; ++j) {
+                const int x = list[j];
+                r += (x > v || (x == v && j < i)) ? 1 : 0;
+            }
+            if (r < k) out[r] = ordered<KIND>(v);
         }
+        for (int i = nlist + threadIdx.x; i < k; i += blockDim.x) out[i] = ordered<KIND>(T);
     } else {
+        // The block sorts them in shared memory (rolled loops).
         const int L = next_pow2(nlist);
         for (int i = nlist + threadIdx.x; i < L; i += blockDim.x) list[i] = INT_MIN;
         block_sort_smem_desc(list, L);
@@ -433,7 +515,7 @@ static_assert(kStreamThreads * (kI32MaxTileMax / 256) >= kI32MaxTileMax &&
               "second stage: every list and tile maximum has a thread slot");
 
 template <int L, int GL, int KIND>
-__global__ void __launch_bounds__(kStreamThreads, 2)
+__global__ void __maxnreg__(112)
 topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t* __restrict__ out,
                        unsigned char* __restrict__ scratch, int cap_limit, int release, int static_pct) {
     constexpr int K = 32 * L;
@@ -480,7 +562,11 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
     // than their shares.)  With fewer blocks than k the k-th largest tile
     // maximum bounds the answer in the second stage.
     const unsigned ntiles = (unsigned)sp.ntiles;
-    const bool use_tmax = (int)G < k && ntiles <= (unsigned)kI32MaxTileMax;
+    // Tile maxima, when the grid has fewer than 2k blocks (their k-th
+    // largest maximum is then a weak bound) and the input is small enough.
+    // Writing them waits for the previous launch first (it may still read
+    // its own), so they stay off where early start pays.
+    const bool use_tmax = (int)G < 2 * k && ntiles <= (unsigned)kI32MaxTileMax;
     // All static (the default): whole tiles round-robin, as many rounds as
     // it takes, no pieces and nothing claimed.
     const bool whole = use_tmax || static_pct >= 100;
@@ -515,16 +601,19 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
     wl.init(INT_MIN);
 
     if (warp == kMonitor) {
-        // Start value from the array's last 256 elements (keeps sorted
+        // Start value from the array's last 256 (k > 64: 512) elements (keeps sorted
         // ascending input cheap), then poll: publish the block's threshold
         // and maximum, pull the grid's threshold and the k-th largest block
         // maximum.  Every value it puts in s_thresh is a valid threshold.
-        if constexpr (GL <= 2) {
+        {
+            // The tail sample: TV vectors per lane, so that its 32*GL groups
+            // of whole vectors are at least k.
+            constexpr int TV = GL > 2 ? GL : 2;
             if (sp.nvec > 0) {
-                int4 s[2];
-                const long long tv = (long long)sp.nvec - kTailVec + 2 * lane;
+                int4 s[TV];
+                const long long tv = (long long)sp.nvec - 32 * TV + TV * lane;
 #pragma unroll
-                for (int q = 0; q < 2; ++q)
+                for (int q = 0; q < TV; ++q)
                     s[q] = tv + q >= 0 ? ordered4<KIND>(__ldg(sp.body + tv + q)) : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
                 const int tseed = seed_from_groups<GL>(s, k, lane);
                 if (lane == 0) atomicMax(&s_thresh, tseed);
@@ -698,8 +787,11 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
                 unsigned cnt;
                 item_span((unsigned)tile, base, cnt);
                 mbar_arrive_expect_tx(&my_bar[st], (uint32_t)(cnt * 16));
-                // Default L2 policy: an evict-first hint measured ~1.5% slower
-                // here (one launch per call, nothing after it to protect).
+                // Default L2 policy.  Evict-first keeps the kernel's code in
+                // L2 for its cold end (ticket, second stage) across
+                // back-to-back launches, but measured slower in the bench
+                // (1e8, k = 20: 71.5 against 66.6 us per call in a stream,
+                // 81.9 against 77.8 us alone after an L2 flush).
                 bulk_copy_g2s(my_ring + (size_t)st * kTileVec, sp.body + base, (uint32_t)(cnt * 16), &my_bar[st]);
             }
             __syncwarp();
@@ -737,7 +829,9 @@ topk_i32_stream_kernel(const int32_t* __restrict__ in, size_t n, int k, int32_t*
             int4 r[kU];
             if (cnt == (unsigned)kTileVec) {
 #pragma unroll
-                for (int u = 0; u < kU; ++u) r[u] = ordered4<KIND>(st[u * 32 + lane]);
+                for (int u = 0; u < kU; ++u) r[u] = st[u * 32 + lane];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) r[u] = ordered4<KIND>(r[u]);
             } else {
 #pragma unroll
                 for (int u = 0; u < kU; ++u)

@@ -222,10 +222,11 @@ __device__ __forceinline__ void for_each_vec(const int32_t* __restrict__ in, siz
 #pragma unroll
         for (int u = 0; u < kRU; ++u) {
             const size_t i = base + (size_t)u * blockDim.x + threadIdx.x;
-            r[u] = i < nvec ? ordered4<KIND>(ld_nc_hint(body + i, policy)) : make_int4(0, 0, 0, 0);
+            r[u] = i < nvec ? ld_nc_hint(body + i, policy) : make_int4(0, 0, 0, 0);
         }
+        // The key map after all kRU loads are out, so that none waits for another.
 #pragma unroll
-        for (int u = 0; u < kRU; ++u) f_vec(r[u], base + (size_t)u * blockDim.x + threadIdx.x < nvec);
+        for (int u = 0; u < kRU; ++u) f_vec(ordered4<KIND>(r[u]), base + (size_t)u * blockDim.x + threadIdx.x < nvec);
     }
     if (blockIdx.x == 0 && threadIdx.x < 32) {
         const size_t ns = head + (n - tail0);

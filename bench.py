@@ -782,7 +782,8 @@ def run_reference(args, world, rank):
     }
 
 
-PROFILE_TARGETS = ("i32_1e8_k20", "i32_1e8_k100", "rows_tied", "large_k1000_i32", "large_k1000_f32", "sort_keys")
+PROFILE_TARGETS = ("i32_1e8_k20", "i32_1e8_k100", "rows_tied", "rows_untied", "large_k1000_i32", "large_k1000_f32",
+                   "sort_keys")
 
 
 def run_profile_target(args):
@@ -796,7 +797,9 @@ def run_profile_target(args):
     name = args.profile
     if name.startswith("rows"):
         w = synth.ROWS_WORKLOAD
-        x = torch.from_numpy(synth.f32_rows_tied(w["rows"], w["cols"], w["seed"], w["tie_frac"])).to(dev)
+        xh = synth.f32_rows_tied(w["rows"], w["cols"], w["seed"], w["tie_frac"]) if name == "rows_tied" else \
+            synth.f32_rows_normal(w["rows"], w["cols"], w["seed"])
+        x = torch.from_numpy(xh).to(dev)
         vals = torch.empty(w["rows"], w["k"], dtype=torch.float32, device=dev)
         idx = torch.empty(w["rows"], w["k"], dtype=torch.int32, device=dev)
         call = lambda: tk.topk_rows_f32_ptr(x.data_ptr(), w["rows"], w["cols"], w["k"], vals.data_ptr(),

@@ -207,3 +207,37 @@ def test_host_pointers_rejected(tk):
     out_i = torch.empty(5, dtype=torch.int64)
     rc = tk.topk_items_f32_ptr(x.data_ptr(), 0, 0, 100, 5, out_s.data_ptr(), out_i.data_ptr(), 0, 0)
     assert rc == 1
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties", "specials", "equal"])
+def test_large_no_filter_ties_across_rows(tk, kind):
+    # From 2^20 positions up the first level cuts the input into ~4096 rows.
+    # Ties across rows (every kind but "normal" ties at the k-th score) must
+    # still go to the lower position, NaN first and -0 == +0; misaligned
+    # bases move the rows' vectors.
+    for n, off in ((1 << 20, 0), ((1 << 20) + 4099, 1), (3_000_017, 3)):
+        x = make(kind, n, n + 11)
+        items = (np.arange(n, dtype=np.int64) * 5 + 1)
+        buf = torch.empty(n + off, dtype=torch.float32, device="cuda")
+        buf[off:].copy_(torch.from_numpy(x))
+        for k in (1, 20, 64, 100, 128):
+            s, i, c = tk.topk_items_f32(buf[off:], k, item=torch.from_numpy(items).cuda())
+            torch.cuda.synchronize()
+            es, ei, ec = oracle.topk_items_f32(x, k, item=items)
+            assert int(c.item()) == ec, (kind, n, k)
+            assert np.array_equal(i.cpu().numpy(), ei), (kind, n, k)
+            assert np.array_equal(bits(s.cpu().numpy()), bits(es)), (kind, n, k)
+
+
+def test_large_back_to_back(tk):
+    # Calls with very different scores, back to back on one stream (each
+    # call's scratch is the next one's).
+    a = synth.f32_normal(2_000_003, 21) + np.float32(100.0)
+    b = synth.f32_normal(1_500_007, 22) - np.float32(100.0)
+    da, db = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    outs = [tk.topk_items_f32(d, 64) for d in (da, db, da, db)]
+    torch.cuda.synchronize()
+    for (s, i, c), x in zip(outs, (a, b, a, b)):
+        es, ei, ec = oracle.topk_items_f32(x, 64)
+        assert np.array_equal(i.cpu().numpy(), ei)
+        assert np.array_equal(bits(s.cpu().numpy()), bits(es))

@@ -480,6 +480,27 @@ def run_rows(tk, dev, stream, args, timer, peak, configs):
         configs[f"C5_{name}"] = {"single_us": round(su, 1), "pipe_us": round(pu, 1),
                                  "frac_single": _frac(nbytes, su, peak), "frac_pipe": _frac(nbytes, pu, peak),
                                  "ok": ok}
+        if not tied:
+            # The same rows at k above 128 (one block per row, radix-select cuts).
+            for kb in (129, 1024):
+                vb = torch.empty(rows, kb, dtype=torch.float32, device=dev)
+                ib = torch.empty(rows, kb, dtype=torch.int32, device=dev)
+
+                def stepb():
+                    rc = tk.topk_rows_f32_ptr(x.data_ptr(), rows, cols, kb, vb.data_ptr(), ib.data_ptr(), h)
+                    if rc != 0:
+                        raise tk.TopKError(rc, "topk_rows_f32 (large k)")
+
+                stepb()
+                sub = timer.single(stepb, 5)
+                pub = timer.pipelined(stepb, 5)
+                evb, eib = oracle.topk_rows_f32(xr[sample[:8]], kb)
+                okb = bool(np.array_equal(ib.cpu().numpy()[sample[:8]], eib))
+                nb = rows * cols * 4 + rows * kb * 8
+                res[f"untied_k{kb}"] = {"single_us": round(sub, 1), "pipe_us": round(pub, 1),
+                                        "frac_single": _frac(nb, sub, peak), "frac_pipe": _frac(nb, pub, peak),
+                                        "parity_8_rows": okb}
+                del vb, ib
         del x
     res["workload"] = "fp32 rows 4096x32768 N(0,1) seed 5, tied: 1% of each row set to the row max; k=64"
     return res

@@ -30,10 +30,13 @@
 //                       histogram the low 8 bits of the keys in it; that
 //                       fixes the k-th key T, and the keys between T and the
 //                       prefix's top are written from the histogram
-//   final    one cluster loads the buffer into its 8 CTAs' shared memory and
-//            selects the k-th key T with four cluster-wide 8-bit digit
-//            histograms (summed through distributed shared memory).  At most
-//            kSmallCap keys above T: rank 0 gathers and sorts them all.
+//   final    when k <= kSmallCap and the buffer fits one CTA's shared memory
+//            (the usual case for such k), one CTA selects the k-th key T with
+//            four 8-bit digit histograms and sorts the keys above it.  Else
+//            one cluster loads the buffer into its 8 CTAs' shared memory and
+//            selects T with four cluster-wide 8-bit digit histograms (summed
+//            through distributed shared memory).  At most kSmallCap keys
+//            above T: rank 0 gathers and sorts them all.
 //            Otherwise their value range is cut into ranges of about 256
 //            keys -- from a cluster-wide histogram of the 10 bits below the
 //            common prefix of [T + 1, max], or, when one bucket is too dense,
@@ -627,6 +630,40 @@ __device__ __forceinline__ void cluster_pick(ClSmem& S, const unsigned* H, unsig
     __syncthreads();
 }
 
+// The same within one CTA: H is this CTA's histogram, complete after a
+// __syncthreads.
+__device__ __forceinline__ void cta_pick(ClSmem& S, const unsigned* H, unsigned need) {
+    const unsigned lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (w == 0) {
+        unsigned c[8], tot = 0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            c[b] = H[lane * 8 + b];
+            tot += c[b];
+        }
+        unsigned x = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_down_sync(kFullMask, x, o);
+            if ((int)lane + o < 32) x += y;
+        }
+        const unsigned above = x - tot;
+        if (above < need && need <= above + tot) {
+            unsigned acc = above;
+#pragma unroll
+            for (int b = 7; b >= 0; --b) {
+                if (acc + c[b] >= need) {
+                    S.pick_digit = lane * 8 + b;
+                    S.pick_above = acc;
+                    break;
+                }
+                acc += c[b];
+            }
+        }
+    }
+    __syncthreads();
+}
+
 // Range of key u: the first q with u >= lb[q] (lb descending, lb[nr-1] <= u).
 __device__ __forceinline__ unsigned range_of(const unsigned* lb, unsigned nr, unsigned u) {
     unsigned lo = 0, hi = nr - 1;
@@ -682,12 +719,33 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
             if (st != kStateSorted || C >= (unsigned)k) C = 0;
         }
     }
-    const unsigned per = (C + kClCtas - 1) / kClCtas;
-    const unsigned lo = min(C, rank * per);
+    // One CTA does the final alone when the buffer fits its shared memory
+    // and the answer is small (the usual case for k <= kSmallCap).  The
+    // other CTAs leave at once (after the control words are read: rank 0
+    // clears them at the end), and nothing below waits on them or reads
+    // their shared memory.
+    const bool solo = mode == kClFinal && (unsigned)k <= kSmallCap && C <= (unsigned)kClSlice;
+    if (solo) cluster_barrier();
+    if (solo && rank != 0) return;
+    const unsigned per = solo ? C : (C + kClCtas - 1) / kClCtas;
+    const unsigned lo = solo ? 0u : min(C, rank * per);
     const unsigned mine = min(C, lo + per) - lo;
 
-    // Load the CTA's keys, histogramming their top digit on the way (level 0
-    // of the select).
+    // The keys to select from lie in [klo, 2^32 - 1]: above the filter's
+    // threshold (or, after exact pass 2 collected them, at or above its
+    // prefix) for the buffer, anywhere otherwise.  So they share klo's
+    // bits above `top0`, and the digit levels start just below those: for a
+    // small k the buffer's keys share their top 12 bits or more.
+    unsigned klo = 0;
+    if (mode == kClFinal && select)
+        klo = __ldcg(&rv.ctrl->exact_mode) == kExactCollectAll ? __ldcg(&rv.ctrl->prefix) : __ldcg(&rv.ctrl->t) + 1u;
+    const int top0 = 32 - __clz((int)~klo);  // klo's leading one bits are the common prefix
+    const unsigned pre0 = top0 >= 32 ? 0u : ~((1u << top0) - 1u);
+    const int sh0 = top0 > 8 ? top0 - 8 : 0;
+    const unsigned dm0 = (1u << (top0 - sh0)) - 1u;
+
+    // Load the CTA's keys, histogramming their first digit on the way (level
+    // 0 of the select).
     if (tid < 256) S.hist[0][tid] = 0u;
     __syncthreads();
     if (mode == kClSample) {
@@ -708,10 +766,10 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
         for (int m = 0; m < kSampleVec; ++m) {
             const uint4 u = make_uint4(key_of(v[m].x), key_of(v[m].y), key_of(v[m].z), key_of(v[m].w));
             *reinterpret_cast<uint4*>(&S.keys[(m * kClThreads + tid) * 4]) = u;
-            hist_add(S.hist[0], u.x >> 24, true);
-            hist_add(S.hist[0], u.y >> 24, true);
-            hist_add(S.hist[0], u.z >> 24, true);
-            hist_add(S.hist[0], u.w >> 24, true);
+            hist_add(S.hist[0], (u.x >> sh0) & dm0, true);
+            hist_add(S.hist[0], (u.y >> sh0) & dm0, true);
+            hist_add(S.hist[0], (u.z >> sh0) & dm0, true);
+            hist_add(S.hist[0], (u.w >> sh0) & dm0, true);
         }
     } else {
         // 16 loads in flight per thread; indices past the slice load its
@@ -731,7 +789,7 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
             for (int u = 0; u < kLd; ++u) {
                 const unsigned i = base + u * kClThreads + tid;
                 if (i < mine) S.keys[i] = v[u];
-                hist_add(S.hist[0], v[u] >> 24, i < mine);
+                hist_add(S.hist[0], (v[u] >> sh0) & dm0, i < mine);
             }
         }
     }
@@ -743,16 +801,19 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
     const unsigned w0 = w * share;
     unsigned cnt = mine > w0 ? min(share, mine - w0) : 0u;
 
-    // Select: four 8-bit digit levels.  Each level after the first drops the
-    // keys below the bucket chosen so far (keys above it stay: they are in
-    // the answer) and histograms the next digit of the keys in it.
+    // Select: digit levels of 8 bits (the last one fewer) below the common
+    // prefix.  Each level after the first drops the keys below the bucket
+    // chosen so far (keys above it stay: they are in the answer) and
+    // histograms the next digit of the keys in it.
     if (select) {
-        unsigned prefix = 0, need = j;
-        for (int level = 0; level < 4; ++level) {
-            const int shift = 24 - 8 * level;
+        unsigned prefix = pre0, need = j;
+        int top = top0;
+        for (int level = 0; top > 0; ++level) {
+            const int shift = top > 8 ? top - 8 : 0;
+            const unsigned dmask = (1u << (top - shift)) - 1u;
             unsigned* H = S.hist[level & 1];
             if (level > 0) {
-                const unsigned fixed = 0xFFFFFFFFu << (32 - 8 * level);
+                const unsigned fixed = ~((1u << top) - 1u);  // top < 32 after the first level
                 if (tid < 256) H[tid] = 0u;
                 __syncthreads();
                 unsigned kept = 0;
@@ -760,7 +821,7 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
                     const unsigned i = m + lane;
                     const bool valid = i < cnt;
                     const unsigned u = valid ? S.keys[w0 + i] : 0u;
-                    hist_add(H, (u >> shift) & 0xFFu, valid && (u & fixed) == prefix);
+                    hist_add(H, (u >> shift) & dmask, valid && (u & fixed) == prefix);
                     const bool keep = valid && (u & fixed) >= prefix;
                     const unsigned b = __ballot_sync(kFullMask, keep);
                     if (keep) S.keys[w0 + kept + __popc(b & lanemask_lt())] = u;
@@ -768,11 +829,17 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
                 }
                 cnt = kept;
             }
-            cluster_barrier();
-            cluster_pick(S, H, need);
+            if (solo) {
+                __syncthreads();
+                cta_pick(S, H, need);
+            } else {
+                cluster_barrier();
+                cluster_pick(S, H, need);
+            }
             prefix |= S.pick_digit << shift;
             need -= S.pick_above;
             __syncthreads();  // the pick and part are rewritten at the next level
+            top = shift;
         }
         T = prefix;
     }
@@ -807,6 +874,21 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
         if (lane == 31) S.mine_count = x;
     }
     __syncthreads();
+    if (solo) {
+        // Every key above T is this CTA's (fewer than k <= kSmallCap): pack,
+        // sort and write them, then copies of T.
+        const unsigned total = S.mine_count;
+        for (unsigned m = lane; m < cw; m += 32) S.mysmall[S.woff[w] + m] = S.keys[w0 + m];
+        const int P = next_pow2(total < 64 ? 64 : (int)total);
+        for (unsigned i = total + tid; i < (unsigned)P; i += kClThreads) S.mysmall[i] = 0u;  // below every key > T
+        __syncthreads();
+        block_sort_reg_desc<unsigned, kClThreads>(S.mysmall, P);
+        for (unsigned i = tid; i < total; i += kClThreads) out[i] = ordered<KIND>(value_of(S.mysmall[i]));
+        for (unsigned i = total + tid; i < (unsigned)k; i += kClThreads) out[i] = ordered<KIND>(value_of(T));
+        if (tid == 0) reinterpret_cast<RadixPlan*>(scratch + kRadixCandOffset)->nranges = 0u;
+        if (tid < (unsigned)kCtrlWords) reinterpret_cast<unsigned*>(rv.ctrl)[tid] = 0u;
+        return;
+    }
     cluster_barrier();  // every CTA's count is out
 
     if (tid < (unsigned)kClCtas) S.ccount[tid] = ld_cluster(&S.mine_count, tid);
@@ -1296,10 +1378,14 @@ cudaError_t radix_launch_kind(cudaStream_t s, const int32_t* in, size_t n, int k
         }
         return e;
     }
-    // Sample rank: k's expected share of the sample plus four standard
-    // deviations and a floor of 16, so that at least k keys are >= t.
+    // Sample rank: k's expected share of the sample, lam, plus four
+    // standard deviations plus 2, so that at least k keys are >= t unless
+    // the sample holds j or more of the input's k largest (a Poisson(lam)
+    // tail: about 2e-5 at lam = 0.33, k = 1000 of 1e8; the exact passes
+    // then take over).  The filter keeps about j * n / kSampleKeys keys, so
+    // a small k's final usually fits one CTA.
     const double lam = (double)k * (double)kSampleKeys / (double)n;
-    const double jd = std::ceil(lam + 4.0 * std::sqrt(lam) + 16.0);
+    const double jd = std::ceil(lam + 4.0 * std::sqrt(lam) + 2.0);
     unsigned j = jd >= (double)kSampleKeys ? kSampleKeys : (unsigned)jd;
     const int opt_j = radix_sample_rank_option();
     if (opt_j > 0) j = (unsigned)opt_j < kSampleKeys ? (unsigned)opt_j : kSampleKeys;

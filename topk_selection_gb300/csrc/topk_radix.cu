@@ -20,8 +20,9 @@
 //              buffer count >= k and it fits   -> select the k-th in the buffer
 //              buffer + equal count >= k       -> t is the k-th key
 //              otherwise                       -> the exact passes
-//   exact    three grid passes that do work only when the sample misled the
-//            filter; otherwise each reads the state word and returns:
+//   exact    one grid launch that does work only when the sample misled the
+//            filter (otherwise every block reads the state word and
+//            returns); its three passes, separated by in-kernel gates:
 //              pass 1   12-bit histogram of the top bits -> bucket b1
 //              pass 2   if every key at or above b1 fits the buffer, collect
 //                       them (then select in the buffer); else histogram the
@@ -32,10 +33,11 @@
 //                       prefix's top are written from the histogram
 //   final    when k <= kSmallCap and the buffer fits one CTA's shared memory
 //            (the usual case for such k), one CTA selects the k-th key T with
-//            four 8-bit digit histograms and sorts the keys above it.  Else
-//            one cluster loads the buffer into its 8 CTAs' shared memory and
-//            selects T with four cluster-wide 8-bit digit histograms (summed
-//            through distributed shared memory).  At most kSmallCap keys
+//            8-bit digit histograms and sorts the keys above it.  Else one
+//            cluster loads the buffer into its 8 CTAs' shared memory and
+//            selects T with cluster-wide 8-bit digit histograms (summed
+//            through distributed shared memory).  The digits start below
+//            the bits that every key in the buffer shares.  At most kSmallCap keys
 //            above T: rank 0 gathers and sorts them all.
 //            Otherwise their value range is cut into ranges of about 256
 //            keys -- from a cluster-wide histogram of the 10 bits below the
@@ -46,9 +48,10 @@
 //            of the output, and each range is then sorted in place by one
 //            warp.  Copies of the k-th key fill the rest of the output.
 // When n fits one cluster, the cluster kernel alone runs, on the input itself.
-// Every decision stays on the device, so a call only enqueues work.  No
-// kernel here waits on another block or CTA except through hardware
-// barriers (__syncthreads, the cluster barrier), so none can hang.
+// Every decision stays on the device, so a call only enqueues work.  The
+// exact passes' blocks wait for one another at their gates with a bounded
+// poll; every other wait in these kernels is a hardware barrier
+// (__syncthreads, the cluster barrier), so none can hang.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -66,6 +69,7 @@ namespace {
 
 constexpr int kRThreads = 512;  // grid passes
 constexpr int kRU = 8;          // 16-byte loads in flight per thread
+constexpr int kFilterPrefetch = 6;  // batches per block fetched into L2 while the sample runs
 constexpr int kBins = 4096;     // 12-bit digits
 
 constexpr int kClCtas = 8;  // CTAs per cluster (portable size)
@@ -97,10 +101,11 @@ struct RadixCtrl {
     unsigned exact_mode;      // kExact*: what pass 2 does
     unsigned long long nbuf;  // keys appended to the buffer (counts past its capacity)
     unsigned long long neq;   // keys equal to t seen by the filter
-    unsigned pad[54];
+    unsigned gate;            // exact passes: the last pass whose bucket is picked
+    unsigned pad[53];
 };
 static_assert(sizeof(RadixCtrl) == 256, "one line");
-constexpr int kCtrlWords = 10;
+constexpr int kCtrlWords = 11;
 
 struct RadixView {
     RadixCtrl* ctrl;
@@ -316,6 +321,24 @@ radix_filter_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned ch
     __shared__ unsigned stage[kRThreads / 32][64];
     __shared__ unsigned long long s_neq;
     __shared__ int s_last;
+    // The input is final before this kernel starts: it is launched only
+    // once every CTA of the sample has passed its own wait for the work
+    // before the plan.  Only the threshold comes from the sample.  So while
+    // the sample runs, each block fetches its first kFilterPrefetch batches
+    // of the input into L2 (the batches for_each_vec reads first).
+    if (threadIdx.x == 0) {
+        const uintptr_t addr = reinterpret_cast<uintptr_t>(in);
+        size_t head = ((16u - (unsigned)(addr & 15u)) & 15u) >> 2;
+        if (head > n) head = n;
+        const int4* body = reinterpret_cast<const int4*>(in + head);
+        const size_t nvec = (n - head) >> 2, batch = (size_t)blockDim.x * kRU;
+        for (int p = 0; p < kFilterPrefetch; ++p) {
+            const size_t v0 = (size_t)blockIdx.x * batch + (size_t)p * gridDim.x * batch;
+            if (v0 >= nvec) break;
+            const size_t nv = nvec - v0 < batch ? nvec - v0 : batch;
+            prefetch_l2(body + v0, (uint32_t)(nv * 16));
+        }
+    }
     grid_dependency_wait();  // launched early (launch_pdl): wait for the previous kernel's writes
     launch_dependents();
     const RadixView rv = radix_view(scratch);
@@ -359,23 +382,60 @@ radix_filter_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned ch
     }
 }
 
-// Exact pass 1: 12-bit histogram of the top bits; the last block picks b1
-// and decides whether pass 2 can collect every key at or above it.
+// Exact passes, one launch.  When the sample did not mislead the filter
+// (the usual case) every block reads the state word and returns.  Else:
+//   pass 1   12-bit histogram of the top bits -> bucket b1
+//   pass 2   if every key at or above b1 fits the buffer, collect them (then
+//            select in the buffer); else histogram the next 12 bits of the
+//            keys in b1 -> bucket b2
+//   pass 3   (after a histogram pass 2) collect the keys above the 24-bit
+//            prefix and histogram the low 8 bits of the keys in it; the last
+//            block fixes the k-th key T and appends the keys in
+//            (T, prefix | 0xFF] from the histogram, value by value.
+// The last block of a pass picks the bucket and opens the pass's gate (a
+// control word); the others wait for it, polling with a bound.  The grid is
+// at most what the SMs hold at once, and the next kernel of the plan is
+// released only when the passes end, so every block of the grid is, or
+// becomes, resident while the others wait.  A wait that runs out sets the
+// status word and goes on (the result is then invalid; every buffer write
+// stays inside the buffer).
+__device__ __forceinline__ void exact_gate_open(const RadixView& rv, unsigned pass) {
+    __threadfence();
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&rv.ctrl->gate), "r"(pass) : "memory");
+}
+__device__ void exact_gate_wait(const RadixView& rv, unsigned pass, unsigned* status) {
+    if (threadIdx.x == 0) {
+        unsigned g = 0;
+        for (int i = 0; i < kWaitSpins; ++i) {
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(&rv.ctrl->gate) : "memory");
+            if (g >= pass) break;
+            __nanosleep(64);
+        }
+        if (g < pass) atomicOr(status, kStatusWaitTimeout);
+    }
+    __syncthreads();
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(kRThreads, 2)
-radix_exact1_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned char* __restrict__ scratch,
-                    unsigned cap) {
+radix_exact_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned char* __restrict__ scratch,
+                   unsigned cap) {
     __shared__ unsigned sh[kBins];
+    __shared__ unsigned stage[kRThreads / 32][64];
     __shared__ unsigned long long s_scan[64];
     __shared__ Bucket s_pick;
+    __shared__ unsigned s_cnt[256], s_off[256];
     __shared__ int s_last, s_go;
+    __shared__ unsigned s_prefix, s_mode, s_need;
     grid_dependency_wait();  // launched early (launch_pdl): wait for the previous kernel's writes
-    launch_dependents();
     const RadixView rv = radix_view(scratch);
+    unsigned* status = reinterpret_cast<unsigned*>(scratch + kI32StatusOffset);
     if (threadIdx.x == 0) s_go = __ldcg(&rv.ctrl->state) == kStateExact;
     for (int i = threadIdx.x; i < kBins; i += blockDim.x) sh[i] = 0u;
     __syncthreads();
-    if (!s_go) return;
+    if (!s_go) return;  // (returning releases the next kernel)
+
+    // Pass 1.
     for_each_key<KIND>(in, n, [&](unsigned u, bool ok) { hist_add(sh, u >> 20, ok); });
     if (pass_done(rv, sh, &s_last)) {
         pick_bucket(rv, kBins, (unsigned)k, s_scan, &s_pick);
@@ -385,34 +445,20 @@ radix_exact1_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned ch
             rv.ctrl->exact_mode = s_pick.above + s_pick.count <= cap ? kExactCollectAll : kExactHistogram;
             rv.ctrl->nbuf = 0ull;
             rv.ctrl->neq = 0ull;
+            exact_gate_open(rv, 1u);
         }
     }
-}
+    exact_gate_wait(rv, 1u, status);
 
-// Exact pass 2: collect every key at or above b1, or histogram the next 12
-// bits of the keys in b1.
-template <int KIND>
-__global__ void __launch_bounds__(kRThreads, 2)
-radix_exact2_kernel(const int32_t* __restrict__ in, size_t n, unsigned char* __restrict__ scratch, unsigned cap) {
-    __shared__ unsigned sh[kBins];
-    __shared__ unsigned stage[kRThreads / 32][64];
-    __shared__ unsigned long long s_scan[64];
-    __shared__ Bucket s_pick;
-    grid_dependency_wait();  // launched early (launch_pdl): wait for the previous kernel's writes
-    launch_dependents();
-    __shared__ int s_last, s_go;
-    __shared__ unsigned s_prefix, s_mode, s_need;
-    const RadixView rv = radix_view(scratch);
+    // Pass 2.
     if (threadIdx.x == 0) {
-        s_go = __ldcg(&rv.ctrl->state) == kStateExact;
         s_prefix = __ldcg(&rv.ctrl->prefix);
         s_mode = __ldcg(&rv.ctrl->exact_mode);
         s_need = __ldcg(&rv.ctrl->need);
     }
     for (int i = threadIdx.x; i < kBins; i += blockDim.x) sh[i] = 0u;
     __syncthreads();
-    if (!s_go) return;
-    const unsigned prefix = s_prefix;
+    unsigned prefix = s_prefix;
     const bool collect = s_mode == kExactCollectAll;
     if (collect) {
         WarpAppender ap{stage[threadIdx.x >> 5], 0u, false};
@@ -434,38 +480,21 @@ radix_exact2_kernel(const int32_t* __restrict__ in, size_t n, unsigned char* __r
             if (threadIdx.x == 0) {
                 rv.ctrl->prefix = prefix | (s_pick.digit << 8);
                 rv.ctrl->need = s_need - s_pick.above;
+                exact_gate_open(rv, 2u);
             }
         }
     }
-}
+    if (collect) return;
+    exact_gate_wait(rv, 2u, status);
 
-// Exact pass 3 (only after a histogram pass 2): collect the keys above the
-// 24-bit prefix, histogram the low 8 bits of the keys in it.  The last block
-// fixes the k-th key T and appends the keys in (T, prefix | 0xFF], which the
-// histogram gives value by value.  Fewer than k keys are above T, so the
-// buffer (cap >= k) holds them all.
-template <int KIND>
-__global__ void __launch_bounds__(kRThreads, 2)
-radix_exact3_kernel(const int32_t* __restrict__ in, size_t n, unsigned char* __restrict__ scratch, unsigned cap) {
-    __shared__ unsigned sh[kBins];
-    __shared__ unsigned stage[kRThreads / 32][64];
-    __shared__ unsigned long long s_scan[64];
-    __shared__ Bucket s_pick;
-    grid_dependency_wait();  // launched early (launch_pdl): wait for the previous kernel's writes
-    launch_dependents();
-    __shared__ unsigned s_cnt[256], s_off[256];
-    __shared__ int s_last, s_go;
-    __shared__ unsigned s_prefix, s_need;
-    const RadixView rv = radix_view(scratch);
+    // Pass 3.
     if (threadIdx.x == 0) {
-        s_go = __ldcg(&rv.ctrl->state) == kStateExact;
         s_prefix = __ldcg(&rv.ctrl->prefix);
         s_need = __ldcg(&rv.ctrl->need);
     }
     for (int i = threadIdx.x; i < kBins; i += blockDim.x) sh[i] = 0u;
     __syncthreads();
-    if (!s_go) return;
-    const unsigned prefix = s_prefix;
+    prefix = s_prefix;
     WarpAppender ap{stage[threadIdx.x >> 5], 0u, false};
     for_each_key<KIND>(in, n, [&](unsigned u, bool ok) {
         ap.push(rv, cap, u, ok && u > (prefix | 0xFFu));
@@ -488,7 +517,8 @@ radix_exact3_kernel(const int32_t* __restrict__ in, size_t n, unsigned char* __r
         }
         __syncthreads();
         for (unsigned e = d + 1; e < 256; ++e)
-            for (unsigned i = threadIdx.x; i < s_cnt[e]; i += blockDim.x) rv.buf[nb + s_off[e] + i] = prefix | e;
+            for (unsigned i = threadIdx.x; i < s_cnt[e]; i += blockDim.x)
+                if ((size_t)nb + s_off[e] + i < cap) rv.buf[nb + s_off[e] + i] = prefix | e;
         if (threadIdx.x == 0) {
             rv.ctrl->t = prefix | d;
             rv.ctrl->nbuf = (unsigned long long)nb + s_pick.above;
@@ -1309,10 +1339,14 @@ cudaError_t radix_fit(int device, RadixFit* out) {
         int sms = 0;
         cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
         if (e != cudaSuccess) return e;
+        // The grid of the grid passes: what the SMs hold at once of every
+        // one of them (the exact passes' blocks wait on one another).
         const void* passes[] = {reinterpret_cast<const void*>(&radix_filter_kernel<kKeyI32>),
-                                reinterpret_cast<const void*>(&radix_exact1_kernel<kKeyI32>),
-                                reinterpret_cast<const void*>(&radix_exact2_kernel<kKeyI32>),
-                                reinterpret_cast<const void*>(&radix_exact3_kernel<kKeyI32>)};
+                                reinterpret_cast<const void*>(&radix_filter_kernel<kKeyU32>),
+                                reinterpret_cast<const void*>(&radix_filter_kernel<kKeyF32>),
+                                reinterpret_cast<const void*>(&radix_exact_kernel<kKeyI32>),
+                                reinterpret_cast<const void*>(&radix_exact_kernel<kKeyU32>),
+                                reinterpret_cast<const void*>(&radix_exact_kernel<kKeyF32>)};
         int per_sm = 1 << 30;
         for (const void* f : passes) {
             int b = 0;
@@ -1397,16 +1431,14 @@ cudaError_t radix_launch_kind(cudaStream_t s, const int32_t* in, size_t n, int k
     e = launch_pdl(radix_cluster_kernel<KIND>, kClCtas, kClThreads, cl_smem, s, in, n, k, j, out, sc, ucap, kClSample,
                    (uint32_t*)nullptr);
     if (e == cudaSuccess) e = launch_pdl(radix_filter_kernel<KIND>, g, kRThreads, 0, s, in, n, k, sc, ucap);
-    if (e == cudaSuccess) e = launch_pdl(radix_exact1_kernel<KIND>, g, kRThreads, 0, s, in, n, k, sc, ucap);
-    if (e == cudaSuccess) e = launch_pdl(radix_exact2_kernel<KIND>, g, kRThreads, 0, s, in, n, sc, ucap);
-    if (e == cudaSuccess) e = launch_pdl(radix_exact3_kernel<KIND>, g, kRThreads, 0, s, in, n, sc, ucap);
+    if (e == cudaSuccess) e = launch_pdl(radix_exact_kernel<KIND>, g, kRThreads, 0, s, in, n, k, sc, ucap);
     if (e == cudaSuccess)
         e = launch_pdl(radix_cluster_kernel<KIND>, kClCtas, kClThreads, cl_smem, s, in, n, k, 0u, out, sc, ucap, kClFinal,
                        bigk);
-    *launches = 6;
+    *launches = 4;
     if (e == cudaSuccess && !bigk) {
         e = launch_pdl(radix_sort_kernel<KIND>, sort_grid, kSortWarps * 32, sort_smem, s, out, sc, release ? 1 : 0);
-        *launches = 7;
+        *launches = 5;
     }
     return e;
 }

@@ -80,8 +80,9 @@ enum topk_status {
  * radix sort", histogram section).  When n exceeds 2^18, a threshold is
  * taken from a 2^16-key sample, one pass over the input keeps the keys above
  * it, and one 8-CTA cluster selects the k-th key among them and sorts the
- * answer (six launches, one input pass; two more input passes run only when
- * the sample misled the filter).  When n <= 2^18 the cluster does it all in
+ * answer (five launches, one input pass; two or three more input passes
+ * run, inside one of those launches, only when the sample misled the
+ * filter).  When n <= 2^18 the cluster does it all in
  * one launch.  k > 32768: the cluster leaves the answer unordered and the
  * library's LSD radix sort (topk_sort_u32's kernels) orders it, plus one
  * launch that writes it out; that form needs about 4k more bytes of

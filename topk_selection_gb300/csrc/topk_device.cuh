@@ -309,12 +309,6 @@ __device__ __forceinline__ void bulk_copy_g2s_hint(void* dst, const void* src, u
         : "memory");
 }
 
-// Fetch `bytes` (a multiple of 16; src 16-byte aligned) of global memory
-// into L2, asynchronously; nothing waits for it.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
 // to this block's shared memory; completion is signalled on `bar`.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -804,6 +804,261 @@ topk_rows_big_kernel(const float* __restrict__ in, int rows, int cols, int k, fl
             if (!mbar_wait(&s_bar[c % kBigStages], (uint32_t)((c / kBigStages) & 1))) break;
 }
 
+// ------------------------------- 128 < k <= 1024, rows up to 64K columns --
+//
+// One block per row at a time (a persistent grid; block b takes rows b,
+// b + G, ...): a radix select on the row's unique 64-bit keys (score key,
+// inverted column), as in "GPU radix sort"'s histogram section, 11-bit
+// digits:
+//   * a pass over the row histograms the next digit of the keys that share
+//     the bits fixed so far (the first pass reads the row from HBM, the
+//     later ones find it in L2);
+//   * the bucket that holds the need-th largest key is picked; when all the
+//     keys at or above that bucket's lower edge fit the candidate buffer, a
+//     last pass collects them, else the bucket's digit is fixed and the next
+//     digit is histogrammed.  The keys are unique, so the last level's
+//     bucket holds one key and the buffer always suffices by then;
+//   * the candidates are sorted in shared memory and the first k written.
+// For N(0,1) rows and k = 129 .. 1024 one level is enough (about 750 .. 1300
+// candidates), so a row is read once from HBM and once from L2.
+constexpr int kSelThreads = 256;
+constexpr int kSelCap = 4096;                 // candidate buffer (32 KiB)
+constexpr int kSelBits = 11;
+constexpr int kSelBins = 1 << kSelBits;
+constexpr int kSelU = 8;                      // 16-byte loads in flight per thread
+constexpr int kSelPer = kSelBins / kSelThreads;  // bins per thread in the bucket scan
+static_assert(kSelPer * kSelThreads == kSelBins, "the bucket scan covers the bins");
+static_assert(1024 <= kSelCap, "k <= 1024");
+static_assert(kSelBins * sizeof(unsigned) >= 1024 * sizeof(u64), "the histogram's space holds the k <= 1024 best");
+
+
+__global__ void __launch_bounds__(kSelThreads, 4)
+topk_rows_select_kernel(const float* __restrict__ in, int rows, int cols, int k, float* __restrict__ vals,
+                        int32_t* __restrict__ idx) {
+    __shared__ __align__(16) u64 buf[kSelCap];
+    __shared__ __align__(16) unsigned hist[kSelBins];
+    __shared__ unsigned s_wsum[kSelThreads / 32];
+    __shared__ unsigned s_digit, s_above, s_cnt, s_n;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+        const RowGeom g = row_geom(in, row, cols);
+        // f(v, col, ok) for every element of the row, warp-uniform calls:
+        // the 16-byte body in batches of kSelU loads per thread, then the
+        // few scalars outside it in warp 0.
+        auto for_row = [&](auto f) {
+            for (int base = 0; base < g.nvec; base += kSelThreads * kSelU) {
+                float4 r[kSelU];
+#pragma unroll
+                for (int u = 0; u < kSelU; ++u) {
+                    const int i = base + u * kSelThreads + tid;
+                    r[u] = i < g.nvec ? g.body[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < kSelU; ++u) {
+                    const int i = base + u * kSelThreads + tid;
+                    const bool ok = i < g.nvec;
+                    const unsigned c = (unsigned)(g.head + 4 * i);
+                    f(r[u].x, c, ok);
+                    f(r[u].y, c + 1u, ok);
+                    f(r[u].z, c + 2u, ok);
+                    f(r[u].w, c + 3u, ok);
+                }
+            }
+            if (warp == 0) {
+                const bool ok = lane < g.ns;
+                const int c = lane < g.head ? lane : g.tail0 + (lane - g.head);
+                f(ok ? g.rp[c] : 0.f, (unsigned)c, ok);
+            }
+        };
+
+        // The bucket of hist (complete after a barrier) that holds the
+        // want-th largest counted key: s_digit, with s_above keys in higher
+        // buckets and s_cnt in it.  Thread t takes bins 2047 - kSelPer t - q.
+        auto pick = [&](unsigned want) {
+            unsigned c[kSelPer], sum = 0;
+#pragma unroll
+            for (int q = 0; q < kSelPer; ++q) {
+                c[q] = hist[kSelBins - 1 - kSelPer * tid - q];
+                sum += c[q];
+            }
+            unsigned x = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned y = __shfl_up_sync(kFullMask, x, o);
+                if (lane >= o) x += y;
+            }
+            if (lane == 31) s_wsum[warp] = x;
+            __syncthreads();
+            unsigned acc = x - sum;
+            for (int w = 0; w < warp; ++w) acc += s_wsum[w];
+#pragma unroll
+            for (int q = 0; q < kSelPer; ++q) {
+                if (acc < want && want <= acc + c[q]) {
+                    s_digit = (unsigned)(kSelBins - 1 - kSelPer * tid - q);
+                    s_above = acc;
+                    s_cnt = c[q];
+                }
+                acc += c[q];
+            }
+            __syncthreads();
+        };
+
+        // Select: fix 11-bit digits from the top until the keys at or above
+        // the chosen bucket fit the buffer.
+        u64 prefix = 0ull;  // the fixed bits [top, 64)
+        int top = 64;
+        unsigned need = (unsigned)k;
+        for (;;) {
+            const int shift = top > kSelBits ? top - kSelBits : 0;
+            const unsigned dmask = (1u << (top - shift)) - 1u;
+            for (int i = tid; i < kSelBins; i += kSelThreads) hist[i] = 0u;
+            __syncthreads();
+            if (top == 64) {
+                for_row([&](float v, unsigned, bool ok) {
+                    if (ok) atomicAdd(&hist[score_key(__float_as_uint(v)) >> (32 - kSelBits)], 1u);
+                });
+            } else {
+                const u64 fixed = prefix >> top;
+                for_row([&](float v, unsigned c, bool ok) {
+                    const u64 key = full_key(v, c);
+                    if (ok && (key >> top) == fixed) atomicAdd(&hist[(unsigned)(key >> shift) & dmask], 1u);
+                });
+            }
+            __syncthreads();
+            pick(need);
+            const unsigned total = ((unsigned)k - need) + s_above + s_cnt;  // keys at or above the bucket
+            prefix |= (u64)s_digit << shift;
+            need -= s_above;
+            // All of the bucket is needed: the keys at or above its lower
+            // edge are the k best (top = 0 marks that).
+            top = need == s_cnt ? 0 : shift;
+            if (total <= (unsigned)kSelCap || top == 0) break;
+        }
+
+        // Collect the keys at or above prefix (its bits below `top` are zero):
+        // a float compare of each vector's largest element against the
+        // bucket's score first (every element at or above it passes, NaN
+        // included); keys only for vectors that pass, and one shared-counter
+        // add per warp and vector round that has any.
+        if (tid == 0) s_n = 0u;
+        __syncthreads();
+        {
+            const float tf = key_float((unsigned)(prefix >> 32));
+            // Append this lane's keys of one round (m: which of the 4 pass).
+            auto append = [&](unsigned m, u64 k0, u64 k1, u64 k2, u64 k3) {
+                const unsigned cnt = __popc(m);
+                unsigned x = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned y = __shfl_up_sync(kFullMask, x, o);
+                    if (lane >= o) x += y;
+                }
+                unsigned at = 0;
+                if (lane == 31 && x) at = atomicAdd(&s_n, x);
+                at = __shfl_sync(kFullMask, at, 31) + (x - cnt);
+                if ((m & 1u) && at < (unsigned)kSelCap) buf[at] = k0;
+                at += m & 1u;
+                if ((m & 2u) && at < (unsigned)kSelCap) buf[at] = k1;
+                at += (m >> 1) & 1u;
+                if ((m & 4u) && at < (unsigned)kSelCap) buf[at] = k2;
+                at += (m >> 2) & 1u;
+                if ((m & 8u) && at < (unsigned)kSelCap) buf[at] = k3;
+            };
+            for (int base = 0; base < g.nvec; base += kSelThreads * kSelU) {
+                float4 r[kSelU];
+#pragma unroll
+                for (int u = 0; u < kSelU; ++u) {
+                    const int i = base + u * kSelThreads + tid;
+                    r[u] = i < g.nvec ? g.body[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < kSelU; ++u) {
+                    const int i = base + u * kSelThreads + tid;
+                    const bool pass = i < g.nvec && !(max_nan(max_nan(r[u].x, r[u].y), max_nan(r[u].z, r[u].w)) < tf);
+                    if (__any_sync(kFullMask, pass)) {
+                        const unsigned c = (unsigned)(g.head + 4 * i);
+                        const u64 k0 = full_key(r[u].x, c), k1 = full_key(r[u].y, c + 1u);
+                        const u64 k2 = full_key(r[u].z, c + 2u), k3 = full_key(r[u].w, c + 3u);
+                        const unsigned m = pass ? (k0 >= prefix ? 1u : 0u) | (k1 >= prefix ? 2u : 0u) |
+                                                      (k2 >= prefix ? 4u : 0u) | (k3 >= prefix ? 8u : 0u)
+                                                : 0u;
+                        append(m, k0, k1, k2, k3);
+                    }
+                }
+            }
+            if (warp == 0) {
+                const bool ok = lane < g.ns;
+                const int c = lane < g.head ? lane : g.tail0 + (lane - g.head);
+                const u64 key = full_key(ok ? g.rp[c] : 0.f, (unsigned)c);
+                append(ok && key >= prefix ? 1u : 0u, key, 0ull, 0ull, 0ull);
+            }
+        }
+        __syncthreads();
+        const int n = (int)kmin(s_n, (unsigned)kSelCap);  // >= k
+
+        // The k best of the candidates.  When they round to the same sort
+        // size as k, sort them all.  Else go on with the select in shared
+        // memory (the keys are unique) until the keys at or above prefix are
+        // exactly the k best, move those to `best` (the histogram's space)
+        // and sort them.
+        u64* best = buf;
+        int nb = n;
+        if (top > 0 && next_pow2(n < 64 ? 64 : n) > next_pow2(k < 64 ? 64 : k)) {
+            while (top > 0) {
+                const int shift = top > kSelBits ? top - kSelBits : 0;
+                const unsigned dmask = (1u << (top - shift)) - 1u;
+                const u64 fixed = prefix >> top;
+                for (int i = tid; i < kSelBins; i += kSelThreads) hist[i] = 0u;
+                __syncthreads();
+                for (int i = tid; i < n; i += kSelThreads) {
+                    const u64 key = buf[i];
+                    if ((key >> top) == fixed) atomicAdd(&hist[(unsigned)(key >> shift) & dmask], 1u);
+                }
+                __syncthreads();
+                pick(need);
+                prefix |= (u64)s_digit << shift;
+                need -= s_above;
+                top = need == s_cnt ? 0 : shift;
+            }
+            best = reinterpret_cast<u64*>(hist);  // kSelBins words = 1024 keys >= k
+            if (tid == 0) s_n = 0u;
+            __syncthreads();
+            for (int base = 0; base < n; base += kSelThreads) {
+                const int i = base + tid;
+                const u64 key = i < n ? buf[i] : 0ull;
+                const bool p = i < n && key >= prefix;
+                const unsigned b = __ballot_sync(kFullMask, p);
+                unsigned at = 0;
+                if (lane == 0 && b) at = atomicAdd(&s_n, (unsigned)__popc(b));
+                at = __shfl_sync(kFullMask, at, 0);
+                if (p) best[at + __popc(b & lanemask_lt())] = key;
+            }
+            __syncthreads();
+            nb = k;
+        }
+        const int P = next_pow2(nb < 64 ? 64 : nb);  // <= 1024
+        for (int j = nb + tid; j < P; j += kSelThreads) best[j] = 0ull;  // below every real key
+        if (P <= 2 * kSelThreads)
+            block_sort_reg_desc<u64, kSelThreads>(best, P);
+        else
+            block_sort_smem_desc(best, P);
+        for (int j = tid; j < k; j += kSelThreads) {
+            const u64 key = best[j];
+            const unsigned col = 0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull);
+            const unsigned u = (unsigned)(key >> 32);
+            float v;
+            if (u == 0x80000000u || u == 0xFFFFFFFFu)
+                v = g.rp[col];  // -0.0 and NaN payloads: the input's bits
+            else
+                v = key_float(u);
+            vals[(size_t)row * k + j] = v;
+            idx[(size_t)row * k + j] = (int32_t)col;
+        }
+        __syncthreads();  // the buffer and histogram are reused by the next row
+    }
+}
+
 }  // namespace
 
 template <int L, bool kMask>
@@ -848,10 +1103,16 @@ cudaError_t launch_stream(cudaStream_t s, const float* in, int rows, int cols, i
                               keep, row_count);
 }
 
+// Rows of at most this many columns take the radix select (a row is read
+// twice, the second time from L2); longer rows the streamed candidate
+// buffer (one read).
+constexpr int kSelMaxCols = 1 << 16;
+
 cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int k, float* vals, int32_t* idx,
                         unsigned* status, bool early, int flags) {
     // k <= 128 streams rows (one warp per row); k > 128 takes one block per
-    // row with a shared-memory candidate buffer.
+    // row: a radix select for rows up to kSelMaxCols, else a streamed
+    // shared-memory candidate buffer.
     const bool stream = k <= 128;
     const uint8_t* nk = nullptr;
     int32_t* nc = nullptr;
@@ -860,16 +1121,16 @@ cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int
     if (stream) return launch_stream<4, false>(s, in, rows, cols, k, vals, idx, status, early, flags, nk, nc);
     constexpr int kMaxDev = 64;
     static std::mutex mu;
-    static int grid_cache[kMaxDev] = {};
+    static int grid_cache[kMaxDev][2] = {};
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
     if (device < 0 || device >= kMaxDev) return cudaErrorInvalidDevice;
-    int full;
+    int full, full_sel;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (grid_cache[device] == 0) {
-            int sms = 0, per_sm = 0;
+        if (grid_cache[device][0] == 0) {
+            int sms = 0, per_sm = 0, per_sm_sel = 0;
             e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
             if (e != cudaSuccess) return e;
             const void* fn = reinterpret_cast<const void*>(&topk_rows_big_kernel);
@@ -877,9 +1138,19 @@ cudaError_t rows_launch(cudaStream_t s, const float* in, int rows, int cols, int
             if (e != cudaSuccess) return e;
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kBigThreads, kBigRingBytes);
             if (e != cudaSuccess) return e;
-            grid_cache[device] = sms * (per_sm < 1 ? 1 : per_sm);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &per_sm_sel, reinterpret_cast<const void*>(&topk_rows_select_kernel), kSelThreads, 0);
+            if (e != cudaSuccess) return e;
+            grid_cache[device][0] = sms * (per_sm < 1 ? 1 : per_sm);
+            grid_cache[device][1] = sms * (per_sm_sel < 1 ? 1 : per_sm_sel);
         }
-        full = grid_cache[device];
+        full = grid_cache[device][0];
+        full_sel = grid_cache[device][1];
+    }
+    if (cols <= kSelMaxCols) {
+        const int grid = rows < full_sel ? rows : full_sel;
+        topk_rows_select_kernel<<<grid, kSelThreads, 0, s>>>(in, rows, cols, k, vals, idx);
+        return cudaGetLastError();
     }
     const int grid = rows < full ? rows : full;
     topk_rows_big_kernel<<<grid, kBigThreads, kBigRingBytes, s>>>(in, rows, cols, k, vals, idx, status);

@@ -803,8 +803,8 @@ def run_reference(args, world, rank):
     }
 
 
-PROFILE_TARGETS = ("i32_1e8_k20", "i32_1e8_k100", "rows_tied", "rows_untied", "large_k1000_i32", "large_k1000_f32",
-                   "sort_keys")
+PROFILE_TARGETS = ("i32_1e8_k20", "i32_1e8_k100", "rows_tied", "rows_untied", "rows_untied_k129", "large_k1000_i32",
+                   "large_k1000_f32", "sort_keys")
 
 
 def run_profile_target(args):
@@ -821,9 +821,10 @@ def run_profile_target(args):
         xh = synth.f32_rows_tied(w["rows"], w["cols"], w["seed"], w["tie_frac"]) if name == "rows_tied" else \
             synth.f32_rows_normal(w["rows"], w["cols"], w["seed"])
         x = torch.from_numpy(xh).to(dev)
-        vals = torch.empty(w["rows"], w["k"], dtype=torch.float32, device=dev)
-        idx = torch.empty(w["rows"], w["k"], dtype=torch.int32, device=dev)
-        call = lambda: tk.topk_rows_f32_ptr(x.data_ptr(), w["rows"], w["cols"], w["k"], vals.data_ptr(),
+        rk = 129 if name == "rows_untied_k129" else w["k"]
+        vals = torch.empty(w["rows"], rk, dtype=torch.float32, device=dev)
+        idx = torch.empty(w["rows"], rk, dtype=torch.int32, device=dev)
+        call = lambda: tk.topk_rows_f32_ptr(x.data_ptr(), w["rows"], w["cols"], rk, vals.data_ptr(),
                                             idx.data_ptr(), h)
     elif name == "sort_keys":
         x = torch.from_numpy(synth.i32_workload(WORKLOAD)).to(dev)

@@ -7,10 +7,10 @@
 //   1. takes the next tile id from a counter (so a tile only ever waits for
 //      tiles whose blocks are already running),
 //   2. ranks its keys stably: per warp, keys go slot by slot (32
-//      consecutive keys per slot); eight ballots, one per digit bit, give
-//      every lane the mask of lanes with its digit (a warp multisplit), so a
-//      key's rank among equal digits follows input order; warps then add the
-//      counts of the warps before them,
+//      consecutive keys per slot); each lane ORs its bit into its warp's
+//      shared word for its digit, so the word is the mask of lanes with that
+//      digit and a key's rank among equal digits follows input order; warps
+//      then add the counts of the warps before them,
 //   3. publishes its per-digit counts and looks back over earlier tiles for
 //      the keys of each digit before it (decoupled look-back: a tile's word
 //      says "my count" or "count of every tile up to me"),
@@ -162,6 +162,7 @@ sort_pass_kernel(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ 
     uint32_t* s_keys = sort_smem;                       // kTile
     uint32_t* s_vals = sort_smem + kTile;               // kTile (with values)
     __shared__ unsigned s_whist[kSW][kRadix];           // per-warp counts, then the warps' offsets
+    __shared__ unsigned s_match[kSW][kRadix];           // per-warp lane masks of one slot's digits (zero between slots)
     __shared__ unsigned s_tcount[kRadix];               // this tile's count per digit
     __shared__ unsigned s_texcl[kRadix];                // where each digit starts in the tile
     __shared__ unsigned s_goff[kRadix];                 // where this tile's keys of each digit go
@@ -174,7 +175,10 @@ sort_pass_kernel(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ 
         s_tile = t;
         if (t == ntiles - 1) h->tile_counter[pass] = 0u;  // every block has its id: reset for the next call
     }
-    for (int i = lane; i < kRadix; i += 32) s_whist[w][i] = 0u;
+    for (int i = lane; i < kRadix; i += 32) {
+        s_whist[w][i] = 0u;
+        s_match[w][i] = 0u;
+    }
     __syncthreads();
     const unsigned tile = s_tile;
     const size_t tbase = (size_t)tile * kTile;
@@ -190,30 +194,32 @@ sort_pass_kernel(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ 
         key[i] = p < tcnt ? kin[tbase + p] : 0xFFFFFFFFu;
         if (kVals) val[i] = p < tcnt ? vin[tbase + p] : 0u;
     }
-    // Stable rank within the warp among keys of the same digit: the lanes
-    // whose digit equals this lane's, from one ballot per digit bit (a warp
-    // multisplit); the lowest of them adds the group to the warp's count.
+    // Stable rank within the warp among keys of the same digit, slot by
+    // slot: every lane ORs its bit into its warp's word for its digit, so
+    // the word is the mask of lanes with that digit and a key's rank among
+    // them follows input order; the highest of them adds the group to the
+    // warp's count and clears the word.  (Keys past the end take no part.)
+    {
+        volatile unsigned* cnt = s_whist[w];
+        volatile unsigned* match = s_match[w];
+        const unsigned bit = 1u << lane;
 #pragma unroll
-    for (int i = 0; i < kSI; ++i) {
-        const unsigned p = (unsigned)(w * 32 * kSI + i * 32 + lane);
-        const bool ok = p < tcnt;
-        const unsigned d = (key[i] >> shift) & 0xFFu;
-        unsigned peers = __ballot_sync(kFullMask, ok);
-#pragma unroll
-        for (int bit = 0; bit < 8; ++bit) {
-            const unsigned bb = __ballot_sync(kFullMask, (d >> bit) & 1u);
-            peers &= ((d >> bit) & 1u) ? bb : ~bb;
+        for (int i = 0; i < kSI; ++i) {
+            const unsigned p = (unsigned)(w * 32 * kSI + i * 32 + lane);
+            const bool ok = p < tcnt;
+            const unsigned d = (key[i] >> shift) & 0xFFu;
+            if (ok) atomicOr((unsigned*)&match[d], bit);
+            __syncwarp();
+            const unsigned peers = ok ? match[d] : bit;
+            const unsigned before = ok ? cnt[d] : 0u;
+            __syncwarp();
+            if (ok && lane == 31 - __clz(peers)) {
+                cnt[d] = before + __popc(peers);
+                match[d] = 0u;
+            }
+            rank[i] = before + __popc(peers & (bit - 1u));
+            __syncwarp();
         }
-        if (!ok) peers = 1u << lane;  // past the end: a group of its own, never counted
-        const int leader = __ffs(peers) - 1;
-        unsigned before = 0;
-        if (lane == leader && ok) {
-            before = s_whist[w][d];
-            s_whist[w][d] = before + __popc(peers);
-        }
-        before = __shfl_sync(kFullMask, before, leader);
-        rank[i] = before + __popc(peers & lanemask_lt());
-        __syncwarp();
     }
     __syncthreads();
     // Per digit: the counts of the warps before each warp, and the tile's count.

@@ -186,13 +186,12 @@ sort_pass_kernel(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ 
 
     // Load: warp w owns tile keys [w*256, w*256 + 256), slot i = keys
     // w*256 + i*32 .. +31 (lane order = input order).
-    uint32_t key[kSI], val[kSI];
+    uint32_t key[kSI];
     unsigned rank[kSI];
 #pragma unroll
     for (int i = 0; i < kSI; ++i) {
         const unsigned p = (unsigned)(w * 32 * kSI + i * 32 + lane);
         key[i] = p < tcnt ? kin[tbase + p] : 0xFFFFFFFFu;
-        if (kVals) val[i] = p < tcnt ? vin[tbase + p] : 0u;
     }
     // Stable rank within the warp among keys of the same digit, slot by
     // slot: every lane ORs its bit into its warp's word for its digit, so
@@ -303,7 +302,7 @@ sort_pass_kernel(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ 
             const unsigned d = (key[i] >> shift) & 0xFFu;
             const unsigned slot = s_texcl[d] + s_whist[w][d] + rank[i];
             s_keys[slot] = key[i];
-            if (kVals) s_vals[slot] = val[i];
+            if (kVals) s_vals[slot] = vin[tbase + p];  // read only now: no registers held through the ranking
         }
     }
     __syncthreads();

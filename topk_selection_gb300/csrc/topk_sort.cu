@@ -11,11 +11,14 @@
 //      shared word for its digit, so the word is the mask of lanes with that
 //      digit and a key's rank among equal digits follows input order; warps
 //      then add the counts of the warps before them,
-//   3. publishes its per-digit counts and looks back over earlier tiles for
-//      the keys of each digit before it (decoupled look-back: a tile's word
-//      says "my count" or "count of every tile up to me"),
-//   4. places its keys in shared memory in digit order and writes them out,
-//      so that keys of one digit go to consecutive addresses.
+//   3. publishes its per-digit counts as soon as the warps' counts give
+//      them, and places its keys (and values) in shared memory in digit
+//      order,
+//   4. looks back over earlier tiles for the keys of each digit before it
+//      (decoupled look-back: a tile's word says "my count" or "count of
+//      every tile up to me"), 16 words per digit per round trip, now that
+//      no key is held in registers, and writes its keys out, so that keys of
+//      one digit go to consecutive addresses.
 // The page's printed scatter increments shared counters without atomics;
 // only its plan (digits, passes, histograms) is kept.
 //
@@ -43,6 +46,7 @@ constexpr int kSI = 16;             // keys per thread (8192-key tiles: measured
 constexpr int kTile = kST * kSI;    // keys per tile
 constexpr int kRadix = 256;
 constexpr int kSpins = 1 << 22;     // polls of one look-back word before giving up
+constexpr int kLookW = 16;          // look-back words read per digit per round trip
 constexpr int kHT = 512, kHU = 8;   // histogram pass: threads, 16-byte loads in flight
 constexpr int kHR = 8;              // histogram pass: copies of each digit histogram
 
@@ -221,7 +225,10 @@ sort_pass_kernel(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ 
         }
     }
     __syncthreads();
-    // Per digit: the counts of the warps before each warp, and the tile's count.
+    // Per digit: the counts of the warps before each warp and the tile's
+    // count, published at once (so that later tiles see it early); then
+    // where each digit starts inside the tile.
+    const unsigned long long tag = (unsigned long long)(epoch & 0x3FFFFFFFu) << 32;
     if (threadIdx.x < kRadix) {
         const int d = threadIdx.x;
         unsigned acc = 0;
@@ -232,60 +239,15 @@ sort_pass_kernel(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ 
             acc += c;
         }
         s_tcount[d] = acc;
-    }
-    __syncthreads();
-    // Publish this tile's counts, then look back (one thread per digit).
-    if (threadIdx.x < kRadix) {
-        const int d = threadIdx.x;
-        const unsigned c = s_tcount[d];
-        const unsigned long long tag = (unsigned long long)(epoch & 0x3FFFFFFFu) << 32;
-        unsigned long long* mine = look + (size_t)tile * kRadix + d;
-        unsigned excl = 0;
-        if (tile == 0) {
-            st_relaxed_u64(mine, kIncl | tag | c);
-        } else {
-            st_relaxed_u64(mine, kAgg | tag | c);
-            // Walk back over the tiles before this one, four words per round
-            // trip: add counts until a word that already covers every tile
-            // before it.  A word not yet written is read again (bounded).
-            long long j = (long long)tile - 1;
-            int spins = 0;
-            bool done = false;
-            while (!done && j >= 0) {
-                unsigned long long v[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) v[q] = j - q >= 0 ? ld_relaxed_u64(look + (size_t)(j - q) * kRadix + d) : 0ull;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (done || j < 0) break;
-                    if ((v[q] & 0x3FFFFFFF00000000ull) != tag || (v[q] >> 62) == 0) {
-                        if (++spins >= max_spins) {  // give up: go on with what has been summed
-                            atomicOr(status, kStatusWaitTimeout);
-                            done = true;
-                        }
-                        break;  // read again from j
-                    }
-                    excl += (unsigned)v[q];
-                    --j;
-                    if ((v[q] >> 62) == 2) done = true;
-                }
-            }
-            st_relaxed_u64(mine, kIncl | tag | (excl + c));
-        }
-        s_goff[d] = __ldcg(&h->base[pass][d]) + excl;
-    }
-    // Where each digit starts inside the tile: exclusive scan of s_tcount.
-    if (threadIdx.x < kRadix) {
-        const unsigned c = s_tcount[threadIdx.x];
-        unsigned x = c;
+        st_relaxed_u64(look + (size_t)tile * kRadix + d, (tile == 0 ? kIncl : kAgg) | tag | acc);
+        unsigned x = acc;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const unsigned y = __shfl_up_sync(kFullMask, x, o);
             if (lane >= o) x += y;
         }
         if (lane == 31) s_scan[w] = x;
-        __syncwarp();
-        s_texcl[threadIdx.x] = x - c;  // within the warp; warps added below
+        s_texcl[d] = x - acc;  // within the warp; warps added below
     }
     __syncthreads();
     if (threadIdx.x < kRadix) {
@@ -304,6 +266,42 @@ sort_pass_kernel(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ 
             s_keys[slot] = key[i];
             if (kVals) s_vals[slot] = vin[tbase + p];  // read only now: no registers held through the ranking
         }
+    }
+    __syncthreads();
+    // Look back (one thread per digit), now that no key or rank is held in
+    // registers: walk back over the tiles before this one, kLookW words per
+    // round trip, adding counts until a word that already covers every tile
+    // before it.  A word not yet written is read again (bounded).
+    if (threadIdx.x < kRadix) {
+        const int d = threadIdx.x;
+        unsigned excl = 0;
+        if (tile != 0) {
+            long long j = (long long)tile - 1;
+            int spins = 0;
+            bool done = false;
+            while (!done && j >= 0) {
+                unsigned long long v[kLookW];
+#pragma unroll
+                for (int q = 0; q < kLookW; ++q)
+                    v[q] = j - q >= 0 ? ld_relaxed_u64(look + (size_t)(j - q) * kRadix + d) : 0ull;
+#pragma unroll
+                for (int q = 0; q < kLookW; ++q) {
+                    if (done || j < 0) break;
+                    if ((v[q] & 0x3FFFFFFF00000000ull) != tag || (v[q] >> 62) == 0) {
+                        if (++spins >= max_spins) {  // give up: go on with what has been summed
+                            atomicOr(status, kStatusWaitTimeout);
+                            done = true;
+                        }
+                        break;  // read again from j
+                    }
+                    excl += (unsigned)v[q];
+                    --j;
+                    if ((v[q] >> 62) == 2) done = true;
+                }
+            }
+            st_relaxed_u64(look + (size_t)tile * kRadix + d, kIncl | tag | (excl + s_tcount[d]));
+        }
+        s_goff[d] = __ldcg(&h->base[pass][d]) + excl;
     }
     __syncthreads();
     for (unsigned i = threadIdx.x; i < tcnt; i += kST) {

@@ -321,7 +321,14 @@ enum topk_option {
      * to wrong places inside the output (never outside it), and
      * topk_check_stream then reports TOPK_ERR_DEVICE_TIMEOUT.  Lower it
      * only to exercise that report. */
-    TOPK_OPT_SORT_SPINS = 7
+    TOPK_OPT_SORT_SPINS = 7,
+    /* 1: the first tile of every digit pass of topk_sort_u32 withholds its
+     * look-back word (0 restores the default).  The tile after it then
+     * polls a word that nothing writes until the poll limit runs out, gives
+     * up, and topk_check_stream reports TOPK_ERR_DEVICE_TIMEOUT; the output
+     * is then wrong but every write stays inside it.  Only to exercise that
+     * report, with TOPK_OPT_SORT_SPINS lowered so that the wait is short. */
+    TOPK_OPT_SORT_WITHHOLD = 8
 };
 
 /* Set a process-wide option; takes effect for calls made afterwards.

@@ -181,7 +181,7 @@ def test_options_accept_and_reject(lib):
     import topk_selection_gb300 as tk
 
     for opt, good, bad in ((tk.OPT_NO_EARLY_START, (1, 0), (2, -1)), (tk.OPT_FAULT_ALLOC, (1, 0), (2, -1)),
-                           (tk.OPT_SORT_SPINS, (1, 0), (-1,)), (tk.OPT_STREAM_STATIC, (1, 101, 0), (102, -1)),
+                           (tk.OPT_SORT_SPINS, (1, 0), (-1,)), (tk.OPT_SORT_WITHHOLD, (1, 0), (-1, 2)), (tk.OPT_STREAM_STATIC, (1, 101, 0), (102, -1)),
                            (tk.OPT_STAGE2_CAP, (64, 0), (3, 1))):
         for v in good:
             tk.set_option(opt, v)

@@ -1,13 +1,15 @@
 """Failure detection without a GPU fault.
 
 * A bounded device-side wait that runs out: the radix sort's decoupled
-  look-back polls words that earlier tiles publish, and TOPK_OPT_SORT_SPINS
-  lowers its poll limit so that tiles give up.  A tile that gives up has
-  summed only some earlier tiles, so its offsets are too small but never
-  below its digit's base: every write stays inside the output (the order is
-  wrong).  topk_check_stream must then report TOPK_ERR_DEVICE_TIMEOUT, and
-  the next sort, at the normal limit, must be right again.  The mbarrier
-  waits on in-flight bulk copies are not shortened by any option.
+  look-back polls words that earlier tiles publish.  TOPK_OPT_SORT_WITHHOLD
+  makes the first tile of each pass withhold its word (a flag that nothing
+  sets), and TOPK_OPT_SORT_SPINS lowers the poll limit, so the tile after it
+  gives up, every time.  A tile that gives up has summed only some earlier
+  tiles, so its offsets are too small but never below its digit's base:
+  every write stays inside the output (the order is wrong).
+  topk_check_stream must then report TOPK_ERR_DEVICE_TIMEOUT, and the next
+  sort, with both options cleared, must be right again.  The mbarrier waits
+  on in-flight bulk copies are not shortened by any option.
 * A host-side allocation failure (TOPK_OPT_FAULT_ALLOC, or the environment
   variable TOPK_FAULT_ALLOC=1): the call returns TOPK_ERR_NO_MEMORY and
   touches nothing; after the hook is cleared the same call succeeds.
@@ -40,7 +42,8 @@ def test_sort_lookback_gives_up_and_is_reported(tk):
     d = torch.from_numpy(keys.view(np.int32)).cuda()
     s = torch.cuda.Stream()
     tk.check_stream(s)  # start from a clean status word
-    tk.set_option(tk.OPT_SORT_SPINS, 1)
+    tk.set_option(tk.OPT_SORT_SPINS, 64)
+    tk.set_option(tk.OPT_SORT_WITHHOLD, 1)
     try:
         with torch.cuda.stream(s):
             tk.sort_u32(d, stream=s)
@@ -48,6 +51,7 @@ def test_sort_lookback_gives_up_and_is_reported(tk):
             tk.check_stream(s)
         assert err.value.status == 5  # TOPK_ERR_DEVICE_TIMEOUT
     finally:
+        tk.set_option(tk.OPT_SORT_WITHHOLD, 0)
         tk.set_option(tk.OPT_SORT_SPINS, 0)
     with torch.cuda.stream(s):
         ko, _ = tk.sort_u32(d, stream=s)

@@ -117,6 +117,7 @@ OPT_STREAM_STATIC = 4
 OPT_NO_EARLY_START = 5
 OPT_FAULT_ALLOC = 6
 OPT_SORT_SPINS = 7
+OPT_SORT_WITHHOLD = 8
 
 
 def set_option(option: int, value: int) -> None:

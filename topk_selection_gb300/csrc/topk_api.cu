@@ -25,6 +25,7 @@ std::atomic<int> g_radix_sample_rank{0};
 std::atomic<int> g_stream_static{0};
 std::atomic<int> g_no_early{0};
 std::atomic<int> g_sort_spins{0};
+std::atomic<int> g_sort_withhold{0};
 std::atomic<int> g_fault_alloc{-1};  // -1: not read yet from TOPK_FAULT_ALLOC
 
 // Fault injection on the host: when set (environment TOPK_FAULT_ALLOC=1 at
@@ -183,6 +184,7 @@ int radix_cap_option() { return g_radix_cap.load(std::memory_order_relaxed); }
 int radix_sample_rank_option() { return g_radix_sample_rank.load(std::memory_order_relaxed); }
 int stream_static_option() { return g_stream_static.load(std::memory_order_relaxed); }
 int sort_spins_option() { return g_sort_spins.load(std::memory_order_relaxed); }
+int sort_withhold_option() { return g_sort_withhold.load(std::memory_order_relaxed); }
 void note_cuda_error(int err) { t_last_cuda_error = err; }
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 void note_unreleased_launch(int device, cudaStream_t s) {
@@ -581,6 +583,10 @@ int topk_set_option(int option, int value) {
         case TOPK_OPT_SORT_SPINS:
             if (value < 0) return TOPK_ERR_INVALID_ARG;
             g_sort_spins.store(value, std::memory_order_relaxed);
+            return TOPK_OK;
+        case TOPK_OPT_SORT_WITHHOLD:
+            if (value != 0 && value != 1) return TOPK_ERR_INVALID_ARG;
+            g_sort_withhold.store(value, std::memory_order_relaxed);
             return TOPK_OK;
         case TOPK_OPT_FAULT_ALLOC:
             if (value != 0 && value != 1) return TOPK_ERR_INVALID_ARG;

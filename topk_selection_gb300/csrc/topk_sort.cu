@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kST, 2)
 sort_pass_kernel(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ vin, uint32_t* __restrict__ kout,
                  uint32_t* __restrict__ vout, size_t n, int shift, SortHeader* __restrict__ h, int pass,
                  unsigned long long* __restrict__ look, unsigned epoch, unsigned ntiles, unsigned* __restrict__ status,
-                 int max_spins) {
+                 int max_spins, int withhold) {
     extern __shared__ __align__(16) uint32_t sort_smem[];
     uint32_t* s_keys = sort_smem;                       // kTile
     uint32_t* s_vals = sort_smem + kTile;               // kTile (with values)
@@ -239,7 +239,8 @@ sort_pass_kernel(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ 
             acc += c;
         }
         s_tcount[d] = acc;
-        st_relaxed_u64(look + (size_t)tile * kRadix + d, (tile == 0 ? kIncl : kAgg) | tag | acc);
+        if (tile != 0 || !withhold)  // (a test option makes the first tile withhold its word)
+            st_relaxed_u64(look + (size_t)tile * kRadix + d, (tile == 0 ? kIncl : kAgg) | tag | acc);
         unsigned x = acc;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -385,14 +386,15 @@ cudaError_t sort_launch(cudaStream_t s, const uint32_t* keys, const uint32_t* va
     // the status word reports it.
     const int opt_spins = sort_spins_option();
     const int spins = opt_spins > 0 ? opt_spins : kSpins;
+    const int withhold = sort_withhold_option();
     for (int p = 0; p < 4; ++p) {
         const unsigned ep = (epoch * 4u + (unsigned)p) & 0x3FFFFFFFu;
         if (vals)
             sort_pass_kernel<true><<<(unsigned)tiles, kST, smem, s>>>(ki[p], vi[p], ko[p], vo[p], n, 8 * p, h, p,
-                                                                     look, ep, (unsigned)tiles, status, spins);
+                                                                     look, ep, (unsigned)tiles, status, spins, withhold);
         else
             sort_pass_kernel<false><<<(unsigned)tiles, kST, smem, s>>>(ki[p], nullptr, ko[p], nullptr, n, 8 * p, h,
-                                                                      p, look, ep, (unsigned)tiles, status, spins);
+                                                                      p, look, ep, (unsigned)tiles, status, spins, withhold);
         *launches += 1;
     }
     return cudaGetLastError();

@@ -135,7 +135,6 @@ int stage2_cap_option();
 int stream_static_option();
 // Current value of TOPK_OPT_SORT_SPINS (0 = default).
 int sort_spins_option();
-int sort_withhold_option();
 
 // Grid for an n-element, k-wide selection on `device` (k <= 128: the
 // streaming plan; larger k use radix_launch).

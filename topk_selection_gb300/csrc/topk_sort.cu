@@ -38,6 +38,8 @@
 
 namespace topk {
 
+int sort_withhold_option();  // test option TOPK_OPT_SORT_WITHHOLD (topk_api.cu)
+
 namespace {
 
 constexpr int kST = 512;            // threads per tile

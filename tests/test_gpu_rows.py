@@ -234,3 +234,21 @@ def test_chained_and_overlapping_calls(tk):
     assert np.array_equal(iy.cpu().numpy(), eiy) and np.array_equal(bits(vy.cpu().numpy()), bits(evy))
     assert np.array_equal(t.cpu().numpy(), oracle.topk_i32(eiy.reshape(-1).astype(np.int32), 5))
     assert np.array_equal(i3.cpu().numpy(), eiy) and np.array_equal(bits(v3.cpu().numpy()), bits(evy))
+
+
+@pytest.mark.parametrize("cols", [65_536, 65_537])
+def test_select_deeper_levels_and_kernel_boundary(tk, cols):
+    # 128 < k <= 1024 on rows up to 65536 columns is a per-row radix select
+    # whose first 11-bit bucket must hold at most 4096 candidates; these rows
+    # make it hold more, so further digit levels (score bits, then column
+    # bits) decide.  65537 columns take the streamed kernel instead.
+    rng = np.random.default_rng(cols)
+    x = rng.standard_normal((8, cols)).astype(np.float32)
+    x[0] = rng.uniform(1.0, 1.25, cols).astype(np.float32)   # every key in one first-level bucket
+    x[1] = np.float32(1.5)
+    x[1, rng.choice(cols, 5000, replace=False)] = np.float32(7.0)  # 5000 copies of the largest value
+    x[2] = np.float32(-3.0)                                   # all equal: columns alone decide
+    x[3] = np.round(x[3] * 64) / 64                           # dense ties everywhere
+    x[4, ::3] = np.nan                                        # NaN above +inf, equal among themselves
+    for k in (129, 777, 1024):
+        assert_rows_equal(tk, x, k)

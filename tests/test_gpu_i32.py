@@ -135,10 +135,12 @@ def test_large_k_exact_passes(tk, kind, n):
     # exact radix passes take over.  Sample rank 1 puts the threshold at the
     # sample's maximum, so the filter keeps fewer than k keys; a buffer capped
     # at k (option value 1) makes the filter overflow and makes the second
-    # exact pass histogram instead of collect.
+    # exact pass histogram instead of collect.  Sample rank 2000 leaves tens
+    # of thousands of candidates, so that the final of a small k runs on the
+    # whole cluster instead of one CTA.
     x = make(kind, n, seed=n + 1)
     try:
-        for rank, cap in ((1, 0), (1, 1), (0, 1), (0, 6000)):
+        for rank, cap in ((1, 0), (1, 1), (0, 1), (0, 6000), (2000, 0)):
             tk.set_option(tk.OPT_RADIX_SAMPLE_RANK, rank)
             tk.set_option(tk.OPT_RADIX_CAP, cap)
             for k in (129, 1000, 5000):

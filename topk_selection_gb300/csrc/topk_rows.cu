@@ -818,9 +818,13 @@ topk_rows_big_kernel(const float* __restrict__ in, int rows, int cols, int k, fl
 //     last pass collects them, else the bucket's digit is fixed and the next
 //     digit is histogrammed.  The keys are unique, so the last level's
 //     bucket holds one key and the buffer always suffices by then;
-//   * the candidates are sorted in shared memory and the first k written.
-// For N(0,1) rows and k = 129 .. 1024 one level is enough (about 750 .. 1300
-// candidates), so a row is read once from HBM and once from L2.
+//   * when the candidates round to the same sort size as k they are all
+//     sorted; else the select goes on over them in shared memory until
+//     exactly the k best are left, and those are sorted; the first k are
+//     written.
+// For N(0,1) rows and k = 129 .. 1024 one level is enough (about 200 .. 1300
+// candidates), so a row is read once from HBM and once from L2.  Four
+// 256-thread blocks per SM keep that many rows in flight.
 constexpr int kSelThreads = 256;
 constexpr int kSelCap = 4096;                 // candidate buffer (32 KiB)
 constexpr int kSelBits = 11;

@@ -612,6 +612,7 @@ struct ClSmem {
     unsigned nranges;                     // (rank 0's is read by the others)
     unsigned pick_digit;
     unsigned pick_above;
+    unsigned pick_cnt;                    // keys in the picked bucket
     unsigned wmax[kClWarps];              // radix range plan: per-warp maxima of the keys above T
     unsigned cmax;                        // the CTA's maximum (read by the others)
     unsigned hi_key;                      // the cluster's maximum
@@ -657,6 +658,7 @@ __device__ __forceinline__ void cluster_pick(ClSmem& S, const unsigned* H, unsig
                 if (acc + c[b] >= need) {
                     S.pick_digit = lane * 8 + b;
                     S.pick_above = acc;
+                    S.pick_cnt = c[b];
                     break;
                 }
                 acc += c[b];
@@ -691,6 +693,7 @@ __device__ __forceinline__ void cta_pick(ClSmem& S, const unsigned* H, unsigned 
                 if (acc + c[b] >= need) {
                     S.pick_digit = lane * 8 + b;
                     S.pick_above = acc;
+                    S.pick_cnt = c[b];
                     break;
                 }
                 acc += c[b];
@@ -874,8 +877,21 @@ radix_cluster_kernel(const int32_t* __restrict__ in, size_t n, int k, unsigned j
             }
             prefix |= S.pick_digit << shift;
             need -= S.pick_above;
+            const unsigned ge = (j - need) + S.pick_cnt;  // keys at or above the bucket's lower edge
             __syncthreads();  // the pick and part are rewritten at the next level
             top = shift;
+            // The sample needs only a threshold with at least j of its keys
+            // above it, not its exact j-th key: once the bucket's lower edge
+            // L (= prefix, lower bits zero) has between j and 2j keys at or
+            // above it, L - 1 serves and the remaining levels are skipped
+            // (for uniform keys, after the second level) -- as long as the
+            // candidates it keeps, about ge * n / kSampleKeys, stay within
+            // half the buffer.
+            if (mode == kClSample && top > 0 && prefix > 0u && ge <= 2u * j &&
+                (unsigned long long)ge * n <= (unsigned long long)kSampleKeys * (cap / 2u)) {
+                prefix -= 1u;
+                break;
+            }
         }
         T = prefix;
     }
